@@ -1,0 +1,242 @@
+// ge_oracle.cpp -- plain CPU oracle for the fused linear-layer path.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or
+// load this file: only the tests, the smoke check and the CPU-baseline leg
+// of the benchmark do. It shares no code, header, table or constant with the
+// CUDA library; the two are compared on identical fp16 bit patterns.
+//
+// What it computes is the plain definition of the fused epilogue GEMM, in
+// fp64, with no blocking, fusion or reordering:
+//
+//   z[m,n] = sum_k A[m,k] * B[k,n]  (k ascending, fp64)          -- the GEMM
+//          + bias[m]                (broadcast over every column) -- BIAS
+//   y[m,n] = act(z[m,n])            NONE | ReLU | tanh-GELU       -- activation
+//   D[m,n] = fp16(y[m,n])           round to nearest even         -- one store
+//   mask   = (z > 0) bit-packed     (RELU_AUX_BIAS only)          -- aux output
+//
+// Sources (page title, section):
+//  * nvmath-python cuBLASLt bias-fusion guide, "Core API and parameter
+//    configuration": D = weights @ x + bias with bias of shape (m,1) added to
+//    every column of the (m,n) product; fp16 inputs and output with a 32-bit
+//    compute type ("Advanced techniques", precision item).
+//  * same page, "Advanced techniques": RELU_BIAS / GELU_BIAS apply ReLU or GELU
+//    to Wx+b; DRELU_BGRAD applies the ReLU gradient mask in the backward pass
+//    and accumulates the bias gradient.
+//  * Fusing bias addition with matrix multiplication using nvmath-python:
+//    Y = ReLU(WX + B); RELU_AUX_BIAS keeps an auxiliary output for backward.
+//  * ops-nn MatMul fusion (codearts), "ops-nn's MatMul fusion strategy",
+//    first level: the fused and the three-step flows compute the same values.
+// Readings where the pages are silent (GELU form = tanh approximation; mask
+// bit = z > 0 on the unrounded pre-activation, 32 bits per word along the
+// contiguous dimension of stored D, rows padded to 16 bytes; bias gradient =
+// sum over tokens of the masked dY) are the plainest ones the pages support.
+//
+// Pins (tests/test_oracle_pins.py): hand-worked 2x3x4 example, brute-force
+// triple loops on tiny inputs in every layout, exhaustive fp16 decode and
+// encode against a library conversion, tanh-GELU against an independent
+// sigmoid identity and a library GELU, ReLU(z) == z*mask, the exact
+// integer-valued case, and the bias gradient against a second summation.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// Epilogue codes of this oracle (its own numbering; the Python wrapper maps
+// names to these).
+enum OraEpi { ORA_NONE = 0, ORA_BIAS = 1, ORA_RELU_BIAS = 2, ORA_GELU_BIAS = 3,
+              ORA_RELU_AUX_BIAS = 4 };
+
+// IEEE-754 binary16 -> binary64, written from the format definition:
+// 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+double f16_decode(uint16_t h) {
+  const int s = h >> 15;
+  const int e = (h >> 10) & 31;
+  const int f = h & 1023;
+  double v;
+  if (e == 0)
+    v = std::ldexp((double)f, -24);             // zero / subnormal: f * 2^-24
+  else if (e == 31)
+    v = f ? std::nan("") : INFINITY;            // inf / NaN
+  else
+    v = std::ldexp((double)(1024 + f), e - 25); // (1 + f/1024) * 2^(e-15)
+  return s ? -v : v;
+}
+
+// Round a non-negative double (< 2^52) to the nearest integer, ties to even.
+double round_half_even(double q) {
+  const double fl = std::floor(q);
+  const double r = q - fl;  // exact for q < 2^52
+  if (r > 0.5) return fl + 1.0;
+  if (r < 0.5) return fl;
+  return std::fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;
+}
+
+// binary64 -> binary16 with round-to-nearest-even, overflow to +-inf,
+// subnormals kept (no flush to zero).
+uint16_t f16_encode(double x) {
+  if (std::isnan(x)) return 0x7E00;
+  const uint16_t s = std::signbit(x) ? 0x8000 : 0;
+  const double a = std::fabs(x);
+  // 65504 is the largest finite half; 65520 is the midpoint to 2^16 and ties
+  // to the even neighbour, which is the overflow, so it rounds to infinity.
+  if (a >= 65520.0) return s | 0x7C00;
+  if (a < std::ldexp(1.0, -14)) {
+    // subnormal range: value = q * 2^-24, q in [0, 1024]; q == 1024 is the
+    // smallest normal, whose bit pattern is also 1024.
+    const double q = round_half_even(std::ldexp(a, 24));
+    return s | (uint16_t)q;
+  }
+  int E;
+  std::frexp(a, &E);           // a = f * 2^E, f in [0.5, 1)
+  int e = E - 1;               // a in [2^e, 2^(e+1))
+  double q = round_half_even(std::ldexp(a, 10 - e));  // in [1024, 2048]
+  if (q == 2048.0) { q = 1024.0; e += 1; }
+  if (e + 15 >= 31) return s | 0x7C00;
+  return s | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0);
+}
+
+// The activation applied after the bias add.
+double activation(int epi, double z) {
+  switch (epi) {
+    case ORA_RELU_BIAS:
+    case ORA_RELU_AUX_BIAS:
+      return z > 0.0 ? z : 0.0;
+    case ORA_GELU_BIAS: {
+      // tanh form: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+      const double c = std::sqrt(2.0 / 3.14159265358979323846);
+      return 0.5 * z * (1.0 + std::tanh(c * (z + 0.044715 * z * z * z)));
+    }
+    default:
+      return z;
+  }
+}
+
+template <class F>
+void parallel_rows(int64_t rows, int nthreads, F fn) {
+  if (nthreads <= 1 || rows < 2) {
+    for (int64_t r = 0; r < rows; ++r) fn(r);
+    return;
+  }
+  if (nthreads > rows) nthreads = (int)rows;
+  std::vector<std::thread> pool;
+  for (int t = 0; t < nthreads; ++t) {
+    pool.emplace_back([=]() {
+      for (int64_t r = t; r < rows; r += nthreads) fn(r);
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+double ora_f16_to_f64(uint16_t h) { return f16_decode(h); }
+// The activation of epilogue `epi` applied to one fp64 pre-activation value
+// (the same function the forward uses); -1 selects nothing and returns NaN.
+double ora_act_f64(int epi, double z) {
+  if (epi < ORA_NONE || epi > ORA_RELU_AUX_BIAS) return std::nan("");
+  return activation(epi, z);
+}
+uint16_t ora_f64_to_f16(double x) { return f16_encode(x); }
+
+void ora_f16_to_f64_array(const uint16_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f16_decode(in[i]);
+}
+void ora_f64_to_f16_array(const double* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f16_encode(in[i]);
+}
+
+// D = act(A.B + bias) for the whole (M, N, K) problem.
+//   A[m,k] at A[m*lda + k] when a_major == 0 (K-major), A[k*lda + m] when 1.
+//   B[k,n] at B[n*ldb + k] when b_major == 0 (K-major), B[k*ldb + n] when 1.
+//   D[m,n] at D[m*ldd + n] when d_layout == 0 (row),     D[n*ldd + m] when 1.
+//   Stored row r / contiguous index c of D: (r,c) = (m,n) row, (n,m) col.
+//   aux (RELU_AUX_BIAS only): bit (c % 32) of aux[r*ld_aux + c/32] = (z > 0);
+//   every word of every stored row is written (padding bits 0).
+//   Z (optional, may be NULL): the fp64 pre-activation z, laid out like D.
+//   bias may be NULL only for ORA_NONE.
+// Returns 0 on success, -1 on a bad argument.
+int ora_linear_forward(int64_t M, int64_t N, int64_t K,
+                       const uint16_t* A, int a_major, int64_t lda,
+                       const uint16_t* B, int b_major, int64_t ldb,
+                       const uint16_t* bias, int epi,
+                       uint16_t* D, int d_layout, int64_t ldd,
+                       uint32_t* aux, int64_t ld_aux, double* Z,
+                       int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || !D) return -1;
+  if (epi < ORA_NONE || epi > ORA_RELU_AUX_BIAS) return -1;
+  if (epi != ORA_NONE && !bias) return -1;
+  if (epi == ORA_RELU_AUX_BIAS && !aux) return -1;
+  const int64_t rows = d_layout == 0 ? M : N;
+  const int64_t cols = d_layout == 0 ? N : M;
+  if (ldd < cols || (aux && ld_aux * 32 < cols)) return -1;
+  if (K > 0 && (!A || !B)) return -1;
+
+  // Layout step only: decode both operands into plain fp64 matrices with k
+  // contiguous, Ad[m][k] = A[m,k] and Bd[n][k] = B[k,n]. The products of two
+  // fp16 values are exact in fp64; the sums below run k = 0, 1, ..., K-1.
+  std::vector<double> Ad((size_t)M * (size_t)K), Bd((size_t)N * (size_t)K);
+  parallel_rows(M, nthreads, [&](int64_t m) {
+    for (int64_t k = 0; k < K; ++k)
+      Ad[m * K + k] = f16_decode(a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
+  });
+  parallel_rows(N, nthreads, [&](int64_t n) {
+    for (int64_t k = 0; k < K; ++k)
+      Bd[n * K + k] = f16_decode(b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
+  });
+
+  parallel_rows(rows, nthreads, [&](int64_t r) {
+    if (epi == ORA_RELU_AUX_BIAS)
+      std::memset(aux + r * ld_aux, 0, sizeof(uint32_t) * ld_aux);
+    for (int64_t c = 0; c < cols; ++c) {
+      const int64_t m = d_layout == 0 ? r : c;
+      const int64_t n = d_layout == 0 ? c : r;
+      const double* a = Ad.data() + m * K;
+      const double* b = Bd.data() + n * K;
+      double z = 0.0;
+      for (int64_t k = 0; k < K; ++k) z += a[k] * b[k];
+      if (epi != ORA_NONE) z += f16_decode(bias[m]);
+      const double y = activation(epi, z);
+      D[r * ldd + c] = f16_encode(y);
+      if (Z) Z[r * ldd + c] = z;
+      if (epi == ORA_RELU_AUX_BIAS && z > 0.0)
+        aux[r * ld_aux + c / 32] |= (uint32_t)1u << (c % 32);
+    }
+  });
+  return 0;
+}
+
+// Backward epilogue (DRELU_BGRAD), from the page's description: apply the
+// stored ReLU mask to the incoming gradient and reduce the bias gradient.
+//   dY, dZ: [M, N] in the forward D's stored layout (d_layout, ldd).
+//   aux: the forward mask (same packing as ora_linear_forward).
+//   dZ[m,n] = dY[m,n] if bit(m,n) else +0.
+//   bgrad[m] = sum over n of dZ[m,n], n ascending, fp64.
+int ora_drelu_bgrad(int64_t M, int64_t N, const uint16_t* dY, int d_layout,
+                    int64_t ldd, const uint32_t* aux, int64_t ld_aux,
+                    uint16_t* dZ, double* bgrad) {
+  if (M < 0 || N < 0 || !dY || !aux || !dZ || !bgrad) return -1;
+  for (int64_t m = 0; m < M; ++m) bgrad[m] = 0.0;
+  for (int64_t m = 0; m < M; ++m) {
+    double s = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const int64_t r = d_layout == 0 ? m : n;
+      const int64_t c = d_layout == 0 ? n : m;
+      const bool bit = (aux[r * ld_aux + c / 32] >> (c % 32)) & 1u;
+      // ReLU'(z) is 1 where the mask bit is set and 0 elsewhere; a masked-out
+      // gradient is +0 (a select, so -0, inf or NaN in dY do not leak).
+      const uint16_t out = bit ? dY[r * ldd + c] : (uint16_t)0;
+      dZ[r * ldd + c] = out;
+      s += f16_decode(out);
+    }
+    bgrad[m] = s;
+  }
+  return 0;
+}
+
+}  // extern "C"

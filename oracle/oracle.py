@@ -1,0 +1,173 @@
+"""Python wrapper of the plain CPU oracle (``ge_oracle.cpp``).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by ``__graft_entry__.smoke``
+and by the CPU-baseline leg of ``bench.py``; never by the library itself. It
+imports nothing from the CUDA package and shares no code with it.
+
+Arrays are numpy: fp16 operands are passed as their uint16 bit patterns, so
+the oracle and the GPU see identical bits. Layout vocabulary (the oracle's
+own; it mirrors the library's documented layouts):
+
+* ``a_major``: ``"k"`` -> A[m,k] at ``A[m*lda + k]``; ``"m"`` -> ``A[k*lda + m]``
+* ``b_major``: ``"k"`` -> B[k,n] at ``B[n*ldb + k]``; ``"n"`` -> ``B[k*ldb + n]``
+* ``d_layout``: ``"row"`` -> D[m,n] at ``D[m*ldd + n]``; ``"col"`` -> ``D[n*ldd + m]``
+
+What is computed, and the pages each step follows, is documented in
+``ge_oracle.cpp``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ge_oracle.cpp")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libge_oracle.so")
+
+EPILOGUES = {"none": 0, "bias": 1, "relu_bias": 2, "gelu_bias": 3, "relu_aux_bias": 4}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (plain -O2, no fast-math, no FP contraction)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math",
+           "-shared", "-fPIC", "-o", tmp, _SRC, "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+            lib.ora_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.ora_f16_to_f64.restype = ctypes.c_double
+            lib.ora_f64_to_f16.argtypes = [ctypes.c_double]
+            lib.ora_f64_to_f16.restype = ctypes.c_uint16
+            lib.ora_act_f64.argtypes = [i32, ctypes.c_double]
+            lib.ora_act_f64.restype = ctypes.c_double
+            lib.ora_f16_to_f64_array.argtypes = [vp, vp, i64]
+            lib.ora_f16_to_f64_array.restype = None
+            lib.ora_f64_to_f16_array.argtypes = [vp, vp, i64]
+            lib.ora_f64_to_f16_array.restype = None
+            lib.ora_linear_forward.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
+                                               vp, i32, vp, i32, i64, vp, i64, vp, i32]
+            lib.ora_linear_forward.restype = i32
+            lib.ora_drelu_bgrad.argtypes = [i64, i64, vp, i32, i64, vp, i64, vp, vp]
+            lib.ora_drelu_bgrad.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def default_ld_aux(contiguous_len: int) -> int:
+    """Mask row pitch in 32-bit words: one bit per element of a stored row of
+    D, rows padded to a multiple of 16 bytes (4 words)."""
+    return ((contiguous_len + 127) // 128) * 4
+
+
+def f16_decode(bits) -> np.ndarray:
+    lib = _load()
+    bits = _u16(bits)
+    out = np.empty(bits.shape, np.float64)
+    lib.ora_f16_to_f64_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def act_f64(epilogue: str, z: float) -> float:
+    """The epilogue's activation applied to one fp64 value (no rounding)."""
+    return float(_load().ora_act_f64(EPILOGUES[epilogue], float(z)))
+
+
+def f16_encode(x) -> np.ndarray:
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    lib.ora_f64_to_f16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def linear_forward(A, B, bias, epilogue: str, M: int, N: int, K: int, *,
+                   a_major: str = "k", b_major: str = "k", d_layout: str = "row",
+                   lda: int | None = None, ldb: int | None = None,
+                   ldd: int | None = None, ld_aux: int | None = None,
+                   threads: int | None = None) -> dict:
+    """D = act(A.B + bias) in fp64, rounded once to fp16.
+
+    Returns ``{"D": uint16 bits, "Z": fp64 pre-activation, "aux": uint32 mask
+    words or None}``; D and Z are flat arrays of ``rows*ldd`` elements in the
+    stored layout, aux is ``rows*ld_aux`` words.
+    """
+    lib = _load()
+    epi = EPILOGUES[epilogue]
+    if lda is None:
+        lda = K if a_major == "k" else M
+    if ldb is None:
+        ldb = K if b_major == "k" else N
+    rows, cols = (M, N) if d_layout == "row" else (N, M)
+    if ldd is None:
+        ldd = cols
+    if ld_aux is None:
+        ld_aux = default_ld_aux(cols)
+    A = _u16(A)
+    B = _u16(B)
+    bias = None if bias is None else _u16(bias)
+    D = np.zeros(rows * ldd, np.uint16)
+    Z = np.zeros(rows * ldd, np.float64)
+    aux = np.zeros(rows * ld_aux, np.uint32) if epilogue == "relu_aux_bias" else None
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.ora_linear_forward(M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
+                                _ptr(B), 0 if b_major == "k" else 1, ldb,
+                                _ptr(bias), epi, _ptr(D), 0 if d_layout == "row" else 1, ldd,
+                                _ptr(aux), ld_aux, _ptr(Z), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return {"D": D, "Z": Z, "aux": aux, "ldd": ldd, "ld_aux": ld_aux}
+
+
+def drelu_bgrad(dY, aux, M: int, N: int, *, d_layout: str = "row",
+                ldd: int | None = None, ld_aux: int | None = None):
+    """Backward epilogue: dZ = dY where the mask bit is set else +0 (fp16 bits),
+    bgrad[m] = sum over n of dZ[m,n] in fp64."""
+    lib = _load()
+    rows, cols = (M, N) if d_layout == "row" else (N, M)
+    if ldd is None:
+        ldd = cols
+    if ld_aux is None:
+        ld_aux = default_ld_aux(cols)
+    dY = _u16(dY)
+    aux = np.ascontiguousarray(aux, dtype=np.uint32)
+    dZ = np.zeros(rows * ldd, np.uint16)
+    bgrad = np.zeros(M, np.float64)
+    rc = lib.ora_drelu_bgrad(M, N, _ptr(dY), 0 if d_layout == "row" else 1, ldd,
+                             _ptr(aux), ld_aux, _ptr(dZ), _ptr(bgrad))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dZ, bgrad

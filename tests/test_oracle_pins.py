@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against something fixed independently of it:
+the hand-worked example (tests/golden), brute-force loops on tiny inputs,
+library conversions (numpy's float16, torch's GELU), closed forms and
+mathematical identities, and exact integer arithmetic.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+EPIS = ["none", "bias", "relu_bias", "gelu_bias", "relu_aux_bias"]
+
+
+def f16_bits(x):
+    return np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
+
+
+def plain_to_layout(Aplain, Bplain, a_major, b_major):
+    """Lay the plain matrices A[M][K], B[K][N] out as the oracle reads them."""
+    A = Aplain if a_major == "k" else Aplain.T
+    B = Bplain.T if b_major == "k" else Bplain
+    return np.ascontiguousarray(A).reshape(-1), np.ascontiguousarray(B).reshape(-1)
+
+
+# ---------------------------------------------------------------- fp16 codec
+
+def test_f16_decode_exhaustive(oracle):
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.f16_decode(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+def test_f16_encode_roundtrip_all_finite(oracle):
+    bits = np.arange(65536, dtype=np.uint16)
+    vals = bits.view(np.float16).astype(np.float64)
+    fin = np.isfinite(vals)
+    assert np.array_equal(oracle.f16_encode(vals[fin]), bits[fin])
+
+
+def test_f16_encode_ties_and_neighbours(oracle):
+    # Midpoints between consecutive positive finite halves round to the even
+    # neighbour; one double-ulp either side rounds to the nearer one.
+    lo = np.arange(0, 0x7BFF, dtype=np.uint16)
+    a = lo.view(np.float16).astype(np.float64)
+    b = (lo + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    mid = (a + b) / 2  # exact in fp64
+    even = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(oracle.f16_encode(mid), even)
+    assert np.array_equal(oracle.f16_encode(np.nextafter(mid, 0)), lo)
+    assert np.array_equal(oracle.f16_encode(np.nextafter(mid, np.inf)), (lo + 1).astype(np.uint16))
+    # negative side mirrors the positive side
+    assert np.array_equal(oracle.f16_encode(-mid), even | 0x8000)
+
+
+def test_f16_encode_boundaries(oracle):
+    enc = lambda x: int(oracle.f16_encode(np.array([x]))[0])
+    assert enc(65504.0) == 0x7BFF
+    assert enc(65519.999) == 0x7BFF
+    assert enc(65520.0) == 0x7C00          # tie to even -> overflow
+    assert enc(-70000.0) == 0xFC00
+    assert enc(math.inf) == 0x7C00
+    assert enc(2.0 ** -24) == 0x0001       # smallest subnormal
+    assert enc(2.0 ** -25) == 0x0000       # tie to even -> zero
+    assert enc(3 * 2.0 ** -25) == 0x0002   # 1.5 ulp -> 2 (even)
+    assert enc(2.0 ** -14) == 0x0400       # smallest normal
+    assert enc(2.0 ** -14 - 2.0 ** -26) == 0x0400  # rounds up into the normals
+    assert enc(-0.0) == 0x8000
+    assert enc(math.nan) & 0x7C00 == 0x7C00 and enc(math.nan) & 0x3FF
+
+
+def test_f16_encode_random_vs_numpy(oracle):
+    rng = np.random.default_rng(7)
+    mag = np.exp2(rng.uniform(-30, 15.99, 200000))
+    x = mag * rng.choice([-1.0, 1.0], mag.size)
+    ref = x.astype(np.float16).view(np.uint16)  # numpy rounds fp64 -> fp16 to nearest even
+    assert np.array_equal(oracle.f16_encode(x), ref)
+
+
+# ------------------------------------------------------------- hand-worked
+
+def test_hand_worked_example(oracle):
+    g = json.load(open(os.path.join(GOLDEN, "hand_2x3x4.json")))
+    M, N, K = g["M"], g["N"], g["K"]
+    A = f16_bits(g["A"]).reshape(-1)
+    B = f16_bits(g["B"]).reshape(-1)
+    bias = f16_bits(g["bias"])
+    # NONE: the plain product
+    r = oracle.linear_forward(A, B, None, "none", M, N, K, a_major="k", b_major="n", d_layout="row")
+    assert np.array_equal(r["Z"].reshape(M, N), np.array(g["AB"], float))
+    # BIAS: product plus bias broadcast over columns
+    r = oracle.linear_forward(A, B, bias, "bias", M, N, K, a_major="k", b_major="n")
+    assert np.array_equal(r["Z"].reshape(M, N), np.array(g["Z"], float))
+    assert np.array_equal(oracle.f16_decode(r["D"]).reshape(M, N), np.array(g["Z"], float))
+    # RELU_AUX_BIAS: ReLU values and the bit-packed mask
+    r = oracle.linear_forward(A, B, bias, "relu_aux_bias", M, N, K, a_major="k", b_major="n")
+    assert np.array_equal(oracle.f16_decode(r["D"]).reshape(M, N), np.array(g["relu"], float))
+    assert r["ld_aux"] == 4
+    assert r["aux"].tolist() == g["mask_words_row_major_ld4"]
+    # DRELU_BGRAD
+    dY = f16_bits(g["dY"]).reshape(-1)
+    dZ, bgrad = oracle.drelu_bgrad(dY, r["aux"], M, N, d_layout="row")
+    assert np.array_equal(oracle.f16_decode(dZ).reshape(M, N), np.array(g["dZ"], float))
+    assert bgrad.tolist() == g["bgrad"]
+
+
+def test_hand_worked_example_all_layouts(oracle):
+    """The same example read through every operand/output layout."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_2x3x4.json")))
+    M, N, K = g["M"], g["N"], g["K"]
+    Ap = np.array(g["A"], float)
+    Bp = np.array(g["B"], float)
+    for am in "km":
+        for bm in "kn":
+            for dl in ("row", "col"):
+                A, B = plain_to_layout(f16_bits(Ap).reshape(M, K), f16_bits(Bp).reshape(K, N), am, bm)
+                r = oracle.linear_forward(A, B, f16_bits(g["bias"]), "relu_aux_bias", M, N, K,
+                                          a_major=am, b_major=bm, d_layout=dl)
+                Z = r["Z"].reshape((M, N) if dl == "row" else (N, M))
+                if dl == "col":
+                    Z = Z.T
+                assert np.array_equal(Z, np.array(g["Z"], float)), (am, bm, dl)
+                rows, cols = (M, N) if dl == "row" else (N, M)
+                words = r["aux"].reshape(rows, r["ld_aux"])
+                bits = np.array([[(words[i, j // 32] >> (j % 32)) & 1 for j in range(cols)]
+                                 for i in range(rows)])
+                if dl == "col":
+                    bits = bits.T
+                assert bits.tolist() == g["mask_rows"], (am, bm, dl)
+
+
+# ------------------------------------------------------------ brute force
+
+def _brute(Aplain, Bplain, bias, epi):
+    """Pure-Python triple loop on the plain matrices (tiny sizes only)."""
+    M, K = Aplain.shape
+    N = Bplain.shape[1]
+    Z = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(Aplain[m, k]) * float(Bplain[k, n])
+            if epi != "none":
+                s += float(bias[m])
+            Z[m, n] = s
+    zt = torch.from_numpy(Z)
+    if epi in ("relu_bias", "relu_aux_bias"):
+        Y = torch.relu(zt).numpy()
+    elif epi == "gelu_bias":
+        Y = torch.nn.functional.gelu(zt, approximate="tanh").numpy()
+    else:
+        Y = Z
+    return Z, Y
+
+
+@pytest.mark.parametrize("am,bm,dl", [(a, b, d) for a in "km" for b in "kn" for d in ("row", "col")])
+def test_brute_force_tiny(oracle, am, bm, dl):
+    rng = np.random.default_rng(100 + "km".index(am) * 4 + "kn".index(bm) * 2 + (dl == "col"))
+    for M in range(1, 6):
+        for N in range(1, 6):
+            for K in (1, 2, 3, 5, 8):
+                epi = EPIS[(M + N + K) % len(EPIS)]
+                Ap = rng.standard_normal((M, K)).astype(np.float16)
+                Bp = rng.standard_normal((K, N)).astype(np.float16)
+                bias = rng.standard_normal(M).astype(np.float16)
+                A, B = plain_to_layout(Ap.view(np.uint16), Bp.view(np.uint16), am, bm)
+                r = oracle.linear_forward(A, B, bias.view(np.uint16), epi, M, N, K,
+                                          a_major=am, b_major=bm, d_layout=dl, threads=1)
+                Z, Y = _brute(Ap.astype(np.float64), Bp.astype(np.float64),
+                              bias.astype(np.float64), epi)
+                shape = (M, N) if dl == "row" else (N, M)
+                Zo = r["Z"].reshape(shape)
+                Do = r["D"].reshape(shape)
+                if dl == "col":
+                    Zo, Do = Zo.T, Do.T
+                assert np.array_equal(Zo, Z), (M, N, K, epi)
+                assert np.array_equal(Do, Y.astype(np.float16).view(np.uint16)), (M, N, K, epi)
+
+
+def test_padded_leading_dimensions(oracle):
+    """Leading dimensions larger than the logical extent are honoured."""
+    rng = np.random.default_rng(3)
+    M, N, K = 5, 7, 9
+    Ap = rng.standard_normal((M, K)).astype(np.float16)
+    Bp = rng.standard_normal((K, N)).astype(np.float16)
+    lda, ldb, ldd = K + 3, K + 5, M + 8
+    A = np.full((M, lda), np.float16(np.nan))
+    A[:, :K] = Ap
+    B = np.full((N, ldb), np.float16(np.nan))  # K-major B: row n holds B[:, n]
+    B[:, :K] = Bp.T
+    r = oracle.linear_forward(A.view(np.uint16).reshape(-1), B.view(np.uint16).reshape(-1), None,
+                              "none", M, N, K, a_major="k", b_major="k", d_layout="col",
+                              lda=lda, ldb=ldb, ldd=ldd)
+    Z = r["Z"].reshape(N, ldd)[:, :M].T
+    assert np.array_equal(Z, _brute(Ap.astype(float), Bp.astype(float), None, "none")[0])
+
+
+# ------------------------------------------------------------------ GELU
+
+def test_gelu_closed_forms(oracle):
+    act = lambda z: oracle.act_f64("gelu_bias", z)
+    assert act(0.0) == 0.0
+    # published value of the tanh approximation at 1
+    assert abs(act(1.0) - 0.8411919906082768) < 1e-15
+    # large |z|: identity above, zero below
+    assert act(12.0) == 12.0
+    assert abs(act(-12.0)) < 1e-40
+    for z in np.linspace(-6, 6, 241):
+        # GELU(z) - GELU(-z) = z holds for the tanh form exactly in real arithmetic
+        assert abs(act(z) - act(-z) - z) <= 4e-16 * max(1.0, abs(z))
+
+
+def test_gelu_sigmoid_identity(oracle):
+    """0.5(1 + tanh(u)) = 1/(1 + exp(-2u)): an independent way to evaluate it."""
+    c = math.sqrt(2.0 / math.pi)
+    for z in np.linspace(-8, 8, 1601):
+        u = c * (z + 0.044715 * z ** 3)
+        ref = z / (1.0 + math.exp(-2.0 * u))
+        assert abs(oracle.act_f64("gelu_bias", z) - ref) <= 1e-14 * max(1.0, abs(z))
+
+
+def test_gelu_close_to_exact_erf_gelu(oracle):
+    """The tanh form approximates z*Phi(z) to within about 5e-4 everywhere."""
+    worst = 0.0
+    for z in np.linspace(-10, 10, 4001):
+        exact = 0.5 * z * (1.0 + math.erf(z / math.sqrt(2.0)))
+        worst = max(worst, abs(oracle.act_f64("gelu_bias", z) - exact))
+    assert worst < 1e-3
+    assert worst > 1e-5  # it is the approximation, not the erf form
+
+
+def test_gelu_matches_torch_tanh_gelu(oracle):
+    z = torch.linspace(-9, 9, 7001, dtype=torch.float64)
+    ref = torch.nn.functional.gelu(z, approximate="tanh").numpy()
+    got = np.array([oracle.act_f64("gelu_bias", float(v)) for v in z])
+    # 1 + tanh(u) cancels for very negative z in both evaluations, so values
+    # below ~1e-15 in magnitude are rounding noise (far below fp16's 6e-8).
+    assert np.allclose(got, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_relu_and_none(oracle):
+    for z in (-3.5, -0.0, 0.0, 1e-30, 2.25):
+        assert oracle.act_f64("relu_bias", z) == max(z, 0.0)
+        assert oracle.act_f64("relu_aux_bias", z) == max(z, 0.0)
+        assert oracle.act_f64("bias", z) == z
+        assert oracle.act_f64("none", z) == z
+
+
+# ------------------------------------------------------ mask / relu identity
+
+def test_relu_equals_z_times_mask(oracle):
+    rng = np.random.default_rng(11)
+    M, N, K = 37, 70, 24
+    A = rng.standard_normal(M * K).astype(np.float16)
+    B = rng.standard_normal(K * N).astype(np.float16)
+    bias = rng.standard_normal(M).astype(np.float16)
+    for dl in ("row", "col"):
+        rb = oracle.linear_forward(A, B, bias, "bias", M, N, K, d_layout=dl)
+        rr = oracle.linear_forward(A, B, bias, "relu_aux_bias", M, N, K, d_layout=dl)
+        rows, cols = (M, N) if dl == "row" else (N, M)
+        ld_aux = rr["ld_aux"]
+        assert ld_aux == 4 * ((cols + 127) // 128)
+        words = rr["aux"].reshape(rows, ld_aux)
+        bits = np.zeros((rows, ld_aux * 32), np.int64)
+        for j in range(ld_aux * 32):
+            bits[:, j] = (words[:, j // 32] >> np.uint32(j % 32)) & 1
+        assert not bits[:, cols:].any()  # padding bits are zero
+        bits = bits[:, :cols].reshape(-1)
+        z = rb["Z"]
+        assert np.array_equal(bits, (z > 0).astype(np.int64))
+        y_bias = oracle.f16_decode(rb["D"])
+        y_relu = oracle.f16_decode(rr["D"])
+        assert np.array_equal(y_relu, y_bias * bits)
+
+
+# ------------------------------------------------------- exact integer case
+
+@pytest.mark.parametrize("M,N,K", [(64, 48, 128), (19, 17, 128)])
+def test_exact_integer_case(oracle, M, N, K):
+    """Integer entries keep every partial sum exact in fp16 inputs, fp32 and
+    fp16 outputs; the oracle must equal integer matrix arithmetic."""
+    rng = np.random.default_rng(M * 1000 + N)
+    Ai = rng.integers(-2, 3, (M, K))
+    Bi = rng.integers(-2, 3, (K, N))
+    bi = rng.integers(-8, 9, M)
+    exact = Ai @ Bi + bi[:, None]
+    assert np.abs(exact).max() < 2048
+    for epi in ("bias", "relu_bias", "relu_aux_bias"):
+        r = oracle.linear_forward(f16_bits(Ai).reshape(-1), f16_bits(Bi).reshape(-1), f16_bits(bi),
+                                  epi, M, N, K, a_major="k", b_major="n")
+        assert np.array_equal(r["Z"].reshape(M, N), exact.astype(float))
+        y = exact if epi == "bias" else np.maximum(exact, 0)
+        assert np.array_equal(r["D"].reshape(M, N), f16_bits(y))
+
+
+def test_none_matches_library_matmul(oracle):
+    rng = np.random.default_rng(5)
+    M, N, K = 33, 29, 64
+    Ap = rng.standard_normal((M, K)).astype(np.float16)
+    Bp = rng.standard_normal((K, N)).astype(np.float16)
+    A, B = plain_to_layout(Ap.view(np.uint16), Bp.view(np.uint16), "m", "k")
+    r = oracle.linear_forward(A, B, None, "none", M, N, K, a_major="m", b_major="k")
+    ref = Ap.astype(np.float64) @ Bp.astype(np.float64)
+    assert np.allclose(r["Z"].reshape(M, N), ref, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- DRELU
+
+def test_drelu_bgrad_against_exact_sum(oracle):
+    rng = np.random.default_rng(21)
+    M, N, K = 45, 300, 16
+    A = rng.standard_normal(M * K).astype(np.float16)
+    B = rng.standard_normal(K * N).astype(np.float16)
+    bias = rng.standard_normal(M).astype(np.float16)
+    for dl in ("row", "col"):
+        rows, cols = (M, N) if dl == "row" else (N, M)
+        fw = oracle.linear_forward(A, B, bias, "relu_aux_bias", M, N, K, d_layout=dl)
+        dY = (rng.standard_normal(rows * cols) * 3).astype(np.float16)
+        dZ, bgrad = oracle.drelu_bgrad(dY, fw["aux"], M, N, d_layout=dl)
+        mask = (fw["Z"] > 0)
+        dYf = dY.astype(np.float64)
+        ref_dz = np.where(mask, dYf, 0.0)
+        assert np.array_equal(oracle.f16_decode(dZ), ref_dz)
+        assert not (dZ[~mask] != 0).any()  # masked-out gradients are +0
+        grid = ref_dz.reshape(rows, cols)
+        per_m = grid if dl == "row" else grid.T
+        for m in range(M):
+            # a sum of fp16 values with this few terms is exact in fp64;
+            # math.fsum (exact, reverse order) must agree to the last bit.
+            assert bgrad[m] == math.fsum(per_m[m][::-1])

@@ -1,0 +1,396 @@
+"""Benchmark of the fused linear-layer hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. forward   D = relu(X W^T + b) with the bit-packed mask (RELU_AUX_BIAS),
+               W[11008, 4096], X[8192, 4096]          (tcgen05 GEMM, fused epilogue)
+  2. backward  dZ = dY * mask, bgrad = sum_tokens dZ  (DRELU_BGRAD stream)
+  3. weight gradient dW = dZ^T X                      (tcgen05 GEMM, NONE epilogue)
+  4. decode    y = gelu(W2 x + b2), W2[4096, 4096], one token (GEMV, GELU_BIAS)
+The LLaMA-7B-like MLP and the hidden-4096 decode projection stand in for the
+pages' workloads (nvmath-python RELU_AUX_BIAS / DRELU_BGRAD, ops-nn decode).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (the path has no
+exchange step); the time is the max over ranks, the value sums all ranks.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+bias+act TFLOP/s & % FP16 tensor peak; M=1 GEMV/bgrad HBM GB/s"
+T_TOK, D_IN, D_OUT, D_DEC = 8192, 4096, 11008, 4096
+WORKLOAD = ("LLaMA-7B-like MLP training step (fwd RELU_AUX_BIAS 11008x8192x4096 + DRELU_BGRAD "
+            "dY[8192,11008] + dW 11008x4096x8192) + decode GEMV GELU_BIAS 4096x1x4096")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "tflops": float(p["bf16_tflops"]),
+                "tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU side
+
+def oracle_sample_rate(rows: int = 256, threads: int | None = None):
+    """The oracle (fp64 CPU) on a bounded sample of the forward GEMM: `rows`
+    tokens of X against the whole W. Returns (TFLOP/s, seconds, threads)."""
+    import numpy as np
+    import torch
+    from gemm_epilogues_gb300.inputs import f16_tensor
+    from oracle import oracle
+    oracle.build()
+    threads = threads or os.cpu_count() or 1
+    W = f16_tensor((D_OUT, D_IN), 3001, "normal", 1 / 64)
+    X = f16_tensor((rows, D_IN), 3002)
+    b = f16_tensor((D_OUT,), 3003, "normal", math.sqrt(0.02))
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    t0 = time.perf_counter()
+    oracle.linear_forward(bits(W), bits(X), bits(b), "relu_aux_bias", D_OUT, rows, D_IN,
+                          a_major="k", b_major="k", d_layout="col", threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * D_OUT * rows * D_IN
+    return flops / dt / 1e12, dt, threads
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle as it stands, timed on the host cores,
+    same metric and unit, each step a bounded sample of the workload."""
+    if rank != 0:
+        return
+    rows = 64
+    for _ in range(args.warmup):
+        oracle_sample_rate(rows)
+    times = []
+    thr = None
+    for _ in range(args.steps):
+        _, dt, thr = oracle_sample_rate(rows)
+        times.append(dt)
+    flops = 2.0 * D_OUT * rows * D_IN
+    value = flops * len(times) / sum(times) / 1e12
+    sample = f"forward GEMM on {rows} of {T_TOK} tokens (all 11008 outputs, K=4096) per step"
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU side
+
+def run_ours(args, world, rank, local):
+    import torch
+    import gemm_epilogues_gb300 as ge
+    from gemm_epilogues_gb300.inputs import f16_tensor
+
+    ge.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    # weights and inputs, resident in HBM
+    W = f16_tensor((D_OUT, D_IN), 3001, "normal", 1 / 64, dev)
+    X = f16_tensor((T_TOK, D_IN), 3002, "normal", 1.0, dev)
+    b = f16_tensor((D_OUT,), 3003, "normal", math.sqrt(0.02), dev)
+    dY = f16_tensor((T_TOK, D_OUT), 3004, "normal", 1.0, dev)
+    W2 = f16_tensor((D_DEC, D_DEC), 2001, "normal", 1 / 64, dev)
+    b2 = f16_tensor((D_DEC,), 2003, "normal", math.sqrt(0.02), dev)
+    x1 = f16_tensor((1, D_DEC), 2002, "normal", 1.0, dev)
+
+    K_, MN = ge.GE_K_MAJOR, ge.GE_MN_MAJOR
+    fwd = ge.Plan(D_OUT, T_TOK, D_IN, ge.GE_EPI_RELU_AUX_BIAS, ge.make_layout(K_, K_, ge.GE_D_COL))
+    bwd = ge.Plan(D_OUT, T_TOK, 0, ge.GE_EPI_DRELU_BGRAD, ge.make_layout(d=ge.GE_D_COL))
+    dwp = ge.Plan(D_OUT, D_IN, T_TOK, ge.GE_EPI_NONE, ge.make_layout(MN, MN, ge.GE_D_ROW))
+    dec = ge.Plan(D_DEC, 1, D_DEC, ge.GE_EPI_GELU_BIAS, ge.make_layout(K_, K_, ge.GE_D_COL))
+    assert dec.path == ge.GE_PATH_GEMV
+
+    Y = torch.empty((T_TOK, D_OUT), dtype=torch.float16, device=dev)
+    aux = torch.empty(fwd.aux_bytes // 4, dtype=torch.int32, device=dev)
+    dZ = torch.empty_like(dY)
+    bgrad = torch.empty(D_OUT, dtype=torch.float32, device=dev)
+    dW = torch.empty((D_OUT, D_IN), dtype=torch.float16, device=dev)
+    y1 = torch.empty((1, D_DEC), dtype=torch.float16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(dev), "L2_cache_size") else 128 << 20
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    names = ["fwd_gemm_relu_aux_bias", "drelu_bgrad", "dw_gemm", "decode_gemv_gelu_bias"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fwd.execute(W, X, b, Y, aux, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        bwd.execute(dY, None, bgrad, dZ, aux, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        dwp.execute(dZ, X, None, dW, None, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        dec.execute(W2, x1, b2, y1, None, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    for p in (fwd, bwd, dwp, dec):
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()  # L2 flushed between timed steps, outside the events
+        step(evs[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    for p in (fwd, bwd, dwp, dec):
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+
+    per = {n: [] for n in names}
+    tot = []
+    for e in evs:
+        for i, n in enumerate(names):
+            per[n].append(e[i].elapsed_time(e[i + 1]))
+        tot.append(e[0].elapsed_time(e[4]))
+    ms_step_local = sum(tot) / len(tot)
+    ms_step = reduce_max(ms_step_local, world)
+
+    flops_gemm = 2.0 * D_OUT * T_TOK * D_IN
+    flops_dec = 2.0 * D_DEC * D_DEC
+    flops_step = 2 * flops_gemm + flops_dec
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    aux_bytes = fwd.aux_bytes
+    bytes_fwd = 2 * (D_OUT * D_IN + T_TOK * D_IN + T_TOK * D_OUT) + 2 * D_OUT + aux_bytes
+    bytes_bwd = 2 * T_TOK * D_OUT * 2 + aux_bytes + 4 * D_OUT
+    bytes_dw = 2 * (T_TOK * D_OUT + T_TOK * D_IN + D_OUT * D_IN)
+    bytes_dec = 2 * (D_DEC * D_DEC + D_DEC + D_DEC + D_DEC)
+    mean = {n: sum(v) / len(v) for n, v in per.items()}
+    kern = {
+        "fwd_gemm_relu_aux_bias": {"ms": mean[names[0]], "tflops": flops_gemm / mean[names[0]] / 1e9},
+        "drelu_bgrad": {"ms": mean[names[1]], "gbs": bytes_bwd / mean[names[1]] / 1e6},
+        "dw_gemm": {"ms": mean[names[2]], "tflops": flops_gemm / mean[names[2]] / 1e9},
+        "decode_gemv_gelu_bias": {"ms": mean[names[3]], "gbs": bytes_dec / mean[names[3]] / 1e6},
+    }
+    for k in ("fwd_gemm_relu_aux_bias", "dw_gemm"):
+        kern[k]["frac_of_peak"] = kern[k]["tflops"] / peaks["tflops"]
+    for k in ("drelu_bgrad", "decode_gemv_gelu_bias"):
+        kern[k]["frac_of_peak"] = kern[k]["gbs"] / peaks["hbm_gbs"]
+    kern["fwd_gemm_relu_aux_bias"]["algorithmic_bytes"] = bytes_fwd
+    kern["drelu_bgrad"]["algorithmic_bytes"] = bytes_bwd
+    kern["dw_gemm"]["algorithmic_bytes"] = bytes_dw
+    kern["decode_gemv_gelu_bias"]["algorithmic_bytes"] = bytes_dec
+    dominant = max(("fwd_gemm_relu_aux_bias", "dw_gemm"), key=lambda k: kern[k]["ms"])
+    achieved = kern[dominant]["tflops"]
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peaks["tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["tflops"], "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 burst (fp16 tensor rate = bf16)"}
+
+    # ---- end to end through the public API: host buffers, copies timed
+    Xh = X.cpu().pin_memory()
+    dYh = dY.cpu().pin_memory()
+    x1h = x1.cpu().pin_memory()
+    dWh = torch.empty(dW.shape, dtype=dW.dtype).pin_memory()
+    bgh = torch.empty(bgrad.shape, dtype=bgrad.dtype).pin_memory()
+    y1h = torch.empty(y1.shape, dtype=y1.dtype).pin_memory()
+    Xd, dYd, x1d = torch.empty_like(X), torch.empty_like(dY), torch.empty_like(x1)
+
+    def e2e_step():
+        Xd.copy_(Xh, non_blocking=True)
+        dYd.copy_(dYh, non_blocking=True)
+        x1d.copy_(x1h, non_blocking=True)
+        fwd.execute(W, Xd, b, Y, aux, stream)
+        bwd.execute(dYd, None, bgrad, dZ, aux, stream)
+        dwp.execute(dZ, Xd, None, dW, None, stream)
+        dec.execute(W2, x1d, b2, y1, None, stream)
+        dWh.copy_(dW, non_blocking=True)
+        bgh.copy_(bgrad, non_blocking=True)
+        y1h.copy_(y1, non_blocking=True)
+
+    h2d = Xh.numel() * 2 + dYh.numel() * 2 + x1h.numel() * 2
+    d2h = dWh.numel() * 2 + bgh.numel() * 4 + y1h.numel() * 2
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(ev0.elapsed_time(ev1) / e_steps, world)
+    e2e_value = flops_step * world / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, dt, thr = oracle_sample_rate(256)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"forward GEMM on 256 of {T_TOK} tokens (all 11008 outputs, K=4096), "
+                         f"{dt:.1f} s wall"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "tokens": T_TOK, "d_in": D_IN, "d_out": D_OUT,
+                           "decode_hidden": D_DEC, "l2": "flushed between timed steps (memset 2x L2)",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "kernels": kern, "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": 4 * args.steps,
+                "clocks": clk}
+        print(json.dumps(line), flush=True)
+    for p in (fwd, bwd, dwp, dec):
+        p.free()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

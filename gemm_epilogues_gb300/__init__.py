@@ -1,0 +1,255 @@
+"""Python binding of the GB300 fused linear-layer engine.
+
+Argument marshalling only: every call forwards to the C ABI of
+``_build/libgemm_epilogues.so`` (declared in ``include/ge.h``), with the same
+names. Buffers are passed as raw device pointers; anything exposing
+``data_ptr()`` (a torch tensor) or a plain integer is accepted. Streams are
+``cudaStream_t`` handles: an integer, an object with ``cuda_stream`` (a torch
+stream) or ``None`` for the legacy default stream.
+
+There is no fallback: if the library has not been built, or cannot be loaded,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgemm_epilogues.so")
+
+# ge_status_t
+GE_OK = 0
+GE_ERR_INVALID_ARG = 1
+GE_ERR_UNSUPPORTED = 2
+GE_ERR_ALIGNMENT = 3
+GE_ERR_DEVICE_MISMATCH = 4
+GE_ERR_CUDA = 5
+GE_ERR_TIMEOUT = 6
+GE_ERR_OOM = 7
+# ge_epilogue_t
+GE_EPI_NONE = 0
+GE_EPI_BIAS = 1
+GE_EPI_RELU_BIAS = 2
+GE_EPI_GELU_BIAS = 3
+GE_EPI_RELU_AUX_BIAS = 4
+GE_EPI_DRELU_BGRAD = 5
+# ge_dtype_t
+GE_F16 = 0
+GE_F32 = 1
+# ge_major_t
+GE_K_MAJOR = 0
+GE_MN_MAJOR = 1
+# ge_dlayout_t
+GE_D_ROW = 0
+GE_D_COL = 1
+# ge_path_t
+GE_PATH_TC_GEMM = 0
+GE_PATH_GEMV = 1
+GE_PATH_DRELU = 2
+
+EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EPI_RELU_BIAS,
+                    "gelu_bias": GE_EPI_GELU_BIAS, "relu_aux_bias": GE_EPI_RELU_AUX_BIAS,
+                    "drelu_bgrad": GE_EPI_DRELU_BGRAD}
+
+# Every function the header declares (checked against include/ge.h by a test).
+ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",
+                 "ge_aux_bytes", "ge_aux_ld", "ge_plan_path", "ge_plan_tile_n",
+                 "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
+                 "ge_version")
+
+
+class ge_layout_t(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_int), ("b", ctypes.c_int), ("d", ctypes.c_int),
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64),
+                ("ld_aux", ctypes.c_int64)]
+
+
+class GeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {ge_status_string(status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library():
+    """Load the CUDA library (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build() "
+                               "(nvcc for sm_103a) first")
+        lib = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        lib.ge_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32, i32, i32, i32, i32,
+                                       ctypes.POINTER(ge_layout_t)]
+        lib.ge_plan_create.restype = i32
+        lib.ge_execute.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        lib.ge_execute.restype = i32
+        lib.ge_execute_unfused.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        lib.ge_execute_unfused.restype = i32
+        lib.ge_plan_free.argtypes = [vp]
+        lib.ge_plan_free.restype = i32
+        lib.ge_aux_bytes.argtypes = [vp]
+        lib.ge_aux_bytes.restype = sz
+        lib.ge_aux_ld.argtypes = [vp]
+        lib.ge_aux_ld.restype = i64
+        lib.ge_plan_path.argtypes = [vp]
+        lib.ge_plan_path.restype = i32
+        lib.ge_plan_tile_n.argtypes = [vp]
+        lib.ge_plan_tile_n.restype = i32
+        lib.ge_get_last_device_error.argtypes = [vp]
+        lib.ge_get_last_device_error.restype = i32
+        lib.ge_status_string.argtypes = [i32]
+        lib.ge_status_string.restype = ctypes.c_char_p
+        lib.ge_debug_wait_timeout.argtypes = [vp, i64, vp]
+        lib.ge_debug_wait_timeout.restype = i32
+        lib.ge_version.argtypes = []
+        lib.ge_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != GE_OK:
+        raise GeError(status, where)
+
+
+def ge_status_string(status: int) -> str:
+    return load_library().ge_status_string(int(status)).decode()
+
+
+def ge_version() -> str:
+    return load_library().ge_version().decode()
+
+
+def ge_plan_create(M: int, N: int, K: int, a: int = GE_F16, b: int = GE_F16, d: int = GE_F16,
+                   compute: int = GE_F32, epi: int = GE_EPI_BIAS, layout: ge_layout_t | None = None,
+                   *, raw: bool = False):
+    """Returns the plan handle (an int); with raw=True returns (status, handle)."""
+    lib = load_library()
+    out = ctypes.c_void_p()
+    st = lib.ge_plan_create(ctypes.byref(out), int(M), int(N), int(K), int(a), int(b), int(d),
+                            int(compute), int(epi), ctypes.byref(layout) if layout is not None else None)
+    if raw:
+        return st, out.value
+    _check(st, "ge_plan_create")
+    return out.value
+
+
+def ge_execute(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool = False):
+    st = load_library().ge_execute(plan, _ptr(A), _ptr(B), _ptr(bias), _ptr(D), _ptr(aux),
+                                   _stream(stream))
+    if raw:
+        return st
+    _check(st, "ge_execute")
+
+
+def ge_execute_unfused(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool = False):
+    st = load_library().ge_execute_unfused(plan, _ptr(A), _ptr(B), _ptr(bias), _ptr(D), _ptr(aux),
+                                           _stream(stream))
+    if raw:
+        return st
+    _check(st, "ge_execute_unfused")
+
+
+def ge_plan_free(plan):
+    _check(load_library().ge_plan_free(plan), "ge_plan_free")
+
+
+def ge_aux_bytes(plan) -> int:
+    return int(load_library().ge_aux_bytes(plan))
+
+
+def ge_aux_ld(plan) -> int:
+    return int(load_library().ge_aux_ld(plan))
+
+
+def ge_plan_path(plan) -> int:
+    return int(load_library().ge_plan_path(plan))
+
+
+def ge_plan_tile_n(plan) -> int:
+    return int(load_library().ge_plan_tile_n(plan))
+
+
+def ge_get_last_device_error(plan) -> int:
+    return int(load_library().ge_get_last_device_error(plan))
+
+
+def ge_debug_wait_timeout(plan, budget_cycles: int, stream=None) -> int:
+    return int(load_library().ge_debug_wait_timeout(plan, int(budget_cycles), _stream(stream)))
+
+
+def make_layout(a: int = GE_K_MAJOR, b: int = GE_MN_MAJOR, d: int = GE_D_ROW, lda: int = 0,
+                ldb: int = 0, ldd: int = 0, ld_aux: int = 0) -> ge_layout_t:
+    return ge_layout_t(a, b, d, lda, ldb, ldd, ld_aux)
+
+
+class Plan:
+    """Context-managed plan: ``with Plan(M, N, K, epi, layout) as p: p.execute(...)``."""
+
+    def __init__(self, M, N, K, epi=GE_EPI_BIAS, layout: ge_layout_t | None = None):
+        self.M, self.N, self.K, self.epi = M, N, K, epi
+        self.handle = ge_plan_create(M, N, K, epi=epi, layout=layout)
+
+    def execute(self, A, B, bias, D, aux=None, stream=None):
+        ge_execute(self.handle, A, B, bias, D, aux, stream)
+
+    def execute_unfused(self, A, B, bias, D, aux=None, stream=None):
+        ge_execute_unfused(self.handle, A, B, bias, D, aux, stream)
+
+    @property
+    def aux_bytes(self) -> int:
+        return ge_aux_bytes(self.handle)
+
+    @property
+    def aux_ld(self) -> int:
+        return ge_aux_ld(self.handle)
+
+    @property
+    def path(self) -> int:
+        return ge_plan_path(self.handle)
+
+    @property
+    def tile_n(self) -> int:
+        return ge_plan_tile_n(self.handle)
+
+    def free(self):
+        if self.handle:
+            ge_plan_free(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass

@@ -1,0 +1,466 @@
+// ge_api.cu -- the C ABI (include/ge.h): argument validation, kernel-path
+// choice, TMA tensor-map encoding and launches.
+//
+// The life cycle follows nvmath-python cuBLASLt bias-fusion guide, "Core API
+// and parameter configuration" and "Advanced techniques" (plan once -- the
+// expensive, blocking step that picks the kernel -- then execute many times,
+// then free), and Fusing bias addition with matrix multiplication using
+// nvmath-python (operands on one device with compatible dtypes, else an
+// error; the plan must be freed).
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "ge_internal.h"
+#include "../../include/ge.h"
+
+namespace {
+
+using namespace ge;
+
+constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s at GB300 clocks
+
+struct Plan {
+  int64_t M = 0, N = 0, K = 0;
+  ge_epilogue_t epi = GE_EPI_NONE;
+  ge_layout_t L{};
+  ge_path_t path = GE_PATH_TC_GEMM;
+  int device = 0;
+  int num_sms = 0;
+  // tensor-core path: kernel-level problem after folding a column-major D
+  bool swap = false;
+  int block_n = 256;
+  int grid = 0;
+  int group_m = 16;
+  // stored D: R rows x C contiguous
+  int64_t R = 0, C = 0;
+  int64_t aux_words = 0;  // ld_aux (words) when a mask is in use
+  // device workspace: [error word | pad to 256 | counters | partials]
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  unsigned int* err = nullptr;
+  unsigned int* counters = nullptr;
+  float* partials = nullptr;
+  int splits = 1;
+  // tensor-map cache (rebuilt when a pointer changes)
+  const void* mapA = nullptr;
+  const void* mapB = nullptr;
+  const void* mapD = nullptr;
+  CUtensorMap tmA{}, tmB{}, tmD{};
+  // last pointers whose device was verified
+  const void* checked[6] = {};
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D fp16 tensor map: inner extent d0 (contiguous), outer d1, row pitch ld
+// elements, box b0 x b1, swizzle mode.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t ld, uint32_t b0,
+              uint32_t b1, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {d0, d1};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {b0, b1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool epi_has_bias(ge_epilogue_t e) {
+  return e == GE_EPI_BIAS || e == GE_EPI_RELU_BIAS || e == GE_EPI_GELU_BIAS ||
+         e == GE_EPI_RELU_AUX_BIAS;
+}
+
+// Verify that `p` is device memory of the plan's device (cached per slot).
+ge_status_t check_device(Plan* pl, int slot, const void* p) {
+  if (!p || pl->checked[slot] == p) return GE_OK;
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_DEVICE_MISMATCH;
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+    return GE_ERR_DEVICE_MISMATCH;
+  if (at.device != pl->device) return GE_ERR_DEVICE_MISMATCH;
+  pl->checked[slot] = p;
+  return GE_OK;
+}
+
+double wave_efficiency(long long tiles, int sms) {
+  const long long waves = (tiles + sms - 1) / sms;
+  return static_cast<double>(tiles) / static_cast<double>(waves * sms);
+}
+
+// Tensor maps for the tensor-core path (kernel-level operands A', B', D').
+ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D) {
+  if (pl->mapA == A && pl->mapB == B && pl->mapD == D) return GE_OK;
+  const ge_layout_t& L = pl->L;
+  const void* Ak = pl->swap ? B : A;
+  const void* Bk = pl->swap ? A : B;
+  const int a_mn = pl->swap ? (L.b == GE_MN_MAJOR) : (L.a == GE_MN_MAJOR);
+  const int b_mn = pl->swap ? (L.a == GE_MN_MAJOR) : (L.b == GE_MN_MAJOR);
+  const int64_t lda = pl->swap ? L.ldb : L.lda;
+  const int64_t ldb = pl->swap ? L.lda : L.ldb;
+  const uint64_t Mk = pl->swap ? pl->N : pl->M;
+  const uint64_t Nk = pl->swap ? pl->M : pl->N;
+  const uint64_t K = pl->K;
+  bool ok = true;
+  if (!a_mn)
+    ok &= make_map(&pl->tmA, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok &= make_map(&pl->tmA, Ak, Mk, K, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!b_mn)
+    ok &= make_map(&pl->tmB, Bk, K, Nk, ldb, 64, pl->block_n, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok &= make_map(&pl->tmB, Bk, Nk, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok &= make_map(&pl->tmD, D, Nk, Mk, L.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!ok) {
+    pl->mapA = pl->mapB = pl->mapD = nullptr;
+    return GE_ERR_CUDA;
+  }
+  pl->mapA = A;
+  pl->mapB = B;
+  pl->mapD = D;
+  return GE_OK;
+}
+
+ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* bias, void* D,
+                           void* aux, int epi_code, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (pl->path == GE_PATH_GEMV) {
+    GemvArgs g{};
+    g.M = static_cast<int>(pl->M);
+    g.N = static_cast<int>(pl->N);
+    g.K = static_cast<int>(pl->K);
+    g.A = static_cast<const __half*>(A);
+    g.lda = pl->L.lda;
+    g.B = static_cast<const __half*>(B);
+    g.ldb = pl->L.ldb;
+    g.D = static_cast<__half*>(D);
+    g.ldd_m = pl->L.d == GE_D_ROW ? pl->L.ldd : 1;
+    g.ldd_n = pl->L.d == GE_D_ROW ? 1 : pl->L.ldd;
+    g.bias = static_cast<const __half*>(bias);
+    g.epi = epi_code;
+    e = launch_gemv(g, pl->num_sms, st);
+  } else {
+    ge_status_t s = build_maps(pl, A, B, D);
+    if (s != GE_OK) return s;
+    GemmArgs g{};
+    g.Mk = static_cast<int>(pl->swap ? pl->N : pl->M);
+    g.Nk = static_cast<int>(pl->swap ? pl->M : pl->N);
+    g.K = static_cast<int>(pl->K);
+    g.a_mn = pl->swap ? (pl->L.b == GE_MN_MAJOR) : (pl->L.a == GE_MN_MAJOR);
+    g.b_mn = pl->swap ? (pl->L.a == GE_MN_MAJOR) : (pl->L.b == GE_MN_MAJOR);
+    g.epi = epi_code;
+    g.bias_per_col = pl->swap ? 1 : 0;
+    g.bias = static_cast<const __half*>(bias);
+    g.aux = static_cast<uint32_t*>(aux);
+    g.ld_aux = pl->aux_words;
+    g.err = pl->err;
+    g.group_m = pl->group_m;
+    g.budget = kWaitBudgetCycles;
+    e = launch_tc_gemm(pl->block_n, pl->tmA, pl->tmB, pl->tmD, g, pl->grid, st);
+  }
+  return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ge_version(void) { return "0.1.0"; }
+
+const char* ge_status_string(ge_status_t s) {
+  switch (s) {
+    case GE_OK: return "GE_OK";
+    case GE_ERR_INVALID_ARG: return "GE_ERR_INVALID_ARG: invalid argument";
+    case GE_ERR_UNSUPPORTED: return "GE_ERR_UNSUPPORTED: dtype/epilogue/layout not supported";
+    case GE_ERR_ALIGNMENT: return "GE_ERR_ALIGNMENT: pointer or leading dimension not 16-byte aligned";
+    case GE_ERR_DEVICE_MISMATCH: return "GE_ERR_DEVICE_MISMATCH: buffer not on the plan's device";
+    case GE_ERR_CUDA: return "GE_ERR_CUDA: CUDA call or launch failed";
+    case GE_ERR_TIMEOUT: return "GE_ERR_TIMEOUT: a bounded device wait expired";
+    case GE_ERR_OOM: return "GE_ERR_OOM: workspace allocation failed";
+  }
+  return "unknown ge_status_t";
+}
+
+ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_dtype_t a,
+                           ge_dtype_t b, ge_dtype_t d, ge_dtype_t compute, ge_epilogue_t epi,
+                           const ge_layout_t* layout) {
+  if (!out) return GE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_DRELU_BGRAD)
+    return GE_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 0) return GE_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (M > lim || N > lim || K > lim) return GE_ERR_INVALID_ARG;
+  if (a != GE_F16 || b != GE_F16 || d != GE_F16 || compute != GE_F32) return GE_ERR_UNSUPPORTED;
+  if (epi == GE_EPI_DRELU_BGRAD) {
+    if (K != 0) return GE_ERR_UNSUPPORTED;
+  } else if (K == 0) {
+    return GE_ERR_INVALID_ARG;
+  }
+  ge_layout_t L{GE_K_MAJOR, GE_MN_MAJOR, GE_D_ROW, 0, 0, 0, 0};
+  if (layout) L = *layout;
+  if ((L.a != GE_K_MAJOR && L.a != GE_MN_MAJOR) || (L.b != GE_K_MAJOR && L.b != GE_MN_MAJOR) ||
+      (L.d != GE_D_ROW && L.d != GE_D_COL))
+    return GE_ERR_INVALID_ARG;
+  if (L.lda < 0 || L.ldb < 0 || L.ldd < 0 || L.ld_aux < 0) return GE_ERR_INVALID_ARG;
+
+  Plan tmp;
+  tmp.M = M;
+  tmp.N = N;
+  tmp.K = K;
+  tmp.epi = epi;
+  tmp.R = L.d == GE_D_ROW ? M : N;
+  tmp.C = L.d == GE_D_ROW ? N : M;
+
+  // A 1-column B (decode) stored N-major with unit pitch is a contiguous
+  // vector, the same bytes as K-major: read it as K-major.
+  if (epi != GE_EPI_DRELU_BGRAD && N == 1 && L.b == GE_MN_MAJOR && (L.ldb == 0 || L.ldb == 1)) {
+    L.b = GE_K_MAJOR;
+    L.ldb = (K + 7) / 8 * 8;
+  }
+  if (epi != GE_EPI_DRELU_BGRAD) {
+    const int64_t min_lda = L.a == GE_K_MAJOR ? K : M;
+    const int64_t min_ldb = L.b == GE_K_MAJOR ? K : N;
+    if (L.lda == 0) L.lda = min_lda;
+    if (L.ldb == 0) L.ldb = min_ldb;
+    if (L.lda < min_lda || L.ldb < min_ldb) return GE_ERR_INVALID_ARG;
+  }
+  if (L.ldd == 0) L.ldd = tmp.C;
+  if (L.ldd < tmp.C) return GE_ERR_INVALID_ARG;
+  const bool has_mask = epi == GE_EPI_RELU_AUX_BIAS || epi == GE_EPI_DRELU_BGRAD;
+  if (has_mask) {
+    const int64_t min_words = (tmp.C + 31) / 32;
+    if (L.ld_aux == 0) L.ld_aux = (tmp.C + 127) / 128 * 4;
+    if (L.ld_aux < min_words) return GE_ERR_INVALID_ARG;
+    if (L.ld_aux % 4 != 0) return GE_ERR_ALIGNMENT;
+    tmp.aux_words = L.ld_aux;
+  }
+
+  // Path choice.
+  if (epi == GE_EPI_DRELU_BGRAD) {
+    tmp.path = GE_PATH_DRELU;
+    if (L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
+  } else if (N <= 16 && L.a == GE_K_MAJOR && L.b == GE_K_MAJOR && epi != GE_EPI_RELU_AUX_BIAS) {
+    tmp.path = GE_PATH_GEMV;
+    if (L.lda % 8 != 0 || L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
+  } else {
+    tmp.path = GE_PATH_TC_GEMM;
+    if (L.lda % 8 != 0 || L.ldb % 8 != 0 || L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
+  }
+  tmp.L = L;
+
+  // Device resources (the only CUDA calls of planning).
+  if (cudaGetDevice(&tmp.device) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  if (cudaDeviceGetAttribute(&tmp.num_sms, cudaDevAttrMultiProcessorCount, tmp.device) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  if (tmp.path == GE_PATH_TC_GEMM) {
+    tmp.swap = L.d == GE_D_COL;
+    const int64_t Mk = tmp.swap ? N : M;
+    const int64_t Nk = tmp.swap ? M : N;
+    const int64_t num_m = (Mk + 127) / 128;
+    const long long t256 = num_m * ((Nk + 255) / 256);
+    const long long t128 = num_m * ((Nk + 127) / 128);
+    const double e256 = wave_efficiency(t256, tmp.num_sms);
+    const double e128 = wave_efficiency(t128, tmp.num_sms);
+    // 128 x 256 tiles re-read A half as often; prefer them unless 128-wide
+    // tiles fill the machine clearly better.
+    tmp.block_n = (Nk <= 128 || e128 > e256 * 1.05) ? 128 : 256;
+    const long long tiles = tmp.block_n == 256 ? t256 : t128;
+    tmp.grid = static_cast<int>(tiles < tmp.num_sms ? tiles : tmp.num_sms);
+    tmp.group_m = static_cast<int>(num_m < 16 ? num_m : 16);
+  }
+  size_t ws = 256;
+  if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
+    tmp.splits = drelu_splits(tmp.R, tmp.C, tmp.num_sms);
+    const int64_t strips = (tmp.C + 255) / 256;
+    ws += static_cast<size_t>(strips) * 4;
+    ws = (ws + 255) / 256 * 256;
+    ws += static_cast<size_t>(tmp.splits) * static_cast<size_t>(tmp.C) * 4;
+  }
+  if (cudaMalloc(&tmp.ws, ws) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_OOM;
+  }
+  if (cudaMemset(tmp.ws, 0, ws) != cudaSuccess) {
+    cudaFree(tmp.ws);
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  tmp.ws_bytes = ws;
+  tmp.err = static_cast<unsigned int*>(tmp.ws);
+  if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
+    tmp.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + 256);
+    const int64_t strips = (tmp.C + 255) / 256;
+    size_t off = 256 + static_cast<size_t>(strips) * 4;
+    off = (off + 255) / 256 * 256;
+    tmp.partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + off);
+  }
+  Plan* pl = new (std::nothrow) Plan(tmp);
+  if (!pl) {
+    cudaFree(tmp.ws);
+    return GE_ERR_OOM;
+  }
+  *out = reinterpret_cast<ge_plan_t>(pl);
+  return GE_OK;
+}
+
+ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B, const void* bias, void* D,
+                       void* aux, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ge_status_t s;
+  if (pl->path == GE_PATH_DRELU) {
+    // A = dY, D = dZ, aux = mask, bias = fp32 bgrad output.
+    if (!A || !D || !aux || !bias) return GE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(D) || !aligned16(aux) || !aligned16(bias)) return GE_ERR_ALIGNMENT;
+    if ((s = check_device(pl, 0, A)) != GE_OK || (s = check_device(pl, 3, D)) != GE_OK ||
+        (s = check_device(pl, 4, aux)) != GE_OK || (s = check_device(pl, 2, bias)) != GE_OK)
+      return s;
+    DreluArgs d{};
+    d.R = pl->R;
+    d.C = pl->C;
+    d.dY = static_cast<const __half*>(A);
+    d.dZ = static_cast<__half*>(D);
+    d.ld = pl->L.ldd;
+    d.mask = static_cast<const uint32_t*>(aux);
+    d.ld_aux = pl->aux_words;
+    d.bgrad = static_cast<float*>(const_cast<void*>(bias));
+    d.partials = pl->partials;
+    d.counters = pl->counters;
+    d.splits = pl->splits;
+    cudaError_t e = launch_drelu_bgrad(d, pl->L.d == GE_D_COL ? 1 : 0, st);
+    return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+  }
+  if (!A || !B || !D) return GE_ERR_INVALID_ARG;
+  if (epi_has_bias(pl->epi) && !bias) return GE_ERR_INVALID_ARG;
+  if (pl->epi == GE_EPI_RELU_AUX_BIAS && !aux) return GE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B)) return GE_ERR_ALIGNMENT;
+  if (pl->path == GE_PATH_TC_GEMM && !aligned16(D)) return GE_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(D) & 1u) || (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)) ||
+      (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)))
+    return GE_ERR_ALIGNMENT;
+  if ((s = check_device(pl, 0, A)) != GE_OK || (s = check_device(pl, 1, B)) != GE_OK ||
+      (s = check_device(pl, 3, D)) != GE_OK)
+    return s;
+  if (epi_has_bias(pl->epi) && (s = check_device(pl, 2, bias)) != GE_OK) return s;
+  if (pl->epi == GE_EPI_RELU_AUX_BIAS && (s = check_device(pl, 4, aux)) != GE_OK) return s;
+  return launch_forward(pl, A, B, epi_has_bias(pl->epi) ? bias : nullptr, D,
+                        pl->epi == GE_EPI_RELU_AUX_BIAS ? aux : nullptr, static_cast<int>(pl->epi), st);
+}
+
+ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B, const void* bias,
+                               void* D, void* aux, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_ERR_INVALID_ARG;
+  if (!epi_has_bias(pl->epi) || pl->path == GE_PATH_DRELU) return GE_ERR_UNSUPPORTED;
+  if (!A || !B || !D || !bias) return GE_ERR_INVALID_ARG;
+  if (pl->epi == GE_EPI_RELU_AUX_BIAS && !aux) return GE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return GE_ERR_ALIGNMENT;
+  if (pl->L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(bias) & 1u) || (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)))
+    return GE_ERR_ALIGNMENT;
+  ge_status_t s;
+  if ((s = check_device(pl, 0, A)) != GE_OK || (s = check_device(pl, 1, B)) != GE_OK ||
+      (s = check_device(pl, 3, D)) != GE_OK || (s = check_device(pl, 2, bias)) != GE_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = launch_forward(pl, A, B, nullptr, D, nullptr, EPI_NONE, st);
+  if (s != GE_OK) return s;
+  __half* Dh = static_cast<__half*>(D);
+  cudaError_t e = launch_bias_add(Dh, pl->R, pl->C, pl->L.ldd, static_cast<const __half*>(bias),
+                                  pl->L.d == GE_D_ROW ? 1 : 0, st);
+  if (e != cudaSuccess) return GE_ERR_CUDA;
+  if (pl->epi != GE_EPI_BIAS) {
+    e = launch_activation(Dh, pl->R, pl->C, pl->L.ldd, static_cast<int>(pl->epi),
+                          pl->epi == GE_EPI_RELU_AUX_BIAS ? static_cast<uint32_t*>(aux) : nullptr,
+                          pl->aux_words, st);
+    if (e != cudaSuccess) return GE_ERR_CUDA;
+  }
+  return GE_OK;
+}
+
+ge_status_t ge_plan_free(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_OK;
+  ge_status_t s = GE_OK;
+  if (pl->ws && cudaFree(pl->ws) != cudaSuccess) {
+    cudaGetLastError();
+    s = GE_ERR_CUDA;
+  }
+  delete pl;
+  return s;
+}
+
+size_t ge_aux_bytes(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl || pl->epi != GE_EPI_RELU_AUX_BIAS) return 0;
+  return static_cast<size_t>(pl->R) * static_cast<size_t>(pl->aux_words) * 4u;
+}
+
+int64_t ge_aux_ld(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  return pl ? pl->aux_words : 0;
+}
+
+int ge_plan_path(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  return pl ? static_cast<int>(pl->path) : -1;
+}
+
+int ge_plan_tile_n(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  return (pl && pl->path == GE_PATH_TC_GEMM) ? pl->block_n : 0;
+}
+
+ge_status_t ge_get_last_device_error(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_ERR_INVALID_ARG;
+  unsigned int w = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&w, pl->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(pl->err, 0, sizeof(w)) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  return w ? GE_ERR_TIMEOUT : GE_OK;
+}
+
+ge_status_t ge_debug_wait_timeout(ge_plan_t plan, int64_t budget_cycles, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl || budget_cycles < 1 || budget_cycles > (int64_t(1) << 31)) return GE_ERR_INVALID_ARG;
+  cudaError_t e = launch_wait_probe(pl->err, budget_cycles, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,408 @@
+// ge_gemm.cu -- persistent, warp-specialised tcgen05 GEMM with the fused
+// bias + activation (+ ReLU mask) epilogue, for sm_103a.
+//
+// What it computes (page title, section):
+//  * nvmath-python cuBLASLt bias-fusion guide, "Core API and parameter
+//    configuration" and "Principle of the performance gain": the product and
+//    the bias add happen in one kernel and the result is written to global
+//    memory once, the bias (m,1) broadcast over the columns.
+//  * same page, "Advanced techniques": ReLU / GELU fused after the bias;
+//    fp16 operands, 32-bit accumulation, fp16 output.
+//  * Fusing bias addition with matrix multiplication using nvmath-python:
+//    the intermediate WX never goes back to global memory; RELU_AUX_BIAS
+//    also keeps the auxiliary output the backward pass needs.
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: A and B k-slices (64 fp16 = one 128-byte
+//               swizzle row) into a STAGES-deep shared-memory ring.
+//   warp 1      owns TMEM (2 x BN fp32 columns: a double-buffered 128 x BN
+//               accumulator) and one lane issues tcgen05.mma 128 x BN x 16.
+//   warps 2..5  epilogue: tcgen05.ld a 32-row x 32-column slab of the
+//               accumulator, add the bias, apply the activation, build the
+//               mask word, round to fp16, stage in 64-byte-swizzled shared
+//               memory and TMA-store it; runs while the MMA warp already
+//               accumulates the next tile into the other TMEM buffer.
+// Every wait is bounded; an expired wait records a bit in the error word,
+// raises a CTA-wide abort flag, and every role drains its in-flight copies
+// before the CTA frees TMEM and exits.
+#include "ge_internal.h"
+#include "ge_ptx.cuh"
+
+namespace ge {
+namespace {
+
+constexpr int BM = 128;            // accumulator rows = TMEM lanes
+constexpr int BK = 64;             // fp16 k-slice per stage (128 bytes)
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 fp16 columns
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+  static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB for base alignment
+  static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "SW128 atoms need 1 KB alignment");
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int& mt,
+                                            int& nt) {
+  const int per_group = group_m * num_n;
+  const int g = tile / per_group;
+  const int first_m = g * group_m;
+  const int gsz = min(num_m - first_m, group_m);
+  const int r = tile - g * per_group;
+  mt = first_m + r % gsz;
+  nt = r / gsz;
+}
+
+__device__ __forceinline__ float apply_act(int epi, float z) {
+  if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
+  if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  return z;
+}
+
+// Epilogue of one 32-column slab held by this thread (one accumulator row).
+// Returns the 32 packed fp16 values in `packed` and the mask bits.
+template <int EPI, bool BIAS_COL>
+__device__ __forceinline__ uint32_t epilogue_slab(const uint32_t (&v)[32], float brow,
+                                                  const float (&bcol)[32], uint32_t (&packed)[16]) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float z0 = __uint_as_float(v[j]);
+    float z1 = __uint_as_float(v[j + 1]);
+    if (EPI != EPI_NONE) {
+      z0 += BIAS_COL ? bcol[j] : brow;
+      z1 += BIAS_COL ? bcol[j + 1] : brow;
+    }
+    if (EPI == EPI_RELU_AUX_BIAS) {
+      bits |= (z0 > 0.0f ? 1u : 0u) << j;
+      bits |= (z1 > 0.0f ? 1u : 0u) << (j + 1);
+    }
+    packed[j / 2] = pack_half2(apply_act(EPI, z0), apply_act(EPI, z1));
+  }
+  return bits;
+}
+
+template <bool BIAS_COL>
+__device__ __forceinline__ uint32_t epilogue_dispatch(int epi, const uint32_t (&v)[32], float brow,
+                                                      const float (&bcol)[32],
+                                                      uint32_t (&packed)[16]) {
+  switch (epi) {
+    case EPI_BIAS: return epilogue_slab<EPI_BIAS, BIAS_COL>(v, brow, bcol, packed);
+    case EPI_RELU_BIAS: return epilogue_slab<EPI_RELU_BIAS, BIAS_COL>(v, brow, bcol, packed);
+    case EPI_GELU_BIAS: return epilogue_slab<EPI_GELU_BIAS, BIAS_COL>(v, brow, bcol, packed);
+    case EPI_RELU_AUX_BIAS:
+      return epilogue_slab<EPI_RELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, packed);
+    default: return epilogue_slab<EPI_NONE, BIAS_COL>(v, brow, bcol, packed);
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_m = (p.Mk + BM - 1) / BM;
+  const int num_n = (p.Nk + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.budget)) {
+            if (!*abort_flag) atomicOr(p.err, ERR_PRODUCER_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const int k0 = kb * BK;
+          if (!p.a_mn) {
+            tma_load_2d(sa, &tmA, fb, k0, mt * BM);
+          } else {
+            tma_load_2d(sa, &tmA, fb, mt * BM, k0);
+            tma_load_2d(sa + 8192, &tmA, fb, mt * BM + 64, k0);
+          }
+          if (!p.b_mn) {
+            tma_load_2d(sb, &tmB, fb, k0, nt * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, nt * BN + 64 * j, k0);
+          }
+          ++fills;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every issued load must land before the CTA may exit.
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (fills > s) {
+          const long long last = s + (long long)C::STAGES * ((fills - 1 - s) / C::STAGES);
+          const uint32_t par = static_cast<uint32_t>((last / C::STAGES) & 1);
+          if (!mbar_wait_bounded(full_bar(s), par, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_f16_f32(BM, BN, p.a_mn, p.b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.budget)) {
+          if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.budget)) {
+            if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // K-major: the 16-wide k step is 32 bytes inside the 128-byte
+            // swizzle row; MN-major: 16 k-rows of 128 bytes = 2 KB.
+            const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                       : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                       : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));  // frees the stage once these MMAs retire
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Drain: all MMAs issued by this thread retire before TMEM is freed.
+      tc_commit(drain_bar);
+      if (!mbar_wait_bounded(drain_bar, 0u, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* stg = smem + C::OFF_EPI + (warp - 2) * 2 * EPI_BUF_BYTES;
+    const bool has_bias = p.epi != EPI_NONE;
+    const bool bias_vec_ok = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int nstore = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.budget) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          if (!*abort_flag) atomicOr(p.err, ERR_EPILOGUE_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const int grow = mt * BM + q * 32 + lane;  // this thread's row of D'
+      float brow = 0.0f;
+      if (has_bias && !p.bias_per_col && grow < p.Mk) brow = __half2float(p.bias[grow]);
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int gcol0 = nt * BN + c * 32;
+        if (gcol0 >= p.Nk) {
+          // Past the end of the row: only the mask's zero padding words
+          // (rows padded to 128 columns) remain to be written.
+          if (p.epi == EPI_RELU_AUX_BIAS && grow < p.Mk && gcol0 < ((p.Nk + 127) & ~127))
+            p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = 0u;
+          continue;
+        }
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + 32u * c, v);
+        tmem_ld_wait();
+        float bcol[32];
+        if (has_bias && p.bias_per_col) {
+          if (bias_vec_ok && gcol0 + 32 <= p.Nk) {
+            const uint4* bp = reinterpret_cast<const uint4*>(p.bias + gcol0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 w = __ldg(bp + i);
+              const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float2 f = __half22float2(h[t]);
+                bcol[8 * i + 2 * t] = f.x;
+                bcol[8 * i + 2 * t + 1] = f.y;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              bcol[j] = gcol0 + j < p.Nk ? __half2float(p.bias[gcol0 + j]) : 0.0f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) bcol[j] = 0.0f;
+        }
+        uint32_t packed[16];
+        uint32_t bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, packed)
+                                       : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed);
+        // Stage the 32x32 fp16 slab (64-byte swizzle: 16-byte chunk j of row
+        // r sits at chunk j ^ ((r >> 1) & 3)) and TMA-store it.
+        uint8_t* buf = stg + (c & 1) * EPI_BUF_BYTES;
+        if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int sw = j ^ ((lane >> 1) & 3);
+          *reinterpret_cast<uint4*>(buf + lane * 64 + sw * 16) =
+              make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, smem_u32(buf), gcol0, mt * BM + q * 32);
+          bulk_commit_group();
+        }
+        ++nstore;
+        if (p.epi == EPI_RELU_AUX_BIAS && grow < p.Mk) {
+          if (p.Nk - gcol0 < 32) bits &= (1u << (p.Nk - gcol0)) - 1u;
+          p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN>
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
+                        const GemmArgs& args, int grid, cudaStream_t stream) {
+  static bool configured[64] = {};  // the attribute is set once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<BN>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  tc_gemm_kernel<BN><<<grid, NUM_THREADS, Cfg<BN>::SMEM_BYTES, stream>>>(tmA, tmB, tmD, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tc_gemm_smem_bytes(int block_n) {
+  return block_n == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES;
+}
+
+cudaError_t launch_tc_gemm(int block_n, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmD, const GemmArgs& args, int grid,
+                           cudaStream_t stream) {
+  if (block_n == 256) return launch_impl<256>(tmA, tmB, tmD, args, grid, stream);
+  return launch_impl<128>(tmA, tmB, tmD, args, grid, stream);
+}
+
+}  // namespace ge

@@ -1,0 +1,95 @@
+// ge_internal.h -- declarations shared by the library's translation units
+// (host planner <-> kernel launchers). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace ge {
+
+// Epilogue codes used by the kernels (forward only).
+enum EpiCode : int {
+  EPI_NONE = 0,
+  EPI_BIAS = 1,
+  EPI_RELU_BIAS = 2,
+  EPI_GELU_BIAS = 3,
+  EPI_RELU_AUX_BIAS = 4
+};
+
+// Device error word bits (the plan's workspace word 0).
+enum ErrBits : unsigned int {
+  ERR_PRODUCER_TIMEOUT = 1u,
+  ERR_MMA_TIMEOUT = 2u,
+  ERR_EPILOGUE_TIMEOUT = 4u,
+  ERR_DRAIN_TIMEOUT = 8u,
+  ERR_PROBE_TIMEOUT = 16u
+};
+
+// Kernel-level problem of the tensor-core GEMM: D'[Mk, Nk] (row-major, via
+// the D tensor map) = act(A'[Mk, K] . B'[K, Nk] + bias), where the planner
+// has already folded a column-major D into swapped operands.
+struct GemmArgs {
+  int Mk, Nk, K;
+  int a_mn;          // A' is M-major (1) or K-major (0)
+  int b_mn;          // B' is N-major (1) or K-major (0)
+  int epi;           // EpiCode
+  int bias_per_col;  // bias indexed by D' column (1) or row (0)
+  const __half* bias;
+  uint32_t* aux;     // mask words, rows of D', ld_aux words per row
+  long long ld_aux;
+  unsigned int* err; // device error word
+  int group_m;       // tile rasterisation group (m-tiles per group)
+  long long budget;  // bounded-wait budget in SM clock cycles
+};
+
+size_t tc_gemm_smem_bytes(int block_n);
+cudaError_t launch_tc_gemm(int block_n, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmD, const GemmArgs& args, int grid,
+                           cudaStream_t stream);
+
+// Weight-streaming GEMV for N <= 16: A K-major [M, K] (lda), B K-major
+// (B[k,n] at B[n*ldb + k]), D[m,n] at m*ldd_m + n*ldd_n.
+struct GemvArgs {
+  int M, N, K;
+  const __half* A;
+  long long lda;
+  const __half* B;
+  long long ldb;
+  __half* D;
+  long long ldd_m, ldd_n;
+  const __half* bias;
+  int epi;
+};
+cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
+
+// DRELU_BGRAD on a stored matrix of R rows x C contiguous columns.
+// reduce_rows = 1: bgrad[c] = sum over rows r (D column-major case);
+// reduce_rows = 0: bgrad[r] = sum over columns c (D row-major case).
+struct DreluArgs {
+  long long R, C;
+  const __half* dY;
+  __half* dZ;
+  long long ld;       // elements
+  const uint32_t* mask;
+  long long ld_aux;   // words
+  float* bgrad;
+  float* partials;    // [splits][C] workspace (reduce_rows only)
+  unsigned int* counters;  // [ceil(C/256)] workspace (reduce_rows only)
+  int splits;
+};
+cudaError_t launch_drelu_bgrad(const DreluArgs& args, int reduce_rows, cudaStream_t stream);
+int drelu_splits(long long R, long long C, int num_sms);
+
+// Unfused baseline kernels, in place on D (R rows x C contiguous, ld).
+cudaError_t launch_bias_add(__half* D, long long R, long long C, long long ld, const __half* bias,
+                            int bias_per_row, cudaStream_t stream);
+cudaError_t launch_activation(__half* D, long long R, long long C, long long ld, int epi,
+                              uint32_t* aux, long long ld_aux, cudaStream_t stream);
+
+// Bounded-wait probe (test hook).
+cudaError_t launch_wait_probe(unsigned int* err, long long budget, cudaStream_t stream);
+
+}  // namespace ge

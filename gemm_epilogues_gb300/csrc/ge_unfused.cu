@@ -1,0 +1,133 @@
+// ge_unfused.cu -- the unfused baseline's elementwise kernels, and the
+// bounded-wait probe used by the failure-path test.
+//
+// ops-nn MatMul fusion (codearts), "ops-nn's MatMul fusion strategy", first
+// level: without fusion the product is written to HBM, read back for the
+// bias add and written again, then read back for the activation and written
+// again. These two kernels are those extra passes; with the GEMM's NONE
+// epilogue in front they form the three-kernel baseline the fused path is
+// measured against. Both work in place on D and are bound by HBM bandwidth.
+#include "ge_internal.h"
+#include "ge_ptx.cuh"
+
+namespace ge {
+namespace {
+
+__device__ __forceinline__ float act_of(int epi, float z) {
+  if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
+  if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  return z;
+}
+
+// D[r, c] += bias[r] (bias_per_row) or bias[c]; 8 contiguous fp16 per thread.
+__global__ void __launch_bounds__(256) bias_add_kernel(__half* D, long long R, long long C,
+                                                        long long ld, const __half* bias,
+                                                        int bias_per_row) {
+  const long long vpr = (C + 7) / 8;  // 8-wide groups per row
+  const long long total = R * vpr;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
+    const long long r = i / vpr;
+    const long long c0 = (i - r * vpr) * 8;
+    __half* row = D + r * ld;
+    if (c0 + 8 <= C) {
+      uint4 v = *reinterpret_cast<const uint4*>(row + c0);
+      __half2* h = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float2 f = __half22float2(h[t]);
+        f.x += __half2float(bias_per_row ? bias[r] : bias[c0 + 2 * t]);
+        f.y += __half2float(bias_per_row ? bias[r] : bias[c0 + 2 * t + 1]);
+        h[t] = __floats2half2_rn(f.x, f.y);
+      }
+      *reinterpret_cast<uint4*>(row + c0) = v;
+    } else {
+      for (long long c = c0; c < C; ++c)
+        row[c] = __float2half_rn(__half2float(row[c]) +
+                                 __half2float(bias_per_row ? bias[r] : bias[c]));
+    }
+  }
+}
+
+// D = act(D) in place; with a mask, one thread owns 32 contiguous elements
+// (one mask word) and writes the word, zero padding included.
+__global__ void __launch_bounds__(256) activation_kernel(__half* D, long long R, long long C,
+                                                          long long ld, int epi, uint32_t* aux,
+                                                          long long ld_aux) {
+  const long long wpr = aux ? ld_aux : (C + 31) / 32;  // 32-wide groups per row
+  const long long total = R * wpr;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
+    const long long r = i / wpr;
+    const long long g = i - r * wpr;
+    const long long c0 = g * 32;
+    __half* row = D + r * ld;
+    uint32_t bits = 0;
+    if (c0 + 32 <= C) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 v = *reinterpret_cast<const uint4*>(row + c0 + 8 * q);
+        __half2* h = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = __half22float2(h[t]);
+          bits |= (f.x > 0.0f ? 1u : 0u) << (8 * q + 2 * t);
+          bits |= (f.y > 0.0f ? 1u : 0u) << (8 * q + 2 * t + 1);
+          h[t] = __floats2half2_rn(act_of(epi, f.x), act_of(epi, f.y));
+        }
+        *reinterpret_cast<uint4*>(row + c0 + 8 * q) = v;
+      }
+    } else {
+      for (long long c = c0; c < C; ++c) {
+        const float f = __half2float(row[c]);
+        bits |= (f > 0.0f ? 1u : 0u) << (c - c0);
+        row[c] = __float2half_rn(act_of(epi, f));
+      }
+    }
+    if (aux && epi == EPI_RELU_AUX_BIAS && c0 < ((C + 127) / 128) * 128) aux[r * ld_aux + g] = bits;
+  }
+}
+
+__global__ void wait_probe_kernel(unsigned int* err, long long budget) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nobody ever arrives on `bar`: the wait must give up after `budget`.
+    if (!mbar_wait_bounded(smem_u32(&bar), 0u, &abort_flag, budget)) atomicOr(err, ERR_PROBE_TIMEOUT);
+  }
+}
+
+int grid_for(long long work, int per_block) {
+  long long b = (work + per_block - 1) / per_block;
+  if (b > 65535LL * 8) b = 65535LL * 8;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_bias_add(__half* D, long long R, long long C, long long ld, const __half* bias,
+                            int bias_per_row, cudaStream_t s) {
+  if (R == 0 || C == 0) return cudaSuccess;
+  bias_add_kernel<<<grid_for(R * ((C + 7) / 8), 256), 256, 0, s>>>(D, R, C, ld, bias, bias_per_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_activation(__half* D, long long R, long long C, long long ld, int epi,
+                              uint32_t* aux, long long ld_aux, cudaStream_t s) {
+  if (R == 0 || C == 0) return cudaSuccess;
+  const long long wpr = aux ? ld_aux : (C + 31) / 32;
+  activation_kernel<<<grid_for(R * wpr, 256), 256, 0, s>>>(D, R, C, ld, epi, aux, ld_aux);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(unsigned int* err, long long budget, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(err, budget);
+  return cudaGetLastError();
+}
+
+}  // namespace ge

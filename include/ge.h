@@ -1,0 +1,219 @@
+/*
+ * ge.h -- C ABI of the GB300 fused linear-layer engine (libgemm_epilogues.so).
+ *
+ * One operation family: D = act(A.B + bias) computed as a single GEMM whose
+ * epilogue adds a broadcast bias vector and applies an activation in
+ * registers before one store of D, plus the matching backward epilogue.
+ *
+ * Sources (page title, section) for what each call computes:
+ *  - nvmath-python cuBLASLt bias-fusion guide, "Core API and parameter
+ *    configuration": the plan -> execute -> free life cycle; weights (m,k)
+ *    times x (k,n) plus a bias of shape (m,1) broadcast over the n columns;
+ *    fp16 operands with a 32-bit compute type and fp16 output.
+ *  - same page, "Advanced techniques": RELU_BIAS and GELU_BIAS fuse the
+ *    activation after the bias; DRELU_BGRAD fuses the ReLU-gradient mask with
+ *    the bias-gradient accumulation in the backward pass; a plan is costly
+ *    and is meant to be reused across many executes.
+ *  - Fusing bias addition with matrix multiplication using nvmath-python:
+ *    Y = ReLU(WX + B); RELU_AUX_BIAS also writes an auxiliary output for the
+ *    backward pass; planning is blocking and chooses the kernel; a plan must
+ *    be freed; operands must live on one device with compatible dtypes or
+ *    the call fails.
+ *  - PyTorch inference cuBLASLt bias-fusion optimization: the epilogue
+ *    attribute and the bias pointer are bound on the matmul descriptor, the
+ *    compute type is 32-bit float.
+ *  - ops-nn MatMul fusion (codearts), "Why MatMul is the inference
+ *    bottleneck": with one token per step the product is bound by reading the
+ *    weights, which selects the weight-streaming GEMV path below.
+ *
+ * Canonical form. D[m,n] = act(sum_k A[m,k] * B[k,n] + bias[m]) for
+ * 0 <= m < M, 0 <= n < N; bias is broadcast over the columns n. For an
+ * nn.Linear layer Y[T,out] = X[T,in] W[out,in]^T + b this is M = out,
+ * N = T, K = in, A = W (K-major), B = X^T (X read as a K-major B), and D
+ * stored column-major, which is Y[T,out] row-major.
+ *
+ * Ownership and threading. The caller owns every device buffer (A, B, bias,
+ * D, aux, and the DRELU_BGRAD outputs). A plan owns its host state and a
+ * small device workspace allocated by ge_plan_create on the device current
+ * at that time (an error word, and for DRELU_BGRAD the reduction partials
+ * and counters). ge_execute never allocates and only enqueues work on the
+ * given stream; the caller synchronises. Executes of one plan must be
+ * ordered on one stream: two executes of the same plan that overlap on the
+ * GPU race on its workspace. Distinct plans are independent.
+ *
+ * Errors. Every call returns a status and never aborts or prints. Arguments
+ * are validated before anything is launched.
+ */
+#ifndef GE_H_
+#define GE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ge_plan_s* ge_plan_t;
+
+typedef enum {
+  GE_OK = 0,
+  GE_ERR_INVALID_ARG = 1,     /* null/negative/inconsistent argument           */
+  GE_ERR_UNSUPPORTED = 2,     /* dtype / epilogue / layout not implemented     */
+  GE_ERR_ALIGNMENT = 3,       /* pointer or leading dimension not 16-B aligned */
+  GE_ERR_DEVICE_MISMATCH = 4, /* a buffer is not on the plan's device          */
+  GE_ERR_CUDA = 5,            /* a CUDA runtime call or a launch failed        */
+  GE_ERR_TIMEOUT = 6,         /* a bounded device-side wait expired            */
+  GE_ERR_OOM = 7              /* plan workspace allocation failed              */
+} ge_status_t;
+
+/* Epilogues (nvmath-python MatmulEpilog names). NONE is D = A.B. */
+typedef enum {
+  GE_EPI_NONE = 0,
+  GE_EPI_BIAS = 1,          /* D = A.B + bias                                  */
+  GE_EPI_RELU_BIAS = 2,     /* D = max(A.B + bias, 0)                          */
+  GE_EPI_GELU_BIAS = 3,     /* D = gelu_tanh(A.B + bias)                       */
+  GE_EPI_RELU_AUX_BIAS = 4, /* RELU_BIAS plus the bit-packed mask (z > 0)      */
+  GE_EPI_DRELU_BGRAD = 5    /* backward: dZ = dY * mask, bgrad = sum_n dZ      */
+} ge_epilogue_t;
+
+typedef enum { GE_F16 = 0, GE_F32 = 1 } ge_dtype_t;
+
+/* Operand storage. A: K_MAJOR -> A[m,k] at A[m*lda + k]; MN_MAJOR -> A[k*lda + m].
+ *                  B: K_MAJOR -> B[k,n] at B[n*ldb + k]; MN_MAJOR -> B[k*ldb + n]. */
+typedef enum { GE_K_MAJOR = 0, GE_MN_MAJOR = 1 } ge_major_t;
+
+/* D storage: ROW -> D[m,n] at D[m*ldd + n]; COL -> D[m,n] at D[n*ldd + m]. */
+typedef enum { GE_D_ROW = 0, GE_D_COL = 1 } ge_dlayout_t;
+
+/* Leading dimensions in elements (ld_aux in 32-bit words); 0 selects the
+ * packed default (K or M/N for the operands, the contiguous extent of D, and
+ * ceil(len/128)*4 words for the mask). Every leading dimension must be a
+ * multiple of 8 elements (16 bytes), ld_aux a multiple of 4 words. */
+typedef struct {
+  ge_major_t a;
+  ge_major_t b;
+  ge_dlayout_t d;
+  int64_t lda, ldb, ldd, ld_aux;
+} ge_layout_t;
+
+/* Kernel path a plan selected (for inspection and benchmarks). */
+typedef enum {
+  GE_PATH_TC_GEMM = 0,   /* tcgen05 tensor-core GEMM with fused epilogue      */
+  GE_PATH_GEMV = 1,      /* weight-streaming GEMV, N <= 16                    */
+  GE_PATH_DRELU = 2      /* DRELU_BGRAD streaming reduction                   */
+} ge_path_t;
+
+/*
+ * ge_plan_create: validate a problem and choose its kernel.
+ *   out      : receives the plan (set to NULL on failure).
+ *   M, N, K  : problem size. M, N >= 1. K >= 1 for the forward epilogues;
+ *              K == 0 selects the standalone DRELU_BGRAD kernel (the only
+ *              form of DRELU_BGRAD; K > 0 with it is GE_ERR_UNSUPPORTED).
+ *              M, N, K < 2^31.
+ *   a, b, d  : operand and output dtypes; GE_F16 only.
+ *   compute  : accumulation dtype; GE_F32 only.
+ *   epi      : epilogue.
+ *   layout   : may be NULL = {A K_MAJOR, B MN_MAJOR, D ROW, packed lds}.
+ * The device current at this call owns the plan's workspace; every execute
+ * must pass buffers that live on that device. Leading dimensions must be
+ * multiples of 8 elements on the tensor-core path (every operand and D), and
+ * for lda/ldb on the GEMV path; ldd for DRELU_BGRAD.
+ * Returns GE_OK, GE_ERR_INVALID_ARG, GE_ERR_UNSUPPORTED, GE_ERR_ALIGNMENT,
+ * GE_ERR_CUDA (no device) or GE_ERR_OOM.
+ */
+ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K,
+                           ge_dtype_t a, ge_dtype_t b, ge_dtype_t d,
+                           ge_dtype_t compute, ge_epilogue_t epi,
+                           const ge_layout_t* layout);
+
+/*
+ * ge_execute: enqueue the planned operation on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream). All pointers are device pointers of
+ * the plan's device (alignment rules at the end of this comment).
+ * Forward epilogues:
+ *   A, B  : fp16 operands in the planned layouts (read only).
+ *   bias  : fp16 [M] (read only); required for every *_BIAS epilogue,
+ *           ignored for NONE.
+ *   D     : fp16 output, written once.
+ *   aux   : RELU_AUX_BIAS only: uint32 mask words, ge_aux_bytes(plan) bytes.
+ *           Bit (c % 32) of word aux[r*ld_aux + c/32] is 1 iff the fp32
+ *           pre-activation of the element at stored row r, contiguous index c
+ *           of D is > 0 ((r,c) = (m,n) for D ROW, (n,m) for D COL). Words up
+ *           to ceil(len/128)*4 of each row are written; bits past the end of
+ *           the row are 0.
+ * DRELU_BGRAD (K == 0; dY and dZ are [M,N] in the planned D layout):
+ *   A     : dY, fp16 (read only).        B : unused (may be NULL).
+ *   aux   : the forward mask (read only). D : dZ, fp16; may alias A.
+ *   bias  : OUTPUT, fp32 [M]: bgrad[m] = sum over n of dZ[m,n], reduced in
+ *           fp32 in a fixed order (deterministic run to run).
+ *   dZ[m,n] = dY[m,n] where the mask bit is set, +0 elsewhere.
+ * Returns GE_OK, GE_ERR_INVALID_ARG (null plan or a required pointer null),
+ * GE_ERR_ALIGNMENT, GE_ERR_DEVICE_MISMATCH (a pointer that is not device
+ * memory of the plan's device) or GE_ERR_CUDA (launch failure). A device-side
+ * wait that expires during the kernel is reported by
+ * ge_get_last_device_error, not here (execute does not synchronise).
+ * Pointer alignment: A, B (and D on the tensor-core path) 16 bytes; bias 2;
+ * aux 4 (16 for DRELU_BGRAD, where A, D and the fp32 bias output are 16).
+ */
+ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B,
+                       const void* bias, void* D, void* aux, void* stream);
+
+/*
+ * ge_execute_unfused: the three-kernel baseline on the same inputs: the
+ * plan's GEMM with no epilogue writes D, then one kernel reads D, adds the
+ * bias and writes D, then one kernel reads D, applies the activation (and
+ * writes the mask for RELU_AUX_BIAS, from the rounded fp16 z) and writes D
+ * (ops-nn MatMul fusion, "ops-nn's MatMul fusion strategy", the unfused
+ * three-step flow). Only for BIAS / RELU_BIAS / GELU_BIAS / RELU_AUX_BIAS
+ * plans. Arguments and errors as ge_execute.
+ */
+ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B,
+                               const void* bias, void* D, void* aux,
+                               void* stream);
+
+/* Release the plan and its device workspace (NULL is accepted). The caller
+ * must make sure no execute of the plan is still running on the GPU. */
+ge_status_t ge_plan_free(ge_plan_t plan);
+
+/* Bytes of mask the caller allocates for RELU_AUX_BIAS (0 otherwise). */
+size_t ge_aux_bytes(ge_plan_t plan);
+
+/* Mask row pitch in 32-bit words chosen by the plan (0 if no mask). */
+int64_t ge_aux_ld(ge_plan_t plan);
+
+/* The kernel path the plan selected, or -1 for a NULL plan. */
+int ge_plan_path(ge_plan_t plan);
+
+/* Output-tile width (columns of one CTA tile, 0 if not a GEMM path). */
+int ge_plan_tile_n(ge_plan_t plan);
+
+/*
+ * Read and clear the plan's device error word. Synchronises the device.
+ * Returns GE_OK when no device-side wait of this plan has expired since the
+ * last read, GE_ERR_TIMEOUT when one has (the kernel then stopped early and
+ * its outputs are undefined), GE_ERR_CUDA if the read itself failed.
+ */
+ge_status_t ge_get_last_device_error(ge_plan_t plan);
+
+/* Static description of a status code; never NULL. */
+const char* ge_status_string(ge_status_t s);
+
+/*
+ * Test hook for the bounded-wait path: launches one CTA that waits on a
+ * shared-memory barrier nobody arrives at, with a budget of `budget_cycles`
+ * SM clock cycles (1 .. 2^31), then records the expiry in the plan's error
+ * word and returns. The GPU context stays usable. Returns the launch status;
+ * read the outcome with ge_get_last_device_error.
+ */
+ge_status_t ge_debug_wait_timeout(ge_plan_t plan, int64_t budget_cycles,
+                                  void* stream);
+
+/* Library version, "major.minor.patch". */
+const char* ge_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GE_H_ */

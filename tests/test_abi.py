@@ -1,0 +1,83 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects invalid plans before touching the device."""
+import os
+import re
+
+import pytest
+
+import gemm_epilogues_gb300 as ge
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ge.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gemm_epilogues_gb300 import build
+    build.build()
+    return ge.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ge_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert header_functions() == sorted(ge.ABI_FUNCTIONS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for s in range(8):
+        assert ge.ge_status_string(s).startswith("GE_")
+    assert ge.ge_status_string(99) == "unknown ge_status_t"
+    assert re.match(r"\d+\.\d+\.\d+", ge.ge_version())
+
+
+def _create(*args, **kw):
+    st, h = ge.ge_plan_create(*args, raw=True, **kw)
+    assert h is None or st == ge.GE_OK
+    return st
+
+
+def test_plan_validation_without_device(lib):
+    E = ge
+    assert _create(0, 8, 8) == E.GE_ERR_INVALID_ARG
+    assert _create(8, -1, 8) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 8, 0, epi=E.GE_EPI_BIAS) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 8, 8, epi=9) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 8, 8, a=E.GE_F32) == E.GE_ERR_UNSUPPORTED
+    assert _create(8, 8, 8, compute=E.GE_F16) == E.GE_ERR_UNSUPPORTED
+    assert _create(8, 8, 8, epi=E.GE_EPI_DRELU_BGRAD) == E.GE_ERR_UNSUPPORTED
+    assert _create(2**31, 8, 8) == E.GE_ERR_INVALID_ARG
+    # leading dimensions smaller than the extent, or not multiples of 8
+    assert _create(64, 64, 64, layout=ge.make_layout(lda=32)) == E.GE_ERR_INVALID_ARG
+    assert _create(64, 60, 64, layout=ge.make_layout()) == E.GE_ERR_ALIGNMENT  # ldd = N = 60
+    assert _create(64, 64, 60, layout=ge.make_layout(a=E.GE_K_MAJOR)) == E.GE_ERR_ALIGNMENT
+    assert _create(64, 64, 0, epi=E.GE_EPI_DRELU_BGRAD,
+                   layout=ge.make_layout(ld_aux=1)) == E.GE_ERR_INVALID_ARG
+    assert _create(64, 300, 0, epi=E.GE_EPI_DRELU_BGRAD,
+                   layout=ge.make_layout(ld_aux=10)) == E.GE_ERR_ALIGNMENT
+    bad_layout = ge.make_layout()
+    bad_layout.d = 7
+    assert _create(64, 64, 64, layout=bad_layout) == E.GE_ERR_INVALID_ARG
+
+
+def test_valid_plan_needs_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _create(256, 128, 512) == ge.GE_ERR_CUDA
+
+
+def test_null_handles(lib):
+    assert ge.load_library().ge_execute(None, None, None, None, None, None, None) == ge.GE_ERR_INVALID_ARG
+    assert ge.load_library().ge_plan_free(None) == ge.GE_OK
+    assert ge.ge_aux_bytes(None) == 0
+    assert ge.ge_plan_path(None) == -1

@@ -1,0 +1,163 @@
+"""Parity of the tcgen05 GEMM + fused epilogue (and the GEMV path) with the
+CPU oracle, element by element, on small and odd shapes in every layout."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_epilogues_gb300 as ge
+from gemm_epilogues_gb300.inputs import Workload, f16_tensor
+
+from _util import (bits, check_f16, check_mask, gpu_forward, oracle_full)
+
+pytestmark = pytest.mark.gpu
+
+EPIS = ["none", "bias", "relu_bias", "gelu_bias", "relu_aux_bias"]
+
+
+def _pad8(x):
+    return (x + 7) // 8 * 8
+
+
+def _run_case(oracle, M, N, K, epi, am, bm, dl, dist=("normal", 1.0), seed=0, exact=False,
+              unfused=False):
+    w = Workload(f"{M}x{N}x{K} {epi} {am}{bm}{dl}", M, N, K, epi, am, bm, dl,
+                 a_dist=dist, b_dist=dist, bias_dist=(dist[0], 4.0 if dist[0] == "int" else 1.0))
+    # storage with padded leading dimensions (multiples of 8 elements)
+    a_rows, a_cols = w.a_shape()
+    b_rows, b_cols = w.b_shape()
+    d_rows, d_cols = w.d_shape()
+    lda, ldb, ldd = _pad8(a_cols), _pad8(b_cols), _pad8(d_cols)
+    g = seed * 10
+    Ap = f16_tensor((a_rows, lda), g + 1, *dist).cuda()
+    Bp = f16_tensor((b_rows, ldb), g + 2, *dist).cuda()
+    if dist[0] == "int":
+        bias = f16_tensor((M,), g + 3, "int", 8).cuda()
+    else:
+        bias = f16_tensor((M,), g + 3, *dist).cuda()
+    # poison the padding so a read past the logical extent shows up
+    Ap[:, a_cols:] = float("nan")
+    Bp[:, b_cols:] = float("nan")
+    ld = dict(lda=lda, ldb=ldb, ldd=ldd)
+    D, aux, path, ld_aux = gpu_forward(w, Ap, Bp, bias, unfused=unfused, ld=ld)
+    ref = oracle_full(oracle, w, Ap.cpu(), Bp.cpu(), bias.cpu(), ld=ld)
+    got = bits(D).reshape(d_rows, ldd)[:, :d_cols].reshape(-1)
+    want = ref["D"].reshape(d_rows, ldd)[:, :d_cols].reshape(-1)
+    if exact:
+        assert np.array_equal(got, want), f"{w.name}: not bit-identical"
+    else:
+        check_f16(oracle, got, want, w.name)
+    # padding columns of D are never written
+    padv = D[:, d_cols:]
+    assert torch.isnan(padv.float()).all(), f"{w.name}: wrote past the logical columns"
+    if epi == "relu_aux_bias":
+        assert ld_aux == ref["ld_aux"]
+        Z = ref["Z"].reshape(d_rows, ldd)[:, :d_cols]
+        gw = aux.cpu().numpy().view(np.uint32)
+        if exact:
+            assert np.array_equal(gw, ref["aux"]), f"{w.name}: mask not bit-identical"
+        else:
+            check_mask(gw, ref["aux"], Z, d_rows, d_cols, ld_aux, w.name)
+    return path
+
+
+def test_config1_bias(oracle):
+    """256x128x512 BIAS, uniform [0,1) data, A K-major, B N-major, D row."""
+    path = _run_case(oracle, 256, 128, 512, "bias", "k", "n", "row", dist=("uniform01", 1.0))
+    assert path == ge.GE_PATH_TC_GEMM
+
+
+@pytest.mark.parametrize("epi", ["bias", "relu_bias", "gelu_bias"])
+def test_config2(oracle, epi):
+    """1024x512x2048, N(0,1)/sqrt(2048) operands, N(0,1) bias."""
+    _run_case(oracle, 1024, 512, 2048, epi, "k", "n", "row", dist=("normal", 2048 ** -0.5), seed=1)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (129, 17, 128)])
+@pytest.mark.parametrize("epi", ["none", "bias", "relu_bias", "relu_aux_bias"])
+@pytest.mark.parametrize("am,bm,dl", [("k", "n", "row"), ("k", "k", "col"), ("m", "n", "row"),
+                                      ("m", "k", "col")])
+def test_exact_integer(oracle, M, N, K, epi, am, bm, dl):
+    """Integer data: every partial sum is exact in fp32 and fp16, so the GPU
+    must reproduce the oracle bit for bit (values and mask)."""
+    _run_case(oracle, M, N, K, epi, am, bm, dl, dist=("int", 2.0), seed=2, exact=True)
+
+
+SHAPES = [(1, 1, 1), (7, 33, 9), (128, 256, 64), (129, 257, 65), (300, 520, 200), (64, 1000, 136),
+          (520, 40, 1032), (257, 129, 4100)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("am,bm,dl", list(itertools.product("km", "kn", ("row", "col"))))
+def test_layouts_ragged(oracle, M, N, K, am, bm, dl):
+    epi = EPIS[(M + N + K + len(am + bm + dl)) % len(EPIS)]
+    _run_case(oracle, M, N, K, epi, am, bm, dl, seed=3)
+
+
+@pytest.mark.parametrize("epi", EPIS)
+def test_every_epilogue_multi_tile(oracle, epi):
+    """Several tiles in both directions, ragged tails, K not a multiple of 64."""
+    _run_case(oracle, 700, 900, 328, epi, "k", "n", "row", seed=4)
+    _run_case(oracle, 700, 900, 328, epi, "k", "k", "col", seed=5)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 13, 16])
+@pytest.mark.parametrize("epi", ["none", "bias", "relu_bias", "gelu_bias"])
+def test_gemv_path(oracle, N, epi):
+    path = _run_case(oracle, 1000, N, 1000, epi, "k", "k", "col", seed=6)
+    assert path == ge.GE_PATH_GEMV
+    path = _run_case(oracle, 333, N, 4104, epi, "k", "k", "row", seed=7)
+    assert path == ge.GE_PATH_GEMV
+
+
+@pytest.mark.parametrize("epi", ["bias", "relu_bias", "gelu_bias", "relu_aux_bias"])
+def test_unfused_baseline(oracle, epi):
+    """The three-kernel baseline computes the same values (its mask comes from
+    the rounded fp16 z, which only differs inside the tolerance band)."""
+    _run_case(oracle, 520, 264, 200, epi, "k", "n", "row", seed=8, unfused=True)
+    _run_case(oracle, 520, 264, 200, epi, "k", "k", "col", seed=9, unfused=True)
+
+
+def test_repeat_is_deterministic():
+    A = f16_tensor((512, 512), 11).cuda()
+    B = f16_tensor((512, 512), 12).cuda()
+    bias = f16_tensor((512,), 13).cuda()
+    w = Workload("det", 512, 512, 512, "gelu_bias", "k", "n", "row")
+    d1, _, _, _ = gpu_forward(w, A, B, bias)
+    d2, _, _, _ = gpu_forward(w, A, B, bias)
+    assert torch.equal(d1.view(torch.int16), d2.view(torch.int16))
+
+
+def test_timeout_probe_reports_and_recovers():
+    """A bounded wait that nothing satisfies expires, is reported once, and
+    leaves the context usable."""
+    with ge.Plan(128, 128, 64, ge.GE_EPI_BIAS) as p:
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+        assert ge.ge_debug_wait_timeout(p.handle, 2_000_000) == ge.GE_OK
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_ERR_TIMEOUT
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK  # read clears it
+        A = torch.ones(128, 64, dtype=torch.float16, device="cuda")
+        B = torch.ones(64, 128, dtype=torch.float16, device="cuda")
+        bias = torch.zeros(128, dtype=torch.float16, device="cuda")
+        D = torch.empty(128, 128, dtype=torch.float16, device="cuda")
+        p.execute(A, B, bias, D)
+        torch.cuda.synchronize()
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+        assert torch.all(D == 64)
+
+
+def test_execute_rejects_bad_buffers():
+    with ge.Plan(128, 128, 64, ge.GE_EPI_RELU_AUX_BIAS) as p:
+        A = torch.ones(128, 64, dtype=torch.float16, device="cuda")
+        B = torch.ones(64, 128, dtype=torch.float16, device="cuda")
+        bias = torch.zeros(128, dtype=torch.float16, device="cuda")
+        D = torch.empty(128, 128, dtype=torch.float16, device="cuda")
+        aux = torch.empty(p.aux_bytes // 4, dtype=torch.int32, device="cuda")
+        assert ge.ge_execute(p.handle, A, B, bias, D, None, raw=True) == ge.GE_ERR_INVALID_ARG
+        assert ge.ge_execute(p.handle, A, B, None, D, aux, raw=True) == ge.GE_ERR_INVALID_ARG
+        assert ge.ge_execute(p.handle, A.data_ptr() + 2, B, bias, D, aux, raw=True) == ge.GE_ERR_ALIGNMENT
+        host = torch.ones(128, 64, dtype=torch.float16)
+        assert ge.ge_execute(p.handle, host, B, bias, D, aux, raw=True) == ge.GE_ERR_DEVICE_MISMATCH
+        assert ge.ge_execute(p.handle, A, B, bias, D, aux, raw=True) == ge.GE_OK
+        torch.cuda.synchronize()

@@ -244,6 +244,30 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[4].record(stream)
 
+    if args.case != "step":
+        # Profiling mode: only one kernel of the step, `steps` times after
+        # `warmup` launches (each launch preceded by the L2 flush).
+        one = {"fwd": lambda: fwd.execute(W, X, b, Y, aux, stream),
+               "bwd": lambda: bwd.execute(dY, None, bgrad, dZ, aux, stream),
+               "dw": lambda: dwp.execute(dZ, X, None, dW, None, stream),
+               "gemv": lambda: dec.execute(W2, x1, b2, y1, None, stream)}[args.case]
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            one()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        for p in (fwd, bwd, dwp, dec):
+            assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+        if rank == 0:
+            print(json.dumps({"case": args.case, "ms": sum(times) / len(times), "min_ms": min(times),
+                              "launches": args.steps}), flush=True)
+        return
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -379,6 +403,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="step", choices=["step", "fwd", "bwd", "dw", "gemv"],
+                    help="profiling mode: time one kernel of the step alone")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     try:

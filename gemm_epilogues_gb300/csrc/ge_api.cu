@@ -177,6 +177,8 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.bias = static_cast<const __half*>(bias);
     g.aux = static_cast<uint32_t*>(aux);
     g.ld_aux = pl->aux_words;
+    g.D = static_cast<__half*>(D);
+    g.ldd = pl->L.ldd;
     g.err = pl->err;
     g.group_m = pl->group_m;
     g.budget = kWaitBudgetCycles;

@@ -333,24 +333,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t packed[16];
         uint32_t bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, packed)
                                        : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed);
-        // Stage the 32x32 fp16 slab (64-byte swizzle: 16-byte chunk j of row
-        // r sits at chunk j ^ ((r >> 1) & 3)) and TMA-store it.
-        uint8_t* buf = stg + (c & 1) * EPI_BUF_BYTES;
-        if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
-        __syncwarp();
+        if (gcol0 + 32 > p.Nk && (p.Nk & 7) != 0) {
+          // Ragged last slab whose end is not on a 16-byte boundary: a TMA
+          // store writes whole 16-byte chunks, which would spill into the
+          // caller's columns past Nk, so these columns are stored directly.
+          if (grow < p.Mk) {
+            __half* drow = p.D + static_cast<long long>(grow) * p.ldd + gcol0;
+            const int nvalid = p.Nk - gcol0;
+            for (int j = 0; j < nvalid; ++j) {
+              const uint32_t w = packed[j >> 1];
+              drow[j] = __ushort_as_half(static_cast<unsigned short>((j & 1) ? (w >> 16) : (w & 0xFFFFu)));
+            }
+          }
+        } else {
+          // Stage the 32x32 fp16 slab (64-byte swizzle: 16-byte chunk j of row
+          // r sits at chunk j ^ ((r >> 1) & 3)) and TMA-store it.
+          // Buffers alternate per issued store, so the newest store in
+          // flight always reads the other buffer than the one written now.
+          uint8_t* buf = stg + (nstore & 1) * EPI_BUF_BYTES;
+          if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+          __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int sw = j ^ ((lane >> 1) & 3);
-          *reinterpret_cast<uint4*>(buf + lane * 64 + sw * 16) =
-              make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+          for (int j = 0; j < 4; ++j) {
+            const int sw = j ^ ((lane >> 1) & 3);
+            *reinterpret_cast<uint4*>(buf + lane * 64 + sw * 16) =
+                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, smem_u32(buf), gcol0, mt * BM + q * 32);
+            bulk_commit_group();
+          }
+          ++nstore;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmD, smem_u32(buf), gcol0, mt * BM + q * 32);
-          bulk_commit_group();
-        }
-        ++nstore;
         if (p.epi == EPI_RELU_AUX_BIAS && grow < p.Mk) {
           if (p.Nk - gcol0 < 32) bits &= (1u << (p.Nk - gcol0)) - 1u;
           p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;

@@ -40,6 +40,8 @@ struct GemmArgs {
   const __half* bias;
   uint32_t* aux;     // mask words, rows of D', ld_aux words per row
   long long ld_aux;
+  __half* D;         // D' base (row-major, ldd elements per row): ragged-edge stores
+  long long ldd;
   unsigned int* err; // device error word
   int group_m;       // tile rasterisation group (m-tiles per group)
   long long budget;  // bounded-wait budget in SM clock cycles

@@ -21,10 +21,12 @@ def run_drelu(oracle, M, N, dl, seed, inplace=False, repeat=1):
     w = Workload("fwd", M, N, K, "relu_aux_bias", "k", "k" if dl == "col" else "n", dl)
     rows, cols = w.d_shape()
     ldd = _pad8(cols)
+    b_rows, b_cols = w.b_shape()
+    ldb = _pad8(b_cols)
     A = f16_tensor(w.a_shape(), seed + 1).cuda()
-    B = f16_tensor(w.b_shape(), seed + 2).cuda()
+    B = f16_tensor((b_rows, ldb), seed + 2).cuda()
     bias = f16_tensor((M,), seed + 3).cuda()
-    _, aux, _, ld_aux = gpu_forward(w, A, B, bias, ld=dict(ldd=ldd))
+    _, aux, _, ld_aux = gpu_forward(w, A, B, bias, ld=dict(ldb=ldb, ldd=ldd))
     dY = f16_tensor((rows, ldd), seed + 4, "normal", 2.0).cuda()
     dY_host = dY.cpu()
     L = ge.make_layout(d=ge.GE_D_ROW if dl == "row" else ge.GE_D_COL, ldd=ldd)

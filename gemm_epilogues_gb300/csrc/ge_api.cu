@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -297,6 +298,11 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     // 128 x 256 tiles re-read A half as often; prefer them unless 128-wide
     // tiles fill the machine clearly better.
     tmp.block_n = (Nk <= 128 || e128 > e256 * 1.05) ? 128 : 256;
+    // GE_TILE_N=128|256 overrides the choice (tile-width sweeps).
+    if (const char* env = std::getenv("GE_TILE_N")) {
+      const int want = std::atoi(env);
+      if (want == 128 || want == 256) tmp.block_n = want;
+    }
     const long long tiles = tmp.block_n == 256 ? t256 : t128;
     tmp.grid = static_cast<int>(tiles < tmp.num_sms ? tiles : tmp.num_sms);
     tmp.group_m = static_cast<int>(num_m < 16 ? num_m : 16);

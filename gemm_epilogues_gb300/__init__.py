@@ -57,7 +57,7 @@ EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EP
 ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",
                  "ge_aux_bytes", "ge_aux_ld", "ge_plan_path", "ge_plan_tile_n",
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
-                 "ge_version")
+                 "ge_version", "ge_drelu_bgrad_static")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -110,6 +110,8 @@ def load_library():
         lib.ge_status_string.restype = ctypes.c_char_p
         lib.ge_debug_wait_timeout.argtypes = [vp, i64, vp]
         lib.ge_debug_wait_timeout.restype = i32
+        lib.ge_drelu_bgrad_static.argtypes = [i64, i64, i32, i64, i64, vp, vp, vp, vp, vp]
+        lib.ge_drelu_bgrad_static.restype = i32
         lib.ge_version.argtypes = []
         lib.ge_version.restype = ctypes.c_char_p
         _lib = lib
@@ -201,6 +203,17 @@ def ge_get_last_device_error(plan) -> int:
 
 def ge_debug_wait_timeout(plan, budget_cycles: int, stream=None) -> int:
     return int(load_library().ge_debug_wait_timeout(plan, int(budget_cycles), _stream(stream)))
+
+
+def ge_drelu_bgrad_static(M: int, N: int, d: int, ldd: int, ld_aux: int, dY, aux, dZ, bgrad,
+                          stream=None, *, raw: bool = False):
+    """DRELU_BGRAD with no allocation (scratch in a fixed device array); see
+    include/ge.h for the callers it serves and its size limit."""
+    st = load_library().ge_drelu_bgrad_static(int(M), int(N), int(d), int(ldd), int(ld_aux), _ptr(dY),
+                                              _ptr(aux), _ptr(dZ), _ptr(bgrad), _stream(stream))
+    if raw:
+        return st
+    _check(st, "ge_drelu_bgrad_static")
 
 
 def make_layout(a: int = GE_K_MAJOR, b: int = GE_MN_MAJOR, d: int = GE_D_ROW, lda: int = 0,

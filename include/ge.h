@@ -209,6 +209,44 @@ const char* ge_status_string(ge_status_t s);
 ge_status_t ge_debug_wait_timeout(ge_plan_t plan, int64_t budget_cycles,
                                   void* stream);
 
+/*
+ * ge_drelu_bgrad_static: DRELU_BGRAD that allocates nothing.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: a framework whose caching allocator owns
+ * all of it, a serving loop that must never block on cudaMalloc's implicit
+ * device synchronisation, or a process held to a fixed memory budget where a
+ * new allocation may fail. A plan needs cudaMalloc for its workspace, so this
+ * entry point takes the problem directly and keeps its reduction scratch in
+ * a fixed file-scope device array of GE_STATIC_SCRATCH_BYTES (4 MiB), which
+ * every GPU that loads the library holds until the process exits.
+ *   M, N, d, ldd, ld_aux : as a DRELU_BGRAD plan (K = 0) with layout d
+ *                          (0 for ldd / ld_aux selects the packed default).
+ *   dY, aux, dZ          : fp16 dY, uint32 mask, fp16 dZ (may alias dY),
+ *                          device pointers, 16-byte aligned.
+ *   bgrad                : OUTPUT fp32 [M], 16-byte aligned.
+ *   stream               : cudaStream_t (NULL = legacy default stream).
+ * Results are the same as the plan-based execute (the fp32 reduction may use
+ * fewer row splits when the scratch is short, so bgrad can differ in the
+ * last bits). The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture. Every call shares the array and it keeps
+ * the last call's contents: the call clears the counters it needs on
+ * `stream` itself, and calls that overlap on the GPU race on the scratch, so
+ * order them on one stream. Allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ * Limit: for d == GE_D_COL, ceil(M/256)*4 bytes rounded up to 256 plus M*4
+ * bytes must fit in GE_STATIC_SCRATCH_BYTES (M up to about one million);
+ * larger problems return GE_ERR_UNSUPPORTED. d == GE_D_ROW uses no scratch.
+ * Returns GE_OK, GE_ERR_INVALID_ARG, GE_ERR_ALIGNMENT, GE_ERR_UNSUPPORTED,
+ * GE_ERR_DEVICE_MISMATCH (a pointer that is not memory of the current
+ * device) or GE_ERR_CUDA.
+ */
+#define GE_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+ge_status_t ge_drelu_bgrad_static(int64_t M, int64_t N, ge_dlayout_t d,
+                                  int64_t ldd, int64_t ld_aux, const void* dY,
+                                  const void* aux, void* dZ, void* bgrad,
+                                  void* stream);
+
 /* Library version, "major.minor.patch". */
 const char* ge_version(void);
 

@@ -8,10 +8,15 @@
 // nothing extra because the result never leaves the chip before the bias and
 // activation are applied ("ops-nn's MatMul fusion strategy", first level).
 //
-// One warp owns one weight row at a time and streams it with 16-byte
-// non-allocating loads (8 fp16 per lane, UNROLL slabs in flight); the N
-// activation vectors are small and stay in L1/L2. fp32 accumulation, a
-// butterfly warp reduction, then bias + activation + fp16 rounding per output.
+// Streaming kernel (N <= 4, K <= 8192): one CTA per SM owns a contiguous
+// share of the weight rows; one producer lane keeps a shared-memory ring of
+// whole rows full with 1-D bulk copies (TMA), so about 200 KB per SM are in
+// flight from the start; eight consumer warps take rows in turn, read them
+// from shared memory with 16-byte loads, read the activations through L1,
+// accumulate in fp32, reduce across the warp and apply bias + activation +
+// fp16 rounding. Every wait is bounded (error word, then drain and exit).
+// Other shapes use the register kernel below: one warp per row, 16-byte
+// non-allocating global loads, UNROLL slabs in flight.
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
@@ -97,6 +102,147 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   }
 }
 
+constexpr int GV_WARPS = 8;                    // consumer warps
+constexpr int GV_THREADS = 32 * (GV_WARPS + 1);  // + one producer warp
+constexpr int GV_RING_BYTES = 200 * 1024;
+
+__device__ __forceinline__ float gemv_act(int epi, float z) {
+  if (epi == EPI_RELU_BIAS) return fmaxf(z, 0.0f);
+  if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  return z;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(GV_THREADS, 1)
+    gemv_stream_kernel(const GemvArgs p, int slots, uint32_t slot_bytes, uint32_t copy_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // [full[slots] | empty[slots] | abort, never] then the ring (128-byte aligned)
+  const uint32_t bar0 = smem_u32(smem);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (slots + s); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * slots);
+  volatile int* never = abort_flag + 1;
+  const uint32_t ring_off = (16u * slots + 8u + 127u) & ~127u;
+  uint8_t* ring = smem + ring_off;
+
+  // Contiguous, balanced share of rows for this CTA.
+  const long long per = p.M / gridDim.x;
+  const long long extra = p.M % gridDim.x;
+  const long long r0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), extra);
+  const long long nr = per + (static_cast<long long>(blockIdx.x) < extra ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < slots; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == GV_WARPS) {
+    if (lane == 0) {
+      long long issued = 0;
+      for (long long j = 0; j < nr; ++j) {
+        const int s = static_cast<int>(j % slots);
+        const uint32_t ph = static_cast<uint32_t>((j / slots) & 1);
+        if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, p.budget)) {
+          if (!*abort_flag) atomicOr(p.err, ERR_GEMV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(s), copy_bytes);
+        bulk_load_1d(smem_u32(ring + static_cast<size_t>(s) * slot_bytes), p.A + (r0 + j) * p.lda,
+                     copy_bytes, full_bar(s));
+        ++issued;
+      }
+      // Drain: every issued copy lands before the CTA may exit.
+      for (long long j = issued - slots > 0 ? issued - slots : 0; j < issued; ++j) {
+        const int s = static_cast<int>(j % slots);
+        if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>((j / slots) & 1), never, p.budget))
+          atomicOr(p.err, ERR_GEMV_TIMEOUT);
+      }
+    }
+  } else {
+    const int K8 = p.K & ~7;
+    for (long long j = warp; j < nr; j += GV_WARPS) {
+      const int s = static_cast<int>(j % slots);
+      const uint32_t ph = static_cast<uint32_t>((j / slots) & 1);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(full_bar(s), ph, abort_flag, p.budget) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          if (!*abort_flag) atomicOr(p.err, ERR_GEMV_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const __half* row = reinterpret_cast<const __half*>(ring + static_cast<size_t>(s) * slot_bytes);
+      float acc[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) acc[n] = 0.0f;
+#pragma unroll 4
+      for (int k = lane * 8; k < K8; k += 256) {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + k);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+          if (n < p.N) acc[n] = dot8(a, __ldg(reinterpret_cast<const uint4*>(p.B + n * p.ldb + k)), acc[n]);
+      }
+      for (int kk = K8 + lane; kk < p.K; kk += 32) {
+        const float av = __half2float(row[kk]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+          if (n < p.N) acc[n] = fmaf(av, __half2float(p.B[n * p.ldb + kk]), acc[n]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));  // the row is in registers now
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], off);
+      }
+      float z = 0.0f;
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+        if (n == lane) z = acc[n];
+      if (lane < p.N) {
+        const long long m = r0 + j;
+        if (p.epi != EPI_NONE) z += __half2float(p.bias[m]);
+        p.D[m * p.ldd_m + static_cast<long long>(lane) * p.ldd_n] = __float2half_rn(gemv_act(p.epi, z));
+      }
+    }
+  }
+}
+
+template <int NT>
+cudaError_t launch_stream(const GemvArgs& a, int num_sms, cudaStream_t s) {
+  const uint32_t copy_bytes = static_cast<uint32_t>(a.K) * 2u;  // K % 8 == 0: 16-byte multiple
+  const uint32_t slot_bytes = (copy_bytes + 127u) & ~127u;
+  const int grid = static_cast<int>(a.M < num_sms ? a.M : num_sms);
+  const long long rows_max = (a.M + grid - 1) / grid;
+  int slots = static_cast<int>(GV_RING_BYTES / slot_bytes);
+  if (slots > rows_max) slots = static_cast<int>(rows_max);
+  if (slots < 1) slots = 1;
+  const size_t smem = ((16u * slots + 8u + 127u) & ~127u) + static_cast<size_t>(slots) * slot_bytes;
+  static bool configured[64] = {};  // the attribute is set once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(gemv_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GV_RING_BYTES + 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  gemv_stream_kernel<NT><<<grid, GV_THREADS, smem, s>>>(a, slots, slot_bytes, copy_bytes);
+  return cudaGetLastError();
+}
+
 template <int NT, int UNROLL>
 cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
   constexpr int threads = 256;
@@ -111,6 +257,15 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
+  // The streaming kernel wants whole rows in the ring (K <= 8192), rows that
+  // are a whole number of 16-byte chunks (K % 8 == 0) starting on 16-byte
+  // boundaries (the planner checks lda % 8 == 0 and A's alignment), and
+  // activations small enough to stay in L1 (N <= 4).
+  if (a.K <= 8192 && a.K % 8 == 0 && a.N <= 4 && a.M >= 1) {
+    if (a.N <= 1) return launch_stream<1>(a, num_sms, s);
+    if (a.N <= 2) return launch_stream<2>(a, num_sms, s);
+    return launch_stream<4>(a, num_sms, s);
+  }
   if (a.N <= 1) return launch_nt<1, 8>(a, num_sms, s);
   if (a.N <= 2) return launch_nt<2, 8>(a, num_sms, s);
   if (a.N <= 4) return launch_nt<4, 4>(a, num_sms, s);

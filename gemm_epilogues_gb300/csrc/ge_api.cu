@@ -34,6 +34,7 @@ struct Plan {
   // tensor-core path: kernel-level problem after folding a column-major D
   bool swap = false;
   int block_n = 256;
+  int pair = 0;  // 2-CTA (cta_group::2) tiles of 256 rows
   int grid = 0;
   int group_m = 16;
   // stored D: R rows x C contiguous
@@ -127,7 +128,8 @@ ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D) {
   else
     ok &= make_map(&pl->tmA, Ak, Mk, K, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!b_mn)
-    ok &= make_map(&pl->tmB, Bk, K, Nk, ldb, 64, pl->block_n, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&pl->tmB, Bk, K, Nk, ldb, 64, pl->pair ? pl->block_n / 2 : pl->block_n,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
   else
     ok &= make_map(&pl->tmB, Bk, Nk, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= make_map(&pl->tmD, D, Nk, Mk, L.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -180,7 +182,7 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.err = pl->err;
     g.group_m = pl->group_m;
     g.budget = kWaitBudgetCycles;
-    e = launch_tc_gemm(pl->block_n, pl->tmA, pl->tmB, pl->tmD, g, pl->grid, st);
+    e = launch_tc_gemm(pl->block_n, pl->pair, pl->tmA, pl->tmB, pl->tmD, g, pl->grid, st);
   }
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
@@ -301,9 +303,24 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       const int want = std::atoi(env);
       if (want == 128 || want == 256) tmp.block_n = want;
     }
-    const long long tiles = tmp.block_n == 256 ? t256 : t128;
-    tmp.grid = static_cast<int>(tiles < tmp.num_sms ? tiles : tmp.num_sms);
-    tmp.group_m = static_cast<int>(num_m < 16 ? num_m : 16);
+    // 2-CTA pairs (256-row tiles) once there are enough of them to give
+    // every pair of SMs at least one tile.
+    const long long num_m2 = (Mk + 255) / 256;
+    const long long pair_tiles = num_m2 * ((Nk + tmp.block_n - 1) / tmp.block_n);
+    tmp.pair = (tmp.block_n == 256 && pair_tiles * 2 >= tmp.num_sms) ? 1 : 0;
+    if (const char* env = std::getenv("GE_PAIR")) {
+      if (env[0] == '0') tmp.pair = 0;
+      if (env[0] == '1') tmp.pair = 1;
+    }
+    if (tmp.pair) {
+      const long long pairs = tc_gemm_max_pairs(tmp.block_n, tmp.num_sms);
+      tmp.grid = static_cast<int>(2 * (pair_tiles < pairs ? pair_tiles : pairs));
+      tmp.group_m = static_cast<int>(num_m2 < 8 ? num_m2 : 8);
+    } else {
+      const long long tiles = tmp.block_n == 256 ? t256 : t128;
+      tmp.grid = static_cast<int>(tiles < tmp.num_sms ? tiles : tmp.num_sms);
+      tmp.group_m = static_cast<int>(num_m < 16 ? num_m : 16);
+    }
   }
   size_t ws = 256;
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {

@@ -22,6 +22,12 @@
 //               mask word, round to fp16, stage in 64-byte-swizzled shared
 //               memory and TMA-store it; runs while the MMA warp already
 //               accumulates the next tile into the other TMEM buffer.
+// Pair mode (PAIR = true, clusters of 2 CTAs on 2 SMs): the tile is 256 x BN;
+// each CTA stages its own 128 rows of A and its own half of B's BN columns,
+// the even CTA issues tcgen05.mma.cta_group::2 (M = 256) which reads both
+// CTAs' shared memory and writes both CTAs' TMEM, and every commit is
+// multicast to both CTAs. Per SM this moves a third less shared-memory
+// traffic per flop than the single-CTA 128 x BN tile.
 // Every wait is bounded; an expired wait records a bit in the error word,
 // raises a CTA-wide abort flag, and every role drains its in-flight copies
 // before the CTA frees TMEM and exits.
@@ -37,12 +43,13 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 fp16 columns
 
-template <int BN>
+template <int BN, bool PAIR>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns staged by one CTA
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
   static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
@@ -50,6 +57,8 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB for base alignment
   static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+  static constexpr int EPI_ARRIVALS = PAIR ? 2 * EPI_WARPS : EPI_WARPS;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "SW128 atoms need 1 KB alignment");
 };
@@ -108,11 +117,11 @@ __device__ __forceinline__ uint32_t epilogue_dispatch(int epi, const uint32_t (&
   }
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -129,6 +138,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // CTA within the pair
+  const bool leader = rank == 0;                         // issues the pair's MMAs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -137,7 +148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), EPI_WARPS);
+      mbar_init(tempty_bar(b), C::EPI_ARRIVALS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -150,18 +161,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // the peer's barriers exist before anything targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_m = (p.Mk + BM - 1) / BM;
+  const int num_m = (p.Mk + C::TILE_M - 1) / C::TILE_M;
   const int num_n = (p.Nk + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int num_kb = (p.K + BK - 1) / BK;
+  const int first_tile = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  bool aborted_here = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -170,9 +192,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       long long fills = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
         int mt, nt;
         tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
+        const int row0 = mt * C::TILE_M + static_cast<int>(rank) * BM;     // this CTA's A rows
+        const int col0 = nt * BN + static_cast<int>(rank) * C::B_ROWS;     // this CTA's B columns
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.budget)) {
             if (!*abort_flag) atomicOr(p.err, ERR_PRODUCER_TIMEOUT);
@@ -180,22 +204,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          uint32_t fb = full_bar(stage);
+          if (!PAIR || leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * C::STAGE_BYTES);
+          if constexpr (PAIR) fb = mapa_shared(fb, 0);  // completion counted by the leader
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * BK;
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+            if constexpr (PAIR)
+              tma_load_2d_pair(dst, map, fb, x, y);
+            else
+              tma_load_2d(dst, map, fb, x, y);
+          };
           if (!p.a_mn) {
-            tma_load_2d(sa, &tmA, fb, k0, mt * BM);
+            load(sa, &tmA, k0, row0);
           } else {
-            tma_load_2d(sa, &tmA, fb, mt * BM, k0);
-            tma_load_2d(sa + 8192, &tmA, fb, mt * BM + 64, k0);
+            load(sa, &tmA, row0, k0);
+            load(sa + 8192, &tmA, row0 + 64, k0);
           }
           if (!p.b_mn) {
-            tma_load_2d(sb, &tmB, fb, k0, nt * BN);
+            load(sb, &tmB, k0, col0);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, nt * BN + 64 * j, k0);
+            for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + 8192 * j, &tmB, col0 + 64 * j, k0);
           }
           ++fills;
           if (++stage == C::STAGES) {
@@ -205,24 +236,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       // Drain: every issued load must land before the CTA may exit.
-      for (int s = 0; s < C::STAGES; ++s) {
-        if (fills > s) {
-          const long long last = s + (long long)C::STAGES * ((fills - 1 - s) / C::STAGES);
-          const uint32_t par = static_cast<uint32_t>((last / C::STAGES) & 1);
-          if (!mbar_wait_bounded(full_bar(s), par, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
+      if (!PAIR || leader) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (fills > s) {
+            const long long last = s + (long long)C::STAGES * ((fills - 1 - s) / C::STAGES);
+            const uint32_t par = static_cast<uint32_t>((last / C::STAGES) & 1);
+            if (!mbar_wait_bounded(full_bar(s), par, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
+          }
+        }
+      } else if (!ok) {
+        // The odd CTA's loads are counted on the leader's barriers; after an
+        // abort give any copy still in flight time to land (~50 us).
+        const long long t0 = clock64();
+        while (clock64() - t0 < 100000LL) {
         }
       }
+      aborted_here = !ok;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || leader)) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_f16_f32(BM, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc = idesc_f16_f32(C::TILE_M, BN, p.a_mn, p.b_mn);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.budget)) {
           if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
           *abort_flag = 1;
@@ -248,21 +288,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                        : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
             const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
                                        : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (PAIR)
+              tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));  // frees the stage once these MMAs retire
+          // frees the stage (in both CTAs of a pair) once these MMAs retire
+          if constexpr (PAIR)
+            tc_commit_pair_mc(empty_bar(stage), 0x3);
+          else
+            tc_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if constexpr (PAIR)
+          tc_commit_pair_mc(tfull_bar(acc), 0x3);
+        else
+          tc_commit(tfull_bar(acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // Drain: all MMAs issued by this thread retire before TMEM is freed.
-      tc_commit(drain_bar);
+      if constexpr (PAIR)
+        tc_commit_pair_mc(drain_bar, 0x1);
+      else
+        tc_commit(drain_bar);
       if (!mbar_wait_bounded(drain_bar, 0u, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
     }
   } else {
@@ -274,7 +328,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int tile = first_tile; tile < num_tiles; tile += tile_step) {
       int mt, nt;
       tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
       int ok = 1;
@@ -288,7 +342,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int grow = mt * BM + q * 32 + lane;  // this thread's row of D'
+      const int rbase = mt * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // warp's first row of D'
+      const int grow = rbase + lane;                                          // this thread's row
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = __half2float(p.bias[grow]);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -340,16 +395,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (grow < p.Mk) {
             __half* drow = p.D + static_cast<long long>(grow) * p.ldd + gcol0;
             const int nvalid = p.Nk - gcol0;
-            for (int j = 0; j < nvalid; ++j) {
-              const uint32_t w = packed[j >> 1];
-              drow[j] = __ushort_as_half(static_cast<unsigned short>((j & 1) ? (w >> 16) : (w & 0xFFFFu)));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {  // static indices keep packed[] in registers
+              if (j < nvalid) {
+                const uint32_t w = packed[j >> 1];
+                drow[j] = __ushort_as_half(static_cast<unsigned short>((j & 1) ? (w >> 16) : (w & 0xFFFFu)));
+              }
             }
           }
-        } else {
+        } else if (rbase < p.Mk) {
           // Stage the 32x32 fp16 slab (64-byte swizzle: 16-byte chunk j of row
-          // r sits at chunk j ^ ((r >> 1) & 3)) and TMA-store it.
-          // Buffers alternate per issued store, so the newest store in
-          // flight always reads the other buffer than the one written now.
+          // r sits at chunk j ^ ((r >> 1) & 3)) and TMA-store it. Buffers
+          // alternate per issued store, so the newest store in flight always
+          // reads the other buffer than the one written now.
           uint8_t* buf = stg + (nstore & 1) * EPI_BUF_BYTES;
           if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
           __syncwarp();
@@ -362,7 +420,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmD, smem_u32(buf), gcol0, mt * BM + q * 32);
+            tma_store_2d(&tmD, smem_u32(buf), gcol0, rbase);
             bulk_commit_group();
           }
           ++nstore;
@@ -374,24 +432,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        // this warp's share of the accumulator is free (the pair's MMA
+        // issuer counts the arrivals of both CTAs' epilogue warps)
+        if (PAIR && !leader)
+          mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
   }
+  (void)aborted_here;
 
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // neither CTA leaves while its peer may still touch it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const GemmArgs& args, int grid, cudaStream_t stream) {
   static bool configured[64] = {};  // the attribute is set once per device
@@ -399,26 +471,86 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<BN>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<BN, PAIR>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    if constexpr (PAIR) {
+      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      cudaGetLastError();
+    }
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  tc_gemm_kernel<BN><<<grid, NUM_THREADS, Cfg<BN>::SMEM_BYTES, stream>>>(tmA, tmB, tmD, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, PAIR>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if constexpr (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, tmA, tmB, tmD, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Largest number of 2-CTA clusters of the pair kernel that can be resident.
+template <int BN>
+int max_pairs(int num_sms) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return num_sms / 2;
+  }
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  cudaFuncSetAttribute(tc_gemm_kernel<BN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       Cfg<BN, true>::SMEM_BYTES);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, true>::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
 }
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes(int block_n) {
-  return block_n == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES;
+size_t tc_gemm_smem_bytes(int block_n, int pair) {
+  if (pair) return block_n == 256 ? Cfg<256, true>::SMEM_BYTES : Cfg<128, true>::SMEM_BYTES;
+  return block_n == 256 ? Cfg<256, false>::SMEM_BYTES : Cfg<128, false>::SMEM_BYTES;
 }
 
-cudaError_t launch_tc_gemm(int block_n, const CUtensorMap& tmA, const CUtensorMap& tmB,
+int tc_gemm_max_pairs(int block_n, int num_sms) {
+  return block_n == 256 ? max_pairs<256>(num_sms) : max_pairs<128>(num_sms);
+}
+
+cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, int grid,
                            cudaStream_t stream) {
-  if (block_n == 256) return launch_impl<256>(tmA, tmB, tmD, args, grid, stream);
-  return launch_impl<128>(tmA, tmB, tmD, args, grid, stream);
+  if (pair) {
+    if (block_n == 256) return launch_impl<256, true>(tmA, tmB, tmD, args, grid, stream);
+    return launch_impl<128, true>(tmA, tmB, tmD, args, grid, stream);
+  }
+  if (block_n == 256) return launch_impl<256, false>(tmA, tmB, tmD, args, grid, stream);
+  return launch_impl<128, false>(tmA, tmB, tmD, args, grid, stream);
 }
 
 }  // namespace ge

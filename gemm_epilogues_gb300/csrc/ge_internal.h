@@ -48,8 +48,11 @@ struct GemmArgs {
   long long budget;  // bounded-wait budget in SM clock cycles
 };
 
-size_t tc_gemm_smem_bytes(int block_n);
-cudaError_t launch_tc_gemm(int block_n, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs
+// (even) and the B tensor map's box is BN/2 rows (K-major B).
+size_t tc_gemm_smem_bytes(int block_n, int pair);
+int tc_gemm_max_pairs(int block_n, int num_sms);
+cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, int grid,
                            cudaStream_t stream);
 

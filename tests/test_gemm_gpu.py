@@ -161,3 +161,25 @@ def test_execute_rejects_bad_buffers():
         assert ge.ge_execute(p.handle, host, B, bias, D, aux, raw=True) == ge.GE_ERR_DEVICE_MISMATCH
         assert ge.ge_execute(p.handle, A, B, bias, D, aux, raw=True) == ge.GE_OK
         torch.cuda.synchronize()
+
+
+PAIR_SHAPES = [(300, 520, 200), (257, 129, 4100), (700, 900, 328), (1000, 2056, 96), (513, 264, 64)]
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+@pytest.mark.parametrize("am,bm,dl", [("k", "n", "row"), ("k", "k", "col"), ("m", "n", "row"),
+                                      ("m", "k", "col")])
+def test_pair_tiles_ragged(oracle, monkeypatch, M, N, K, am, bm, dl):
+    """2-CTA (256-row) tiles forced on: ragged edges, every operand major."""
+    monkeypatch.setenv("GE_PAIR", "1")
+    monkeypatch.setenv("GE_TILE_N", "256")
+    epi = EPIS[(M + N + K) % len(EPIS)]
+    _run_case(oracle, M, N, K, epi, am, bm, dl, seed=20)
+
+
+@pytest.mark.parametrize("epi", ["none", "bias", "relu_aux_bias"])
+def test_pair_tiles_exact_integer(oracle, monkeypatch, epi):
+    monkeypatch.setenv("GE_PAIR", "1")
+    monkeypatch.setenv("GE_TILE_N", "256")
+    _run_case(oracle, 520, 776, 128, epi, "k", "n", "row", dist=("int", 2.0), seed=21, exact=True)
+    _run_case(oracle, 520, 776, 128, epi, "m", "k", "col", dist=("int", 2.0), seed=22, exact=True)

@@ -36,6 +36,17 @@ WORKLOAD = ("LLaMA-7B-like MLP training step (fwd RELU_AUX_BIAS 11008x8192x4096 
             "dY[8192,11008] + dW 11008x4096x8192) + decode GEMV GELU_BIAS 4096x1x4096")
 
 
+# Timing-only cases for the other workload configs: key -> (workload key, unfused?)
+CONFIG_CASES = {
+    "cfg_c1": ("c1", False), "cfg_c2_bias": ("c2_bias", False),
+    "cfg_c2_relu_bias": ("c2_relu_bias", False), "cfg_c2_gelu_bias": ("c2_gelu_bias", False),
+    "cfg_c2_gelu_bias_unfused": ("c2_gelu_bias", True),
+    "cfg_c3_T512": ("c3_T512", False), "cfg_c3_T512_unfused": ("c3_T512", True),
+    "cfg_c3_T2048": ("c3_T2048", False), "cfg_c3_T2048_unfused": ("c3_T2048", True),
+    "cfg_c5": ("c5", False), "cfg_c5_unfused": ("c5", True),
+}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -138,6 +149,9 @@ def barrier(world: int):
 
 # ----------------------------------------------------------------- CPU side
 
+_ORACLE_INPUTS = {}
+
+
 def oracle_sample_rate(rows: int = 256, threads: int | None = None):
     """The oracle (fp64 CPU) on a bounded sample of the forward GEMM: `rows`
     tokens of X against the whole W. Returns (TFLOP/s, seconds, threads)."""
@@ -147,12 +161,14 @@ def oracle_sample_rate(rows: int = 256, threads: int | None = None):
     from oracle import oracle
     oracle.build()
     threads = threads or os.cpu_count() or 1
-    W = f16_tensor((D_OUT, D_IN), 3001, "normal", 1 / 64)
-    X = f16_tensor((rows, D_IN), 3002)
-    b = f16_tensor((D_OUT,), 3003, "normal", math.sqrt(0.02))
     bits = lambda t: t.view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    if rows not in _ORACLE_INPUTS:  # generated once, outside the timed call
+        _ORACLE_INPUTS[rows] = (bits(f16_tensor((D_OUT, D_IN), 3001, "normal", 1 / 64)),
+                                bits(f16_tensor((rows, D_IN), 3002)),
+                                bits(f16_tensor((D_OUT,), 3003, "normal", math.sqrt(0.02))))
+    W, X, b = _ORACLE_INPUTS[rows]
     t0 = time.perf_counter()
-    oracle.linear_forward(bits(W), bits(X), bits(b), "relu_aux_bias", D_OUT, rows, D_IN,
+    oracle.linear_forward(W, X, b, "relu_aux_bias", D_OUT, rows, D_IN,
                           a_major="k", b_major="k", d_layout="col", threads=threads)
     dt = time.perf_counter() - t0
     flops = 2.0 * D_OUT * rows * D_IN
@@ -189,6 +205,50 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------- GPU side
+
+def run_config(args, rank):
+    """Time one workload config (fused or the unfused three-kernel sequence):
+    `steps` launches after `warmup`, each after a read-only L2 flush."""
+    import torch
+    import gemm_epilogues_gb300 as ge
+    from gemm_epilogues_gb300.inputs import pages_workloads
+    key, unfused = CONFIG_CASES[args.case]
+    w = pages_workloads()[key]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    A, B, bias = w.make(dev)
+    major = {"k": ge.GE_K_MAJOR, "m": ge.GE_MN_MAJOR, "n": ge.GE_MN_MAJOR}
+    L = ge.make_layout(major[w.a_major], major[w.b_major], ge.GE_D_ROW if w.d_layout == "row" else ge.GE_D_COL)
+    plan = ge.Plan(w.M, w.N, w.K, ge.EPILOGUE_BY_NAME[w.epilogue], L)
+    D = torch.empty(w.d_shape(), dtype=torch.float16, device=dev)
+    aux = torch.empty(max(plan.aux_bytes // 4, 1), dtype=torch.int32, device=dev)
+    bias_arg = bias if w.epilogue != "none" else None
+    aux_arg = aux if w.epilogue == "relu_aux_bias" else None
+    flush_buf = torch.ones((256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    run = plan.execute_unfused if unfused else plan.execute
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.sum(flush_buf, dim=0, out=flush_out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(A, B, bias_arg, D, aux_arg, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
+    ms = sum(times) / len(times)
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    line = {"case": args.case, "workload": w.name, "unfused": unfused, "path": plan.path,
+            "tile_n": plan.tile_n, "ms": ms, "min_ms": min(times), "tflops": tflops,
+            "frac_of_peak": tflops / peaks["tflops"],
+            "gbs_algorithmic": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}
+    plan.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
 
 def run_ours(args, world, rank, local):
     import torch
@@ -259,6 +319,7 @@ def run_ours(args, world, rank, local):
         # Profiling mode: only one kernel of the step, `steps` times after
         # `warmup` launches (each launch preceded by the L2 flush).
         one = {"fwd": lambda: fwd.execute(W, X, b, Y, aux, stream),
+               "fwd_unfused": lambda: fwd.execute_unfused(W, X, b, Y, aux, stream),
                "bwd": lambda: bwd.execute(dY, None, bgrad, dZ, aux, stream),
                "dw": lambda: dwp.execute(dZ, X, None, dW, None, stream),
                "gemv": lambda: dec.execute(W2, x1, b2, y1, None, stream)}[args.case]
@@ -342,6 +403,45 @@ def run_ours(args, world, rank, local):
                 "unit": "TFLOP/s", "frac": achieved / peaks["tflops"], "traffic": None,
                 "peak_source": f"{peaks['source']} bf16 burst (fp16 tensor rate = bf16)"}
 
+    # ---- baselines and the back-to-back decode measurement (outside the step)
+    # (1) the unfused three-kernel sequence on the forward's inputs
+    ut = []
+    for i in range(8):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fwd.execute_unfused(W, X, b, Y, aux, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            ut.append(e0.elapsed_time(e1))
+    fwd.execute(W, X, b, Y, aux, stream)  # leave the fused result in Y
+    unf_ms = sum(ut) / len(ut)
+    kern["fwd_unfused_baseline"] = {"ms": unf_ms, "tflops": flops_gemm / unf_ms / 1e9,
+                                    "frac_of_peak": flops_gemm / unf_ms / 1e9 / peaks["tflops"],
+                                    "fused_speedup": unf_ms / kern["fwd_gemm_relu_aux_bias"]["ms"]}
+    # (2) decode GEMV launched back to back over 8 weight copies (268 MB, more
+    # than L2), the pattern of a decode step through several layers
+    W2s = [W2] + [f16_tensor((D_DEC, D_DEC), 2100 + i, "normal", 1 / 64, dev) for i in range(7)]
+    for Wi in W2s:
+        dec.execute(Wi, x1, b2, y1, None, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rounds = 6
+    e0.record(stream)
+    for _ in range(rounds):
+        for Wi in W2s:
+            dec.execute(Wi, x1, b2, y1, None, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    b2b_ms = e0.elapsed_time(e1) / (rounds * len(W2s))
+    kern["decode_gemv_back_to_back"] = {"ms": b2b_ms, "gbs": bytes_dec / b2b_ms / 1e6,
+                                        "frac_of_peak": bytes_dec / b2b_ms / 1e6 / peaks["hbm_gbs"],
+                                        "launches": rounds * len(W2s), "weights": "8 x 33.5 MB rotating"}
+    del W2s
+    assert ge.ge_get_last_device_error(dec.handle) == ge.GE_OK
+    assert ge.ge_get_last_device_error(fwd.handle) == ge.GE_OK
+
     # ---- end to end through the public API: host buffers, copies timed
     Xh = X.cpu().pin_memory()
     dYh = dY.cpu().pin_memory()
@@ -384,9 +484,10 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rate, dt, thr = oracle_sample_rate(256)
+        rows = 4096
+        rate, dt, thr = oracle_sample_rate(rows)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-               "sample": f"forward GEMM on 256 of {T_TOK} tokens (all 11008 outputs, K=4096), "
+               "sample": f"forward GEMM on {rows} of {T_TOK} tokens (all 11008 outputs, K=4096), "
                          f"{dt:.1f} s wall"}
 
     if rank == 0:
@@ -414,13 +515,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="step", choices=["step", "fwd", "bwd", "dw", "gemv"],
-                    help="profiling mode: time one kernel of the step alone")
+    ap.add_argument("--case", default="step",
+                    choices=["step", "fwd", "bwd", "dw", "gemv", "fwd_unfused"] + sorted(CONFIG_CASES),
+                    help="time one kernel of the step alone, or one of the workload configs")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.case in CONFIG_CASES:
+            run_config(args, rank)
         else:
             run_ours(args, world, rank, local)
     finally:

@@ -9,12 +9,13 @@
 // activation are applied ("ops-nn's MatMul fusion strategy", first level).
 //
 // Streaming kernel (N <= 4, K <= 8192): one CTA per SM owns a contiguous
-// share of the weight rows; one producer lane keeps a shared-memory ring of
-// whole rows full with 1-D bulk copies (TMA), so about 200 KB per SM are in
-// flight from the start; eight consumer warps take rows in turn, read them
-// from shared memory with 16-byte loads, read the activations through L1,
-// accumulate in fp32, reduce across the warp and apply bias + activation +
-// fp16 rounding. Every wait is bounded (error word, then drain and exit).
+// share of the weight rows; one producer lane first bulk-copies the N
+// activation vectors into shared memory, then keeps a shared-memory ring of
+// whole weight rows full with 1-D bulk copies (TMA), so about 200 KB per SM
+// are in flight from the start; eight consumer warps take rows in turn, read
+// rows and activations from shared memory with 16-byte loads, accumulate in
+// fp32, reduce across the warp and apply bias + activation + fp16 rounding.
+// Every wait is bounded (error word, then drain and exit).
 // Other shapes use the register kernel below: one warp per row, 16-byte
 // non-allocating global loads, UNROLL slabs in flight.
 #include "ge_internal.h"
@@ -114,18 +115,23 @@ __device__ __forceinline__ float gemv_act(int epi, float z) {
 
 template <int NT>
 __global__ void __launch_bounds__(GV_THREADS, 1)
-    gemv_stream_kernel(const GemvArgs p, int slots, uint32_t slot_bytes, uint32_t copy_bytes) {
+    gemv_stream_kernel(const GemvArgs p, int slots, uint32_t slot_bytes, uint32_t x_stride_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // [full[slots] | empty[slots] | abort, never] then the ring (128-byte aligned)
+  // [full[slots] | empty[slots] | xbar | abort, never] [x: N rows of K fp16]
+  // [ring of weight rows]; x and the ring start on 128-byte boundaries.
   const uint32_t bar0 = smem_u32(smem);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (slots + s); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * slots);
+  const uint32_t x_bar = bar0 + 16u * slots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * slots + 8);
   volatile int* never = abort_flag + 1;
-  const uint32_t ring_off = (16u * slots + 8u + 127u) & ~127u;
-  uint8_t* ring = smem + ring_off;
+  const uint32_t x_off = (16u * slots + 16u + 127u) & ~127u;
+  const __half* xs = reinterpret_cast<const __half*>(smem + x_off);
+  uint8_t* ring = smem + x_off + static_cast<uint32_t>(p.N) * x_stride_bytes;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.K) * 2u;  // K % 8 == 0
+  const int x_stride = static_cast<int>(x_stride_bytes / 2);
 
   // Contiguous, balanced share of rows for this CTA.
   const long long per = p.M / gridDim.x;
@@ -138,6 +144,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
+    mbar_init(x_bar, 1);
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
@@ -146,6 +153,11 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
 
   if (warp == GV_WARPS) {
     if (lane == 0) {
+      // the activations first (N contiguous K-vectors), then the weight rows
+      mbar_arrive_expect_tx(x_bar, static_cast<uint32_t>(p.N) * row_bytes);
+      for (int n = 0; n < p.N; ++n)
+        bulk_load_1d(smem_u32(smem + x_off) + static_cast<uint32_t>(n) * x_stride_bytes,
+                     p.B + n * p.ldb, row_bytes, x_bar);
       long long issued = 0;
       for (long long j = 0; j < nr; ++j) {
         const int s = static_cast<int>(j % slots);
@@ -155,12 +167,13 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(full_bar(s), copy_bytes);
+        mbar_arrive_expect_tx(full_bar(s), row_bytes);
         bulk_load_1d(smem_u32(ring + static_cast<size_t>(s) * slot_bytes), p.A + (r0 + j) * p.lda,
-                     copy_bytes, full_bar(s));
+                     row_bytes, full_bar(s));
         ++issued;
       }
       // Drain: every issued copy lands before the CTA may exit.
+      if (!mbar_wait_bounded(x_bar, 0u, never, p.budget)) atomicOr(p.err, ERR_GEMV_TIMEOUT);
       for (long long j = issued - slots > 0 ? issued - slots : 0; j < issued; ++j) {
         const int s = static_cast<int>(j % slots);
         if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>((j / slots) & 1), never, p.budget))
@@ -168,11 +181,16 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
       }
     }
   } else {
-    const int K8 = p.K & ~7;
-    for (long long j = warp; j < nr; j += GV_WARPS) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(x_bar, 0u, abort_flag, p.budget) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) {
+      if (!*abort_flag) atomicOr(p.err, ERR_GEMV_TIMEOUT);
+      *abort_flag = 1;
+    }
+    for (long long j = warp; ok && j < nr; j += GV_WARPS) {
       const int s = static_cast<int>(j % slots);
       const uint32_t ph = static_cast<uint32_t>((j / slots) & 1);
-      int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(full_bar(s), ph, abort_flag, p.budget) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -187,17 +205,11 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
 #pragma unroll
       for (int n = 0; n < NT; ++n) acc[n] = 0.0f;
 #pragma unroll 4
-      for (int k = lane * 8; k < K8; k += 256) {
+      for (int k = lane * 8; k < p.K; k += 256) {
         const uint4 a = *reinterpret_cast<const uint4*>(row + k);
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-          if (n < p.N) acc[n] = dot8(a, __ldg(reinterpret_cast<const uint4*>(p.B + n * p.ldb + k)), acc[n]);
-      }
-      for (int kk = K8 + lane; kk < p.K; kk += 32) {
-        const float av = __half2float(row[kk]);
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-          if (n < p.N) acc[n] = fmaf(av, __half2float(p.B[n * p.ldb + kk]), acc[n]);
+          if (n < p.N) acc[n] = dot8(a, *reinterpret_cast<const uint4*>(xs + n * x_stride + k), acc[n]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(s));  // the row is in registers now
@@ -221,14 +233,16 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
 
 template <int NT>
 cudaError_t launch_stream(const GemvArgs& a, int num_sms, cudaStream_t s) {
-  const uint32_t copy_bytes = static_cast<uint32_t>(a.K) * 2u;  // K % 8 == 0: 16-byte multiple
-  const uint32_t slot_bytes = (copy_bytes + 127u) & ~127u;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
+  const uint32_t slot_bytes = (row_bytes + 127u) & ~127u;
+  const uint32_t x_stride_bytes = slot_bytes;
   const int grid = static_cast<int>(a.M < num_sms ? a.M : num_sms);
   const long long rows_max = (a.M + grid - 1) / grid;
-  int slots = static_cast<int>(GV_RING_BYTES / slot_bytes);
+  const uint32_t x_bytes = static_cast<uint32_t>(a.N) * x_stride_bytes;
+  int slots = static_cast<int>((GV_RING_BYTES - x_bytes) / slot_bytes);
   if (slots > rows_max) slots = static_cast<int>(rows_max);
   if (slots < 1) slots = 1;
-  const size_t smem = ((16u * slots + 8u + 127u) & ~127u) + static_cast<size_t>(slots) * slot_bytes;
+  const size_t smem = ((16u * slots + 16u + 127u) & ~127u) + x_bytes + static_cast<size_t>(slots) * slot_bytes;
   static bool configured[64] = {};  // the attribute is set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -239,7 +253,7 @@ cudaError_t launch_stream(const GemvArgs& a, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  gemv_stream_kernel<NT><<<grid, GV_THREADS, smem, s>>>(a, slots, slot_bytes, copy_bytes);
+  gemv_stream_kernel<NT><<<grid, GV_THREADS, smem, s>>>(a, slots, slot_bytes, x_stride_bytes);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,8 @@ struct Plan {
   bool swap = false;
   int block_n = 256;
   int pair = 0;  // 2-CTA (cta_group::2) tiles of 256 rows
+  int tail_start = 0;  // split-K tail (see GemmArgs); `partials` holds its pieces
+  int split = 1;
   int grid = 0;
   int group_m = 16;
   // stored D: R rows x C contiguous
@@ -182,7 +184,11 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.err = pl->err;
     g.group_m = pl->group_m;
     g.budget = kWaitBudgetCycles;
+    g.tail_start = pl->tail_start;
+    g.split = pl->split;
+    g.partials = pl->partials;
     e = launch_tc_gemm(pl->block_n, pl->pair, pl->tmA, pl->tmB, pl->tmD, g, pl->grid, st);
+    if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, st);
   }
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
@@ -312,17 +318,53 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       if (env[0] == '0') tmp.pair = 0;
       if (env[0] == '1') tmp.pair = 1;
     }
+    long long tiles = 0, workers = 0;
     if (tmp.pair) {
-      const long long pairs = tc_gemm_max_pairs(tmp.block_n, tmp.num_sms);
-      tmp.grid = static_cast<int>(2 * (pair_tiles < pairs ? pair_tiles : pairs));
+      workers = tc_gemm_max_pairs(tmp.block_n, tmp.num_sms);
+      tiles = pair_tiles;
       tmp.group_m = static_cast<int>(num_m2 < 8 ? num_m2 : 8);
     } else {
-      const long long tiles = tmp.block_n == 256 ? t256 : t128;
-      tmp.grid = static_cast<int>(tiles < tmp.num_sms ? tiles : tmp.num_sms);
+      workers = tmp.num_sms;
+      tiles = tmp.block_n == 256 ? t256 : t128;
       tmp.group_m = static_cast<int>(num_m < 16 ? num_m : 16);
     }
+    // Split-K tail: when the last wave would leave most workers idle (or the
+    // whole problem has fewer tiles than half the workers), the tiles of that
+    // wave are split along K into just enough pieces to occupy the workers
+    // (at least 4 k-blocks per piece, at most 16 pieces); a fixup kernel adds
+    // the fp32 pieces in order and applies the epilogue.
+    const long long num_kb = (K + 63) / 64;
+    const long long rem = tiles % workers;
+    if (rem != 0 && rem * 2 <= workers) {
+      long long S = workers / rem;
+      if (S > num_kb / 4) S = num_kb / 4;
+      if (S > 16) S = 16;
+      if (S >= 2) {
+        tmp.split = static_cast<int>(S);
+        tmp.tail_start = static_cast<int>(tiles - rem);
+      }
+    }
+    if (const char* env = std::getenv("GE_SPLIT_TAIL")) {
+      if (env[0] == '0') {
+        tmp.split = 1;
+        tmp.tail_start = 0;
+      }
+    }
+    if (tmp.split == 1) tmp.tail_start = static_cast<int>(tiles);
+    const long long units = tmp.tail_start + (tiles - tmp.tail_start) * tmp.split;
+    const long long g = units < workers ? units : workers;
+    tmp.grid = static_cast<int>(tmp.pair ? 2 * g : g);
   }
   size_t ws = 256;
+  size_t partial_off = 0;
+  if (tmp.path == GE_PATH_TC_GEMM && tmp.split > 1) {
+    const int64_t Mk = tmp.swap ? N : M;
+    const int64_t Nk = tmp.swap ? M : N;
+    const int64_t tile_m = tmp.pair ? 256 : 128;
+    const int64_t tiles = ((Mk + tile_m - 1) / tile_m) * ((Nk + tmp.block_n - 1) / tmp.block_n);
+    partial_off = ws;
+    ws += static_cast<size_t>(tiles - tmp.tail_start) * tmp.split * tile_m * tmp.block_n * 4;
+  }
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
     tmp.splits = drelu_splits(tmp.R, tmp.C, tmp.num_sms);
     const int64_t strips = (tmp.C + 255) / 256;
@@ -341,6 +383,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   }
   tmp.ws_bytes = ws;
   tmp.err = static_cast<unsigned int*>(tmp.ws);
+  if (partial_off) tmp.partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + partial_off);
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
     tmp.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + 256);
     const int64_t strips = (tmp.C + 255) / 256;

@@ -74,6 +74,25 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   nt = r / gsz;
 }
 
+// Work unit u -> tile and k-block range. Units below tail_start are whole
+// tiles; the rest are `split` consecutive k-ranges of each tail tile.
+// v >= 0 is the unit's index into the partial-sum workspace.
+__device__ __forceinline__ void unit_info(int u, int tail_start, int split, int num_kb, int& tile,
+                                          int& kb0, int& kb1, int& v) {
+  if (u < tail_start) {
+    tile = u;
+    kb0 = 0;
+    kb1 = num_kb;
+    v = -1;
+  } else {
+    v = u - tail_start;
+    tile = tail_start + v / split;
+    const int s = v % split;
+    kb0 = s * num_kb / split;
+    kb1 = (s + 1) * num_kb / split;
+  }
+}
+
 __device__ __forceinline__ float apply_act(int epi, float z) {
   if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
   if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
@@ -181,6 +200,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_n = (p.Nk + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int num_kb = (p.K + BK - 1) / BK;
+  const int num_units = p.tail_start + (num_tiles - p.tail_start) * p.split;
   const int first_tile = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   bool aborted_here = false;
@@ -192,12 +212,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       long long fills = 0;
       bool ok = true;
-      for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
+      for (int u = first_tile; u < num_units && ok; u += tile_step) {
+        int tile, kb0, kb1, v;
+        unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
         int mt, nt;
         tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
         const int row0 = mt * C::TILE_M + static_cast<int>(rank) * BM;     // this CTA's A rows
         const int col0 = nt * BN + static_cast<int>(rank) * C::B_ROWS;     // this CTA's B columns
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.budget)) {
             if (!*abort_flag) atomicOr(p.err, ERR_PRODUCER_TIMEOUT);
             *abort_flag = 1;
@@ -262,7 +284,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = first_tile; tile < num_tiles && ok; tile += tile_step) {
+      for (int u = first_tile; u < num_units && ok; u += tile_step) {
+        int tile, kb0, kb1, v;
+        unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.budget)) {
           if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
           *abort_flag = 1;
@@ -270,7 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.budget)) {
             if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
             *abort_flag = 1;
@@ -289,9 +313,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
                                        : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
             if constexpr (PAIR)
-              tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
             else
-              tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_f16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           // frees the stage (in both CTAs of a pair) once these MMAs retire
           if constexpr (PAIR)
@@ -328,7 +352,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
-    for (int tile = first_tile; tile < num_tiles; tile += tile_step) {
+    for (int u = first_tile; u < num_units; u += tile_step) {
+      int tile, kb0, kb1, v;
+      unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
       int mt, nt;
       tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
       int ok = 1;
@@ -342,6 +368,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
+      if (v >= 0) {
+        // Split-K unit: spill the fp32 accumulator rows to the workspace
+        // (the fixup kernel adds the splits and applies the epilogue).
+        float* prow = p.partials + (static_cast<long long>(v) * C::TILE_M + static_cast<int>(rank) * BM +
+                                    q * 32 + lane) * BN;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t vv[32];
+          tmem_ld_32x32b_x32(t_row + 32u * c, vv);
+          tmem_ld_wait();
+          uint4* dst = reinterpret_cast<uint4*>(prow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[i] = make_uint4(vv[4 * i], vv[4 * i + 1], vv[4 * i + 2], vv[4 * i + 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR && !leader)
+            mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+          else
+            mbar_arrive(tempty_bar(acc));
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
       const int rbase = mt * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // warp's first row of D'
       const int grow = rbase + lane;                                          // this thread's row
       float brow = 0.0f;
@@ -499,6 +553,46 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   return cudaGetLastError();
 }
 
+// Split-K fixup: one warp per (tail tile, row, 32-column slab); lane = column.
+// Adds the tile's split partials in split order, then bias, activation, mask
+// bit (ballot over the slab = one mask word) and the fp16 store.
+__global__ void __launch_bounds__(256) tc_gemm_fixup_kernel(const GemmArgs p, int tile_m, int bn) {
+  const int lane = threadIdx.x & 31;
+  const int num_m = (p.Mk + tile_m - 1) / tile_m;
+  const int num_n = (p.Nk + bn - 1) / bn;
+  const int num_tiles = num_m * num_n;
+  const int tail = num_tiles - p.tail_start;
+  const int slabs = bn / 32;
+  const long long work = static_cast<long long>(tail) * tile_m * slabs;
+  const long long split_stride = static_cast<long long>(tile_m) * bn;
+  const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < work; w += nw) {
+    const int t = static_cast<int>(w / (static_cast<long long>(tile_m) * slabs));
+    const int rem = static_cast<int>(w - static_cast<long long>(t) * tile_m * slabs);
+    const int r = rem / slabs;
+    const int c = rem - r * slabs;
+    int mt, nt;
+    tile_coords(p.tail_start + t, num_m, num_n, p.group_m, mt, nt);
+    const int grow = mt * tile_m + r;
+    const int gcol0 = nt * bn + c * 32;
+    if (grow >= p.Mk) continue;
+    const int gcol = gcol0 + lane;
+    const float* src = p.partials + static_cast<long long>(t) * p.split * split_stride +
+                       static_cast<long long>(r) * bn + c * 32 + lane;
+    float z = 0.0f;
+    for (int s = 0; s < p.split; ++s) z += __ldcg(src + s * split_stride);
+    if (p.epi != EPI_NONE && gcol < p.Nk)
+      z += __half2float(p.bias_per_col ? p.bias[gcol] : p.bias[grow]);
+    const bool in = gcol < p.Nk;
+    if (in) p.D[static_cast<long long>(grow) * p.ldd + gcol] = __float2half_rn(apply_act(p.epi, z));
+    if (p.epi == EPI_RELU_AUX_BIAS) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, in && z > 0.0f);
+      if (lane == 0 && gcol0 < ((p.Nk + 127) & ~127))
+        p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;
+    }
+  }
+}
+
 // Largest number of 2-CTA clusters of the pair kernel that can be resident.
 template <int BN>
 int max_pairs(int num_sms) {
@@ -540,6 +634,18 @@ size_t tc_gemm_smem_bytes(int block_n, int pair) {
 
 int tc_gemm_max_pairs(int block_n, int num_sms) {
   return block_n == 256 ? max_pairs<256>(num_sms) : max_pairs<128>(num_sms);
+}
+
+cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream) {
+  const int tile_m = pair ? 2 * BM : BM;
+  const long long num_tiles = static_cast<long long>((args.Mk + tile_m - 1) / tile_m) *
+                              ((args.Nk + block_n - 1) / block_n);
+  const long long warps = (num_tiles - args.tail_start) * tile_m * (block_n / 32);
+  if (warps <= 0) return cudaSuccess;
+  long long blocks = (warps + 7) / 8;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  tc_gemm_fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, tile_m, block_n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,

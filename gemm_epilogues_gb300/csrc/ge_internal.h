@@ -46,12 +46,19 @@ struct GemmArgs {
   unsigned int* err; // device error word
   int group_m;       // tile rasterisation group (m-tiles per group)
   long long budget;  // bounded-wait budget in SM clock cycles
+  // Split-K tail: tiles >= tail_start are computed as `split` k-ranges whose
+  // fp32 accumulators go to `partials` ([tile - tail_start][split][TILE_M][BN]);
+  // tc_gemm_fixup then adds them in split order and applies the epilogue.
+  int tail_start;
+  int split;
+  float* partials;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs
 // (even) and the B tensor map's box is BN/2 rows (K-major B).
 size_t tc_gemm_smem_bytes(int block_n, int pair);
 int tc_gemm_max_pairs(int block_n, int num_sms);
+cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream);
 cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, int grid,
                            cudaStream_t stream);

@@ -183,3 +183,27 @@ def test_pair_tiles_exact_integer(oracle, monkeypatch, epi):
     monkeypatch.setenv("GE_TILE_N", "256")
     _run_case(oracle, 520, 776, 128, epi, "k", "n", "row", dist=("int", 2.0), seed=21, exact=True)
     _run_case(oracle, 520, 776, 128, epi, "m", "k", "col", dist=("int", 2.0), seed=22, exact=True)
+
+
+@pytest.mark.parametrize("epi", ["none", "bias", "relu_aux_bias"])
+def test_split_tail_exact_integer(oracle, epi):
+    """Split-K tail (4 tiles split 4 ways, then the fixup kernel): integer
+    data keeps every partial sum exact, so the result is still bit-identical."""
+    _run_case(oracle, 256, 256, 1024, epi, "k", "n", "row", dist=("int", 1.0), seed=30, exact=True)
+    _run_case(oracle, 256, 256, 1024, epi, "m", "k", "col", dist=("int", 1.0), seed=31, exact=True)
+
+
+@pytest.mark.parametrize("epi", EPIS)
+def test_split_tail_pair_ragged(oracle, monkeypatch, epi):
+    """Pair tiles with a split-K tail on ragged extents."""
+    monkeypatch.setenv("GE_PAIR", "1")
+    monkeypatch.setenv("GE_TILE_N", "256")
+    _run_case(oracle, 1000, 2056, 520, epi, "k", "n", "row", seed=32)
+    _run_case(oracle, 1000, 2056, 520, epi, "k", "k", "col", seed=33)
+
+
+def test_split_tail_matches_unsplit(oracle, monkeypatch):
+    """The same problem with and without the split tail agrees with the oracle."""
+    for flag in ("0", "1"):
+        monkeypatch.setenv("GE_SPLIT_TAIL", flag)
+        _run_case(oracle, 300, 520, 1024, "gelu_bias", "k", "n", "row", seed=34)

@@ -211,6 +211,51 @@ int ora_linear_forward(int64_t M, int64_t N, int64_t K,
   return 0;
 }
 
+// DRELU_BGRAD as the epilogue of a GEMM (the backward product dH = A.B whose
+// result is masked before it is stored), from the same description: the
+// ReLU-gradient mask is applied to the product and the bias gradient is
+// accumulated from the masked values.
+//   z[m,n]    = sum_k A[m,k] B[k,n]           (fp64, k ascending; no bias)
+//   dZ[m,n]   = fp16(z[m,n]) if bit(m,n) else +0
+//   bgrad[m]  = sum over n of z[m,n]*bit(m,n)  (fp64, n ascending, unrounded z)
+// Layouts as ora_linear_forward; aux is the forward mask in D's layout.
+int ora_gemm_drelu_bgrad(int64_t M, int64_t N, int64_t K,
+                         const uint16_t* A, int a_major, int64_t lda,
+                         const uint16_t* B, int b_major, int64_t ldb,
+                         const uint32_t* aux, int64_t ld_aux,
+                         uint16_t* dZ, int d_layout, int64_t ldd, double* bgrad,
+                         int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || !dZ || !aux || !bgrad) return -1;
+  const int64_t cols = d_layout == 0 ? N : M;
+  if (ldd < cols || ld_aux * 32 < cols) return -1;
+  if (K > 0 && (!A || !B)) return -1;
+  std::vector<double> Ad((size_t)M * (size_t)K), Bd((size_t)N * (size_t)K);
+  parallel_rows(M, nthreads, [&](int64_t m) {
+    for (int64_t k = 0; k < K; ++k)
+      Ad[m * K + k] = f16_decode(a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
+  });
+  parallel_rows(N, nthreads, [&](int64_t n) {
+    for (int64_t k = 0; k < K; ++k)
+      Bd[n * K + k] = f16_decode(b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
+  });
+  parallel_rows(M, nthreads, [&](int64_t m) {
+    double s = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const double* a = Ad.data() + m * K;
+      const double* b = Bd.data() + n * K;
+      double z = 0.0;
+      for (int64_t k = 0; k < K; ++k) z += a[k] * b[k];
+      const int64_t r = d_layout == 0 ? m : n;
+      const int64_t c = d_layout == 0 ? n : m;
+      const bool bit = (aux[r * ld_aux + c / 32] >> (c % 32)) & 1u;
+      dZ[r * ldd + c] = bit ? f16_encode(z) : (uint16_t)0;
+      if (bit) s += z;
+    }
+    bgrad[m] = s;
+  });
+  return 0;
+}
+
 // Backward epilogue (DRELU_BGRAD), from the page's description: apply the
 // stored ReLU mask to the incoming gradient and reduce the bias gradient.
 //   dY, dZ: [M, N] in the forward D's stored layout (d_layout, ldd).

@@ -68,6 +68,9 @@ def _load():
             lib.ora_linear_forward.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
                                                vp, i32, vp, i32, i64, vp, i64, vp, i32]
             lib.ora_linear_forward.restype = i32
+            lib.ora_gemm_drelu_bgrad.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64, vp, i64,
+                                                 vp, i32, i64, vp, i32]
+            lib.ora_gemm_drelu_bgrad.restype = i32
             lib.ora_drelu_bgrad.argtypes = [i64, i64, vp, i32, i64, vp, i64, vp, vp]
             lib.ora_drelu_bgrad.restype = i32
             _lib = lib
@@ -168,6 +171,36 @@ def drelu_bgrad(dY, aux, M: int, N: int, *, d_layout: str = "row",
     bgrad = np.zeros(M, np.float64)
     rc = lib.ora_drelu_bgrad(M, N, _ptr(dY), 0 if d_layout == "row" else 1, ldd,
                              _ptr(aux), ld_aux, _ptr(dZ), _ptr(bgrad))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dZ, bgrad
+
+
+def gemm_drelu_bgrad(A, B, aux, M: int, N: int, K: int, *, a_major: str = "k", b_major: str = "k",
+                     d_layout: str = "row", lda: int | None = None, ldb: int | None = None,
+                     ldd: int | None = None, ld_aux: int | None = None, threads: int | None = None):
+    """DRELU_BGRAD applied to a product: dZ = fp16(A.B) where the mask bit is
+    set else +0; bgrad[m] = sum over n of the unrounded masked product (fp64)."""
+    lib = _load()
+    if lda is None:
+        lda = K if a_major == "k" else M
+    if ldb is None:
+        ldb = K if b_major == "k" else N
+    rows, cols = (M, N) if d_layout == "row" else (N, M)
+    if ldd is None:
+        ldd = cols
+    if ld_aux is None:
+        ld_aux = default_ld_aux(cols)
+    A = _u16(A)
+    B = _u16(B)
+    aux = np.ascontiguousarray(aux, dtype=np.uint32)
+    dZ = np.zeros(rows * ldd, np.uint16)
+    bgrad = np.zeros(M, np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.ora_gemm_drelu_bgrad(M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda, _ptr(B),
+                                  0 if b_major == "k" else 1, ldb, _ptr(aux), ld_aux, _ptr(dZ),
+                                  0 if d_layout == "row" else 1, ldd, _ptr(bgrad), int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dZ, bgrad

@@ -340,3 +340,49 @@ def test_drelu_bgrad_against_exact_sum(oracle):
             # a sum of fp16 values with this few terms is exact in fp64;
             # math.fsum (exact, reverse order) must agree to the last bit.
             assert bgrad[m] == math.fsum(per_m[m][::-1])
+
+
+# ------------------------------------------------ DRELU_BGRAD on a product
+
+def test_gemm_drelu_bgrad_hand_worked(oracle):
+    """The hand-worked example's product A.B = [[0,13,3],[-2,5,1]] masked by
+    [[1,1,1],[0,1,0]] gives dZ = [[0,13,3],[0,5,0]] and bgrad = [16, 5]."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_2x3x4.json")))
+    M, N, K = g["M"], g["N"], g["K"]
+    A = f16_bits(g["A"]).reshape(-1)
+    B = f16_bits(g["B"]).reshape(-1)
+    aux = np.array(g["mask_words_row_major_ld4"], np.uint32)
+    dZ, bgrad = oracle.gemm_drelu_bgrad(A, B, aux, M, N, K, a_major="k", b_major="n", d_layout="row")
+    assert oracle.f16_decode(dZ).reshape(M, N).tolist() == [[0, 13, 3], [0, 5, 0]]
+    assert bgrad.tolist() == [16.0, 5.0]
+
+
+@pytest.mark.parametrize("am,bm,dl", [("k", "n", "row"), ("k", "k", "col"), ("m", "n", "row"), ("m", "k", "col")])
+def test_gemm_drelu_bgrad_brute_force(oracle, am, bm, dl):
+    rng = np.random.default_rng(40 + "km".index(am) * 4 + "kn".index(bm) * 2 + (dl == "col"))
+    for (M, N, K) in [(1, 1, 1), (3, 5, 7), (5, 33, 4), (37, 2, 9)]:
+        Ap = rng.standard_normal((M, K)).astype(np.float16)
+        Bp = rng.standard_normal((K, N)).astype(np.float16)
+        rows, cols = (M, N) if dl == "row" else (N, M)
+        ld_aux = 4 * ((cols + 127) // 128)
+        bitmat = rng.integers(0, 2, (M, N))
+        aux = np.zeros(rows * ld_aux, np.uint32)
+        for m in range(M):
+            for n in range(N):
+                r, c = (m, n) if dl == "row" else (n, m)
+                if bitmat[m, n]:
+                    aux[r * ld_aux + c // 32] |= np.uint32(1 << (c % 32))
+        A, B = plain_to_layout(Ap.view(np.uint16), Bp.view(np.uint16), am, bm)
+        dZ, bgrad = oracle.gemm_drelu_bgrad(A, B, aux, M, N, K, a_major=am, b_major=bm, d_layout=dl, threads=1)
+        Z, _ = _brute(Ap.astype(np.float64), Bp.astype(np.float64), None, "none")
+        masked = np.where(bitmat == 1, Z, 0.0)
+        want = np.where(bitmat == 1, Z, 0.0).astype(np.float16).view(np.uint16)
+        got = dZ.reshape(rows, cols)
+        if dl == "col":
+            got = got.T
+        assert np.array_equal(got, want)
+        for m in range(M):
+            s = 0.0
+            for n in range(N):
+                s += masked[m, n]
+            assert bgrad[m] == s

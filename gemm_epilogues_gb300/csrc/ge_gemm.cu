@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // -------------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* stg = smem + C::OFF_EPI + (warp - 2) * 2 * EPI_BUF_BYTES;
-    const bool has_bias = p.epi != EPI_NONE;
+    const bool has_bias = p.epi != EPI_NONE && p.epi != EPI_DRELU_BGRAD;
     const bool bias_vec_ok = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -400,6 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int grow = rbase + lane;                                          // this thread's row
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = __half2float(p.bias[grow]);
+      float bg_row = 0.0f;  // DRELU_BGRAD, bias per D' row: this tile's row sum
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -440,8 +441,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j) bcol[j] = 0.0f;
         }
         uint32_t packed[16];
-        uint32_t bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, packed)
-                                       : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed);
+        uint32_t bits = 0;
+        if (p.epi == EPI_DRELU_BGRAD) {
+          // dZ = z where the forward mask bit is set, else +0; the masked
+          // fp32 values feed the bias-gradient partial sums.
+          uint32_t w = 0;
+          if (grow < p.Mk) w = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
+          if (p.Nk - gcol0 < 32) w &= (1u << (p.Nk - gcol0)) - 1u;
+          float zm[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) zm[j] = ((w >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) packed[j] = pack_half2(zm[2 * j], zm[2 * j + 1]);
+          if (p.bias_per_col) {
+            // bgrad indexes D' columns: reduce the 32 rows of this warp for
+            // each of its 32 columns (lane l ends with column gcol0 + l).
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+              const bool upper = (lane & off) != 0;
+#pragma unroll
+              for (int i = 0; i < off; ++i) {
+                const float send = upper ? zm[i] : zm[i + off];
+                const float keep = upper ? zm[i + off] : zm[i];
+                zm[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+              }
+            }
+            if (rbase < p.Mk && gcol0 + lane < p.Nk)
+              p.bg_partials[static_cast<long long>(rbase >> 5) * p.Nk + gcol0 + lane] = zm[0];
+          } else {
+            float srow = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) srow += zm[j];
+            bg_row += srow;
+          }
+        } else {
+          bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, packed)
+                                : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed);
+        }
         if (gcol0 + 32 > p.Nk && (p.Nk & 7) != 0) {
           // Ragged last slab whose end is not on a 16-byte boundary: a TMA
           // store writes whole 16-byte chunks, which would spill into the
@@ -484,6 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;
         }
       }
+      if (p.epi == EPI_DRELU_BGRAD && !p.bias_per_col && grow < p.Mk)
+        p.bg_partials[static_cast<long long>(nt) * p.Mk + grow] = bg_row;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -593,6 +631,15 @@ __global__ void __launch_bounds__(256) tc_gemm_fixup_kernel(const GemmArgs p, in
   }
 }
 
+__global__ void __launch_bounds__(256) bgrad_reduce_kernel(const float* part, long long rows,
+                                                           long long len, float* out) {
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < len; i += gridDim.x * 256LL) {
+    float s = 0.0f;
+    for (long long j = 0; j < rows; ++j) s += __ldcg(part + j * len + i);
+    out[i] = s;
+  }
+}
+
 // Largest number of 2-CTA clusters of the pair kernel that can be resident.
 template <int BN>
 int max_pairs(int num_sms) {
@@ -645,6 +692,15 @@ cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cu
   long long blocks = (warps + 7) / 8;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
   tc_gemm_fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, tile_m, block_n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
+                                cudaStream_t stream) {
+  if (len <= 0) return cudaSuccess;
+  long long blocks = (len + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  bgrad_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, rows, len, out);
   return cudaGetLastError();
 }
 

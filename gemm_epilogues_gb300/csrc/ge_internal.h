@@ -16,7 +16,8 @@ enum EpiCode : int {
   EPI_BIAS = 1,
   EPI_RELU_BIAS = 2,
   EPI_GELU_BIAS = 3,
-  EPI_RELU_AUX_BIAS = 4
+  EPI_RELU_AUX_BIAS = 4,
+  EPI_DRELU_BGRAD = 5  // GEMM epilogue form: aux is the input mask
 };
 
 // Device error word bits (the plan's workspace word 0).
@@ -52,6 +53,11 @@ struct GemmArgs {
   int tail_start;
   int split;
   float* partials;
+  // DRELU_BGRAD epilogue: per-block bias-gradient partial sums, reduced by
+  // launch_bgrad_reduce into `bgrad`. Row case (bias per D' row): bg_partials
+  // is [num n-tiles][Mk]; column case: [ceil(Mk/32)][Nk].
+  float* bg_partials;
+  float* bgrad;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs
@@ -59,6 +65,9 @@ struct GemmArgs {
 size_t tc_gemm_smem_bytes(int block_n, int pair);
 int tc_gemm_max_pairs(int block_n, int num_sms);
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream);
+// out[i] = sum over j = 0..rows-1 (in order) of part[j * len + i], fp32.
+cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
+                                cudaStream_t stream);
 cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, int grid,
                            cudaStream_t stream);

@@ -108,9 +108,9 @@ typedef enum {
  * ge_plan_create: validate a problem and choose its kernel.
  *   out      : receives the plan (set to NULL on failure).
  *   M, N, K  : problem size. M, N >= 1. K >= 1 for the forward epilogues;
- *              K == 0 selects the standalone DRELU_BGRAD kernel (the only
- *              form of DRELU_BGRAD; K > 0 with it is GE_ERR_UNSUPPORTED).
- *              M, N, K < 2^31.
+ *              with DRELU_BGRAD, K == 0 selects the standalone kernel on a
+ *              stored dY and K >= 1 the GEMM-epilogue form (the mask is
+ *              applied to the product A.B). M, N, K < 2^31.
  *   a, b, d  : operand and output dtypes; GE_F16 only.
  *   compute  : accumulation dtype; GE_F32 only.
  *   epi      : epilogue.
@@ -142,7 +142,15 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K,
  *           of D is > 0 ((r,c) = (m,n) for D ROW, (n,m) for D COL). Words up
  *           to ceil(len/128)*4 of each row are written; bits past the end of
  *           the row are 0.
- * DRELU_BGRAD (K == 0; dY and dZ are [M,N] in the planned D layout):
+ * DRELU_BGRAD as a GEMM epilogue (K >= 1): the backward product dH = A.B
+ * (fp32 accumulate) is masked before its single store:
+ *   A, B  : fp16 operands as for the forward epilogues.
+ *   aux   : the forward mask (read only), same packing as RELU_AUX_BIAS.
+ *   D     : dZ, fp16: dZ[m,n] = fp16(dH[m,n]) where the bit is set, else +0.
+ *   bias  : OUTPUT, fp32 [M]: bgrad[m] = sum over n of the masked fp32 dH,
+ *           reduced in a fixed order (per-tile partial sums in the plan
+ *           workspace, then one ordered pass), 16-byte aligned.
+ * DRELU_BGRAD standalone (K == 0; dY and dZ are [M,N] in the planned D layout):
  *   A     : dY, fp16 (read only).        B : unused (may be NULL).
  *   aux   : the forward mask (read only). D : dZ, fp16; may alias A.
  *   bias  : OUTPUT, fp32 [M]: bgrad[m] = sum over n of dZ[m,n], reduced in

@@ -54,7 +54,7 @@ def test_plan_validation_without_device(lib):
     assert _create(8, 8, 8, epi=9) == E.GE_ERR_INVALID_ARG
     assert _create(8, 8, 8, a=E.GE_F32) == E.GE_ERR_UNSUPPORTED
     assert _create(8, 8, 8, compute=E.GE_F16) == E.GE_ERR_UNSUPPORTED
-    assert _create(8, 8, 8, epi=E.GE_EPI_DRELU_BGRAD) == E.GE_ERR_UNSUPPORTED
+    assert _create(8, 8, 0, epi=E.GE_EPI_BIAS) == E.GE_ERR_INVALID_ARG
     assert _create(2**31, 8, 8) == E.GE_ERR_INVALID_ARG
     # leading dimensions smaller than the extent, or not multiples of 8
     assert _create(64, 64, 64, layout=ge.make_layout(lda=32)) == E.GE_ERR_INVALID_ARG

@@ -207,3 +207,11 @@ def test_split_tail_matches_unsplit(oracle, monkeypatch):
     for flag in ("0", "1"):
         monkeypatch.setenv("GE_SPLIT_TAIL", flag)
         _run_case(oracle, 300, 520, 1024, "gelu_bias", "k", "n", "row", seed=34)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 1, 8192), (4096, 3, 8192), (2000, 2, 1024), (1500, 4, 4096)])
+def test_gemv_ring_wraps(oracle, M, N, K):
+    """Streaming GEMV with more rows per SM than ring slots (the ring wraps
+    and every slot is refilled several times)."""
+    path = _run_case(oracle, M, N, K, "gelu_bias", "k", "k", "col", seed=60 + N)
+    assert path == ge.GE_PATH_GEMV

@@ -44,6 +44,9 @@ CONFIG_CASES = {
     "cfg_c3_T512": ("c3_T512", False), "cfg_c3_T512_unfused": ("c3_T512", True),
     "cfg_c3_T2048": ("c3_T2048", False), "cfg_c3_T2048_unfused": ("c3_T2048", True),
     "cfg_c5": ("c5", False), "cfg_c5_unfused": ("c5", True),
+    # backward GEMM dH = G W2^T (11008 x 8192 x 4096) with DRELU_BGRAD fused
+    # in its epilogue, vs. the GEMM followed by the standalone DRELU_BGRAD
+    "cfg_bwd_gemm_drelu": ("bwd", False), "cfg_bwd_gemm_drelu_unfused": ("bwd", True),
 }
 
 
@@ -213,6 +216,8 @@ def run_config(args, rank):
     import gemm_epilogues_gb300 as ge
     from gemm_epilogues_gb300.inputs import pages_workloads
     key, unfused = CONFIG_CASES[args.case]
+    if key == "bwd":
+        return run_bwd_gemm_drelu(args, rank, unfused)
     w = pages_workloads()[key]
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
@@ -246,6 +251,57 @@ def run_config(args, rank):
             "frac_of_peak": tflops / peaks["tflops"],
             "gbs_algorithmic": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}
     plan.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_bwd_gemm_drelu(args, rank, unfused):
+    """dH[8192 tokens, 11008] = G[8192, 4096] W2[11008, 4096]^T masked by the
+    forward ReLU mask: fused (one GEMM with the DRELU_BGRAD epilogue) or
+    unfused (GEMM with no epilogue, then the standalone DRELU_BGRAD pass)."""
+    import torch
+    import gemm_epilogues_gb300 as ge
+    from gemm_epilogues_gb300.inputs import f16_tensor
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    M, N, K = D_OUT, T_TOK, D_IN
+    G = f16_tensor((N, K), 6001, "normal", 1.0, dev)
+    W2 = f16_tensor((M, K), 6002, "normal", 1 / 64, dev)
+    ld_aux = (M + 127) // 128 * 4
+    g = torch.Generator(device=dev)
+    g.manual_seed(6003)
+    aux = torch.randint(-2**31, 2**31 - 1, (N * ld_aux,), generator=g, device=dev, dtype=torch.int32)
+    dZ = torch.empty((N, M), dtype=torch.float16, device=dev)
+    bgrad = torch.empty(M, dtype=torch.float32, device=dev)
+    Kl = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    gemm = ge.Plan(M, N, K, ge.GE_EPI_NONE if unfused else ge.GE_EPI_DRELU_BGRAD, Kl)
+    drelu = ge.Plan(M, N, 0, ge.GE_EPI_DRELU_BGRAD, ge.make_layout(d=ge.GE_D_COL)) if unfused else None
+    flush_buf = torch.ones((256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.sum(flush_buf, dim=0, out=flush_out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if unfused:
+            gemm.execute(W2, G, None, dZ, None, stream)
+            drelu.execute(dZ, None, bgrad, dZ, aux, stream)
+        else:
+            gemm.execute(W2, G, bgrad, dZ, aux, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    assert ge.ge_get_last_device_error(gemm.handle) == ge.GE_OK
+    ms = sum(times) / len(times)
+    flops = 2.0 * M * N * K
+    line = {"case": args.case, "workload": "backward GEMM 11008x8192x4096 + DRELU_BGRAD",
+            "unfused": unfused, "ms": ms, "min_ms": min(times), "tflops": flops / ms / 1e9,
+            "frac_of_peak": flops / ms / 1e9 / peaks["tflops"]}
+    gemm.free()
+    if drelu:
+        drelu.free()
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -355,6 +355,7 @@ def run_ours(args, world, rank, local):
     dwp = ge.Plan(D_OUT, D_IN, T_TOK, ge.GE_EPI_NONE, ge.make_layout(MN, MN, ge.GE_D_ROW))
     dec = ge.Plan(D_DEC, 1, D_DEC, ge.GE_EPI_GELU_BIAS, ge.make_layout(K_, K_, ge.GE_D_COL))
     assert dec.path == ge.GE_PATH_GEMV
+    dec.set_attr(ge.GE_ATTR_STATIC_A, 1)  # decode weights are never written by earlier work
 
     Y = torch.empty((T_TOK, D_OUT), dtype=torch.float16, device=dev)
     aux = torch.empty(fwd.aux_bytes // 4, dtype=torch.int32, device=dev)
@@ -507,6 +508,8 @@ def run_ours(args, world, rank, local):
     # out of the capture.
     W2s = [W2] + [f16_tensor((D_DEC, D_DEC), 2100 + i, "normal", 1 / 64, dev) for i in range(7)]
     decs = [ge.Plan(D_DEC, 1, D_DEC, ge.GE_EPI_GELU_BIAS, ge.make_layout(K_, K_, ge.GE_D_COL)) for _ in W2s]
+    for pl in decs:
+        pl.set_attr(ge.GE_ATTR_STATIC_A, 1)
     for pl, Wi in zip(decs, W2s):
         pl.execute(Wi, x1, b2, y1, None, stream)
     torch.cuda.synchronize()

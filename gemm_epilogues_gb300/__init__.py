@@ -44,6 +44,8 @@ GE_MN_MAJOR = 1
 # ge_dlayout_t
 GE_D_ROW = 0
 GE_D_COL = 1
+# ge_plan_attr_t
+GE_ATTR_STATIC_A = 0
 # ge_path_t
 GE_PATH_TC_GEMM = 0
 GE_PATH_GEMV = 1
@@ -57,7 +59,7 @@ EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EP
 ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",
                  "ge_aux_bytes", "ge_aux_ld", "ge_plan_path", "ge_plan_tile_n",
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
-                 "ge_version", "ge_drelu_bgrad_static")
+                 "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -112,6 +114,8 @@ def load_library():
         lib.ge_debug_wait_timeout.restype = i32
         lib.ge_drelu_bgrad_static.argtypes = [i64, i64, i32, i64, i64, vp, vp, vp, vp, vp]
         lib.ge_drelu_bgrad_static.restype = i32
+        lib.ge_plan_set_attr.argtypes = [vp, i32, i64]
+        lib.ge_plan_set_attr.restype = i32
         lib.ge_version.argtypes = []
         lib.ge_version.restype = ctypes.c_char_p
         _lib = lib
@@ -177,6 +181,13 @@ def ge_execute_unfused(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool 
     _check(st, "ge_execute_unfused")
 
 
+def ge_plan_set_attr(plan, attr: int, value: int, *, raw: bool = False):
+    st = load_library().ge_plan_set_attr(plan, int(attr), int(value))
+    if raw:
+        return st
+    _check(st, "ge_plan_set_attr")
+
+
 def ge_plan_free(plan):
     _check(load_library().ge_plan_free(plan), "ge_plan_free")
 
@@ -230,6 +241,9 @@ class Plan:
 
     def execute(self, A, B, bias, D, aux=None, stream=None):
         ge_execute(self.handle, A, B, bias, D, aux, stream)
+
+    def set_attr(self, attr: int, value: int):
+        ge_plan_set_attr(self.handle, attr, value)
 
     def execute_unfused(self, A, B, bias, D, aux=None, stream=None):
         ge_execute_unfused(self.handle, A, B, bias, D, aux, stream)

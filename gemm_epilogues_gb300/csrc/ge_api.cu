@@ -44,6 +44,7 @@ struct Plan {
   // stored D: R rows x C contiguous
   int64_t R = 0, C = 0;
   int64_t aux_words = 0;  // ld_aux (words) when a mask is in use
+  int static_a = 0;       // GE_ATTR_STATIC_A
   // device workspace: [error word | pad to 256 | counters | partials]
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -166,6 +167,7 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.epi = epi_code;
     g.err = pl->err;
     g.budget = kWaitBudgetCycles;
+    g.static_a = pl->static_a;
     e = launch_gemv(g, pl->num_sms, st);
   } else {
     ge_status_t s = build_maps(pl, A, B, D);
@@ -509,6 +511,18 @@ ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B, con
     if (e != cudaSuccess) return GE_ERR_CUDA;
   }
   return GE_OK;
+}
+
+ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_ERR_INVALID_ARG;
+  switch (attr) {
+    case GE_ATTR_STATIC_A:
+      if (value != 0 && value != 1) return GE_ERR_INVALID_ARG;
+      pl->static_a = static_cast<int>(value);
+      return GE_OK;
+  }
+  return GE_ERR_INVALID_ARG;
 }
 
 ge_status_t ge_plan_free(ge_plan_t plan) {

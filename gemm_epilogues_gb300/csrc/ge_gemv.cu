@@ -154,13 +154,24 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
 
   if (warp == GV_WARPS) {
     if (lane == 0) {
-      // the activations first (N contiguous K-vectors), then the weight rows
+      // The first ring's worth of weight rows are requested before waiting
+      // for the previous grid on the stream (with programmatic dependent
+      // launch that grid may still be running; A is static by contract).
+      long long issued = 0;
+      const long long first = nr < slots ? nr : slots;
+      for (long long j = 0; j < first; ++j) {
+        mbar_arrive_expect_tx(full_bar(static_cast<int>(j)), row_bytes);
+        bulk_load_1d(smem_u32(ring + static_cast<size_t>(j) * slot_bytes), p.A + (r0 + j) * p.lda,
+                     row_bytes, full_bar(static_cast<int>(j)));
+        ++issued;
+      }
+      grid_launch_dependents();
+      grid_dependency_wait();  // the activations may come from the previous grid
       mbar_arrive_expect_tx(x_bar, static_cast<uint32_t>(p.N) * row_bytes);
       for (int n = 0; n < p.N; ++n)
         bulk_load_1d(smem_u32(smem + x_off) + static_cast<uint32_t>(n) * x_stride_bytes,
                      p.B + n * p.ldb, row_bytes, x_bar);
-      long long issued = 0;
-      for (long long j = 0; j < nr; ++j) {
+      for (long long j = first; j < nr; ++j) {
         const int s = static_cast<int>(j % slots);
         const uint32_t ph = static_cast<uint32_t>((j / slots) & 1);
         if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, p.budget)) {
@@ -182,6 +193,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
       }
     }
   } else {
+    grid_dependency_wait();  // D may still be read by the previous grid
     int ok = 1;
     if (lane == 0) ok = mbar_wait_bounded(x_bar, 0u, abort_flag, p.budget) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -263,7 +275,20 @@ cudaError_t launch_stream(const GemvArgs& a, int num_sms, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  gemv_stream_kernel<NT><<<grid, GV_THREADS, smem, s>>>(a, slots, slot_bytes, x_stride_bytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(GV_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (a.static_a) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<NT>, a, slots, slot_bytes, x_stride_bytes);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

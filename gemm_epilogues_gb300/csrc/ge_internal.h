@@ -86,6 +86,7 @@ struct GemvArgs {
   int epi;
   unsigned int* err;  // device error word (bounded waits of the streaming kernel)
   long long budget;   // bounded-wait budget in SM clock cycles
+  int static_a;       // launch with programmatic dependent launch (A never written upstream)
 };
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
 

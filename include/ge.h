@@ -180,6 +180,24 @@ ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B,
                                const void* bias, void* D, void* aux,
                                void* stream);
 
+/* Plan attributes (ge_plan_set_attr). */
+typedef enum {
+  /* value 1: A is never written by work queued earlier on the execute's
+   * stream (model weights). Decode-sized plans (GE_PATH_GEMV) then launch
+   * with programmatic dependent launch: the kernel may start while the
+   * previous kernel on the stream is still running, streams its first weight
+   * rows into shared memory, and only then waits for that kernel to finish
+   * before it reads B (the activations) or writes D. Chains of decode
+   * projections overlap one layer's weight fetch with the previous layer's
+   * tail. Value 0 (default): the kernel starts after earlier work. Other
+   * paths ignore the attribute. */
+  GE_ATTR_STATIC_A = 0
+} ge_plan_attr_t;
+
+/* Set a plan attribute. Returns GE_OK, or GE_ERR_INVALID_ARG for a NULL
+ * plan, an unknown attribute or a value outside its range. */
+ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value);
+
 /* Release the plan and its device workspace (NULL is accepted). The caller
  * must make sure no execute of the plan is still running on the GPU. */
 ge_status_t ge_plan_free(ge_plan_t plan);

@@ -76,6 +76,10 @@ def test_valid_plan_needs_a_device(lib):
     assert _create(256, 128, 512) == ge.GE_ERR_CUDA
 
 
+def test_plan_attr_validation(lib):
+    assert ge.ge_plan_set_attr(None, ge.GE_ATTR_STATIC_A, 1, raw=True) == ge.GE_ERR_INVALID_ARG
+
+
 def test_null_handles(lib):
     assert ge.load_library().ge_execute(None, None, None, None, None, None, None) == ge.GE_ERR_INVALID_ARG
     assert ge.load_library().ge_plan_free(None) == ge.GE_OK

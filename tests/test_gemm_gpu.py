@@ -215,3 +215,48 @@ def test_gemv_ring_wraps(oracle, M, N, K):
     and every slot is refilled several times)."""
     path = _run_case(oracle, M, N, K, "gelu_bias", "k", "k", "col", seed=60 + N)
     assert path == ge.GE_PATH_GEMV
+
+
+def test_gemv_chain_with_static_weights(oracle):
+    """A chain of decode projections (each layer's output is the next one's
+    input, ping-pong buffers) launched with programmatic dependent launch:
+    every layer still waits for its input and for the previous reader of its
+    output buffer. Checked layer by layer against the oracle's own chain."""
+    H, layers = 2048, 4
+    Ws = [f16_tensor((H, H), 700 + i, "normal", H ** -0.5).cuda() for i in range(layers)]
+    bs = [f16_tensor((H,), 710 + i, "normal", 0.1).cuda() for i in range(layers)]
+    x0 = f16_tensor((1, H), 720).cuda()
+    bufs = [x0.clone(), torch.empty_like(x0)]
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    plans = [ge.Plan(H, 1, H, ge.GE_EPI_GELU_BIAS, L) for _ in range(layers)]
+    for p in plans:
+        p.set_attr(ge.GE_ATTR_STATIC_A, 1)
+        assert p.path == ge.GE_PATH_GEMV
+    for i, p in enumerate(plans):
+        src, dst = bufs[i % 2], bufs[(i + 1) % 2]  # layer i+1 overwrites layer i's input
+        p.execute(Ws[i], src, bs[i], dst)
+    torch.cuda.synchronize()
+    for p in plans:
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+        p.free()
+    # the same chain with a fresh buffer per layer, to compare every stage
+    got = []
+    cur = x0.clone()
+    plans = [ge.Plan(H, 1, H, ge.GE_EPI_GELU_BIAS, L) for _ in range(layers)]
+    for i, p in enumerate(plans):
+        p.set_attr(ge.GE_ATTR_STATIC_A, 1)
+        nxt = torch.empty_like(x0)
+        p.execute(Ws[i], cur, bs[i], nxt)
+        got.append(nxt)
+        cur = nxt
+    torch.cuda.synchronize()
+    # the ping-pong chain's final output equals the step-by-step one
+    assert torch.equal(bufs[layers % 2], got[-1])
+    ref_in = bits(x0)
+    for i in range(layers):
+        r = oracle.linear_forward(bits(Ws[i]), ref_in, bits(bs[i]), "gelu_bias", H, 1, H,
+                                  a_major="k", b_major="k", d_layout="col")
+        check_f16(oracle, bits(got[i]), r["D"], f"chain layer {i}")
+        ref_in = r["D"]
+    for p in plans:
+        p.free()

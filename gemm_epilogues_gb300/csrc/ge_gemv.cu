@@ -18,6 +18,8 @@
 // Every wait is bounded (error word, then drain and exit).
 // Other shapes use the register kernel below: one warp per row, 16-byte
 // non-allocating global loads, UNROLL slabs in flight.
+#include <cstdlib>
+
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
@@ -52,6 +54,15 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
   const int K8 = p.K & ~7;
   constexpr int SLAB = 32 * 8;  // elements one warp covers per 16-byte load
+  {
+    // Ask L2 for this warp's first weight row before waiting on the previous
+    // grid (with programmatic dependent launch that grid may still run).
+    const long long m0 = blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (lane == 0 && m0 < p.M && (p.K & 7) == 0)
+      bulk_prefetch_l2(p.A + m0 * p.lda, static_cast<uint32_t>(p.K) * 2u);
+  }
+  grid_launch_dependents();
+  grid_dependency_wait();  // B may come from, and D may be read by, the previous grid
   for (long long m = blockIdx.x * wpb + (threadIdx.x >> 5); m < p.M; m += nwarps) {
     const __half* arow = p.A + m * p.lda;
     float acc[NT];
@@ -299,7 +310,19 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  gemv_kernel<NT, UNROLL><<<static_cast<int>(blocks), threads, 0, s>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (a.static_a) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -310,7 +333,12 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
   // are a whole number of 16-byte chunks (K % 8 == 0) starting on 16-byte
   // boundaries (the planner checks lda % 8 == 0 and A's alignment), and
   // activations small enough to stay in L1 (N <= 4).
-  if (a.K <= 8192 && a.K % 8 == 0 && a.N <= 4 && a.M >= 1) {
+  // GE_GEMV_KERNEL=stream|reg selects the kernel (A/B measurements).
+  bool stream_ok = a.K <= 8192 && a.K % 8 == 0 && a.N <= 4 && a.M >= 1;
+  if (const char* env = std::getenv("GE_GEMV_KERNEL")) {
+    if (env[0] == 'r') stream_ok = false;
+  }
+  if (stream_ok) {
     if (a.N <= 1) return launch_stream<1>(a, num_sms, s);
     if (a.N <= 2) return launch_stream<2>(a, num_sms, s);
     return launch_stream<4>(a, num_sms, s);

@@ -10,7 +10,7 @@
 //
 //   z[m,n] = sum_k A[m,k] * B[k,n]  (k ascending, fp64)          -- the GEMM
 //          + bias[m]                (broadcast over every column) -- BIAS
-//   y[m,n] = act(z[m,n])            NONE | ReLU | tanh-GELU       -- activation
+//   y[m,n] = act(z[m,n])            NONE | ReLU | tanh-GELU | erf-GELU
 //   D[m,n] = fp16(y[m,n])           round to nearest even         -- one store
 //   mask   = (z > 0) bit-packed     (RELU_AUX_BIAS only)          -- aux output
 //
@@ -48,7 +48,7 @@ namespace {
 // Epilogue codes of this oracle (its own numbering; the Python wrapper maps
 // names to these).
 enum OraEpi { ORA_NONE = 0, ORA_BIAS = 1, ORA_RELU_BIAS = 2, ORA_GELU_BIAS = 3,
-              ORA_RELU_AUX_BIAS = 4 };
+              ORA_RELU_AUX_BIAS = 4, ORA_GELU_ERF_BIAS = 6 };
 
 // IEEE-754 binary16 -> binary64, written from the format definition:
 // 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -110,9 +110,16 @@ double activation(int epi, double z) {
       const double c = std::sqrt(2.0 / 3.14159265358979323846);
       return 0.5 * z * (1.0 + std::tanh(c * (z + 0.044715 * z * z * z)));
     }
+    case ORA_GELU_ERF_BIAS:
+      // exact form: z * Phi(z) = 0.5 z (1 + erf(z / sqrt(2)))
+      return 0.5 * z * (1.0 + std::erf(z / std::sqrt(2.0)));
     default:
       return z;
   }
+}
+
+bool valid_forward_epi(int epi) {
+  return (epi >= ORA_NONE && epi <= ORA_RELU_AUX_BIAS) || epi == ORA_GELU_ERF_BIAS;
 }
 
 template <class F>
@@ -139,7 +146,7 @@ double ora_f16_to_f64(uint16_t h) { return f16_decode(h); }
 // The activation of epilogue `epi` applied to one fp64 pre-activation value
 // (the same function the forward uses); -1 selects nothing and returns NaN.
 double ora_act_f64(int epi, double z) {
-  if (epi < ORA_NONE || epi > ORA_RELU_AUX_BIAS) return std::nan("");
+  if (!valid_forward_epi(epi)) return std::nan("");
   return activation(epi, z);
 }
 uint16_t ora_f64_to_f16(double x) { return f16_encode(x); }
@@ -169,7 +176,7 @@ int ora_linear_forward(int64_t M, int64_t N, int64_t K,
                        uint32_t* aux, int64_t ld_aux, double* Z,
                        int nthreads) {
   if (M < 0 || N < 0 || K < 0 || !D) return -1;
-  if (epi < ORA_NONE || epi > ORA_RELU_AUX_BIAS) return -1;
+  if (!valid_forward_epi(epi)) return -1;
   if (epi != ORA_NONE && !bias) return -1;
   if (epi == ORA_RELU_AUX_BIAS && !aux) return -1;
   const int64_t rows = d_layout == 0 ? M : N;

@@ -29,7 +29,8 @@ _SRC = os.path.join(_HERE, "ge_oracle.cpp")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libge_oracle.so")
 
-EPILOGUES = {"none": 0, "bias": 1, "relu_bias": 2, "gelu_bias": 3, "relu_aux_bias": 4}
+EPILOGUES = {"none": 0, "bias": 1, "relu_bias": 2, "gelu_bias": 3, "relu_aux_bias": 4,
+             "gelu_erf_bias": 6}
 
 _lock = threading.Lock()
 _lib = None

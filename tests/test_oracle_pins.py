@@ -386,3 +386,44 @@ def test_gemm_drelu_bgrad_brute_force(oracle, am, bm, dl):
             for n in range(N):
                 s += masked[m, n]
             assert bgrad[m] == s
+
+
+# ------------------------------------------------------------- erf GELU
+
+def test_gelu_erf_closed_forms(oracle):
+    act = lambda z: oracle.act_f64("gelu_erf_bias", z)
+    assert act(0.0) == 0.0
+    assert abs(act(1.0) - 0.8413447460685429) < 1e-15  # Phi(1) = 0.841344746...
+    assert act(12.0) == 12.0
+    for z in np.linspace(-6, 6, 241):
+        # z Phi(z) - (-z) Phi(-z) = z (Phi(z) + Phi(-z)) = z
+        assert abs(act(z) - act(-z) - z) <= 4e-16 * max(1.0, abs(z))
+
+
+def test_gelu_erf_matches_library(oracle):
+    z = torch.linspace(-9, 9, 7001, dtype=torch.float64)
+    ref = torch.nn.functional.gelu(z, approximate="none").numpy()
+    got = np.array([oracle.act_f64("gelu_erf_bias", float(v)) for v in z])
+    assert np.allclose(got, ref, rtol=1e-14, atol=1e-15)
+    # and it is not the tanh approximation
+    tanh_form = np.array([oracle.act_f64("gelu_bias", float(v)) for v in z])
+    assert np.abs(got - tanh_form).max() > 1e-5
+
+
+def test_gelu_erf_forward_brute_force(oracle):
+    rng = np.random.default_rng(77)
+    M, N, K = 4, 5, 6
+    Ap = rng.standard_normal((M, K)).astype(np.float16)
+    Bp = rng.standard_normal((K, N)).astype(np.float16)
+    bias = rng.standard_normal(M).astype(np.float16)
+    A, B = plain_to_layout(Ap.view(np.uint16), Bp.view(np.uint16), "k", "n")
+    r = oracle.linear_forward(A, B, bias.view(np.uint16), "gelu_erf_bias", M, N, K, a_major="k", b_major="n")
+    Z = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(Ap[m, k]) * float(Bp[k, n])
+            Z[m, n] = s + float(bias[m])
+    want = torch.nn.functional.gelu(torch.from_numpy(Z), approximate="none").numpy()
+    assert np.array_equal(r["D"].reshape(M, N), want.astype(np.float16).view(np.uint16))

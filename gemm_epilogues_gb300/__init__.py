@@ -35,6 +35,7 @@ GE_EPI_RELU_BIAS = 2
 GE_EPI_GELU_BIAS = 3
 GE_EPI_RELU_AUX_BIAS = 4
 GE_EPI_DRELU_BGRAD = 5
+GE_EPI_GELU_ERF_BIAS = 6
 # ge_dtype_t
 GE_F16 = 0
 GE_F32 = 1
@@ -53,7 +54,7 @@ GE_PATH_DRELU = 2
 
 EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EPI_RELU_BIAS,
                     "gelu_bias": GE_EPI_GELU_BIAS, "relu_aux_bias": GE_EPI_RELU_AUX_BIAS,
-                    "drelu_bgrad": GE_EPI_DRELU_BGRAD}
+                    "drelu_bgrad": GE_EPI_DRELU_BGRAD, "gelu_erf_bias": GE_EPI_GELU_ERF_BIAS}
 
 # Every function the header declares (checked against include/ge.h by a test).
 ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",

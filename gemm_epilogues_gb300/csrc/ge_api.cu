@@ -95,7 +95,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool epi_has_bias(ge_epilogue_t e) {
   return e == GE_EPI_BIAS || e == GE_EPI_RELU_BIAS || e == GE_EPI_GELU_BIAS ||
-         e == GE_EPI_RELU_AUX_BIAS;
+         e == GE_EPI_RELU_AUX_BIAS || e == GE_EPI_GELU_ERF_BIAS;
 }
 
 // Verify that `p` is device memory of the plan's device (cached per slot).
@@ -227,7 +227,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
                            const ge_layout_t* layout) {
   if (!out) return GE_ERR_INVALID_ARG;
   *out = nullptr;
-  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_DRELU_BGRAD)
+  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_GELU_ERF_BIAS)
     return GE_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 0) return GE_ERR_INVALID_ARG;
   const int64_t lim = (int64_t(1) << 31) - 1;

@@ -96,6 +96,7 @@ __device__ __forceinline__ void unit_info(int u, int tail_start, int split, int 
 __device__ __forceinline__ float apply_act(int epi, float z) {
   if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
   if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  if (epi == EPI_GELU_ERF_BIAS) return gelu_erf(z);
   return z;
 }
 
@@ -130,6 +131,7 @@ __device__ __forceinline__ uint32_t epilogue_dispatch(int epi, const uint32_t (&
     case EPI_BIAS: return epilogue_slab<EPI_BIAS, BIAS_COL>(v, brow, bcol, packed);
     case EPI_RELU_BIAS: return epilogue_slab<EPI_RELU_BIAS, BIAS_COL>(v, brow, bcol, packed);
     case EPI_GELU_BIAS: return epilogue_slab<EPI_GELU_BIAS, BIAS_COL>(v, brow, bcol, packed);
+    case EPI_GELU_ERF_BIAS: return epilogue_slab<EPI_GELU_ERF_BIAS, BIAS_COL>(v, brow, bcol, packed);
     case EPI_RELU_AUX_BIAS:
       return epilogue_slab<EPI_RELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, packed);
     default: return epilogue_slab<EPI_NONE, BIAS_COL>(v, brow, bcol, packed);

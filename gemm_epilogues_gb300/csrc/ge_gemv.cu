@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
       float y = z;
       if (p.epi == EPI_RELU_BIAS) y = fmaxf(z, 0.0f);
       else if (p.epi == EPI_GELU_BIAS) y = gelu_tanh(z);
+      else if (p.epi == EPI_GELU_ERF_BIAS) y = gelu_erf(z);
       p.D[m * p.ldd_m + static_cast<long long>(lane) * p.ldd_n] = __float2half_rn(y);
     }
   }
@@ -122,6 +123,7 @@ constexpr int GV_SLOTS = 8;  // rows in flight per CTA
 __device__ __forceinline__ float gemv_act(int epi, float z) {
   if (epi == EPI_RELU_BIAS) return fmaxf(z, 0.0f);
   if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  if (epi == EPI_GELU_ERF_BIAS) return gelu_erf(z);
   return z;
 }
 

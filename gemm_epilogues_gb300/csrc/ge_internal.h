@@ -17,7 +17,8 @@ enum EpiCode : int {
   EPI_RELU_BIAS = 2,
   EPI_GELU_BIAS = 3,
   EPI_RELU_AUX_BIAS = 4,
-  EPI_DRELU_BGRAD = 5  // GEMM epilogue form: aux is the input mask
+  EPI_DRELU_BGRAD = 5,  // GEMM epilogue form: aux is the input mask
+  EPI_GELU_ERF_BIAS = 6
 };
 
 // Device error word bits (the plan's workspace word 0).

@@ -313,6 +313,11 @@ __device__ __forceinline__ float gelu_tanh(float z) {
   return fmaf(hz, tanh_approx(u), hz);
 }
 
+// exact GELU: z * Phi(z) = 0.5 z (1 + erf(z / sqrt(2))), with CUDA's erff.
+__device__ __forceinline__ float gelu_erf(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);

@@ -16,6 +16,7 @@ namespace {
 __device__ __forceinline__ float act_of(int epi, float z) {
   if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
   if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  if (epi == EPI_GELU_ERF_BIAS) return gelu_erf(z);
   return z;
 }
 

@@ -74,7 +74,8 @@ typedef enum {
   GE_EPI_RELU_BIAS = 2,     /* D = max(A.B + bias, 0)                          */
   GE_EPI_GELU_BIAS = 3,     /* D = gelu_tanh(A.B + bias)                       */
   GE_EPI_RELU_AUX_BIAS = 4, /* RELU_BIAS plus the bit-packed mask (z > 0)      */
-  GE_EPI_DRELU_BGRAD = 5    /* backward: dZ = dY * mask, bgrad = sum_n dZ      */
+  GE_EPI_DRELU_BGRAD = 5,   /* backward: dZ = dY * mask, bgrad = sum_n dZ      */
+  GE_EPI_GELU_ERF_BIAS = 6  /* D = z * Phi(z), z = A.B + bias (exact erf GELU) */
 } ge_epilogue_t;
 
 typedef enum { GE_F16 = 0, GE_F32 = 1 } ge_dtype_t;

@@ -260,3 +260,17 @@ def test_gemv_chain_with_static_weights(oracle):
         ref_in = r["D"]
     for p in plans:
         p.free()
+
+
+@pytest.mark.parametrize("am,bm,dl", [("k", "n", "row"), ("k", "k", "col"), ("m", "n", "row"), ("m", "k", "col")])
+def test_gelu_erf_epilogue(oracle, am, bm, dl):
+    """Exact (erf) GELU: single-CTA tiles, ragged edges, every operand major."""
+    _run_case(oracle, 300, 520, 200, "gelu_erf_bias", am, bm, dl, seed=80)
+
+
+def test_gelu_erf_pair_gemv_unfused(oracle, monkeypatch):
+    _run_case(oracle, 1000, 3, 1000, "gelu_erf_bias", "k", "k", "col", seed=81)      # GEMV
+    _run_case(oracle, 520, 264, 200, "gelu_erf_bias", "k", "n", "row", seed=82, unfused=True)
+    monkeypatch.setenv("GE_PAIR", "1")
+    monkeypatch.setenv("GE_TILE_N", "256")
+    _run_case(oracle, 1000, 2056, 520, "gelu_erf_bias", "k", "k", "col", seed=83)  # pairs + split tail

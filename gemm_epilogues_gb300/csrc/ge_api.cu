@@ -165,8 +165,6 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.ldd_n = pl->L.d == GE_D_ROW ? 1 : pl->L.ldd;
     g.bias = static_cast<const __half*>(bias);
     g.epi = epi_code;
-    g.err = pl->err;
-    g.budget = kWaitBudgetCycles;
     g.static_a = pl->static_a;
     e = launch_gemv(g, pl->num_sms, st);
   } else {

@@ -27,8 +27,7 @@ enum ErrBits : unsigned int {
   ERR_MMA_TIMEOUT = 2u,
   ERR_EPILOGUE_TIMEOUT = 4u,
   ERR_DRAIN_TIMEOUT = 8u,
-  ERR_PROBE_TIMEOUT = 16u,
-  ERR_GEMV_TIMEOUT = 32u
+  ERR_PROBE_TIMEOUT = 16u
 };
 
 // Kernel-level problem of the tensor-core GEMM: D'[Mk, Nk] (row-major, via
@@ -85,8 +84,6 @@ struct GemvArgs {
   long long ldd_m, ldd_n;
   const __half* bias;
   int epi;
-  unsigned int* err;  // device error word (bounded waits of the streaming kernel)
-  long long budget;   // bounded-wait budget in SM clock cycles
   int static_a;       // launch with programmatic dependent launch (A never written upstream)
 };
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);

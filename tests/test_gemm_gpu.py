@@ -210,9 +210,8 @@ def test_split_tail_matches_unsplit(oracle, monkeypatch):
 
 
 @pytest.mark.parametrize("M,N,K", [(4096, 1, 8192), (4096, 3, 8192), (2000, 2, 1024), (1500, 4, 4096)])
-def test_gemv_ring_wraps(oracle, M, N, K):
-    """Streaming GEMV with more rows per SM than ring slots (the ring wraps
-    and every slot is refilled several times)."""
+def test_gemv_many_rows_per_warp(oracle, M, N, K):
+    """GEMV shapes with more rows than warps of the grid, K up to 8192."""
     path = _run_case(oracle, M, N, K, "gelu_bias", "k", "k", "col", seed=60 + N)
     assert path == ge.GE_PATH_GEMV
 

@@ -403,6 +403,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = __half2float(p.bias[grow]);
       float bg_row = 0.0f;  // DRELU_BGRAD, bias per D' row: this tile's row sum
+      // DRELU_BGRAD: this row's mask words for the tile's slabs, loaded up
+      // front so the loads overlap (slabs past Nk read nothing).
+      uint32_t mwords[BN / 32];
+      if (p.epi == EPI_DRELU_BGRAD) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          const int g0 = nt * BN + c * 32;
+          mwords[c] = (grow < p.Mk && g0 < p.Nk) ? p.aux[static_cast<long long>(grow) * p.ld_aux + (g0 >> 5)] : 0u;
+        }
+      }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -448,7 +458,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // dZ = z where the forward mask bit is set, else +0; the masked
           // fp32 values feed the bias-gradient partial sums.
           uint32_t w = 0;
-          if (grow < p.Mk) w = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
+#pragma unroll
+          for (int i = 0; i < BN / 32; ++i)
+            if (i == c) w = mwords[i];  // static indices keep mwords[] in registers
           if (p.Nk - gcol0 < 32) w &= (1u << (p.Nk - gcol0)) - 1u;
           float zm[32];
 #pragma unroll

@@ -60,7 +60,8 @@ EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EP
 ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",
                  "ge_aux_bytes", "ge_aux_ld", "ge_plan_path", "ge_plan_tile_n",
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
-                 "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr")
+                 "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr",
+                 "ge_plan_autotune", "ge_plan_config")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -117,6 +118,10 @@ def load_library():
         lib.ge_drelu_bgrad_static.restype = i32
         lib.ge_plan_set_attr.argtypes = [vp, i32, i64]
         lib.ge_plan_set_attr.restype = i32
+        lib.ge_plan_autotune.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32]
+        lib.ge_plan_autotune.restype = i32
+        lib.ge_plan_config.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.ge_plan_config.restype = i32
         lib.ge_version.argtypes = []
         lib.ge_version.restype = ctypes.c_char_p
         _lib = lib
@@ -189,6 +194,21 @@ def ge_plan_set_attr(plan, attr: int, value: int, *, raw: bool = False):
     _check(st, "ge_plan_set_attr")
 
 
+def ge_plan_autotune(plan, A, B, bias, D, aux=None, stream=None, reps: int = 5, *, raw: bool = False):
+    st = load_library().ge_plan_autotune(plan, _ptr(A), _ptr(B), _ptr(bias), _ptr(D), _ptr(aux),
+                                         _stream(stream), int(reps))
+    if raw:
+        return st
+    _check(st, "ge_plan_autotune")
+
+
+def ge_plan_config(plan):
+    """(path, block_n, pair, split) of the plan."""
+    bn, pr, sp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    path = load_library().ge_plan_config(plan, ctypes.byref(bn), ctypes.byref(pr), ctypes.byref(sp))
+    return path, bn.value, pr.value, sp.value
+
+
 def ge_plan_free(plan):
     _check(load_library().ge_plan_free(plan), "ge_plan_free")
 
@@ -245,6 +265,13 @@ class Plan:
 
     def set_attr(self, attr: int, value: int):
         ge_plan_set_attr(self.handle, attr, value)
+
+    def autotune(self, A, B, bias, D, aux=None, stream=None, reps: int = 5):
+        ge_plan_autotune(self.handle, A, B, bias, D, aux, stream, reps)
+
+    @property
+    def config(self):
+        return ge_plan_config(self.handle)
 
     def execute_unfused(self, A, B, bias, D, aux=None, stream=None):
         ge_execute_unfused(self.handle, A, B, bias, D, aux, stream)

@@ -35,8 +35,11 @@ struct Plan {
   bool swap = false;
   int block_n = 256;
   int pair = 0;  // 2-CTA (cta_group::2) tiles of 256 rows
-  int tail_start = 0;  // split-K tail (see GemmArgs); `partials` holds its pieces
+  int tail_start = 0;  // split-K tail (see GemmArgs); `tail_ws` holds its pieces
   int split = 1;
+  void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
+  size_t tail_ws_bytes = 0;
+  bool tc_allow_split = true;
   float* bg_partials = nullptr;  // DRELU_BGRAD GEMM epilogue: bias-gradient partials
   long long bg_rows = 0, bg_len = 0;
   int grid = 0;
@@ -111,6 +114,80 @@ ge_status_t check_device(Plan* pl, int slot, const void* p) {
     return GE_ERR_DEVICE_MISMATCH;
   if (at.device != pl->device) return GE_ERR_DEVICE_MISMATCH;
   pl->checked[slot] = p;
+  return GE_OK;
+}
+
+// Tensor-core launch configuration for a tile width and pair mode: work
+// units, grid, rasterisation group and the split-K tail.
+struct TcConfig {
+  int block_n = 256, pair = 0, split = 1, tail_start = 0, grid = 1, group_m = 1;
+};
+
+TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
+  TcConfig c;
+  c.block_n = block_n;
+  c.pair = pair;
+  const int64_t Mk = pl.swap ? pl.N : pl.M;
+  const int64_t Nk = pl.swap ? pl.M : pl.N;
+  const int64_t tile_m = pair ? 256 : 128;
+  const long long num_m = (Mk + tile_m - 1) / tile_m;
+  const long long tiles = num_m * ((Nk + block_n - 1) / block_n);
+  const long long workers = pair ? tc_gemm_max_pairs(block_n, pl.num_sms) : pl.num_sms;
+  c.group_m = static_cast<int>(num_m < (pair ? 8 : 16) ? num_m : (pair ? 8 : 16));
+  // Split-K tail: when the last of several waves would leave most workers
+  // idle, the tiles of that wave are split along K into just enough pieces
+  // to occupy the workers (at least 4 k-blocks per piece, at most 16); a
+  // fixup kernel adds the fp32 pieces in order and applies the epilogue.
+  // (Measured: dW 11008x4096x8192 0.423 -> 0.397 ms. Under-filled single-wave
+  // problems are left alone: there the fixup launch costs more than it saves.)
+  const long long num_kb = (pl.K + 63) / 64;
+  const long long rem = tiles % workers;
+  if (allow_split && tiles > workers && rem != 0 && rem * 2 <= workers) {
+    long long S = workers / rem;
+    if (S > num_kb / 4) S = num_kb / 4;
+    if (S > 16) S = 16;
+    if (S >= 2) {
+      c.split = static_cast<int>(S);
+      c.tail_start = static_cast<int>(tiles - rem);
+    }
+  }
+  if (c.split == 1) c.tail_start = static_cast<int>(tiles);
+  const long long units = c.tail_start + (tiles - c.tail_start) * c.split;
+  const long long g = units < workers ? units : workers;
+  c.grid = static_cast<int>(pair ? 2 * g : g);
+  return c;
+}
+
+size_t tc_tail_bytes(const Plan& pl, const TcConfig& c) {
+  if (c.split <= 1) return 0;
+  const int64_t Mk = pl.swap ? pl.N : pl.M;
+  const int64_t Nk = pl.swap ? pl.M : pl.N;
+  const int64_t tile_m = c.pair ? 256 : 128;
+  const int64_t tiles = ((Mk + tile_m - 1) / tile_m) * ((Nk + c.block_n - 1) / c.block_n);
+  return static_cast<size_t>(tiles - c.tail_start) * c.split * tile_m * c.block_n * 4;
+}
+
+// Make `c` the plan's configuration (re-sizing the tail workspace).
+ge_status_t apply_config(Plan* pl, const TcConfig& c) {
+  const size_t need = tc_tail_bytes(*pl, c);
+  if (need > pl->tail_ws_bytes) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) {
+      cudaGetLastError();
+      return GE_ERR_OOM;
+    }
+    if (pl->tail_ws) cudaFree(pl->tail_ws);
+    pl->tail_ws = p;
+    pl->tail_ws_bytes = need;
+  }
+  pl->block_n = c.block_n;
+  pl->pair = c.pair;
+  pl->split = c.split;
+  pl->tail_start = c.tail_start;
+  pl->grid = c.grid;
+  pl->group_m = c.group_m;
+  pl->partials = static_cast<float*>(pl->tail_ws);
+  pl->mapA = pl->mapB = pl->mapD = nullptr;  // B's box depends on the pair mode
   return GE_OK;
 }
 
@@ -194,8 +271,10 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     if (epi_code == EPI_DRELU_BGRAD) g.bias = nullptr;
     e = launch_tc_gemm(pl->block_n, pl->pair, pl->tmA, pl->tmB, pl->tmD, g, pl->grid, st);
     if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, st);
-    if (e == cudaSuccess && epi_code == EPI_DRELU_BGRAD)
-      e = launch_bgrad_reduce(pl->bg_partials, pl->bg_rows, pl->bg_len, g.bgrad, st);
+    if (e == cudaSuccess && epi_code == EPI_DRELU_BGRAD) {
+      const long long rows = pl->swap ? pl->bg_rows : (g.Nk + pl->block_n - 1) / pl->block_n;
+      e = launch_bgrad_reduce(pl->bg_partials, rows, pl->bg_len, g.bgrad, st);
+    }
   }
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
@@ -296,82 +375,35 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     cudaGetLastError();
     return GE_ERR_CUDA;
   }
+  int tc_block_n = 256, tc_pair = 0;
+  bool tc_split = true;
   if (tmp.path == GE_PATH_TC_GEMM) {
     tmp.swap = L.d == GE_D_COL;
     const int64_t Mk = tmp.swap ? N : M;
     const int64_t Nk = tmp.swap ? M : N;
-    const int64_t num_m = (Mk + 127) / 128;
-    const long long t256 = num_m * ((Nk + 255) / 256);
-    const long long t128 = num_m * ((Nk + 127) / 128);
+    const long long t256 = ((Mk + 127) / 128) * ((Nk + 255) / 256);
     // 128 x 256 tiles move a third less shared-memory traffic per flop than
     // 128 x 128 ones (measured: the 11008x4096x8192 dW GEMM runs 1.54x faster
     // with them), so 128-wide tiles are used only when 256-wide ones would
     // leave more than half of the SMs without a tile.
-    tmp.block_n = (Nk <= 128 || t256 * 2 < tmp.num_sms) ? 128 : 256;
-    (void)t128;
-    // GE_TILE_N=128|256 overrides the choice (tile-width sweeps).
-    if (const char* env = std::getenv("GE_TILE_N")) {
+    tc_block_n = (Nk <= 128 || t256 * 2 < tmp.num_sms) ? 128 : 256;
+    if (const char* env = std::getenv("GE_TILE_N")) {  // tile-width sweeps
       const int want = std::atoi(env);
-      if (want == 128 || want == 256) tmp.block_n = want;
+      if (want == 128 || want == 256) tc_block_n = want;
     }
     // 2-CTA pairs (256-row tiles) once there are enough of them to give
     // every pair of SMs at least one tile.
-    const long long num_m2 = (Mk + 255) / 256;
-    const long long pair_tiles = num_m2 * ((Nk + tmp.block_n - 1) / tmp.block_n);
-    tmp.pair = (tmp.block_n == 256 && pair_tiles * 2 >= tmp.num_sms) ? 1 : 0;
+    const long long pair_tiles = ((Mk + 255) / 256) * ((Nk + tc_block_n - 1) / tc_block_n);
+    tc_pair = (tc_block_n == 256 && pair_tiles * 2 >= tmp.num_sms) ? 1 : 0;
     if (const char* env = std::getenv("GE_PAIR")) {
-      if (env[0] == '0') tmp.pair = 0;
-      if (env[0] == '1') tmp.pair = 1;
+      if (env[0] == '0') tc_pair = 0;
+      if (env[0] == '1') tc_pair = 1;
     }
-    long long tiles = 0, workers = 0;
-    if (tmp.pair) {
-      workers = tc_gemm_max_pairs(tmp.block_n, tmp.num_sms);
-      tiles = pair_tiles;
-      tmp.group_m = static_cast<int>(num_m2 < 8 ? num_m2 : 8);
-    } else {
-      workers = tmp.num_sms;
-      tiles = tmp.block_n == 256 ? t256 : t128;
-      tmp.group_m = static_cast<int>(num_m < 16 ? num_m : 16);
-    }
-    // Split-K tail: when the last of several waves would leave most workers
-    // idle, the tiles of that wave are split along K into just enough pieces
-    // to occupy the workers (at least 4 k-blocks per piece, at most 16); a
-    // fixup kernel adds the fp32 pieces in order and applies the epilogue.
-    // (Measured: dW 11008x4096x8192 0.423 -> 0.397 ms. Under-filled single-wave
-    // problems are left alone: there the fixup launch costs more than it saves.)
-    const long long num_kb = (K + 63) / 64;
-    const long long rem = tiles % workers;
-    if (tiles > workers && rem != 0 && rem * 2 <= workers) {
-      long long S = workers / rem;
-      if (S > num_kb / 4) S = num_kb / 4;
-      if (S > 16) S = 16;
-      if (S >= 2) {
-        tmp.split = static_cast<int>(S);
-        tmp.tail_start = static_cast<int>(tiles - rem);
-      }
-    }
-    if (const char* env = std::getenv("GE_SPLIT_TAIL")) {
-      if (env[0] == '0') {
-        tmp.split = 1;
-        tmp.tail_start = 0;
-      }
-    }
-    if (epi == GE_EPI_DRELU_BGRAD) tmp.split = 1;  // its bias-gradient partials are per tile
-    if (tmp.split == 1) tmp.tail_start = static_cast<int>(tiles);
-    const long long units = tmp.tail_start + (tiles - tmp.tail_start) * tmp.split;
-    const long long g = units < workers ? units : workers;
-    tmp.grid = static_cast<int>(tmp.pair ? 2 * g : g);
+    if (const char* env = std::getenv("GE_SPLIT_TAIL"))
+      if (env[0] == '0') tc_split = false;
+    if (epi == GE_EPI_DRELU_BGRAD) tc_split = false;  // its bias-gradient partials are per tile
   }
   size_t ws = 256;
-  size_t partial_off = 0;
-  if (tmp.path == GE_PATH_TC_GEMM && tmp.split > 1) {
-    const int64_t Mk = tmp.swap ? N : M;
-    const int64_t Nk = tmp.swap ? M : N;
-    const int64_t tile_m = tmp.pair ? 256 : 128;
-    const int64_t tiles = ((Mk + tile_m - 1) / tile_m) * ((Nk + tmp.block_n - 1) / tmp.block_n);
-    partial_off = ws;
-    ws += static_cast<size_t>(tiles - tmp.tail_start) * tmp.split * tile_m * tmp.block_n * 4;
-  }
   size_t bg_off = 0;
   if (tmp.path == GE_PATH_TC_GEMM && epi == GE_EPI_DRELU_BGRAD) {
     const int64_t Mk = tmp.swap ? N : M;
@@ -379,8 +411,8 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (tmp.swap) {  // bgrad indexes D' columns: partials per 32-row block
       tmp.bg_rows = (Mk + 31) / 32;
       tmp.bg_len = Nk;
-    } else {         // bgrad indexes D' rows: partials per n-tile
-      tmp.bg_rows = (Nk + tmp.block_n - 1) / tmp.block_n;
+    } else {         // bgrad indexes D' rows: partials per n-tile (capacity: 128-wide tiles)
+      tmp.bg_rows = (Nk + 127) / 128;
       tmp.bg_len = Mk;
     }
     ws = (ws + 255) / 256 * 256;
@@ -405,7 +437,6 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   }
   tmp.ws_bytes = ws;
   tmp.err = static_cast<unsigned int*>(tmp.ws);
-  if (partial_off) tmp.partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + partial_off);
   if (bg_off) tmp.bg_partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + bg_off);
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
     tmp.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + 256);
@@ -418,6 +449,15 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   if (!pl) {
     cudaFree(tmp.ws);
     return GE_ERR_OOM;
+  }
+  if (pl->path == GE_PATH_TC_GEMM) {
+    pl->tc_allow_split = tc_split;
+    ge_status_t st = apply_config(pl, tc_config(*pl, tc_block_n, tc_pair, tc_split));
+    if (st != GE_OK) {
+      cudaFree(pl->ws);
+      delete pl;
+      return st;
+    }
   }
   *out = reinterpret_cast<ge_plan_t>(pl);
   return GE_OK;
@@ -511,6 +551,67 @@ ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B, con
   return GE_OK;
 }
 
+ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const void* bias, void* D,
+                             void* aux, void* stream, int reps) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl || reps < 1 || reps > 1000) return GE_ERR_INVALID_ARG;
+  if (pl->path != GE_PATH_TC_GEMM) return GE_OK;  // nothing to choose
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const TcConfig current = tc_config(*pl, pl->block_n, pl->pair, pl->split > 1 || pl->tc_allow_split);
+  TcConfig cands[6];
+  int n = 0;
+  for (int bn : {128, 256})
+    for (int pair : {0, 1}) {
+      if (pair && bn != 256) continue;
+      cands[n++] = tc_config(*pl, bn, pair, false);
+      if (pl->tc_allow_split) {
+        const TcConfig c = tc_config(*pl, bn, pair, true);
+        if (c.split > 1) cands[n++] = c;
+      }
+    }
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  int best = -1;
+  float best_ms = 0.0f;
+  ge_status_t s = GE_OK;
+  for (int i = 0; i < n && s == GE_OK; ++i) {
+    if ((s = apply_config(pl, cands[i])) != GE_OK) break;
+    if ((s = ge_execute(plan, A, B, bias, D, aux, stream)) != GE_OK) break;  // warm-up, checks args
+    cudaEventRecord(e0, st);
+    for (int r = 0; r < reps && s == GE_OK; ++r) s = ge_execute(plan, A, B, bias, D, aux, stream);
+    cudaEventRecord(e1, st);
+    if (cudaEventSynchronize(e1) != cudaSuccess) {
+      cudaGetLastError();
+      s = GE_ERR_CUDA;
+      break;
+    }
+    float ms = 0.0f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (best < 0 || ms < best_ms) {
+      best = i;
+      best_ms = ms;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  const ge_status_t s2 = apply_config(pl, best >= 0 ? cands[best] : current);
+  if (s != GE_OK) return s;
+  if (s2 != GE_OK) return s2;
+  return ge_execute(plan, A, B, bias, D, aux, stream);  // outputs of the chosen configuration
+}
+
+int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return -1;
+  if (block_n) *block_n = pl->path == GE_PATH_TC_GEMM ? pl->block_n : 0;
+  if (pair) *pair = pl->path == GE_PATH_TC_GEMM ? pl->pair : 0;
+  if (split) *split = pl->path == GE_PATH_TC_GEMM ? pl->split : 0;
+  return static_cast<int>(pl->path);
+}
+
 ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl) return GE_ERR_INVALID_ARG;
@@ -528,6 +629,10 @@ ge_status_t ge_plan_free(ge_plan_t plan) {
   if (!pl) return GE_OK;
   ge_status_t s = GE_OK;
   if (pl->ws && cudaFree(pl->ws) != cudaSuccess) {
+    cudaGetLastError();
+    s = GE_ERR_CUDA;
+  }
+  if (pl->tail_ws && cudaFree(pl->tail_ws) != cudaSuccess) {
     cudaGetLastError();
     s = GE_ERR_CUDA;
   }

@@ -199,6 +199,28 @@ typedef enum {
  * plan, an unknown attribute or a value outside its range. */
 ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value);
 
+/*
+ * ge_plan_autotune: choose the plan's kernel configuration by timing.
+ * Planning picks a configuration from the problem's shape; this call instead
+ * runs every candidate of the tensor-core path (128- or 256-column tiles,
+ * single-CTA or 2-SM pair tiles, with and without the split-K tail) `reps`
+ * times on the caller's buffers (same meaning as ge_execute), keeps the
+ * fastest for every later execute, and finishes with one execute in that
+ * configuration, so D / aux / bias hold its results. It blocks the host until
+ * the timing runs finish and may re-allocate the plan's tail workspace.
+ * Plans of the other paths are left unchanged (GE_OK). reps in 1..1000.
+ * Returns GE_OK or the first failing status (the plan then keeps a valid
+ * configuration).
+ */
+ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B,
+                             const void* bias, void* D, void* aux, void* stream,
+                             int reps);
+
+/* The plan's tensor-core configuration: tile width, 2-SM pair mode (0/1)
+ * and split-K pieces of the tail (1 = none); zeros for other paths. Any
+ * pointer may be NULL. Returns the path, or -1 for a NULL plan. */
+int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split);
+
 /* Release the plan and its device workspace (NULL is accepted). The caller
  * must make sure no execute of the plan is still running on the GPU. */
 ge_status_t ge_plan_free(ge_plan_t plan);

@@ -273,3 +273,27 @@ def test_gelu_erf_pair_gemv_unfused(oracle, monkeypatch):
     monkeypatch.setenv("GE_PAIR", "1")
     monkeypatch.setenv("GE_TILE_N", "256")
     _run_case(oracle, 1000, 2056, 520, "gelu_erf_bias", "k", "k", "col", seed=83)  # pairs + split tail
+
+
+def test_autotune_picks_a_candidate_and_stays_correct(oracle):
+    """Plan-time selection by timing: the chosen configuration is one of the
+    candidates, the outputs it leaves are correct, and later executes agree."""
+    M, N, K = 1500, 2056, 1024
+    w = Workload("autotune", M, N, K, "relu_aux_bias", "k", "n", "row")
+    A, B, bias = w.make("cuda")
+    with ge.Plan(M, N, K, ge.GE_EPI_RELU_AUX_BIAS, ge.make_layout(ge.GE_K_MAJOR, ge.GE_MN_MAJOR, ge.GE_D_ROW)) as p:
+        D = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        aux = torch.empty(p.aux_bytes // 4, dtype=torch.int32, device="cuda")
+        p.autotune(A, B, bias, D, aux, reps=3)
+        torch.cuda.synchronize()
+        path, bn, pair, split = p.config
+        assert path == ge.GE_PATH_TC_GEMM and bn in (128, 256) and pair in (0, 1) and split >= 1
+        assert not (pair and bn != 256)
+        ref = oracle_full(oracle, w, A.cpu(), B.cpu(), bias.cpu())
+        check_f16(oracle, bits(D), ref["D"], "autotuned")
+        check_mask(aux.cpu().numpy().view(np.uint32), ref["aux"], ref["Z"], M, N, p.aux_ld, "autotuned")
+        D2 = torch.empty_like(D)
+        p.execute(A, B, bias, D2, aux)
+        torch.cuda.synchronize()
+        assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK

@@ -49,41 +49,55 @@ __global__ void __launch_bounds__(256) bias_add_kernel(__half* D, long long R, l
   }
 }
 
-// D = act(D) in place; with a mask, one thread owns 32 contiguous elements
-// (one mask word) and writes the word, zero padding included.
+// D = act(D) in place, 8 contiguous fp16 per lane (a warp reads 512
+// contiguous bytes). With a mask, four consecutive lanes cover one 32-element
+// mask word: each builds its byte and lane 0 of the four writes the word
+// (padding words up to the row's 128-column boundary included).
 __global__ void __launch_bounds__(256) activation_kernel(__half* D, long long R, long long C,
                                                           long long ld, int epi, uint32_t* aux,
                                                           long long ld_aux) {
-  const long long wpr = aux ? ld_aux : (C + 31) / 32;  // 32-wide groups per row
-  const long long total = R * wpr;
+  const long long wpr = aux ? ld_aux : (C + 31) / 32;  // 32-element words per row
+  const long long units = R * wpr * 4;                 // one unit = 8 elements
+  const long long pad_cols = ((C + 127) / 128) * 128;
+  // the loop bound is a multiple of 32 so whole warps iterate together
+  const long long total = (units + 31) & ~31LL;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
-    const long long r = i / wpr;
-    const long long g = i - r * wpr;
-    const long long c0 = g * 32;
-    __half* row = D + r * ld;
-    uint32_t bits = 0;
-    if (c0 + 32 <= C) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 v = *reinterpret_cast<const uint4*>(row + c0 + 8 * q);
+    uint32_t byte = 0;
+    long long r = 0, word = 0, c0 = 0;
+    const bool live = i < units;
+    if (live) {
+      const long long u = i >> 2;
+      r = u / wpr;
+      word = u - r * wpr;
+      c0 = word * 32 + (i & 3) * 8;
+      __half* row = D + r * ld;
+      if (c0 + 8 <= C) {
+        uint4 v = *reinterpret_cast<const uint4*>(row + c0);
         __half2* h = reinterpret_cast<__half2*>(&v);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float2 f = __half22float2(h[t]);
-          bits |= (f.x > 0.0f ? 1u : 0u) << (8 * q + 2 * t);
-          bits |= (f.y > 0.0f ? 1u : 0u) << (8 * q + 2 * t + 1);
+          byte |= (f.x > 0.0f ? 1u : 0u) << (2 * t);
+          byte |= (f.y > 0.0f ? 1u : 0u) << (2 * t + 1);
           h[t] = __floats2half2_rn(act_of(epi, f.x), act_of(epi, f.y));
         }
-        *reinterpret_cast<uint4*>(row + c0 + 8 * q) = v;
-      }
-    } else {
-      for (long long c = c0; c < C; ++c) {
-        const float f = __half2float(row[c]);
-        bits |= (f > 0.0f ? 1u : 0u) << (c - c0);
-        row[c] = __float2half_rn(act_of(epi, f));
+        *reinterpret_cast<uint4*>(row + c0) = v;
+      } else {
+        for (long long c = c0; c < C && c < c0 + 8; ++c) {
+          const float f = __half2float(row[c]);
+          byte |= (f > 0.0f ? 1u : 0u) << (c - c0);
+          row[c] = __float2half_rn(act_of(epi, f));
+        }
       }
     }
-    if (aux && epi == EPI_RELU_AUX_BIAS && c0 < ((C + 127) / 128) * 128) aux[r * ld_aux + g] = bits;
+    if (aux && epi == EPI_RELU_AUX_BIAS) {
+      const int lane = threadIdx.x & 31;
+      const int base = lane & ~3;
+      uint32_t wv = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) wv |= __shfl_sync(0xffffffffu, byte, base + q) << (8 * q);
+      if (live && (lane & 3) == 0 && word * 32 < pad_cols) aux[r * ld_aux + word] = wv;
+    }
   }
 }
 
@@ -122,7 +136,7 @@ cudaError_t launch_activation(__half* D, long long R, long long C, long long ld,
                               uint32_t* aux, long long ld_aux, cudaStream_t s) {
   if (R == 0 || C == 0) return cudaSuccess;
   const long long wpr = aux ? ld_aux : (C + 31) / 32;
-  activation_kernel<<<grid_for(R * wpr, 256), 256, 0, s>>>(D, R, C, ld, epi, aux, ld_aux);
+  activation_kernel<<<grid_for(R * wpr * 4, 256), 256, 0, s>>>(D, R, C, ld, epi, aux, ld_aux);
   return cudaGetLastError();
 }
 

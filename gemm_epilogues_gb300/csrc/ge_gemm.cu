@@ -403,16 +403,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = __half2float(p.bias[grow]);
       float bg_row = 0.0f;  // DRELU_BGRAD, bias per D' row: this tile's row sum
-      // DRELU_BGRAD: this row's mask words for the tile's slabs, loaded up
-      // front so the loads overlap (slabs past Nk read nothing).
-      uint32_t mwords[BN / 32];
-      if (p.epi == EPI_DRELU_BGRAD) {
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          const int g0 = nt * BN + c * 32;
-          mwords[c] = (grow < p.Mk && g0 < p.Nk) ? p.aux[static_cast<long long>(grow) * p.ld_aux + (g0 >> 5)] : 0u;
-        }
-      }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -425,6 +415,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = 0u;
           continue;
         }
+        // DRELU_BGRAD: the slab's mask word is requested before the TMEM load
+        // so the two latencies overlap.
+        uint32_t mword = 0;
+        if (p.epi == EPI_DRELU_BGRAD && grow < p.Mk)
+          mword = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + 32u * c, v);
         tmem_ld_wait();
@@ -457,10 +452,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (p.epi == EPI_DRELU_BGRAD) {
           // dZ = z where the forward mask bit is set, else +0; the masked
           // fp32 values feed the bias-gradient partial sums.
-          uint32_t w = 0;
-#pragma unroll
-          for (int i = 0; i < BN / 32; ++i)
-            if (i == c) w = mwords[i];  // static indices keep mwords[] in registers
+          uint32_t w = mword;
           if (p.Nk - gcol0 < 32) w &= (1u << (p.Nk - gcol0)) - 1u;
           float zm[32];
 #pragma unroll

@@ -297,3 +297,42 @@ def test_autotune_picks_a_candidate_and_stays_correct(oracle):
         torch.cuda.synchronize()
         assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
         assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+
+
+@pytest.mark.parametrize("epi", EPIS + ["gelu_erf_bias"])
+@pytest.mark.parametrize("kind", ["zeros", "overflow", "nan"])
+def test_degenerate_values(oracle, epi, kind):
+    """Zero operands (D = act(bias)), results beyond fp16 range (rounded to
+    +-inf on both sides) and NaN inputs (propagated by the product; ReLU maps
+    NaN to 0 on both sides, the mask bit of NaN is 0)."""
+    M, N, K = 160, 96, 64
+    w = Workload(f"{kind} {epi}", M, N, K, epi, "k", "n", "row")
+    A = f16_tensor((M, K), 90, "normal", 1.0)
+    B = f16_tensor((K, N), 91, "normal", 1.0)
+    bias = f16_tensor((M,), 92, "normal", 1.0)
+    if kind == "zeros":
+        A.zero_()
+    elif kind == "overflow":
+        A[:8] = 200.0           # 64 * 200 * |B| exceeds 65504 for many entries
+        B[:, :8] = 250.0
+    else:
+        A[3, 5] = float("nan")  # row 3 of D is NaN (before the activation)
+        B[7, 11] = float("nan")  # column 11 of D is NaN
+    A, B, bias = A.cuda(), B.cuda(), bias.cuda()
+    D, aux, path, ld_aux = gpu_forward(w, A, B, bias)
+    ref = oracle_full(oracle, w, A.cpu(), B.cpu(), bias.cpu())
+    got = oracle.f16_decode(bits(D))
+    want = oracle.f16_decode(ref["D"])
+    assert np.array_equal(np.isnan(got), np.isnan(want)), "NaN positions differ"
+    assert np.array_equal(np.isinf(got), np.isinf(want)), "inf positions differ"
+    fin = np.isfinite(want)
+    assert np.array_equal(np.sign(got[~fin & ~np.isnan(want)]), np.sign(want[~fin & ~np.isnan(want)]))
+    err = np.abs(got[fin] - want[fin])
+    assert (err <= 1e-2 * np.maximum(1.0, np.abs(want[fin]))).all()
+    if epi == "relu_aux_bias":
+        z = ref["Z"].reshape(M, N)
+        sure = np.abs(np.nan_to_num(z, nan=1.0)) > 1e-3
+        from _util import mask_bits
+        g = mask_bits(aux.cpu().numpy().view(np.uint32), M, ld_aux, N)
+        r = mask_bits(ref["aux"], M, ld_aux, N)
+        assert np.array_equal(g[sure], r[sure])

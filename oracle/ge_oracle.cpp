@@ -12,6 +12,7 @@
 //          + bias[m]                (broadcast over every column) -- BIAS
 //   y[m,n] = act(z[m,n])            NONE | ReLU | tanh-GELU | erf-GELU
 //   D[m,n] = fp16(y[m,n])           round to nearest even         -- one store
+//            (or bfloat16: the *_dt entry points take the element type)
 //   mask   = (z > 0) bit-packed     (RELU_AUX_BIAS only)          -- aux output
 //
 // Sources (page title, section):
@@ -99,6 +100,46 @@ uint16_t f16_encode(double x) {
   return s | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0);
 }
 
+// bfloat16 -> binary64: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.
+double bf16_decode(uint16_t h) {
+  const int s = h >> 15;
+  const int e = (h >> 7) & 255;
+  const int f = h & 127;
+  double v;
+  if (e == 0)
+    v = std::ldexp((double)f, -133);             // zero / subnormal: f * 2^-133
+  else if (e == 255)
+    v = f ? std::nan("") : INFINITY;
+  else
+    v = std::ldexp((double)(128 + f), e - 134);  // (1 + f/128) * 2^(e-127)
+  return s ? -v : v;
+}
+
+// binary64 -> bfloat16, round to nearest even, overflow to +-inf, subnormals kept.
+uint16_t bf16_encode(double x) {
+  if (std::isnan(x)) return 0x7FC0;
+  const uint16_t s = std::signbit(x) ? 0x8000 : 0;
+  const double a = std::fabs(x);
+  // largest finite: (2 - 2^-7) 2^127; the midpoint to 2^128 ties to the
+  // even neighbour, which is the overflow.
+  if (a >= std::ldexp(511.0, 119)) return s | 0x7F80;  // midpoint (2 - 2^-8) 2^127 = 511 * 2^119
+  if (a < std::ldexp(1.0, -126)) {
+    const double q = round_half_even(std::ldexp(a, 133));  // units of 2^-133, q <= 128
+    return s | (uint16_t)q;
+  }
+  int E;
+  std::frexp(a, &E);
+  int e = E - 1;                                        // a in [2^e, 2^(e+1))
+  double q = round_half_even(std::ldexp(a, 7 - e));     // in [128, 256]
+  if (q == 256.0) { q = 128.0; e += 1; }
+  if (e + 127 >= 255) return s | 0x7F80;
+  return s | (uint16_t)((e + 127) << 7) | (uint16_t)(q - 128.0);
+}
+
+// Element type of the operands, bias and output: 0 = fp16, 1 = bfloat16.
+double decode(int dt, uint16_t h) { return dt == 0 ? f16_decode(h) : bf16_decode(h); }
+uint16_t encode(int dt, double x) { return dt == 0 ? f16_encode(x) : bf16_encode(x); }
+
 // The activation applied after the bias add.
 double activation(int epi, double z) {
   switch (epi) {
@@ -143,6 +184,14 @@ void parallel_rows(int64_t rows, int nthreads, F fn) {
 extern "C" {
 
 double ora_f16_to_f64(uint16_t h) { return f16_decode(h); }
+double ora_bf16_to_f64(uint16_t h) { return bf16_decode(h); }
+uint16_t ora_f64_to_bf16(double x) { return bf16_encode(x); }
+void ora_bf16_to_f64_array(const uint16_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = bf16_decode(in[i]);
+}
+void ora_f64_to_bf16_array(const double* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = bf16_encode(in[i]);
+}
 // The activation of epilogue `epi` applied to one fp64 pre-activation value
 // (the same function the forward uses); -1 selects nothing and returns NaN.
 double ora_act_f64(int epi, double z) {
@@ -168,13 +217,16 @@ void ora_f64_to_f16_array(const double* in, uint16_t* out, int64_t n) {
 //   Z (optional, may be NULL): the fp64 pre-activation z, laid out like D.
 //   bias may be NULL only for ORA_NONE.
 // Returns 0 on success, -1 on a bad argument.
-int ora_linear_forward(int64_t M, int64_t N, int64_t K,
-                       const uint16_t* A, int a_major, int64_t lda,
-                       const uint16_t* B, int b_major, int64_t ldb,
-                       const uint16_t* bias, int epi,
-                       uint16_t* D, int d_layout, int64_t ldd,
-                       uint32_t* aux, int64_t ld_aux, double* Z,
-                       int nthreads) {
+// Same as ora_linear_forward with every operand, the bias and D of element
+// type `dt` (0 = fp16, 1 = bfloat16).
+int ora_linear_forward_dt(int dt, int64_t M, int64_t N, int64_t K,
+                          const uint16_t* A, int a_major, int64_t lda,
+                          const uint16_t* B, int b_major, int64_t ldb,
+                          const uint16_t* bias, int epi,
+                          uint16_t* D, int d_layout, int64_t ldd,
+                          uint32_t* aux, int64_t ld_aux, double* Z,
+                          int nthreads) {
+  if (dt != 0 && dt != 1) return -1;
   if (M < 0 || N < 0 || K < 0 || !D) return -1;
   if (!valid_forward_epi(epi)) return -1;
   if (epi != ORA_NONE && !bias) return -1;
@@ -190,11 +242,11 @@ int ora_linear_forward(int64_t M, int64_t N, int64_t K,
   std::vector<double> Ad((size_t)M * (size_t)K), Bd((size_t)N * (size_t)K);
   parallel_rows(M, nthreads, [&](int64_t m) {
     for (int64_t k = 0; k < K; ++k)
-      Ad[m * K + k] = f16_decode(a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
+      Ad[m * K + k] = decode(dt, a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
   });
   parallel_rows(N, nthreads, [&](int64_t n) {
     for (int64_t k = 0; k < K; ++k)
-      Bd[n * K + k] = f16_decode(b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
+      Bd[n * K + k] = decode(dt, b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
   });
 
   parallel_rows(rows, nthreads, [&](int64_t r) {
@@ -207,15 +259,26 @@ int ora_linear_forward(int64_t M, int64_t N, int64_t K,
       const double* b = Bd.data() + n * K;
       double z = 0.0;
       for (int64_t k = 0; k < K; ++k) z += a[k] * b[k];
-      if (epi != ORA_NONE) z += f16_decode(bias[m]);
+      if (epi != ORA_NONE) z += decode(dt, bias[m]);
       const double y = activation(epi, z);
-      D[r * ldd + c] = f16_encode(y);
+      D[r * ldd + c] = encode(dt, y);
       if (Z) Z[r * ldd + c] = z;
       if (epi == ORA_RELU_AUX_BIAS && z > 0.0)
         aux[r * ld_aux + c / 32] |= (uint32_t)1u << (c % 32);
     }
   });
   return 0;
+}
+
+int ora_linear_forward(int64_t M, int64_t N, int64_t K,
+                       const uint16_t* A, int a_major, int64_t lda,
+                       const uint16_t* B, int b_major, int64_t ldb,
+                       const uint16_t* bias, int epi,
+                       uint16_t* D, int d_layout, int64_t ldd,
+                       uint32_t* aux, int64_t ld_aux, double* Z,
+                       int nthreads) {
+  return ora_linear_forward_dt(0, M, N, K, A, a_major, lda, B, b_major, ldb, bias, epi, D,
+                               d_layout, ldd, aux, ld_aux, Z, nthreads);
 }
 
 // DRELU_BGRAD as the epilogue of a GEMM (the backward product dH = A.B whose
@@ -226,12 +289,13 @@ int ora_linear_forward(int64_t M, int64_t N, int64_t K,
 //   dZ[m,n]   = fp16(z[m,n]) if bit(m,n) else +0
 //   bgrad[m]  = sum over n of z[m,n]*bit(m,n)  (fp64, n ascending, unrounded z)
 // Layouts as ora_linear_forward; aux is the forward mask in D's layout.
-int ora_gemm_drelu_bgrad(int64_t M, int64_t N, int64_t K,
-                         const uint16_t* A, int a_major, int64_t lda,
-                         const uint16_t* B, int b_major, int64_t ldb,
-                         const uint32_t* aux, int64_t ld_aux,
-                         uint16_t* dZ, int d_layout, int64_t ldd, double* bgrad,
-                         int nthreads) {
+int ora_gemm_drelu_bgrad_dt(int dt, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* A, int a_major, int64_t lda,
+                            const uint16_t* B, int b_major, int64_t ldb,
+                            const uint32_t* aux, int64_t ld_aux,
+                            uint16_t* dZ, int d_layout, int64_t ldd, double* bgrad,
+                            int nthreads) {
+  if (dt != 0 && dt != 1) return -1;
   if (M < 0 || N < 0 || K < 0 || !dZ || !aux || !bgrad) return -1;
   const int64_t cols = d_layout == 0 ? N : M;
   if (ldd < cols || ld_aux * 32 < cols) return -1;
@@ -239,11 +303,11 @@ int ora_gemm_drelu_bgrad(int64_t M, int64_t N, int64_t K,
   std::vector<double> Ad((size_t)M * (size_t)K), Bd((size_t)N * (size_t)K);
   parallel_rows(M, nthreads, [&](int64_t m) {
     for (int64_t k = 0; k < K; ++k)
-      Ad[m * K + k] = f16_decode(a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
+      Ad[m * K + k] = decode(dt, a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
   });
   parallel_rows(N, nthreads, [&](int64_t n) {
     for (int64_t k = 0; k < K; ++k)
-      Bd[n * K + k] = f16_decode(b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
+      Bd[n * K + k] = decode(dt, b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
   });
   parallel_rows(M, nthreads, [&](int64_t m) {
     double s = 0.0;
@@ -255,12 +319,22 @@ int ora_gemm_drelu_bgrad(int64_t M, int64_t N, int64_t K,
       const int64_t r = d_layout == 0 ? m : n;
       const int64_t c = d_layout == 0 ? n : m;
       const bool bit = (aux[r * ld_aux + c / 32] >> (c % 32)) & 1u;
-      dZ[r * ldd + c] = bit ? f16_encode(z) : (uint16_t)0;
+      dZ[r * ldd + c] = bit ? encode(dt, z) : (uint16_t)0;
       if (bit) s += z;
     }
     bgrad[m] = s;
   });
   return 0;
+}
+
+int ora_gemm_drelu_bgrad(int64_t M, int64_t N, int64_t K,
+                         const uint16_t* A, int a_major, int64_t lda,
+                         const uint16_t* B, int b_major, int64_t ldb,
+                         const uint32_t* aux, int64_t ld_aux,
+                         uint16_t* dZ, int d_layout, int64_t ldd, double* bgrad,
+                         int nthreads) {
+  return ora_gemm_drelu_bgrad_dt(0, M, N, K, A, a_major, lda, B, b_major, ldb, aux, ld_aux, dZ,
+                                 d_layout, ldd, bgrad, nthreads);
 }
 
 // Backward epilogue (DRELU_BGRAD), from the page's description: apply the
@@ -269,9 +343,10 @@ int ora_gemm_drelu_bgrad(int64_t M, int64_t N, int64_t K,
 //   aux: the forward mask (same packing as ora_linear_forward).
 //   dZ[m,n] = dY[m,n] if bit(m,n) else +0.
 //   bgrad[m] = sum over n of dZ[m,n], n ascending, fp64.
-int ora_drelu_bgrad(int64_t M, int64_t N, const uint16_t* dY, int d_layout,
-                    int64_t ldd, const uint32_t* aux, int64_t ld_aux,
-                    uint16_t* dZ, double* bgrad) {
+int ora_drelu_bgrad_dt(int dt, int64_t M, int64_t N, const uint16_t* dY, int d_layout,
+                       int64_t ldd, const uint32_t* aux, int64_t ld_aux,
+                       uint16_t* dZ, double* bgrad) {
+  if (dt != 0 && dt != 1) return -1;
   if (M < 0 || N < 0 || !dY || !aux || !dZ || !bgrad) return -1;
   for (int64_t m = 0; m < M; ++m) bgrad[m] = 0.0;
   for (int64_t m = 0; m < M; ++m) {
@@ -284,11 +359,17 @@ int ora_drelu_bgrad(int64_t M, int64_t N, const uint16_t* dY, int d_layout,
       // gradient is +0 (a select, so -0, inf or NaN in dY do not leak).
       const uint16_t out = bit ? dY[r * ldd + c] : (uint16_t)0;
       dZ[r * ldd + c] = out;
-      s += f16_decode(out);
+      s += decode(dt, out);
     }
     bgrad[m] = s;
   }
   return 0;
+}
+
+int ora_drelu_bgrad(int64_t M, int64_t N, const uint16_t* dY, int d_layout,
+                    int64_t ldd, const uint32_t* aux, int64_t ld_aux,
+                    uint16_t* dZ, double* bgrad) {
+  return ora_drelu_bgrad_dt(0, M, N, dY, d_layout, ldd, aux, ld_aux, dZ, bgrad);
 }
 
 }  // extern "C"

@@ -62,6 +62,18 @@ def _load():
             lib.ora_f64_to_f16.restype = ctypes.c_uint16
             lib.ora_act_f64.argtypes = [i32, ctypes.c_double]
             lib.ora_act_f64.restype = ctypes.c_double
+            lib.ora_bf16_to_f64_array.argtypes = [vp, vp, i64]
+            lib.ora_bf16_to_f64_array.restype = None
+            lib.ora_f64_to_bf16_array.argtypes = [vp, vp, i64]
+            lib.ora_f64_to_bf16_array.restype = None
+            lib.ora_linear_forward_dt.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64,
+                                                  vp, i32, vp, i32, i64, vp, i64, vp, i32]
+            lib.ora_linear_forward_dt.restype = i32
+            lib.ora_drelu_bgrad_dt.argtypes = [i32, i64, i64, vp, i32, i64, vp, i64, vp, vp]
+            lib.ora_drelu_bgrad_dt.restype = i32
+            lib.ora_gemm_drelu_bgrad_dt.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64, vp,
+                                                    i64, vp, i32, i64, vp, i32]
+            lib.ora_gemm_drelu_bgrad_dt.restype = i32
             lib.ora_f16_to_f64_array.argtypes = [vp, vp, i64]
             lib.ora_f16_to_f64_array.restype = None
             lib.ora_f64_to_f16_array.argtypes = [vp, vp, i64]
@@ -82,6 +94,9 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+DTYPES = {"f16": 0, "bf16": 1}
+
+
 def _u16(a):
     a = np.ascontiguousarray(a)
     if a.dtype == np.float16:
@@ -96,11 +111,25 @@ def default_ld_aux(contiguous_len: int) -> int:
     return ((contiguous_len + 127) // 128) * 4
 
 
-def f16_decode(bits) -> np.ndarray:
+def f16_decode(bits, dtype: str = "f16") -> np.ndarray:
+    """Bit patterns of fp16 (or, with dtype="bf16", bfloat16) values -> fp64."""
     lib = _load()
     bits = _u16(bits)
     out = np.empty(bits.shape, np.float64)
-    lib.ora_f16_to_f64_array(_ptr(bits), _ptr(out), bits.size)
+    fn = lib.ora_f16_to_f64_array if dtype == "f16" else lib.ora_bf16_to_f64_array
+    fn(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def bf16_decode(bits) -> np.ndarray:
+    return f16_decode(bits, "bf16")
+
+
+def bf16_encode(x) -> np.ndarray:
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    lib.ora_f64_to_bf16_array(_ptr(x), _ptr(out), x.size)
     return out
 
 
@@ -121,8 +150,9 @@ def linear_forward(A, B, bias, epilogue: str, M: int, N: int, K: int, *,
                    a_major: str = "k", b_major: str = "k", d_layout: str = "row",
                    lda: int | None = None, ldb: int | None = None,
                    ldd: int | None = None, ld_aux: int | None = None,
-                   threads: int | None = None) -> dict:
-    """D = act(A.B + bias) in fp64, rounded once to fp16.
+                   threads: int | None = None, dtype: str = "f16") -> dict:
+    """D = act(A.B + bias) in fp64, rounded once to fp16 (or bfloat16 with
+    dtype="bf16"; A, B, bias and D all of that type).
 
     Returns ``{"D": uint16 bits, "Z": fp64 pre-activation, "aux": uint32 mask
     words or None}``; D and Z are flat arrays of ``rows*ldd`` elements in the
@@ -147,17 +177,17 @@ def linear_forward(A, B, bias, epilogue: str, M: int, N: int, K: int, *,
     aux = np.zeros(rows * ld_aux, np.uint32) if epilogue == "relu_aux_bias" else None
     if threads is None:
         threads = os.cpu_count() or 1
-    rc = lib.ora_linear_forward(M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
-                                _ptr(B), 0 if b_major == "k" else 1, ldb,
-                                _ptr(bias), epi, _ptr(D), 0 if d_layout == "row" else 1, ldd,
-                                _ptr(aux), ld_aux, _ptr(Z), int(threads))
+    rc = lib.ora_linear_forward_dt(DTYPES[dtype], M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
+                                   _ptr(B), 0 if b_major == "k" else 1, ldb,
+                                   _ptr(bias), epi, _ptr(D), 0 if d_layout == "row" else 1, ldd,
+                                   _ptr(aux), ld_aux, _ptr(Z), int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return {"D": D, "Z": Z, "aux": aux, "ldd": ldd, "ld_aux": ld_aux}
 
 
 def drelu_bgrad(dY, aux, M: int, N: int, *, d_layout: str = "row",
-                ldd: int | None = None, ld_aux: int | None = None):
+                ldd: int | None = None, ld_aux: int | None = None, dtype: str = "f16"):
     """Backward epilogue: dZ = dY where the mask bit is set else +0 (fp16 bits),
     bgrad[m] = sum over n of dZ[m,n] in fp64."""
     lib = _load()
@@ -170,8 +200,8 @@ def drelu_bgrad(dY, aux, M: int, N: int, *, d_layout: str = "row",
     aux = np.ascontiguousarray(aux, dtype=np.uint32)
     dZ = np.zeros(rows * ldd, np.uint16)
     bgrad = np.zeros(M, np.float64)
-    rc = lib.ora_drelu_bgrad(M, N, _ptr(dY), 0 if d_layout == "row" else 1, ldd,
-                             _ptr(aux), ld_aux, _ptr(dZ), _ptr(bgrad))
+    rc = lib.ora_drelu_bgrad_dt(DTYPES[dtype], M, N, _ptr(dY), 0 if d_layout == "row" else 1, ldd,
+                                _ptr(aux), ld_aux, _ptr(dZ), _ptr(bgrad))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dZ, bgrad
@@ -179,7 +209,8 @@ def drelu_bgrad(dY, aux, M: int, N: int, *, d_layout: str = "row",
 
 def gemm_drelu_bgrad(A, B, aux, M: int, N: int, K: int, *, a_major: str = "k", b_major: str = "k",
                      d_layout: str = "row", lda: int | None = None, ldb: int | None = None,
-                     ldd: int | None = None, ld_aux: int | None = None, threads: int | None = None):
+                     ldd: int | None = None, ld_aux: int | None = None, threads: int | None = None,
+                     dtype: str = "f16"):
     """DRELU_BGRAD applied to a product: dZ = fp16(A.B) where the mask bit is
     set else +0; bgrad[m] = sum over n of the unrounded masked product (fp64)."""
     lib = _load()
@@ -199,9 +230,9 @@ def gemm_drelu_bgrad(A, B, aux, M: int, N: int, K: int, *, a_major: str = "k", b
     bgrad = np.zeros(M, np.float64)
     if threads is None:
         threads = os.cpu_count() or 1
-    rc = lib.ora_gemm_drelu_bgrad(M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda, _ptr(B),
-                                  0 if b_major == "k" else 1, ldb, _ptr(aux), ld_aux, _ptr(dZ),
-                                  0 if d_layout == "row" else 1, ldd, _ptr(bgrad), int(threads))
+    rc = lib.ora_gemm_drelu_bgrad_dt(DTYPES[dtype], M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
+                                     _ptr(B), 0 if b_major == "k" else 1, ldb, _ptr(aux), ld_aux, _ptr(dZ),
+                                     0 if d_layout == "row" else 1, ldd, _ptr(bgrad), int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dZ, bgrad

@@ -427,3 +427,72 @@ def test_gelu_erf_forward_brute_force(oracle):
             Z[m, n] = s + float(bias[m])
     want = torch.nn.functional.gelu(torch.from_numpy(Z), approximate="none").numpy()
     assert np.array_equal(r["D"].reshape(M, N), want.astype(np.float16).view(np.uint16))
+
+
+# --------------------------------------------------------------- bfloat16
+
+def test_bf16_decode_exhaustive(oracle):
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_decode(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_bf16_encode_roundtrip_and_ties(oracle):
+    bits = np.arange(0, 0x7F80, dtype=np.uint16)      # every finite positive bfloat16
+    vals = oracle.bf16_decode(bits)
+    assert np.array_equal(oracle.bf16_encode(vals), bits)
+    assert np.array_equal(oracle.bf16_encode(-vals), bits | 0x8000)
+    lo = bits[:-1]
+    a, b = vals[:-1], vals[1:]
+    mid = (a + b) / 2                                  # exact in fp64
+    even = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(oracle.bf16_encode(mid), even)
+    assert np.array_equal(oracle.bf16_encode(np.nextafter(mid, 0)), lo)
+    assert np.array_equal(oracle.bf16_encode(np.nextafter(mid, np.inf)), (lo + 1).astype(np.uint16))
+
+
+def test_bf16_encode_vs_library_on_float32_values(oracle):
+    # For doubles that are exact float32 values, torch's float32 -> bfloat16
+    # conversion (round to nearest even) is a single rounding: it must agree.
+    rng = np.random.default_rng(9)
+    x = (np.exp2(rng.uniform(-140, 127.9, 200000)) * rng.choice([-1.0, 1.0], 200000)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_encode(x.astype(np.float64)), ref)
+
+
+def test_bf16_encode_boundaries(oracle):
+    enc = lambda v: int(oracle.bf16_encode(np.array([v]))[0])
+    big = (2 - 2 ** -7) * 2.0 ** 127
+    assert enc(big) == 0x7F7F
+    assert enc((2 - 2 ** -8) * 2.0 ** 127) == 0x7F80   # tie to even -> overflow
+    assert enc(2.0 ** -133) == 0x0001
+    assert enc(2.0 ** -134) == 0x0000                 # tie to even -> zero
+    assert enc(2.0 ** -126) == 0x0080
+
+
+def test_bf16_forward_brute_force(oracle):
+    rng = np.random.default_rng(78)
+    M, N, K = 5, 4, 7
+    tb = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    Ap = tb(rng.standard_normal((M, K)).astype(np.float32))
+    Bp = tb(rng.standard_normal((K, N)).astype(np.float32))
+    bias = tb(rng.standard_normal(M).astype(np.float32))
+    bitsof = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    r = oracle.linear_forward(bitsof(Ap), bitsof(Bp.T.contiguous()), bitsof(bias), "relu_bias", M, N, K,
+                              a_major="k", b_major="k", dtype="bf16")
+    Z = np.zeros((M, N))
+    A64, B64, b64 = Ap.double().numpy(), Bp.double().numpy(), bias.double().numpy()
+    for m in range(M):
+        for n in range(N):
+            s = 0.0
+            for k in range(K):
+                s += A64[m, k] * B64[k, n]
+            Z[m, n] = max(s + b64[m], 0.0)
+    want = torch.from_numpy(Z.astype(np.float32)).to(torch.bfloat16)  # Z is not exact in fp32:
+    got = oracle.bf16_decode(r["D"]).reshape(M, N)
+    # compare against round-to-nearest of the fp64 value instead (one rounding)
+    assert np.array_equal(r["D"].reshape(M, N), oracle.bf16_encode(Z))
+    assert np.allclose(got, want.double().numpy(), rtol=2 ** -7)

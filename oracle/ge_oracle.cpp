@@ -49,7 +49,7 @@ namespace {
 // Epilogue codes of this oracle (its own numbering; the Python wrapper maps
 // names to these).
 enum OraEpi { ORA_NONE = 0, ORA_BIAS = 1, ORA_RELU_BIAS = 2, ORA_GELU_BIAS = 3,
-              ORA_RELU_AUX_BIAS = 4, ORA_GELU_ERF_BIAS = 6 };
+              ORA_RELU_AUX_BIAS = 4, ORA_GELU_ERF_BIAS = 6, ORA_GELU_AUX_BIAS = 7 };
 
 // IEEE-754 binary16 -> binary64, written from the format definition:
 // 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -146,7 +146,8 @@ double activation(int epi, double z) {
     case ORA_RELU_BIAS:
     case ORA_RELU_AUX_BIAS:
       return z > 0.0 ? z : 0.0;
-    case ORA_GELU_BIAS: {
+    case ORA_GELU_BIAS:
+    case ORA_GELU_AUX_BIAS: {
       // tanh form: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
       const double c = std::sqrt(2.0 / 3.14159265358979323846);
       return 0.5 * z * (1.0 + std::tanh(c * (z + 0.044715 * z * z * z)));
@@ -159,8 +160,19 @@ double activation(int epi, double z) {
   }
 }
 
+// Derivative of the tanh-form GELU with respect to its input, by the product
+// and chain rules: with u = c (z + a z^3), t = tanh(u),
+//   d/dz [0.5 z (1 + t)] = 0.5 (1 + t) + 0.5 z (1 - t^2) c (1 + 3 a z^2).
+double gelu_tanh_grad(double z) {
+  const double c = std::sqrt(2.0 / 3.14159265358979323846);
+  const double a = 0.044715;
+  const double t = std::tanh(c * (z + a * z * z * z));
+  return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * c * (1.0 + 3.0 * a * z * z);
+}
+
 bool valid_forward_epi(int epi) {
-  return (epi >= ORA_NONE && epi <= ORA_RELU_AUX_BIAS) || epi == ORA_GELU_ERF_BIAS;
+  return (epi >= ORA_NONE && epi <= ORA_RELU_AUX_BIAS) || epi == ORA_GELU_ERF_BIAS ||
+         epi == ORA_GELU_AUX_BIAS;
 }
 
 template <class F>
@@ -217,23 +229,30 @@ void ora_f64_to_f16_array(const double* in, uint16_t* out, int64_t n) {
 //   Z (optional, may be NULL): the fp64 pre-activation z, laid out like D.
 //   bias may be NULL only for ORA_NONE.
 // Returns 0 on success, -1 on a bad argument.
-// Same as ora_linear_forward with every operand, the bias and D of element
-// type `dt` (0 = fp16, 1 = bfloat16).
-int ora_linear_forward_dt(int dt, int64_t M, int64_t N, int64_t K,
-                          const uint16_t* A, int a_major, int64_t lda,
-                          const uint16_t* B, int b_major, int64_t ldb,
-                          const uint16_t* bias, int epi,
-                          uint16_t* D, int d_layout, int64_t ldd,
-                          uint32_t* aux, int64_t ld_aux, double* Z,
-                          int nthreads) {
+
+}  // extern "C"
+
+namespace {
+
+// The forward with both kinds of auxiliary output: `aux` (bit mask, for
+// RELU_AUX_BIAS) and `zaux` (the pre-activation rounded to the element type,
+// for GELU_AUX_BIAS, at zaux[r*ld_zaux + c] in D's stored layout).
+int forward_impl(int dt, int64_t M, int64_t N, int64_t K,
+                 const uint16_t* A, int a_major, int64_t lda,
+                 const uint16_t* B, int b_major, int64_t ldb,
+                 const uint16_t* bias, int epi,
+                 uint16_t* D, int d_layout, int64_t ldd,
+                 uint32_t* aux, int64_t ld_aux, uint16_t* zaux, int64_t ld_zaux, double* Z,
+                 int nthreads) {
   if (dt != 0 && dt != 1) return -1;
   if (M < 0 || N < 0 || K < 0 || !D) return -1;
   if (!valid_forward_epi(epi)) return -1;
   if (epi != ORA_NONE && !bias) return -1;
   if (epi == ORA_RELU_AUX_BIAS && !aux) return -1;
+  if (epi == ORA_GELU_AUX_BIAS && !zaux) return -1;
   const int64_t rows = d_layout == 0 ? M : N;
   const int64_t cols = d_layout == 0 ? N : M;
-  if (ldd < cols || (aux && ld_aux * 32 < cols)) return -1;
+  if (ldd < cols || (aux && ld_aux * 32 < cols) || (zaux && ld_zaux < cols)) return -1;
   if (K > 0 && (!A || !B)) return -1;
 
   // Layout step only: decode both operands into plain fp64 matrices with k
@@ -265,9 +284,40 @@ int ora_linear_forward_dt(int dt, int64_t M, int64_t N, int64_t K,
       if (Z) Z[r * ldd + c] = z;
       if (epi == ORA_RELU_AUX_BIAS && z > 0.0)
         aux[r * ld_aux + c / 32] |= (uint32_t)1u << (c % 32);
+      if (epi == ORA_GELU_AUX_BIAS) zaux[r * ld_zaux + c] = encode(dt, z);
     }
   });
   return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Same as ora_linear_forward with every operand, the bias and D of element
+// type `dt` (0 = fp16, 1 = bfloat16).
+int ora_linear_forward_dt(int dt, int64_t M, int64_t N, int64_t K,
+                          const uint16_t* A, int a_major, int64_t lda,
+                          const uint16_t* B, int b_major, int64_t ldb,
+                          const uint16_t* bias, int epi,
+                          uint16_t* D, int d_layout, int64_t ldd,
+                          uint32_t* aux, int64_t ld_aux, double* Z,
+                          int nthreads) {
+  if (epi == ORA_GELU_AUX_BIAS) return -1;  // needs the 16-bit z output below
+  return forward_impl(dt, M, N, K, A, a_major, lda, B, b_major, ldb, bias, epi, D, d_layout, ldd,
+                      aux, ld_aux, nullptr, 0, Z, nthreads);
+}
+
+// GELU_AUX_BIAS: D = tanh-GELU(z) as GELU_BIAS, and zaux = z rounded to the
+// element type, stored like D (zaux[r*ld_zaux + c]); the backward pass
+// (DGELU_BGRAD) reads it to evaluate the GELU derivative.
+int ora_gelu_aux_forward_dt(int dt, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* A, int a_major, int64_t lda,
+                            const uint16_t* B, int b_major, int64_t ldb,
+                            const uint16_t* bias, uint16_t* D, int d_layout, int64_t ldd,
+                            uint16_t* zaux, int64_t ld_zaux, double* Z, int nthreads) {
+  return forward_impl(dt, M, N, K, A, a_major, lda, B, b_major, ldb, bias, ORA_GELU_AUX_BIAS, D,
+                      d_layout, ldd, nullptr, 0, zaux, ld_zaux, Z, nthreads);
 }
 
 int ora_linear_forward(int64_t M, int64_t N, int64_t K,
@@ -370,6 +420,85 @@ int ora_drelu_bgrad(int64_t M, int64_t N, const uint16_t* dY, int d_layout,
                     int64_t ldd, const uint32_t* aux, int64_t ld_aux,
                     uint16_t* dZ, double* bgrad) {
   return ora_drelu_bgrad_dt(0, M, N, dY, d_layout, ldd, aux, ld_aux, dZ, bgrad);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+// Derivative of the tanh-form GELU at one fp64 value (for the pins).
+double ora_gelu_grad_f64(double z) { return gelu_tanh_grad(z); }
+
+// DGELU_BGRAD standalone, the GELU counterpart of DRELU_BGRAD (cuBLASLt's
+// backward epilogue family named on the nvmath-python bias-fusion guide,
+// "Advanced techniques"): the incoming gradient is multiplied by the GELU
+// derivative at the stored pre-activation, and the bias gradient is reduced.
+//   dY, zaux, dZ: [M, N] in the forward D's stored layout (d_layout, ldd);
+//   zaux holds z rounded to the element type (GELU_AUX_BIAS's output).
+//   g[m,n]    = dY[m,n] * gelu'(z[m,n])          (fp64)
+//   dZ[m,n]   = g[m,n] rounded to the element type
+//   bgrad[m]  = sum over n of g[m,n]              (fp64, unrounded g)
+int ora_dgelu_bgrad_dt(int dt, int64_t M, int64_t N, const uint16_t* dY, int d_layout,
+                       int64_t ldd, const uint16_t* zaux, int64_t ld_zaux,
+                       uint16_t* dZ, double* bgrad) {
+  if (dt != 0 && dt != 1) return -1;
+  if (M < 0 || N < 0 || !dY || !zaux || !dZ || !bgrad) return -1;
+  const int64_t cols = d_layout == 0 ? N : M;
+  if (ldd < cols || ld_zaux < cols) return -1;
+  for (int64_t m = 0; m < M; ++m) {
+    double s = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const int64_t r = d_layout == 0 ? m : n;
+      const int64_t c = d_layout == 0 ? n : m;
+      const double g = decode(dt, dY[r * ldd + c]) * gelu_tanh_grad(decode(dt, zaux[r * ld_zaux + c]));
+      dZ[r * ldd + c] = encode(dt, g);
+      s += g;
+    }
+    bgrad[m] = s;
+  }
+  return 0;
+}
+
+// DGELU_BGRAD as the epilogue of the backward GEMM: the product dH = A.B
+// (fp64, k ascending) takes the place of dY above.
+//   dZ[m,n]  = (dH[m,n] * gelu'(z[m,n])) rounded to the element type
+//   bgrad[m] = sum over n of dH[m,n] * gelu'(z[m,n])   (fp64, n ascending)
+int ora_gemm_dgelu_bgrad_dt(int dt, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* A, int a_major, int64_t lda,
+                            const uint16_t* B, int b_major, int64_t ldb,
+                            const uint16_t* zaux, int64_t ld_zaux,
+                            uint16_t* dZ, int d_layout, int64_t ldd, double* bgrad,
+                            int nthreads) {
+  if (dt != 0 && dt != 1) return -1;
+  if (M < 0 || N < 0 || K < 0 || !dZ || !zaux || !bgrad) return -1;
+  const int64_t cols = d_layout == 0 ? N : M;
+  if (ldd < cols || ld_zaux < cols) return -1;
+  if (K > 0 && (!A || !B)) return -1;
+  std::vector<double> Ad((size_t)M * (size_t)K), Bd((size_t)N * (size_t)K);
+  parallel_rows(M, nthreads, [&](int64_t m) {
+    for (int64_t k = 0; k < K; ++k)
+      Ad[m * K + k] = decode(dt, a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
+  });
+  parallel_rows(N, nthreads, [&](int64_t n) {
+    for (int64_t k = 0; k < K; ++k)
+      Bd[n * K + k] = decode(dt, b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
+  });
+  parallel_rows(M, nthreads, [&](int64_t m) {
+    double s = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const double* a = Ad.data() + m * K;
+      const double* b = Bd.data() + n * K;
+      double h = 0.0;
+      for (int64_t k = 0; k < K; ++k) h += a[k] * b[k];
+      const int64_t r = d_layout == 0 ? m : n;
+      const int64_t c = d_layout == 0 ? n : m;
+      const double g = h * gelu_tanh_grad(decode(dt, zaux[r * ld_zaux + c]));
+      dZ[r * ldd + c] = encode(dt, g);
+      s += g;
+    }
+    bgrad[m] = s;
+  });
+  return 0;
 }
 
 }  // extern "C"

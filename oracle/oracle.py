@@ -30,7 +30,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libge_oracle.so")
 
 EPILOGUES = {"none": 0, "bias": 1, "relu_bias": 2, "gelu_bias": 3, "relu_aux_bias": 4,
-             "gelu_erf_bias": 6}
+             "gelu_erf_bias": 6, "gelu_aux_bias": 7}
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +86,16 @@ def _load():
             lib.ora_gemm_drelu_bgrad.restype = i32
             lib.ora_drelu_bgrad.argtypes = [i64, i64, vp, i32, i64, vp, i64, vp, vp]
             lib.ora_drelu_bgrad.restype = i32
+            lib.ora_gelu_aux_forward_dt.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64,
+                                                    vp, vp, i32, i64, vp, i64, vp, i32]
+            lib.ora_gelu_aux_forward_dt.restype = i32
+            lib.ora_gelu_grad_f64.argtypes = [ctypes.c_double]
+            lib.ora_gelu_grad_f64.restype = ctypes.c_double
+            lib.ora_dgelu_bgrad_dt.argtypes = [i32, i64, i64, vp, i32, i64, vp, i64, vp, vp]
+            lib.ora_dgelu_bgrad_dt.restype = i32
+            lib.ora_gemm_dgelu_bgrad_dt.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64, vp,
+                                                    i64, vp, i32, i64, vp, i32]
+            lib.ora_gemm_dgelu_bgrad_dt.restype = i32
             _lib = lib
     return _lib
 
@@ -150,13 +160,17 @@ def linear_forward(A, B, bias, epilogue: str, M: int, N: int, K: int, *,
                    a_major: str = "k", b_major: str = "k", d_layout: str = "row",
                    lda: int | None = None, ldb: int | None = None,
                    ldd: int | None = None, ld_aux: int | None = None,
-                   threads: int | None = None, dtype: str = "f16") -> dict:
+                   threads: int | None = None, dtype: str = "f16",
+                   ld_zaux: int | None = None) -> dict:
     """D = act(A.B + bias) in fp64, rounded once to fp16 (or bfloat16 with
     dtype="bf16"; A, B, bias and D all of that type).
 
     Returns ``{"D": uint16 bits, "Z": fp64 pre-activation, "aux": uint32 mask
     words or None}``; D and Z are flat arrays of ``rows*ldd`` elements in the
-    stored layout, aux is ``rows*ld_aux`` words.
+    stored layout, aux is ``rows*ld_aux`` words. For "gelu_aux_bias" the
+    result also holds ``"zaux"``: z rounded to the element type, ``rows *
+    ld_zaux`` elements stored like D (ld_zaux defaults to the contiguous
+    length rounded up to 8).
     """
     lib = _load()
     epi = EPILOGUES[epilogue]
@@ -177,6 +191,16 @@ def linear_forward(A, B, bias, epilogue: str, M: int, N: int, K: int, *,
     aux = np.zeros(rows * ld_aux, np.uint32) if epilogue == "relu_aux_bias" else None
     if threads is None:
         threads = os.cpu_count() or 1
+    if epilogue == "gelu_aux_bias":
+        ld_zaux = ld_zaux or default_ld_zaux(cols)
+        zaux = np.zeros(rows * ld_zaux, np.uint16)
+        rc = lib.ora_gelu_aux_forward_dt(DTYPES[dtype], M, N, K, _ptr(A), 0 if a_major == "k" else 1,
+                                         lda, _ptr(B), 0 if b_major == "k" else 1, ldb, _ptr(bias),
+                                         _ptr(D), 0 if d_layout == "row" else 1, ldd, _ptr(zaux), ld_zaux,
+                                         _ptr(Z), int(threads))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments")
+        return {"D": D, "Z": Z, "aux": None, "zaux": zaux, "ldd": ldd, "ld_zaux": ld_zaux}
     rc = lib.ora_linear_forward_dt(DTYPES[dtype], M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
                                    _ptr(B), 0 if b_major == "k" else 1, ldb,
                                    _ptr(bias), epi, _ptr(D), 0 if d_layout == "row" else 1, ldd,
@@ -233,6 +257,64 @@ def gemm_drelu_bgrad(A, B, aux, M: int, N: int, K: int, *, a_major: str = "k", b
     rc = lib.ora_gemm_drelu_bgrad_dt(DTYPES[dtype], M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
                                      _ptr(B), 0 if b_major == "k" else 1, ldb, _ptr(aux), ld_aux, _ptr(dZ),
                                      0 if d_layout == "row" else 1, ldd, _ptr(bgrad), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dZ, bgrad
+
+
+def default_ld_zaux(contiguous_len: int) -> int:
+    """Row pitch (elements) of a GELU_AUX_BIAS pre-activation output: the
+    contiguous length rounded up to 8 elements (16 bytes)."""
+    return (contiguous_len + 7) // 8 * 8
+
+
+def gelu_grad_f64(z: float) -> float:
+    """Derivative of the tanh-form GELU at z (fp64)."""
+    return _load().ora_gelu_grad_f64(float(z))
+
+
+def dgelu_bgrad(dY, zaux, M: int, N: int, *, d_layout: str = "row", ldd: int | None = None,
+                ld_zaux: int | None = None, dtype: str = "f16"):
+    """Backward epilogue of GELU_AUX_BIAS: g = dY * gelu'(z) with z the stored
+    (rounded) pre-activation; dZ = g rounded to the element type; bgrad[m] =
+    sum over n of the unrounded g (fp64)."""
+    lib = _load()
+    rows, cols = (M, N) if d_layout == "row" else (N, M)
+    ldd = ldd or cols
+    ld_zaux = ld_zaux or default_ld_zaux(cols)
+    dY = _u16(dY)
+    zaux = _u16(zaux)
+    dZ = np.zeros(rows * ldd, np.uint16)
+    bgrad = np.zeros(M, np.float64)
+    rc = lib.ora_dgelu_bgrad_dt(DTYPES[dtype], M, N, _ptr(dY), 0 if d_layout == "row" else 1, ldd,
+                                _ptr(zaux), ld_zaux, _ptr(dZ), _ptr(bgrad))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dZ, bgrad
+
+
+def gemm_dgelu_bgrad(A, B, zaux, M: int, N: int, K: int, *, a_major: str = "k", b_major: str = "k",
+                     d_layout: str = "row", lda: int | None = None, ldb: int | None = None,
+                     ldd: int | None = None, ld_zaux: int | None = None, threads: int | None = None,
+                     dtype: str = "f16"):
+    """DGELU_BGRAD applied to a product dH = A.B: dZ = (dH * gelu'(z)) rounded;
+    bgrad[m] = sum over n of the unrounded dH * gelu'(z) (fp64)."""
+    lib = _load()
+    lda = lda or (K if a_major == "k" else M)
+    ldb = ldb or (K if b_major == "k" else N)
+    rows, cols = (M, N) if d_layout == "row" else (N, M)
+    ldd = ldd or cols
+    ld_zaux = ld_zaux or default_ld_zaux(cols)
+    A = _u16(A)
+    B = _u16(B)
+    zaux = _u16(zaux)
+    dZ = np.zeros(rows * ldd, np.uint16)
+    bgrad = np.zeros(M, np.float64)
+    threads = threads or (os.cpu_count() or 1)
+    rc = lib.ora_gemm_dgelu_bgrad_dt(DTYPES[dtype], M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
+                                     _ptr(B), 0 if b_major == "k" else 1, ldb, _ptr(zaux), ld_zaux,
+                                     _ptr(dZ), 0 if d_layout == "row" else 1, ldd, _ptr(bgrad),
+                                     int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dZ, bgrad

@@ -496,3 +496,146 @@ def test_bf16_forward_brute_force(oracle):
     # compare against round-to-nearest of the fp64 value instead (one rounding)
     assert np.array_equal(r["D"].reshape(M, N), oracle.bf16_encode(Z))
     assert np.allclose(got, want.double().numpy(), rtol=2 ** -7)
+
+
+# ------------------------------------------- GELU_AUX_BIAS and DGELU_BGRAD
+
+def _torch_gelu_grad(z):
+    """d/dz of the library's tanh-form GELU, by autograd in fp64."""
+    t = torch.tensor(np.asarray(z, np.float64), requires_grad=True)
+    torch.nn.functional.gelu(t, approximate="tanh").sum().backward()
+    return t.grad.numpy()
+
+
+def test_gelu_grad_finite_difference(oracle):
+    """The derivative matches a central difference of the (separately pinned)
+    forward GELU: a wrong coefficient or a dropped chain-rule factor fails."""
+    h = 1e-5
+    for z in np.linspace(-8, 8, 401):
+        fd = (oracle.act_f64("gelu_bias", z + h) - oracle.act_f64("gelu_bias", z - h)) / (2 * h)
+        assert abs(oracle.gelu_grad_f64(z) - fd) < 1e-8, z
+
+
+def test_gelu_grad_matches_library_autograd(oracle):
+    z = np.linspace(-10, 10, 4001)
+    got = np.array([oracle.gelu_grad_f64(v) for v in z])
+    # For |z| > 7, 1 - t^2 is a few ulps of 1 in both evaluations, so their
+    # absolute difference there is rounding noise of order 1e-15.
+    assert np.allclose(got, _torch_gelu_grad(z), rtol=1e-13, atol=1e-14)
+
+
+def test_gelu_grad_special_values(oracle):
+    assert oracle.gelu_grad_f64(0.0) == 0.5
+    assert abs(oracle.gelu_grad_f64(12.0) - 1.0) < 1e-15
+    assert abs(oracle.gelu_grad_f64(-12.0)) < 1e-15
+    # the derivative is negative for z below about -0.75 (minimum near -1.42)
+    # and exceeds 1 for z above about 0.75
+    assert oracle.gelu_grad_f64(-0.7) > 0 > oracle.gelu_grad_f64(-0.8)
+    assert oracle.gelu_grad_f64(-1.5) < oracle.gelu_grad_f64(-1.2)
+    assert oracle.gelu_grad_f64(-1.5) < oracle.gelu_grad_f64(-1.8)
+    assert oracle.gelu_grad_f64(1.5) > 1
+
+
+@pytest.mark.parametrize("dl", ["row", "col"])
+def test_gelu_aux_forward(oracle, dl):
+    """GELU_AUX_BIAS: D is the GELU_BIAS output and zaux is z = A.B + bias
+    (brute force, fp64) rounded once to fp16 by the library conversion; the
+    padding of each zaux row is left untouched."""
+    rng = np.random.default_rng(90)
+    M, N, K = 7, 11, 13
+    Ap = rng.standard_normal((M, K)).astype(np.float16)
+    Bp = rng.standard_normal((K, N)).astype(np.float16)
+    bias = rng.standard_normal(M).astype(np.float16)
+    A, B = plain_to_layout(Ap.view(np.uint16), Bp.view(np.uint16), "k", "n")
+    rows, cols = (M, N) if dl == "row" else (N, M)
+    r = oracle.linear_forward(A, B, bias.view(np.uint16), "gelu_aux_bias", M, N, K, a_major="k",
+                              b_major="n", d_layout=dl)
+    g = oracle.linear_forward(A, B, bias.view(np.uint16), "gelu_bias", M, N, K, a_major="k",
+                              b_major="n", d_layout=dl)
+    assert np.array_equal(r["D"], g["D"])
+    ld = r["ld_zaux"]
+    assert ld == (cols + 7) // 8 * 8
+    Z = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(Ap[m, k]) * float(Bp[k, n])
+            Z[m, n] = s + float(bias[m])
+    want = Z if dl == "row" else Z.T
+    zaux = r["zaux"].reshape(rows, ld)
+    assert np.array_equal(zaux[:, :cols], want.astype(np.float16).view(np.uint16))
+    assert not zaux[:, cols:].any()
+
+
+@pytest.mark.parametrize("dl", ["row", "col"])
+def test_dgelu_bgrad_standalone(oracle, dl):
+    """dZ = dY * gelu'(z) rounded once; bgrad = sum over n of the unrounded
+    products. gelu' comes from the library's autograd here."""
+    rng = np.random.default_rng(91)
+    M, N = 9, 40
+    rows, cols = (M, N) if dl == "row" else (N, M)
+    ldd, ldz = cols + 3, cols + 5
+    dY = (rng.standard_normal((rows, ldd)) * 2).astype(np.float16)
+    z = (rng.standard_normal((rows, ldz)) * 3).astype(np.float16)
+    dZ, bgrad = oracle.dgelu_bgrad(dY.view(np.uint16).reshape(-1), z.view(np.uint16).reshape(-1), M, N,
+                                   d_layout=dl, ldd=ldd, ld_zaux=ldz)
+    g = dY[:, :cols].astype(np.float64) * _torch_gelu_grad(z[:, :cols].astype(np.float64))
+    got = dZ.reshape(rows, ldd)
+    assert np.array_equal(got[:, :cols], g.astype(np.float16).view(np.uint16))
+    assert not got[:, cols:].any()  # padding untouched
+    per_m = g if dl == "row" else g.T
+    assert np.allclose(bgrad, [math.fsum(per_m[m]) for m in range(M)], rtol=1e-13, atol=1e-13)
+
+
+def test_dgelu_bgrad_special_values(oracle):
+    """gelu'(0) = 1/2 (exact halving), gelu'(8) rounds to 1 (dZ = dY) and
+    gelu'(-8) is below 1e-19 in magnitude (dZ is a zero)."""
+    dY = np.array([1.5, -3.0, 2.0], np.float16)
+    z = np.array([0.0, 8.0, -8.0], np.float16)
+    dZ, bgrad = oracle.dgelu_bgrad(dY.view(np.uint16), z.view(np.uint16), 1, 3)
+    assert dZ[:2].tolist() == [np.float16(0.75).view(np.uint16), np.float16(-3.0).view(np.uint16)]
+    assert dZ[2] & 0x7FFF == 0
+    assert abs(bgrad[0] - (0.75 - 3.0)) < 1e-15
+
+
+@pytest.mark.parametrize("am,bm,dl", [("k", "n", "row"), ("k", "k", "col"), ("m", "n", "row"), ("m", "k", "col")])
+def test_gemm_dgelu_bgrad_brute_force(oracle, am, bm, dl):
+    rng = np.random.default_rng(92 + "km".index(am) * 4 + "kn".index(bm) * 2 + (dl == "col"))
+    for (M, N, K) in [(1, 1, 1), (3, 5, 7), (6, 33, 4)]:
+        Ap = rng.standard_normal((M, K)).astype(np.float16)
+        Bp = rng.standard_normal((K, N)).astype(np.float16)
+        rows, cols = (M, N) if dl == "row" else (N, M)
+        ldz = (cols + 7) // 8 * 8
+        zs = (rng.standard_normal((rows, ldz)) * 2).astype(np.float16)
+        A, B = plain_to_layout(Ap.view(np.uint16), Bp.view(np.uint16), am, bm)
+        dZ, bgrad = oracle.gemm_dgelu_bgrad(A, B, zs.view(np.uint16).reshape(-1), M, N, K, a_major=am,
+                                            b_major=bm, d_layout=dl, threads=1)
+        H, _ = _brute(Ap.astype(np.float64), Bp.astype(np.float64), None, "none")
+        zmn = zs[:, :cols].astype(np.float64)
+        if dl == "col":
+            zmn = zmn.T
+        g = H * _torch_gelu_grad(zmn)
+        got = dZ.reshape(rows, cols)
+        if dl == "col":
+            got = got.T
+        assert np.array_equal(got, g.astype(np.float16).view(np.uint16))
+        assert np.allclose(bgrad, g.sum(axis=1), rtol=1e-13, atol=1e-14)
+
+
+def test_dgelu_bgrad_bf16(oracle):
+    """bf16 elements: the same products rounded by the (separately pinned)
+    bf16 encoder."""
+    rng = np.random.default_rng(93)
+    tb = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    bitsof = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    M, N = 6, 17
+    dY = tb(rng.standard_normal((M, N)) * 2)
+    z = tb(rng.standard_normal((M, N)) * 3)
+    ldz = (N + 7) // 8 * 8
+    zp = torch.zeros((M, ldz), dtype=torch.bfloat16)
+    zp[:, :N] = z
+    dZ, bgrad = oracle.dgelu_bgrad(bitsof(dY), bitsof(zp), M, N, ld_zaux=ldz, dtype="bf16")
+    g = dY.double().numpy() * _torch_gelu_grad(z.double().numpy())
+    assert np.array_equal(dZ.reshape(M, N), oracle.bf16_encode(g))
+    assert np.allclose(bgrad, g.sum(axis=1), rtol=1e-13, atol=1e-14)

@@ -502,3 +502,72 @@ int ora_gemm_dgelu_bgrad_dt(int dt, int64_t M, int64_t N, int64_t K,
 }
 
 }  // extern "C"
+
+extern "C" {
+
+// MatMul + bias + residual + normalisation over the output features: the
+// structural fusion of ops-nn MatMul fusion (codearts), "ops-nn's MatMul
+// fusion strategy", second level (MatMul + LayerNorm / RMSNorm + residual,
+// where the norm reduces across the channel dimension).
+//   h[m,n] = sum_k A[m,k] B[k,n] + bias[m] + res[m,n]      (fp64)
+//   H[m,n] = h rounded to the element type (the new residual stream)
+// for every token n, over the M features m (population statistics):
+//   kind 0, RMSNorm:   y = h / sqrt(mean_m(h^2) + eps) * gamma[m]
+//   kind 1, LayerNorm: y = (h - mu) / sqrt(mean_m((h - mu)^2) + eps) * gamma[m]
+//                          + beta[m],   mu = mean_m(h)
+//   Y[m,n] = y rounded to the element type.
+// res, H and Y are stored like D (d_layout, ldd); gamma and beta are [M]
+// vectors of the element type (beta unused by RMSNorm). Statistics use the
+// unrounded fp64 h, summed in ascending m.
+int ora_linear_norm_dt(int dt, int kind, int64_t M, int64_t N, int64_t K,
+                       const uint16_t* A, int a_major, int64_t lda,
+                       const uint16_t* B, int b_major, int64_t ldb,
+                       const uint16_t* bias, const uint16_t* res,
+                       const uint16_t* gamma, const uint16_t* beta, double eps,
+                       uint16_t* H, uint16_t* Y, int d_layout, int64_t ldd, int nthreads) {
+  if (dt != 0 && dt != 1) return -1;
+  if (kind != 0 && kind != 1) return -1;
+  if (M < 1 || N < 0 || K < 0 || !bias || !res || !gamma || !H || !Y) return -1;
+  if (kind == 1 && !beta) return -1;
+  if (!(eps >= 0.0)) return -1;
+  const int64_t cols = d_layout == 0 ? N : M;
+  if (ldd < cols) return -1;
+  if (K > 0 && (!A || !B)) return -1;
+  std::vector<double> Ad((size_t)M * (size_t)K), Bd((size_t)N * (size_t)K);
+  parallel_rows(M, nthreads, [&](int64_t m) {
+    for (int64_t k = 0; k < K; ++k)
+      Ad[m * K + k] = decode(dt, a_major == 0 ? A[m * lda + k] : A[k * lda + m]);
+  });
+  parallel_rows(N, nthreads, [&](int64_t n) {
+    for (int64_t k = 0; k < K; ++k)
+      Bd[n * K + k] = decode(dt, b_major == 0 ? B[n * ldb + k] : B[k * ldb + n]);
+  });
+  auto at = [&](int64_t m, int64_t n) { return d_layout == 0 ? m * ldd + n : n * ldd + m; };
+  parallel_rows(N, nthreads, [&](int64_t n) {
+    std::vector<double> h((size_t)M);
+    for (int64_t m = 0; m < M; ++m) {
+      const double* a = Ad.data() + m * K;
+      const double* b = Bd.data() + n * K;
+      double z = 0.0;
+      for (int64_t k = 0; k < K; ++k) z += a[k] * b[k];
+      h[m] = z + decode(dt, bias[m]) + decode(dt, res[at(m, n)]);
+      H[at(m, n)] = encode(dt, h[m]);
+    }
+    double mu = 0.0;
+    if (kind == 1) {
+      for (int64_t m = 0; m < M; ++m) mu += h[m];
+      mu /= (double)M;
+    }
+    double ss = 0.0;
+    for (int64_t m = 0; m < M; ++m) ss += (h[m] - mu) * (h[m] - mu);
+    const double inv = 1.0 / std::sqrt(ss / (double)M + eps);
+    for (int64_t m = 0; m < M; ++m) {
+      double y = (h[m] - mu) * inv * decode(dt, gamma[m]);
+      if (kind == 1) y += decode(dt, beta[m]);
+      Y[at(m, n)] = encode(dt, y);
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"

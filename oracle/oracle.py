@@ -96,6 +96,9 @@ def _load():
             lib.ora_gemm_dgelu_bgrad_dt.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64, vp,
                                                     i64, vp, i32, i64, vp, i32]
             lib.ora_gemm_dgelu_bgrad_dt.restype = i32
+            lib.ora_linear_norm_dt.argtypes = [i32, i32, i64, i64, i64, vp, i32, i64, vp, i32, i64, vp, vp,
+                                               vp, vp, ctypes.c_double, vp, vp, i32, i64, i32]
+            lib.ora_linear_norm_dt.restype = i32
             _lib = lib
     return _lib
 
@@ -318,3 +321,33 @@ def gemm_dgelu_bgrad(A, B, zaux, M: int, N: int, K: int, *, a_major: str = "k", 
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dZ, bgrad
+
+
+NORMS = {"rmsnorm": 0, "layernorm": 1}
+
+
+def linear_norm(A, B, bias, res, gamma, beta, norm: str, M: int, N: int, K: int, *, eps: float = 1e-5,
+                a_major: str = "k", b_major: str = "k", d_layout: str = "col", lda: int | None = None,
+                ldb: int | None = None, ldd: int | None = None, threads: int | None = None,
+                dtype: str = "f16"):
+    """MatMul + bias + residual, then RMSNorm / LayerNorm over the M output
+    features of every token n. Returns (H, Y): the rounded h = A.B + bias +
+    res and the rounded normalised output, both stored like D (flat uint16,
+    rows * ldd)."""
+    lib = _load()
+    lda = lda or (K if a_major == "k" else M)
+    ldb = ldb or (K if b_major == "k" else N)
+    rows, cols = (M, N) if d_layout == "row" else (N, M)
+    ldd = ldd or cols
+    A, B, bias, res, gamma = _u16(A), _u16(B), _u16(bias), _u16(res), _u16(gamma)
+    beta = None if beta is None else _u16(beta)
+    H = np.zeros(rows * ldd, np.uint16)
+    Y = np.zeros(rows * ldd, np.uint16)
+    threads = threads or (os.cpu_count() or 1)
+    rc = lib.ora_linear_norm_dt(DTYPES[dtype], NORMS[norm], M, N, K, _ptr(A), 0 if a_major == "k" else 1, lda,
+                                _ptr(B), 0 if b_major == "k" else 1, ldb, _ptr(bias), _ptr(res), _ptr(gamma),
+                                _ptr(beta), float(eps), _ptr(H), _ptr(Y), 0 if d_layout == "row" else 1, ldd,
+                                int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return H, Y

@@ -639,3 +639,140 @@ def test_dgelu_bgrad_bf16(oracle):
     g = dY.double().numpy() * _torch_gelu_grad(z.double().numpy())
     assert np.array_equal(dZ.reshape(M, N), oracle.bf16_encode(g))
     assert np.allclose(bgrad, g.sum(axis=1), rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------- MatMul + bias + residual + RMSNorm / LayerNorm
+
+def _norm_inputs(rng, M, N, K, dtype=np.float16):
+    A = rng.standard_normal((M, K)).astype(dtype)
+    B = rng.standard_normal((K, N)).astype(dtype)
+    bias = rng.standard_normal(M).astype(dtype)
+    res = rng.standard_normal((M, N)).astype(dtype)
+    gamma = (1 + 0.5 * rng.standard_normal(M)).astype(dtype)
+    beta = rng.standard_normal(M).astype(dtype)
+    return A, B, bias, res, gamma, beta
+
+
+def _run_norm(oracle, A, B, bias, res, gamma, beta, norm, eps, dl="col"):
+    """A [M,K], B [K,N], res [M,N] plain fp16 arrays; returns H, Y as [M,N] fp64."""
+    M, K = A.shape
+    N = B.shape[1]
+    Ak, Bk = plain_to_layout(A.view(np.uint16), B.view(np.uint16), "k", "n")
+    r = res if dl == "row" else res.T
+    H, Y = oracle.linear_norm(Ak, Bk, bias.view(np.uint16), np.ascontiguousarray(r).view(np.uint16).reshape(-1),
+                              gamma.view(np.uint16), None if beta is None else beta.view(np.uint16), norm, M, N, K,
+                              eps=eps, a_major="k", b_major="n", d_layout=dl)
+    rows, cols = (M, N) if dl == "row" else (N, M)
+    H = oracle.f16_decode(H).reshape(rows, cols)
+    Y = oracle.f16_decode(Y).reshape(rows, cols)
+    return (H, Y) if dl == "row" else (H.T, Y.T)
+
+
+def test_layernorm_two_features_is_plus_minus_one(oracle):
+    """Over two features LayerNorm gives +-sqrt(v/(v+eps)) (v = the variance):
+    exactly +1 / -1 with eps = 0, for the hand-worked example's z."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_2x3x4.json")))
+    A = np.array(g["A"], np.float16)
+    B = np.array(g["B"], np.float16)
+    bias = np.array(g["bias"], np.float16)
+    zeros = np.zeros((2, 3), np.float16)
+    one = np.ones(2, np.float16)
+    H, Y = _run_norm(oracle, A, B, bias, zeros, one, np.zeros(2, np.float16), "layernorm", 0.0)
+    assert H.tolist() == [[0.5, 13.5, 3.5], [-5, 2, -2]]
+    assert Y.tolist() == [[1, 1, 1], [-1, -1, -1]]
+    # eps > 0: token 0 has h = (0.5, -5), variance 2.75^2
+    _, Y = _run_norm(oracle, A, B, bias, zeros, one, np.zeros(2, np.float16), "layernorm", 1.0)
+    want = np.sqrt(2.75 ** 2 / (2.75 ** 2 + 1.0))
+    assert Y[0, 0] == np.float16(want) and Y[1, 0] == np.float16(-want)
+
+
+def test_rmsnorm_closed_forms(oracle):
+    """h = (3, 4): rms = sqrt(12.5), so y = (3, 4) * sqrt(2) / 5; a constant
+    row c gives sign(c) * gamma (eps = 0)."""
+    A = np.array([[3.0], [4.0]], np.float16)
+    B = np.array([[1.0, -2.0]], np.float16)
+    z2 = np.zeros(2, np.float16)
+    _, Y = _run_norm(oracle, A, B, z2, np.zeros((2, 2), np.float16), np.ones(2, np.float16), None, "rmsnorm", 0.0)
+    s2 = 1.4142135623730951
+    assert Y[:, 0].tolist() == [float(np.float16(3 * s2 / 5)), float(np.float16(4 * s2 / 5))]
+    assert Y[:, 1].tolist() == [float(np.float16(-3 * s2 / 5)), float(np.float16(-4 * s2 / 5))]
+    M = 7
+    A = np.full((M, 1), 0.75, np.float16)
+    gamma = np.linspace(-2, 2, M).astype(np.float16)
+    _, Y = _run_norm(oracle, A, np.array([[1.0, -3.0]], np.float16), np.zeros(M, np.float16),
+                     np.zeros((M, 2), np.float16), gamma, None, "rmsnorm", 0.0)
+    assert np.array_equal(Y[:, 0], gamma.astype(np.float64))
+    assert np.array_equal(Y[:, 1], -gamma.astype(np.float64))
+
+
+def test_norm_scale_invariance(oracle):
+    """With eps = 0 both norms ignore a common scale of h: doubling A, the
+    bias and the residual (exact in fp16) doubles H and leaves Y unchanged."""
+    rng = np.random.default_rng(95)
+    A, B, bias, res, gamma, beta = _norm_inputs(rng, 24, 5, 9)
+    for norm in ("rmsnorm", "layernorm"):
+        H1, Y1 = _run_norm(oracle, A, B, bias, res, gamma, beta, norm, 0.0)
+        H2, Y2 = _run_norm(oracle, A * np.float16(2), B, bias * np.float16(2), res * np.float16(2), gamma, beta,
+                           norm, 0.0)
+        assert np.array_equal(H2, 2 * H1)
+        assert np.array_equal(Y1, Y2)
+
+
+def test_layernorm_output_moments(oracle):
+    """gamma = 1, beta = 0: each token's outputs have mean 0 and variance
+    v / (v + eps) up to the fp16 rounding of Y."""
+    rng = np.random.default_rng(96)
+    M, N, K = 256, 6, 16
+    A, B, bias, res, _, _ = _norm_inputs(rng, M, N, K)
+    eps = 0.5
+    H, Y = _run_norm(oracle, A, B, bias, res, np.ones(M, np.float16), np.zeros(M, np.float16), "layernorm", eps)
+    h = A.astype(np.float64) @ B.astype(np.float64) + bias.astype(np.float64)[:, None] + res.astype(np.float64)
+    v = h.var(axis=0)
+    assert np.abs(Y.mean(axis=0)).max() < 2e-3
+    assert np.abs(Y.var(axis=0) - v / (v + eps)).max() < 4e-3
+
+
+@pytest.mark.parametrize("norm", ["rmsnorm", "layernorm"])
+@pytest.mark.parametrize("dl", ["row", "col"])
+def test_norm_brute_force(oracle, norm, dl):
+    """Brute force on tiny inputs: h by explicit loops, the statistics by
+    numpy's mean and (population) variance, one rounding by the library."""
+    rng = np.random.default_rng(97 + (norm == "layernorm") * 2 + (dl == "col"))
+    for (M, N, K) in [(1, 1, 1), (5, 3, 7), (33, 4, 5)]:
+        A, B, bias, res, gamma, beta = _norm_inputs(rng, M, N, K)
+        H, Y = _run_norm(oracle, A, B, bias, res, gamma, beta if norm == "layernorm" else None, norm, 1e-5, dl)
+        h = np.zeros((M, N))
+        for m in range(M):
+            for n in range(N):
+                s = 0.0
+                for k in range(K):
+                    s += float(A[m, k]) * float(B[k, n])
+                h[m, n] = s + float(bias[m]) + float(res[m, n])
+        assert np.array_equal(H, h.astype(np.float16).astype(np.float64))
+        if norm == "rmsnorm":
+            y = h / np.sqrt((h * h).mean(axis=0) + 1e-5) * gamma.astype(np.float64)[:, None]
+        else:
+            y = (h - h.mean(axis=0)) / np.sqrt(h.var(axis=0) + 1e-5) * gamma.astype(np.float64)[:, None] \
+                + beta.astype(np.float64)[:, None]
+        # Y is y rounded once: within half an fp16 step of the brute-force y
+        half_step = np.spacing(np.abs(y).astype(np.float16)).astype(np.float64) / 2
+        assert (np.abs(Y - y) <= half_step * (1 + 1e-9) + 1e-300).all(), "Y differs from the brute force"
+
+
+def test_norm_bf16(oracle):
+    rng = np.random.default_rng(99)
+    M, N, K = 16, 3, 5
+    tb = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+    bitsof = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    A, B = tb(rng.standard_normal((M, K))), tb(rng.standard_normal((K, N)))
+    bias, res = tb(rng.standard_normal(M)), tb(rng.standard_normal((N, M)))
+    gamma, beta = tb(1 + 0.3 * rng.standard_normal(M)), tb(rng.standard_normal(M))
+    H, Y = oracle.linear_norm(bitsof(A), bitsof(B.T), bitsof(bias), bitsof(res), bitsof(gamma), bitsof(beta),
+                              "layernorm", M, N, K, eps=1e-5, a_major="k", b_major="k", d_layout="col",
+                              dtype="bf16")
+    h = A.double().numpy() @ B.double().numpy() + bias.double().numpy()[:, None] + res.double().numpy().T
+    y = (h - h.mean(axis=0)) / np.sqrt(h.var(axis=0) + 1e-5) * gamma.double().numpy()[:, None] \
+        + beta.double().numpy()[:, None]
+    assert np.array_equal(H.reshape(N, M), oracle.bf16_encode(h.T))
+    got = oracle.bf16_decode(Y).reshape(N, M)
+    assert np.abs(got - y.T).max() <= np.abs(y).max() * 2 ** -8

@@ -47,6 +47,10 @@ CONFIG_CASES = {
     # backward GEMM dH = G W2^T (11008 x 8192 x 4096) with DRELU_BGRAD fused
     # in its epilogue, vs. the GEMM followed by the standalone DRELU_BGRAD
     "cfg_bwd_gemm_drelu": ("bwd", False), "cfg_bwd_gemm_drelu_unfused": ("bwd", True),
+    # the same workloads with bfloat16 operands, bias and output
+    "cfg_c4_fwd": ("c4_fwd", False), "cfg_c4_fwd_bf16": ("c4_fwd", False, "bf16"),
+    "cfg_c4_dw_bf16": ("c4_dw", False, "bf16"), "cfg_c3_T1_bf16": ("c3_T1", False, "bf16"),
+    "cfg_c5_bf16": ("c5", False, "bf16"),
 }
 
 
@@ -239,17 +243,20 @@ def run_config(args, rank):
     import torch
     import gemm_epilogues_gb300 as ge
     from gemm_epilogues_gb300.inputs import pages_workloads
-    key, unfused = CONFIG_CASES[args.case]
+    key, unfused, *rest = CONFIG_CASES[args.case]
+    dtype = rest[0] if rest else "f16"
     if key == "bwd":
         return run_bwd_gemm_drelu(args, rank, unfused)
     w = pages_workloads()[key]
+    w.dtype = dtype
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
     A, B, bias = w.make(dev)
     major = {"k": ge.GE_K_MAJOR, "m": ge.GE_MN_MAJOR, "n": ge.GE_MN_MAJOR}
     L = ge.make_layout(major[w.a_major], major[w.b_major], ge.GE_D_ROW if w.d_layout == "row" else ge.GE_D_COL)
-    plan = ge.Plan(w.M, w.N, w.K, ge.EPILOGUE_BY_NAME[w.epilogue], L)
-    D = torch.empty(w.d_shape(), dtype=torch.float16, device=dev)
+    plan = ge.Plan(w.M, w.N, w.K, ge.EPILOGUE_BY_NAME[w.epilogue], L,
+                   dtype=ge.GE_BF16 if dtype == "bf16" else ge.GE_F16)
+    D = torch.empty(w.d_shape(), dtype=A.dtype, device=dev)
     aux = torch.empty(max(plan.aux_bytes // 4, 1), dtype=torch.int32, device=dev)
     bias_arg = bias if w.epilogue != "none" else None
     aux_arg = aux if w.epilogue == "relu_aux_bias" else None
@@ -270,7 +277,7 @@ def run_config(args, rank):
     assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
     ms = sum(times) / len(times)
     tflops = w.flops / (ms * 1e-3) / 1e12
-    line = {"case": args.case, "workload": w.name, "unfused": unfused, "path": plan.path,
+    line = {"case": args.case, "workload": w.name, "dtype": dtype, "unfused": unfused, "path": plan.path,
             "tile_n": plan.tile_n, "ms": ms, "min_ms": min(times), "tflops": tflops,
             "frac_of_peak": tflops / peaks["tflops"],
             "gbs_algorithmic": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}

@@ -36,9 +36,14 @@ GE_EPI_GELU_BIAS = 3
 GE_EPI_RELU_AUX_BIAS = 4
 GE_EPI_DRELU_BGRAD = 5
 GE_EPI_GELU_ERF_BIAS = 6
+GE_EPI_GELU_AUX_BIAS = 7
+GE_EPI_DGELU_BGRAD = 8
+GE_EPI_BIAS_RESIDUAL_RMSNORM = 9
+GE_EPI_BIAS_RESIDUAL_LAYERNORM = 10
 # ge_dtype_t
 GE_F16 = 0
 GE_F32 = 1
+GE_BF16 = 2
 # ge_major_t
 GE_K_MAJOR = 0
 GE_MN_MAJOR = 1
@@ -54,14 +59,16 @@ GE_PATH_DRELU = 2
 
 EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EPI_RELU_BIAS,
                     "gelu_bias": GE_EPI_GELU_BIAS, "relu_aux_bias": GE_EPI_RELU_AUX_BIAS,
-                    "drelu_bgrad": GE_EPI_DRELU_BGRAD, "gelu_erf_bias": GE_EPI_GELU_ERF_BIAS}
+                    "drelu_bgrad": GE_EPI_DRELU_BGRAD, "gelu_erf_bias": GE_EPI_GELU_ERF_BIAS,
+                    "gelu_aux_bias": GE_EPI_GELU_AUX_BIAS, "dgelu_bgrad": GE_EPI_DGELU_BGRAD,
+                    "rmsnorm": GE_EPI_BIAS_RESIDUAL_RMSNORM, "layernorm": GE_EPI_BIAS_RESIDUAL_LAYERNORM}
 
 # Every function the header declares (checked against include/ge.h by a test).
 ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",
                  "ge_aux_bytes", "ge_aux_ld", "ge_plan_path", "ge_plan_tile_n",
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
                  "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr",
-                 "ge_plan_autotune", "ge_plan_config")
+                 "ge_plan_autotune", "ge_plan_config", "ge_execute_norm", "ge_execute_norm_unfused")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -98,6 +105,9 @@ def load_library():
         lib.ge_execute.restype = i32
         lib.ge_execute_unfused.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         lib.ge_execute_unfused.restype = i32
+        for fn in (lib.ge_execute_norm, lib.ge_execute_norm_unfused):
+            fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
+            fn.restype = i32
         lib.ge_plan_free.argtypes = [vp]
         lib.ge_plan_free.restype = i32
         lib.ge_aux_bytes.argtypes = [vp]
@@ -179,6 +189,19 @@ def ge_execute(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool = False)
     _check(st, "ge_execute")
 
 
+def ge_execute_norm(plan, A, B, bias, residual, gamma, beta, H, Y, eps=1e-5, stream=None, *,
+                    raw: bool = False, unfused: bool = False):
+    """MatMul + bias + residual + RMSNorm/LayerNorm (``unfused=True``: the
+    separate-kernel flow ge_execute_norm_unfused)."""
+    lib = load_library()
+    fn = lib.ge_execute_norm_unfused if unfused else lib.ge_execute_norm
+    st = fn(plan, _ptr(A), _ptr(B), _ptr(bias), _ptr(residual), _ptr(gamma), _ptr(beta), _ptr(H), _ptr(Y),
+            float(eps), _stream(stream))
+    if raw:
+        return st
+    _check(st, "ge_execute_norm_unfused" if unfused else "ge_execute_norm")
+
+
 def ge_execute_unfused(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool = False):
     st = load_library().ge_execute_unfused(plan, _ptr(A), _ptr(B), _ptr(bias), _ptr(D), _ptr(aux),
                                            _stream(stream))
@@ -254,11 +277,12 @@ def make_layout(a: int = GE_K_MAJOR, b: int = GE_MN_MAJOR, d: int = GE_D_ROW, ld
 
 
 class Plan:
-    """Context-managed plan: ``with Plan(M, N, K, epi, layout) as p: p.execute(...)``."""
+    """Context-managed plan: ``with Plan(M, N, K, epi, layout) as p: p.execute(...)``.
+    ``dtype`` is the element type of A, B, D and the bias (GE_F16 or GE_BF16)."""
 
-    def __init__(self, M, N, K, epi=GE_EPI_BIAS, layout: ge_layout_t | None = None):
-        self.M, self.N, self.K, self.epi = M, N, K, epi
-        self.handle = ge_plan_create(M, N, K, epi=epi, layout=layout)
+    def __init__(self, M, N, K, epi=GE_EPI_BIAS, layout: ge_layout_t | None = None, dtype: int = GE_F16):
+        self.M, self.N, self.K, self.epi, self.dtype = M, N, K, epi, dtype
+        self.handle = ge_plan_create(M, N, K, dtype, dtype, dtype, epi=epi, layout=layout)
 
     def execute(self, A, B, bias, D, aux=None, stream=None):
         ge_execute(self.handle, A, B, bias, D, aux, stream)
@@ -275,6 +299,9 @@ class Plan:
 
     def execute_unfused(self, A, B, bias, D, aux=None, stream=None):
         ge_execute_unfused(self.handle, A, B, bias, D, aux, stream)
+
+    def execute_norm(self, A, B, bias, residual, gamma, beta, H, Y, eps=1e-5, stream=None, unfused=False):
+        ge_execute_norm(self.handle, A, B, bias, residual, gamma, beta, H, Y, eps, stream, unfused=unfused)
 
     @property
     def aux_bytes(self) -> int:

@@ -46,8 +46,9 @@ struct Plan {
   int group_m = 16;
   // stored D: R rows x C contiguous
   int64_t R = 0, C = 0;
-  int64_t aux_words = 0;  // ld_aux (words) when a mask is in use
+  int64_t aux_words = 0;  // ld_aux: mask words, or elements of the 16-bit z (GELU_AUX / DGELU)
   int static_a = 0;       // GE_ATTR_STATIC_A
+  int bf16 = 0;           // element type of A, B, D and bias: 0 fp16, 1 bf16
   // device workspace: [error word | pad to 256 | counters | partials]
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -59,7 +60,8 @@ struct Plan {
   const void* mapA = nullptr;
   const void* mapB = nullptr;
   const void* mapD = nullptr;
-  CUtensorMap tmA{}, tmB{}, tmD{};
+  const void* mapZ = nullptr;
+  CUtensorMap tmA{}, tmB{}, tmD{}, tmZ{};
   // last pointers whose device was verified
   const void* checked[6] = {};
 };
@@ -78,17 +80,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D fp16 tensor map: inner extent d0 (contiguous), outer d1, row pitch ld
-// elements, box b0 x b1, swizzle mode.
-bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t ld, uint32_t b0,
-              uint32_t b1, CUtensorMapSwizzle sw) {
+// 2-D tensor map of 16-bit elements (fp16, or bf16 when `bf16`): inner extent
+// d0 (contiguous), outer d1, row pitch ld elements, box b0 x b1, swizzle mode.
+bool make_map(CUtensorMap* m, int bf16, const void* base, uint64_t d0, uint64_t d1, uint64_t ld,
+              uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {d0, d1};
   cuuint64_t strides[1] = {ld * 2};
   cuuint32_t box[2] = {b0, b1};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -96,9 +98,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool epi_is_norm(ge_epilogue_t e) {
+  return e == GE_EPI_BIAS_RESIDUAL_RMSNORM || e == GE_EPI_BIAS_RESIDUAL_LAYERNORM;
+}
+
 bool epi_has_bias(ge_epilogue_t e) {
   return e == GE_EPI_BIAS || e == GE_EPI_RELU_BIAS || e == GE_EPI_GELU_BIAS ||
-         e == GE_EPI_RELU_AUX_BIAS || e == GE_EPI_GELU_ERF_BIAS;
+         e == GE_EPI_RELU_AUX_BIAS || e == GE_EPI_GELU_ERF_BIAS || e == GE_EPI_GELU_AUX_BIAS;
 }
 
 // Verify that `p` is device memory of the plan's device (cached per slot).
@@ -187,13 +193,16 @@ ge_status_t apply_config(Plan* pl, const TcConfig& c) {
   pl->grid = c.grid;
   pl->group_m = c.group_m;
   pl->partials = static_cast<float*>(pl->tail_ws);
-  pl->mapA = pl->mapB = pl->mapD = nullptr;  // B's box depends on the pair mode
+  pl->mapA = pl->mapB = pl->mapD = pl->mapZ = nullptr;  // B's box depends on the pair mode
   return GE_OK;
 }
 
-// Tensor maps for the tensor-core path (kernel-level operands A', B', D').
-ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D) {
-  if (pl->mapA == A && pl->mapB == B && pl->mapD == D) return GE_OK;
+// Tensor maps for the tensor-core path (kernel-level operands A', B', D' and,
+// for GELU_AUX_BIAS, the z output Z' stored like D'; otherwise tmZ repeats
+// D's map and is not used).
+ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D, void* Z) {
+  if (!Z) Z = D;
+  if (pl->mapA == A && pl->mapB == B && pl->mapD == D && pl->mapZ == Z) return GE_OK;
   const ge_layout_t& L = pl->L;
   const void* Ak = pl->swap ? B : A;
   const void* Bk = pl->swap ? A : B;
@@ -206,22 +215,25 @@ ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D) {
   const uint64_t K = pl->K;
   bool ok = true;
   if (!a_mn)
-    ok &= make_map(&pl->tmA, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&pl->tmA, pl->bf16, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   else
-    ok &= make_map(&pl->tmA, Ak, Mk, K, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&pl->tmA, pl->bf16, Ak, Mk, K, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!b_mn)
-    ok &= make_map(&pl->tmB, Bk, K, Nk, ldb, 64, pl->pair ? pl->block_n / 2 : pl->block_n,
+    ok &= make_map(&pl->tmB, pl->bf16, Bk, K, Nk, ldb, 64, pl->pair ? pl->block_n / 2 : pl->block_n,
                    CU_TENSOR_MAP_SWIZZLE_128B);
   else
-    ok &= make_map(&pl->tmB, Bk, Nk, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok &= make_map(&pl->tmD, D, Nk, Mk, L.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= make_map(&pl->tmB, pl->bf16, Bk, Nk, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok &= make_map(&pl->tmD, pl->bf16, D, Nk, Mk, L.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= make_map(&pl->tmZ, pl->bf16, Z, Nk, Mk, Z == D ? L.ldd : L.ld_aux, 32, 32,
+                 CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) {
-    pl->mapA = pl->mapB = pl->mapD = nullptr;
+    pl->mapA = pl->mapB = pl->mapD = pl->mapZ = nullptr;
     return GE_ERR_CUDA;
   }
   pl->mapA = A;
   pl->mapB = B;
   pl->mapD = D;
+  pl->mapZ = Z;
   return GE_OK;
 }
 
@@ -241,11 +253,14 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.ldd_m = pl->L.d == GE_D_ROW ? pl->L.ldd : 1;
     g.ldd_n = pl->L.d == GE_D_ROW ? 1 : pl->L.ldd;
     g.bias = static_cast<const __half*>(bias);
+    g.res = epi_code == EPI_BIAS_RESIDUAL ? static_cast<const unsigned short*>(aux) : nullptr;
     g.epi = epi_code;
     g.static_a = pl->static_a;
+    g.bf16 = pl->bf16;
     e = launch_gemv(g, pl->num_sms, st);
   } else {
-    ge_status_t s = build_maps(pl, A, B, D);
+    const bool zout = epi_code == EPI_GELU_AUX_BIAS;
+    ge_status_t s = build_maps(pl, A, B, D, zout ? aux : nullptr);
     if (s != GE_OK) return s;
     GemmArgs g{};
     g.Mk = static_cast<int>(pl->swap ? pl->N : pl->M);
@@ -256,8 +271,12 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.epi = epi_code;
     g.bias_per_col = pl->swap ? 1 : 0;
     g.bias = static_cast<const __half*>(bias);
-    g.aux = static_cast<uint32_t*>(aux);
+    const bool zaux = epi_code == EPI_GELU_AUX_BIAS || epi_code == EPI_DGELU_BGRAD ||
+                      epi_code == EPI_BIAS_RESIDUAL;
+    g.aux = zaux ? nullptr : static_cast<uint32_t*>(aux);
     g.ld_aux = pl->aux_words;
+    g.zaux = zaux ? static_cast<unsigned short*>(aux) : nullptr;
+    g.ld_zaux = pl->aux_words;
     g.D = static_cast<__half*>(D);
     g.ldd = pl->L.ldd;
     g.err = pl->err;
@@ -267,16 +286,52 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.split = pl->split;
     g.partials = pl->partials;
     g.bg_partials = pl->bg_partials;
-    g.bgrad = epi_code == EPI_DRELU_BGRAD ? static_cast<float*>(const_cast<void*>(bias)) : nullptr;
-    if (epi_code == EPI_DRELU_BGRAD) g.bias = nullptr;
-    e = launch_tc_gemm(pl->block_n, pl->pair, pl->tmA, pl->tmB, pl->tmD, g, pl->grid, st);
+    g.bf16 = pl->bf16;
+    const bool backward = epi_code == EPI_DRELU_BGRAD || epi_code == EPI_DGELU_BGRAD;
+    g.bgrad = backward ? static_cast<float*>(const_cast<void*>(bias)) : nullptr;
+    if (backward) g.bias = nullptr;
+    e = launch_tc_gemm(pl->block_n, pl->pair, pl->tmA, pl->tmB, pl->tmD, pl->tmZ, g, pl->grid, st);
     if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, st);
-    if (e == cudaSuccess && epi_code == EPI_DRELU_BGRAD) {
+    if (e == cudaSuccess && backward) {
       const long long rows = pl->swap ? pl->bg_rows : (g.Nk + pl->block_n - 1) / pl->block_n;
       e = launch_bgrad_reduce(pl->bg_partials, rows, pl->bg_len, g.bgrad, st);
     }
   }
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+// Checks shared by the fused and unfused norm entry points.
+ge_status_t check_norm_args(Plan* pl, const void* A, const void* B, const void* bias, const void* residual,
+                            const void* gamma, const void* beta, const void* H, const void* Y) {
+  if (!pl) return GE_ERR_INVALID_ARG;
+  if (!epi_is_norm(pl->epi)) return GE_ERR_UNSUPPORTED;
+  const bool layer = pl->epi == GE_EPI_BIAS_RESIDUAL_LAYERNORM;
+  if (!A || !B || !bias || !residual || !gamma || !H || !Y || (layer && !beta)) return GE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(H) || !aligned16(Y) || !aligned16(residual) ||
+      !aligned16(gamma) || (layer && !aligned16(beta)) || (reinterpret_cast<uintptr_t>(bias) & 1u))
+    return GE_ERR_ALIGNMENT;
+  ge_status_t s;
+  if ((s = check_device(pl, 0, A)) != GE_OK || (s = check_device(pl, 1, B)) != GE_OK ||
+      (s = check_device(pl, 2, bias)) != GE_OK || (s = check_device(pl, 3, H)) != GE_OK ||
+      (s = check_device(pl, 4, residual)) != GE_OK || (s = check_device(pl, 5, Y)) != GE_OK)
+    return s;
+  return GE_OK;
+}
+
+ge_status_t launch_norm_pass(Plan* pl, const void* gamma, const void* beta, const void* H, void* Y, float eps,
+                             cudaStream_t st) {
+  NormArgs n{};
+  n.R = pl->N;  // tokens: rows of the column-major D
+  n.C = pl->M;  // features
+  n.ld = pl->L.ldd;
+  n.H = static_cast<const unsigned short*>(H);
+  n.Y = static_cast<unsigned short*>(Y);
+  n.gamma = static_cast<const unsigned short*>(gamma);
+  n.beta = static_cast<const unsigned short*>(beta);
+  n.eps = eps;
+  n.layer = pl->epi == GE_EPI_BIAS_RESIDUAL_LAYERNORM ? 1 : 0;
+  n.bf16 = pl->bf16;
+  return launch_norm(n, pl->num_sms, st) == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 
 }  // namespace
@@ -304,31 +359,38 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
                            const ge_layout_t* layout) {
   if (!out) return GE_ERR_INVALID_ARG;
   *out = nullptr;
-  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_GELU_ERF_BIAS)
+  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_BIAS_RESIDUAL_LAYERNORM)
     return GE_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 0) return GE_ERR_INVALID_ARG;
   const int64_t lim = (int64_t(1) << 31) - 1;
   if (M > lim || N > lim || K > lim) return GE_ERR_INVALID_ARG;
-  if (a != GE_F16 || b != GE_F16 || d != GE_F16 || compute != GE_F32) return GE_ERR_UNSUPPORTED;
-  if (epi != GE_EPI_DRELU_BGRAD && K == 0) return GE_ERR_INVALID_ARG;
+  // A, B, D (and the bias) share one 16-bit element type; products are
+  // accumulated in fp32 either way.
+  if (a != b || a != d || (a != GE_F16 && a != GE_BF16) || compute != GE_F32) return GE_ERR_UNSUPPORTED;
+  const bool backward = epi == GE_EPI_DRELU_BGRAD || epi == GE_EPI_DGELU_BGRAD;
+  if (!backward && K == 0) return GE_ERR_INVALID_ARG;
   ge_layout_t L{GE_K_MAJOR, GE_MN_MAJOR, GE_D_ROW, 0, 0, 0, 0};
   if (layout) L = *layout;
   if ((L.a != GE_K_MAJOR && L.a != GE_MN_MAJOR) || (L.b != GE_K_MAJOR && L.b != GE_MN_MAJOR) ||
       (L.d != GE_D_ROW && L.d != GE_D_COL))
     return GE_ERR_INVALID_ARG;
   if (L.lda < 0 || L.ldb < 0 || L.ldd < 0 || L.ld_aux < 0) return GE_ERR_INVALID_ARG;
+  // The norm runs over the M features of each token: they must be the
+  // contiguous index of D (D column-major, i.e. Y[N tokens][M features]).
+  if (epi_is_norm(epi) && L.d != GE_D_COL) return GE_ERR_UNSUPPORTED;
 
   Plan tmp;
   tmp.M = M;
   tmp.N = N;
   tmp.K = K;
   tmp.epi = epi;
+  tmp.bf16 = a == GE_BF16 ? 1 : 0;
   tmp.R = L.d == GE_D_ROW ? M : N;
   tmp.C = L.d == GE_D_ROW ? N : M;
 
   // A 1-column B (decode) stored N-major with unit pitch is a contiguous
   // vector, the same bytes as K-major: read it as K-major.
-  const bool standalone_drelu = epi == GE_EPI_DRELU_BGRAD && K == 0;
+  const bool standalone_drelu = backward && K == 0;
   if (!standalone_drelu && N == 1 && L.b == GE_MN_MAJOR && (L.ldb == 0 || L.ldb == 1)) {
     L.b = GE_K_MAJOR;
     L.ldb = (K + 7) / 8 * 8;
@@ -350,13 +412,21 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (L.ld_aux % 4 != 0) return GE_ERR_ALIGNMENT;
     tmp.aux_words = L.ld_aux;
   }
+  const bool has_zaux = epi == GE_EPI_GELU_AUX_BIAS || epi == GE_EPI_DGELU_BGRAD;
+  if (epi_is_norm(epi)) tmp.aux_words = L.ldd;  // residual, H and Y share D's layout
+  if (has_zaux) {  // 16-bit z stored like D: ld_aux in elements, 16-byte rows
+    if (L.ld_aux == 0) L.ld_aux = (tmp.C + 7) / 8 * 8;
+    if (L.ld_aux < tmp.C) return GE_ERR_INVALID_ARG;
+    if (L.ld_aux % 8 != 0) return GE_ERR_ALIGNMENT;
+    tmp.aux_words = L.ld_aux;
+  }
 
   // Path choice.
   if (standalone_drelu) {
     tmp.path = GE_PATH_DRELU;
     if (L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
   } else if (N <= 16 && L.a == GE_K_MAJOR && L.b == GE_K_MAJOR && epi != GE_EPI_RELU_AUX_BIAS &&
-             epi != GE_EPI_DRELU_BGRAD) {
+             !has_zaux && !backward) {
     tmp.path = GE_PATH_GEMV;
     if (L.lda % 8 != 0 || L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
   } else {
@@ -401,11 +471,11 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     }
     if (const char* env = std::getenv("GE_SPLIT_TAIL"))
       if (env[0] == '0') tc_split = false;
-    if (epi == GE_EPI_DRELU_BGRAD) tc_split = false;  // its bias-gradient partials are per tile
+    if (backward) tc_split = false;  // their bias-gradient partials are per tile
   }
   size_t ws = 256;
   size_t bg_off = 0;
-  if (tmp.path == GE_PATH_TC_GEMM && epi == GE_EPI_DRELU_BGRAD) {
+  if (tmp.path == GE_PATH_TC_GEMM && backward) {
     const int64_t Mk = tmp.swap ? N : M;
     const int64_t Nk = tmp.swap ? M : N;
     if (tmp.swap) {  // bgrad indexes D' columns: partials per 32-row block
@@ -420,7 +490,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     ws += static_cast<size_t>(tmp.bg_rows) * static_cast<size_t>(tmp.bg_len) * 4;
   }
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
-    tmp.splits = drelu_splits(tmp.R, tmp.C, tmp.num_sms);
+    tmp.splits = drelu_splits(tmp.R, tmp.C, tmp.num_sms, epi == GE_EPI_DGELU_BGRAD ? 1 : 0);
     const int64_t strips = (tmp.C + 255) / 256;
     ws += static_cast<size_t>(strips) * 4;
     ws = (ws + 255) / 256 * 256;
@@ -469,6 +539,7 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B, const void*
   if (!pl) return GE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ge_status_t s;
+  if (epi_is_norm(pl->epi)) return GE_ERR_UNSUPPORTED;  // ge_execute_norm
   if (pl->path == GE_PATH_DRELU) {
     // A = dY, D = dZ, aux = mask, bias = fp32 bgrad output.
     if (!A || !D || !aux || !bias) return GE_ERR_INVALID_ARG;
@@ -488,25 +559,35 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B, const void*
     d.partials = pl->partials;
     d.counters = pl->counters;
     d.splits = pl->splits;
+    d.bf16 = pl->bf16;
+    if (pl->epi == GE_EPI_DGELU_BGRAD) {  // aux is the stored pre-activation z
+      d.gelu = 1;
+      d.mask = nullptr;
+      d.zaux = static_cast<const unsigned short*>(aux);
+      d.ld_zaux = pl->aux_words;
+    }
     cudaError_t e = launch_drelu_bgrad(d, pl->L.d == GE_D_COL ? 1 : 0, st);
     return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
   }
   if (!A || !B || !D) return GE_ERR_INVALID_ARG;
-  if (pl->epi == GE_EPI_DRELU_BGRAD) {
-    // GEMM-epilogue form: aux = forward mask (input), bias = fp32 bgrad output.
+  if (pl->epi == GE_EPI_DRELU_BGRAD || pl->epi == GE_EPI_DGELU_BGRAD) {
+    // GEMM-epilogue form: aux = forward mask or z (input), bias = fp32 bgrad output.
     if (!aux || !bias) return GE_ERR_INVALID_ARG;
+    const uintptr_t aux_align = pl->epi == GE_EPI_DGELU_BGRAD ? 15u : 3u;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(bias) ||
-        (reinterpret_cast<uintptr_t>(aux) & 3u))
+        (reinterpret_cast<uintptr_t>(aux) & aux_align))
       return GE_ERR_ALIGNMENT;
     if ((s = check_device(pl, 0, A)) != GE_OK || (s = check_device(pl, 1, B)) != GE_OK ||
         (s = check_device(pl, 3, D)) != GE_OK || (s = check_device(pl, 2, bias)) != GE_OK ||
         (s = check_device(pl, 4, aux)) != GE_OK)
       return s;
-    return launch_forward(pl, A, B, bias, D, aux, EPI_DRELU_BGRAD, st);
+    return launch_forward(pl, A, B, bias, D, aux, static_cast<int>(pl->epi), st);
   }
   if (epi_has_bias(pl->epi) && !bias) return GE_ERR_INVALID_ARG;
-  if (pl->epi == GE_EPI_RELU_AUX_BIAS && !aux) return GE_ERR_INVALID_ARG;
+  const bool needs_aux = pl->epi == GE_EPI_RELU_AUX_BIAS || pl->epi == GE_EPI_GELU_AUX_BIAS;
+  if (needs_aux && !aux) return GE_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B)) return GE_ERR_ALIGNMENT;
+  if (pl->epi == GE_EPI_GELU_AUX_BIAS && !aligned16(aux)) return GE_ERR_ALIGNMENT;
   if (pl->path == GE_PATH_TC_GEMM && !aligned16(D)) return GE_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(D) & 1u) || (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)) ||
       (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)))
@@ -515,20 +596,22 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B, const void*
       (s = check_device(pl, 3, D)) != GE_OK)
     return s;
   if (epi_has_bias(pl->epi) && (s = check_device(pl, 2, bias)) != GE_OK) return s;
-  if (pl->epi == GE_EPI_RELU_AUX_BIAS && (s = check_device(pl, 4, aux)) != GE_OK) return s;
-  return launch_forward(pl, A, B, epi_has_bias(pl->epi) ? bias : nullptr, D,
-                        pl->epi == GE_EPI_RELU_AUX_BIAS ? aux : nullptr, static_cast<int>(pl->epi), st);
+  if (needs_aux && (s = check_device(pl, 4, aux)) != GE_OK) return s;
+  return launch_forward(pl, A, B, epi_has_bias(pl->epi) ? bias : nullptr, D, needs_aux ? aux : nullptr,
+                        static_cast<int>(pl->epi), st);
 }
 
 ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B, const void* bias,
                                void* D, void* aux, void* stream) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl) return GE_ERR_INVALID_ARG;
-  if (!epi_has_bias(pl->epi) || pl->path == GE_PATH_DRELU) return GE_ERR_UNSUPPORTED;
+  if (!epi_has_bias(pl->epi) || pl->path == GE_PATH_DRELU || epi_is_norm(pl->epi)) return GE_ERR_UNSUPPORTED;
   if (!A || !B || !D || !bias) return GE_ERR_INVALID_ARG;
-  if (pl->epi == GE_EPI_RELU_AUX_BIAS && !aux) return GE_ERR_INVALID_ARG;
+  const bool needs_aux = pl->epi == GE_EPI_RELU_AUX_BIAS || pl->epi == GE_EPI_GELU_AUX_BIAS;
+  if (needs_aux && !aux) return GE_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return GE_ERR_ALIGNMENT;
   if (pl->L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
+  if (pl->epi == GE_EPI_GELU_AUX_BIAS && !aligned16(aux)) return GE_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(bias) & 1u) || (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)))
     return GE_ERR_ALIGNMENT;
   ge_status_t s;
@@ -540,15 +623,52 @@ ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B, con
   if (s != GE_OK) return s;
   __half* Dh = static_cast<__half*>(D);
   cudaError_t e = launch_bias_add(Dh, pl->R, pl->C, pl->L.ldd, static_cast<const __half*>(bias),
-                                  pl->L.d == GE_D_ROW ? 1 : 0, st);
+                                  pl->L.d == GE_D_ROW ? 1 : 0, pl->bf16, st);
   if (e != cudaSuccess) return GE_ERR_CUDA;
   if (pl->epi != GE_EPI_BIAS) {
+    const bool zout = pl->epi == GE_EPI_GELU_AUX_BIAS;
     e = launch_activation(Dh, pl->R, pl->C, pl->L.ldd, static_cast<int>(pl->epi),
                           pl->epi == GE_EPI_RELU_AUX_BIAS ? static_cast<uint32_t*>(aux) : nullptr,
-                          pl->aux_words, st);
+                          pl->aux_words, zout ? static_cast<unsigned short*>(aux) : nullptr,
+                          pl->aux_words, pl->bf16, st);
     if (e != cudaSuccess) return GE_ERR_CUDA;
   }
   return GE_OK;
+}
+
+ge_status_t ge_execute_norm(ge_plan_t plan, const void* A, const void* B, const void* bias,
+                            const void* residual, const void* gamma, const void* beta, void* H, void* Y,
+                            float eps, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  ge_status_t s = check_norm_args(pl, A, B, bias, residual, gamma, beta, H, Y);
+  if (s != GE_OK) return s;
+  if (!(eps >= 0.0f)) return GE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // h = A.B + bias + residual in the GEMM (or GEMV) epilogue, stored once as H
+  s = launch_forward(pl, A, B, bias, H, const_cast<void*>(residual), EPI_BIAS_RESIDUAL, st);
+  if (s != GE_OK) return s;
+  return launch_norm_pass(pl, gamma, beta, H, Y, eps, st);
+}
+
+ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B, const void* bias,
+                                    const void* residual, const void* gamma, const void* beta, void* H,
+                                    void* Y, float eps, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  ge_status_t s = check_norm_args(pl, A, B, bias, residual, gamma, beta, H, Y);
+  if (s != GE_OK) return s;
+  if (!(eps >= 0.0f)) return GE_ERR_INVALID_ARG;
+  if (H == residual) return GE_ERR_INVALID_ARG;  // the GEMM writes H before the residual is added
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = launch_forward(pl, A, B, nullptr, H, nullptr, EPI_NONE, st);
+  if (s != GE_OK) return s;
+  __half* Hh = static_cast<__half*>(H);
+  if (launch_bias_add(Hh, pl->R, pl->C, pl->L.ldd, static_cast<const __half*>(bias), 0, pl->bf16, st) !=
+      cudaSuccess)
+    return GE_ERR_CUDA;
+  if (launch_residual_add(Hh, pl->R, pl->C, pl->L.ldd, static_cast<const unsigned short*>(residual), pl->bf16,
+                          st) != cudaSuccess)
+    return GE_ERR_CUDA;
+  return launch_norm_pass(pl, gamma, beta, H, Y, eps, st);
 }
 
 ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const void* bias, void* D,
@@ -642,8 +762,12 @@ ge_status_t ge_plan_free(ge_plan_t plan) {
 
 size_t ge_aux_bytes(ge_plan_t plan) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
-  if (!pl || pl->epi != GE_EPI_RELU_AUX_BIAS) return 0;
-  return static_cast<size_t>(pl->R) * static_cast<size_t>(pl->aux_words) * 4u;
+  if (!pl) return 0;
+  if (pl->epi == GE_EPI_RELU_AUX_BIAS)
+    return static_cast<size_t>(pl->R) * static_cast<size_t>(pl->aux_words) * 4u;
+  if (pl->epi == GE_EPI_GELU_AUX_BIAS)
+    return static_cast<size_t>(pl->R) * static_cast<size_t>(pl->aux_words) * 2u;
+  return 0;
 }
 
 int64_t ge_aux_ld(ge_plan_t plan) {

@@ -13,6 +13,12 @@
 // The work is a stream over dY (read once, 16-byte loads), the mask (1/16 of
 // dY) and dZ (written once): bound by HBM bandwidth.
 //
+// DGELU_BGRAD, the same pass for a GELU_AUX_BIAS forward, reads the stored
+// pre-activation z (16-bit, laid out like dY) instead of mask bits:
+//   dZ[m,n]  = dY[m,n] * gelu'(z[m,n])      (fp32 product, rounded once)
+//   bgrad[m] = sum over n of the fp32 products
+// (the GELU counterpart of the backward epilogue on the same pages).
+//
 // Column case (D column-major: rows of storage are tokens n, the contiguous
 // index is m, so bgrad is a sum down each storage column): a block covers
 // 256 contiguous columns (32 lanes x 8 fp16) and one of `splits` row ranges;
@@ -51,22 +57,69 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
 
 // Keep the fp16 lanes of `v` whose mask bit (bits 0..7 of `bits`) is set,
 // zero the others, and add the kept values to acc[0..7].
-__device__ __forceinline__ uint4 mask_accumulate(uint4 v, uint32_t bits, float (&acc)[8]) {
+__device__ __forceinline__ uint4 mask_accumulate(uint4 v, uint32_t bits, float (&acc)[8], bool bf16) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t keep = ((bits >> (2 * i)) & 1u ? 0x0000FFFFu : 0u) |
                           ((bits >> (2 * i + 1)) & 1u ? 0xFFFF0000u : 0u);
-    w[i] &= keep;
-    const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-    const float2 f = __half22float2(h);
+    w[i] &= keep;  // the select is on the bit pattern: +0 for both element types
+    const float2 f = to_f32x2(bf16, w[i]);
     acc[2 * i] += f.x;
     acc[2 * i + 1] += f.y;
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__global__ void __launch_bounds__(256, MIN_BLOCKS) drelu_cols_kernel(const DreluArgs p) {
+// dZ = dY * gelu'(z) for the eight 16-bit lanes of `v` (dY) and `z`; the fp32
+// products are added to acc[0..7] before rounding.
+__device__ __forceinline__ uint4 gelu_accumulate(uint4 v, uint4 z, float (&acc)[8], bool bf16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t zz[4] = {z.x, z.y, z.z, z.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 g = to_f32x2(bf16, w[i]);
+    const float2 zf = to_f32x2(bf16, zz[i]);
+    const float p0 = g.x * gelu_tanh_grad(zf.x);
+    const float p1 = g.y * gelu_tanh_grad(zf.y);
+    acc[2 * i] += p0;
+    acc[2 * i + 1] += p1;
+    o[i] = pack2(bf16, p0, p1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One 16-byte group (8 columns at c0 of row r) of either kind: mask bits
+// (bits 0..7 of `bits`) or the pre-activations `z`.
+template <bool GELU>
+__device__ __forceinline__ uint4 apply_group(uint4 v, uint32_t bits, uint4 z, float (&acc)[8], bool bf16) {
+  if constexpr (GELU)
+    return gelu_accumulate(v, z, acc, bf16);
+  else
+    return mask_accumulate(v, bits, acc, bf16);
+}
+
+// Ragged element (column c of row r): the kept / scaled value and its fp32.
+template <bool GELU>
+__device__ __forceinline__ unsigned short apply_one(const DreluArgs& p, long long r, long long c,
+                                                    unsigned short g, float& f, bool bf16) {
+  if constexpr (GELU) {
+    f = to_f32(bf16, g) * gelu_tanh_grad(to_f32(bf16, p.zaux[r * p.ld_zaux + c]));
+    return from_f32(bf16, f);
+  } else {
+    const bool keep = (__ldg(p.mask + r * p.ld_aux + (c >> 5)) >> (c & 31)) & 1u;
+    const unsigned short o = keep ? g : static_cast<unsigned short>(0);
+    f = to_f32(bf16, o);
+    return o;
+  }
+}
+
+// DGELU_BGRAD keeps two blocks per SM: its derivative needs more registers.
+template <bool GELU>
+__global__ void __launch_bounds__(256, GELU ? 2 : MIN_BLOCKS) drelu_cols_kernel(const DreluArgs p) {
+  constexpr int U = GELU ? UNROLL / 2 : UNROLL;  // the z loads double the registers in flight
+  const bool bf16 = p.bf16 != 0;
   const int tx = threadIdx.x & 31;
   const int ty = threadIdx.x >> 5;
   const long long c0 = static_cast<long long>(blockIdx.x) * COLS_PER_BLOCK + tx * 8;
@@ -83,35 +136,43 @@ __global__ void __launch_bounds__(256, MIN_BLOCKS) drelu_cols_kernel(const Drelu
   if (c0 < p.C) {
     long long r = r_begin + ty;
     if (full) {
-      for (; r + (UNROLL - 1) * ROW_PHASES < r_end; r += UNROLL * ROW_PHASES) {
-        uint4 v[UNROLL];
-        uint32_t w[UNROLL];
+      for (; r + (U - 1) * ROW_PHASES < r_end; r += U * ROW_PHASES) {
+        uint4 v[U];
+        uint32_t w[U];
+        uint4 z[U];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < U; ++u) {
           const long long rr = r + u * ROW_PHASES;
           v[u] = ld_stream(p.dY + rr * p.ld + c0);
-          w[u] = __ldg(p.mask + rr * p.ld_aux + widx);
+          if constexpr (GELU)
+            z[u] = __ldg(reinterpret_cast<const uint4*>(p.zaux + rr * p.ld_zaux + c0));
+          else
+            w[u] = __ldg(p.mask + rr * p.ld_aux + widx);
         }
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < U; ++u) {
           const long long rr = r + u * ROW_PHASES;
-          const uint4 o = mask_accumulate(v[u], w[u] >> bit_off, acc);
+          const uint4 o = apply_group<GELU>(v[u], w[u] >> bit_off, z[u], acc, bf16);
           st_stream(p.dZ + rr * p.ld + c0, o);
         }
       }
       for (; r < r_end; r += ROW_PHASES) {
         const uint4 v = ld_stream(p.dY + r * p.ld + c0);
-        const uint32_t w = __ldg(p.mask + r * p.ld_aux + widx);
-        st_stream(p.dZ + r * p.ld + c0, mask_accumulate(v, w >> bit_off, acc));
+        uint32_t w = 0;
+        uint4 z = make_uint4(0, 0, 0, 0);
+        if constexpr (GELU)
+          z = __ldg(reinterpret_cast<const uint4*>(p.zaux + r * p.ld_zaux + c0));
+        else
+          w = __ldg(p.mask + r * p.ld_aux + widx);
+        st_stream(p.dZ + r * p.ld + c0, apply_group<GELU>(v, w >> bit_off, z, acc, bf16));
       }
     } else {
       for (; r < r_end; r += ROW_PHASES) {  // ragged last strip: element-wise
-        const uint32_t w = __ldg(p.mask + r * p.ld_aux + widx) >> bit_off;
         for (int j = 0; j < 8 && c0 + j < p.C; ++j) {
-          const __half g = p.dY[r * p.ld + c0 + j];
-          const __half o = (w >> j) & 1u ? g : __ushort_as_half(0);
-          p.dZ[r * p.ld + c0 + j] = o;
-          acc[j] += __half2float(o);
+          const unsigned short g = reinterpret_cast<const unsigned short*>(p.dY)[r * p.ld + c0 + j];
+          float f;
+          reinterpret_cast<unsigned short*>(p.dZ)[r * p.ld + c0 + j] = apply_one<GELU>(p, r, c0 + j, g, f, bf16);
+          acc[j] += f;
         }
       }
     }
@@ -148,7 +209,9 @@ __global__ void __launch_bounds__(256, MIN_BLOCKS) drelu_cols_kernel(const Drelu
   }
 }
 
+template <bool GELU>
 __global__ void __launch_bounds__(256) drelu_rows_kernel(const DreluArgs p) {
+  const bool bf16 = p.bf16 != 0;
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
   const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
@@ -162,17 +225,22 @@ __global__ void __launch_bounds__(256) drelu_rows_kernel(const DreluArgs p) {
     const uint32_t* mrow = p.mask + r * p.ld_aux;
     for (long long c = lane * 8; c < C8; c += 256) {
       const uint4 v = ld_stream(src + c);
-      const uint32_t w = __ldg(mrow + (c >> 5)) >> (c & 31);
-      st_stream(dst + c, mask_accumulate(v, w, acc));
+      uint32_t w = 0;
+      uint4 z = make_uint4(0, 0, 0, 0);
+      if constexpr (GELU)
+        z = __ldg(reinterpret_cast<const uint4*>(p.zaux + r * p.ld_zaux + c));
+      else
+        w = __ldg(mrow + (c >> 5)) >> (c & 31);
+      st_stream(dst + c, apply_group<GELU>(v, w, z, acc, bf16));
     }
     float s = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) s += acc[j];
     for (long long c = C8 + lane; c < p.C; c += 32) {  // ragged tail
-      const uint32_t w = (__ldg(mrow + (c >> 5)) >> (c & 31)) & 1u;
-      const __half o = w ? src[c] : __ushort_as_half(0);
-      dst[c] = o;
-      s += __half2float(o);
+      float f;
+      reinterpret_cast<unsigned short*>(dst)[c] =
+          apply_one<GELU>(p, r, c, reinterpret_cast<const unsigned short*>(src)[c], f, bf16);
+      s += f;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -182,22 +250,29 @@ __global__ void __launch_bounds__(256) drelu_rows_kernel(const DreluArgs p) {
 
 }  // namespace
 
-// Row splits for the column case: about 1.3 waves of resident blocks (the
-// fastest setting measured for dY[8192, 11008] with 3 blocks per SM: 14
-// splits, 68 us against 72 us for two waves), at least 64 rows per split, at
-// most 256 splits. GE_DRELU_SPLITS overrides (sweeps).
-int drelu_splits(long long R, long long C, int num_sms) {
-  static int occ = 0;
-  if (occ == 0) {
+// Row splits for the column case: one wave of resident blocks (measured on
+// dY[8192, 11008], 43 strips, 3 blocks per SM: 8 or 10 splits (0.75 and 0.94
+// waves) take 58 us, 12 splits (1.13 waves) 75 us, 15 and 18 splits 65 and
+// 62 us), at least 64 rows per split, at most 256 splits. GE_DRELU_SPLITS
+// overrides (sweeps).
+int drelu_splits(long long R, long long C, int num_sms, int gelu) {
+  static int occ[2] = {0, 0};
+  if (occ[gelu ? 1 : 0] == 0) {
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, drelu_cols_kernel, 256, 0) != cudaSuccess || o < 1) {
+    const cudaError_t e =
+        gelu ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, drelu_cols_kernel<true>, 256, 0)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, drelu_cols_kernel<false>, 256, 0);
+    if (e != cudaSuccess || o < 1) {
       cudaGetLastError();
-      o = MIN_BLOCKS;
+      o = gelu ? 2 : MIN_BLOCKS;
     }
-    occ = o;
+    occ[gelu ? 1 : 0] = o;
   }
+  const int occupancy = occ[gelu ? 1 : 0];
   const long long strips = (C + COLS_PER_BLOCK - 1) / COLS_PER_BLOCK;
-  long long want = (4LL * occ * num_sms / 3 + strips - 1) / strips;
+  // One wave: the largest split count whose blocks are all resident at once.
+  // A partly filled second wave leaves most SMs idle while its blocks run.
+  long long want = static_cast<long long>(occupancy) * num_sms / strips;
   if (const char* env = std::getenv("GE_DRELU_SPLITS")) {
     const long long v = std::atoll(env);
     if (v >= 1) want = v;
@@ -214,11 +289,17 @@ cudaError_t launch_drelu_bgrad(const DreluArgs& a, int reduce_rows, cudaStream_t
   if (reduce_rows) {
     const long long strips = (a.C + COLS_PER_BLOCK - 1) / COLS_PER_BLOCK;
     dim3 grid(static_cast<unsigned>(strips), static_cast<unsigned>(a.splits));
-    drelu_cols_kernel<<<grid, 256, 0, s>>>(a);
+    if (a.gelu)
+      drelu_cols_kernel<true><<<grid, 256, 0, s>>>(a);
+    else
+      drelu_cols_kernel<false><<<grid, 256, 0, s>>>(a);
   } else {
     long long blocks = (a.R + 7) / 8;
     if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-    drelu_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    if (a.gelu)
+      drelu_rows_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    else
+      drelu_rows_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

@@ -95,16 +95,20 @@ __device__ __forceinline__ void unit_info(int u, int tail_start, int split, int 
 
 __device__ __forceinline__ float apply_act(int epi, float z) {
   if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
-  if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  if (epi == EPI_GELU_BIAS || epi == EPI_GELU_AUX_BIAS) return gelu_tanh(z);
   if (epi == EPI_GELU_ERF_BIAS) return gelu_erf(z);
   return z;
 }
 
 // Epilogue of one 32-column slab held by this thread (one accumulator row).
-// Returns the 32 packed fp16 values in `packed` and the mask bits.
+// Returns the 32 packed 16-bit values in `packed`, the mask bits, and for
+// GELU_AUX_BIAS the packed pre-activations in `zpacked`. BIAS_RESIDUAL adds
+// the slab's residual values `rw` (packed pairs) after the bias.
 template <int EPI, bool BIAS_COL>
 __device__ __forceinline__ uint32_t epilogue_slab(const uint32_t (&v)[32], float brow,
-                                                  const float (&bcol)[32], uint32_t (&packed)[16]) {
+                                                  const float (&bcol)[32], const uint32_t (&rw)[16],
+                                                  uint32_t (&packed)[16], uint32_t (&zpacked)[16],
+                                                  bool bf16) {
   uint32_t bits = 0;
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
@@ -114,34 +118,92 @@ __device__ __forceinline__ uint32_t epilogue_slab(const uint32_t (&v)[32], float
       z0 += BIAS_COL ? bcol[j] : brow;
       z1 += BIAS_COL ? bcol[j + 1] : brow;
     }
+    if (EPI == EPI_BIAS_RESIDUAL) {
+      const float2 r = to_f32x2(bf16, rw[j / 2]);
+      z0 += r.x;
+      z1 += r.y;
+    }
     if (EPI == EPI_RELU_AUX_BIAS) {
       bits |= (z0 > 0.0f ? 1u : 0u) << j;
       bits |= (z1 > 0.0f ? 1u : 0u) << (j + 1);
     }
-    packed[j / 2] = pack_half2(apply_act(EPI, z0), apply_act(EPI, z1));
+    if (EPI == EPI_GELU_AUX_BIAS) zpacked[j / 2] = pack2(bf16, z0, z1);
+    packed[j / 2] = pack2(bf16, apply_act(EPI, z0), apply_act(EPI, z1));
   }
   return bits;
 }
 
 template <bool BIAS_COL>
 __device__ __forceinline__ uint32_t epilogue_dispatch(int epi, const uint32_t (&v)[32], float brow,
-                                                      const float (&bcol)[32],
-                                                      uint32_t (&packed)[16]) {
+                                                      const float (&bcol)[32], const uint32_t (&rw)[16],
+                                                      uint32_t (&packed)[16], uint32_t (&zp)[16],
+                                                      bool bf16) {
   switch (epi) {
-    case EPI_BIAS: return epilogue_slab<EPI_BIAS, BIAS_COL>(v, brow, bcol, packed);
-    case EPI_RELU_BIAS: return epilogue_slab<EPI_RELU_BIAS, BIAS_COL>(v, brow, bcol, packed);
-    case EPI_GELU_BIAS: return epilogue_slab<EPI_GELU_BIAS, BIAS_COL>(v, brow, bcol, packed);
-    case EPI_GELU_ERF_BIAS: return epilogue_slab<EPI_GELU_ERF_BIAS, BIAS_COL>(v, brow, bcol, packed);
+    case EPI_BIAS: return epilogue_slab<EPI_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    case EPI_RELU_BIAS: return epilogue_slab<EPI_RELU_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    case EPI_GELU_BIAS: return epilogue_slab<EPI_GELU_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    case EPI_GELU_ERF_BIAS:
+      return epilogue_slab<EPI_GELU_ERF_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
     case EPI_RELU_AUX_BIAS:
-      return epilogue_slab<EPI_RELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, packed);
-    default: return epilogue_slab<EPI_NONE, BIAS_COL>(v, brow, bcol, packed);
+      return epilogue_slab<EPI_RELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    case EPI_GELU_AUX_BIAS:
+      return epilogue_slab<EPI_GELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    case EPI_BIAS_RESIDUAL:
+      return epilogue_slab<EPI_BIAS_RESIDUAL, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    default: return epilogue_slab<EPI_NONE, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+  }
+}
+
+// One 32x32 slab of 16-bit values (row `grow` of this thread; the warp's 32
+// rows start at `rbase`) to global memory at columns gcol0.. of a row-major
+// matrix `dst` (ld elements per row, tensor map `map`). A slab whose end
+// runs past Nk at a column that is not on a 16-byte boundary is stored
+// element by element (a TMA store writes whole 16-byte chunks and would
+// spill into the caller's columns). Otherwise the slab is staged in shared
+// memory (64-byte swizzle: 16-byte chunk j of row r sits at chunk
+// j ^ ((r >> 1) & 3)) and TMA-stored; the two staging buffers alternate per
+// issued store, so the newest store in flight always reads the other buffer.
+__device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const CUtensorMap* map,
+                                           unsigned short* dst, long long ld, int gcol0, int rbase,
+                                           int grow, int Mk, int Nk, uint8_t* stg, int& nstore,
+                                           int lane) {
+  if (gcol0 + 32 > Nk && (Nk & 7) != 0) {
+    if (grow < Mk) {
+      unsigned short* drow = dst + static_cast<long long>(grow) * ld + gcol0;
+      const int nvalid = Nk - gcol0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {  // static indices keep packed[] in registers
+        if (j < nvalid) {
+          const uint32_t w = packed[j >> 1];
+          drow[j] = static_cast<unsigned short>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+        }
+      }
+    }
+  } else if (rbase < Mk) {
+    uint8_t* buf = stg + (nstore & 1) * EPI_BUF_BYTES;
+    if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int sw = j ^ ((lane >> 1) & 3);
+      *reinterpret_cast<uint4*>(buf + lane * 64 + sw * 16) =
+          make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, smem_u32(buf), gcol0, rbase);
+      bulk_commit_group();
+    }
+    ++nstore;
   }
 }
 
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
+                   const GemmArgs p) {
   using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -180,6 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD);
+    if (p.epi == EPI_GELU_AUX_BIAS) tma_prefetch_desc(&tmZ);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -280,7 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && (!PAIR || leader)) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_f16_f32(C::TILE_M, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc = idesc_f16_f32(C::TILE_M, BN, p.a_mn, p.b_mn, p.bf16 ? 1u : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -349,7 +412,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // -------------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* stg = smem + C::OFF_EPI + (warp - 2) * 2 * EPI_BUF_BYTES;
-    const bool has_bias = p.epi != EPI_NONE && p.epi != EPI_DRELU_BGRAD;
+    const bool backward = p.epi == EPI_DRELU_BGRAD || p.epi == EPI_DGELU_BGRAD;
+    const bool has_bias = p.epi != EPI_NONE && !backward;
+    const bool bf16 = p.bf16 != 0;
+    const unsigned short* bias16 = reinterpret_cast<const unsigned short*>(p.bias);
     const bool bias_vec_ok = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -401,8 +467,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int rbase = mt * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // warp's first row of D'
       const int grow = rbase + lane;                                          // this thread's row
       float brow = 0.0f;
-      if (has_bias && !p.bias_per_col && grow < p.Mk) brow = __half2float(p.bias[grow]);
-      float bg_row = 0.0f;  // DRELU_BGRAD, bias per D' row: this tile's row sum
+      if (has_bias && !p.bias_per_col && grow < p.Mk) brow = to_f32(bf16, bias16[grow]);
+      float bg_row = 0.0f;  // D*_BGRAD, bias per D' row: this tile's row sum
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -420,6 +486,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t mword = 0;
         if (p.epi == EPI_DRELU_BGRAD && grow < p.Mk)
           mword = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
+        // DGELU_BGRAD: the slab's 32 stored pre-activations, likewise early;
+        // BIAS_RESIDUAL: the slab's 32 residual values.
+        uint32_t zw[16];
+        if (p.epi == EPI_DGELU_BGRAD || p.epi == EPI_BIAS_RESIDUAL) {
+          const unsigned short* zrow = p.zaux + static_cast<long long>(grow) * p.ld_zaux + gcol0;
+          if (grow < p.Mk && gcol0 + 32 <= p.Nk) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 w = __ldg(reinterpret_cast<const uint4*>(zrow) + i);
+              zw[4 * i] = w.x;
+              zw[4 * i + 1] = w.y;
+              zw[4 * i + 2] = w.z;
+              zw[4 * i + 3] = w.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t lo = grow < p.Mk && gcol0 + 2 * j < p.Nk ? zrow[2 * j] : 0u;
+              const uint32_t hi = grow < p.Mk && gcol0 + 2 * j + 1 < p.Nk ? zrow[2 * j + 1] : 0u;
+              zw[j] = lo | (hi << 16);
+            }
+          }
+        }
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + 32u * c, v);
         tmem_ld_wait();
@@ -430,10 +519,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const uint4 w = __ldg(bp + i);
-              const __half2* h = reinterpret_cast<const __half2*>(&w);
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
-                const float2 f = __half22float2(h[t]);
+                const float2 f = to_f32x2(bf16, ww[t]);
                 bcol[8 * i + 2 * t] = f.x;
                 bcol[8 * i + 2 * t + 1] = f.y;
               }
@@ -441,24 +530,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              bcol[j] = gcol0 + j < p.Nk ? __half2float(p.bias[gcol0 + j]) : 0.0f;
+              bcol[j] = gcol0 + j < p.Nk ? to_f32(bf16, bias16[gcol0 + j]) : 0.0f;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) bcol[j] = 0.0f;
         }
         uint32_t packed[16];
+        uint32_t zpacked[16];
         uint32_t bits = 0;
-        if (p.epi == EPI_DRELU_BGRAD) {
-          // dZ = z where the forward mask bit is set, else +0; the masked
-          // fp32 values feed the bias-gradient partial sums.
-          uint32_t w = mword;
-          if (p.Nk - gcol0 < 32) w &= (1u << (p.Nk - gcol0)) - 1u;
+        if (backward) {
+          // DRELU_BGRAD: dZ = dH where the forward mask bit is set, else +0.
+          // DGELU_BGRAD: dZ = dH * gelu'(z) with z the stored pre-activation.
+          // The fp32 values (before rounding) feed the bias-gradient sums;
+          // columns past Nk contribute 0.
           float zm[32];
+          if (p.epi == EPI_DRELU_BGRAD) {
+            uint32_t w = mword;
+            if (p.Nk - gcol0 < 32) w &= (1u << (p.Nk - gcol0)) - 1u;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) zm[j] = ((w >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
+            for (int j = 0; j < 32; ++j) zm[j] = ((w >> j) & 1u) ? __uint_as_float(v[j]) : 0.0f;
+          } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) packed[j] = pack_half2(zm[2 * j], zm[2 * j + 1]);
+            for (int j = 0; j < 16; ++j) {
+              const float2 z = to_f32x2(bf16, zw[j]);
+              zm[2 * j] = gcol0 + 2 * j < p.Nk ? __uint_as_float(v[2 * j]) * gelu_tanh_grad(z.x) : 0.0f;
+              zm[2 * j + 1] =
+                  gcol0 + 2 * j + 1 < p.Nk ? __uint_as_float(v[2 * j + 1]) * gelu_tanh_grad(z.y) : 0.0f;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) packed[j] = pack2(bf16, zm[2 * j], zm[2 * j + 1]);
           if (p.bias_per_col) {
             // bgrad indexes D' columns: reduce the 32 rows of this warp for
             // each of its 32 columns (lane l ends with column gcol0 + l).
@@ -481,52 +583,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bg_row += srow;
           }
         } else {
-          bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, packed)
-                                : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed);
+          bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, zw, packed, zpacked, bf16)
+                                : epilogue_dispatch<false>(p.epi, v, brow, bcol, zw, packed, zpacked, bf16);
         }
-        if (gcol0 + 32 > p.Nk && (p.Nk & 7) != 0) {
-          // Ragged last slab whose end is not on a 16-byte boundary: a TMA
-          // store writes whole 16-byte chunks, which would spill into the
-          // caller's columns past Nk, so these columns are stored directly.
-          if (grow < p.Mk) {
-            __half* drow = p.D + static_cast<long long>(grow) * p.ldd + gcol0;
-            const int nvalid = p.Nk - gcol0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {  // static indices keep packed[] in registers
-              if (j < nvalid) {
-                const uint32_t w = packed[j >> 1];
-                drow[j] = __ushort_as_half(static_cast<unsigned short>((j & 1) ? (w >> 16) : (w & 0xFFFFu)));
-              }
-            }
-          }
-        } else if (rbase < p.Mk) {
-          // Stage the 32x32 fp16 slab (64-byte swizzle: 16-byte chunk j of row
-          // r sits at chunk j ^ ((r >> 1) & 3)) and TMA-store it. Buffers
-          // alternate per issued store, so the newest store in flight always
-          // reads the other buffer than the one written now.
-          uint8_t* buf = stg + (nstore & 1) * EPI_BUF_BYTES;
-          if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int sw = j ^ ((lane >> 1) & 3);
-            *reinterpret_cast<uint4*>(buf + lane * 64 + sw * 16) =
-                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmD, smem_u32(buf), gcol0, rbase);
-            bulk_commit_group();
-          }
-          ++nstore;
-        }
+        store_slab(packed, &tmD, reinterpret_cast<unsigned short*>(p.D), p.ldd, gcol0, rbase, grow,
+                   p.Mk, p.Nk, stg, nstore, lane);
+        if (p.epi == EPI_GELU_AUX_BIAS)
+          store_slab(zpacked, &tmZ, p.zaux, p.ld_zaux, gcol0, rbase, grow, p.Mk, p.Nk, stg, nstore, lane);
         if (p.epi == EPI_RELU_AUX_BIAS && grow < p.Mk) {
           if (p.Nk - gcol0 < 32) bits &= (1u << (p.Nk - gcol0)) - 1u;
           p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;
         }
       }
-      if (p.epi == EPI_DRELU_BGRAD && !p.bias_per_col && grow < p.Mk)
+      if (backward && !p.bias_per_col && grow < p.Mk)
         p.bg_partials[static_cast<long long>(nt) * p.Mk + grow] = bg_row;
       tc_fence_before();
       __syncwarp();
@@ -563,7 +632,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int BN, bool PAIR>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
-                        const GemmArgs& args, int grid, cudaStream_t stream) {
+                        const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
   static bool configured[64] = {};  // the attribute is set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -592,7 +661,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, tmA, tmB, tmD, args);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, tmA, tmB, tmD, tmZ, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -625,10 +694,17 @@ __global__ void __launch_bounds__(256) tc_gemm_fixup_kernel(const GemmArgs p, in
                        static_cast<long long>(r) * bn + c * 32 + lane;
     float z = 0.0f;
     for (int s = 0; s < p.split; ++s) z += __ldcg(src + s * split_stride);
-    if (p.epi != EPI_NONE && gcol < p.Nk)
-      z += __half2float(p.bias_per_col ? p.bias[gcol] : p.bias[grow]);
+    const bool bf16 = p.bf16 != 0;
+    const unsigned short* bias16 = reinterpret_cast<const unsigned short*>(p.bias);
+    if (p.epi != EPI_NONE && gcol < p.Nk) z += to_f32(bf16, p.bias_per_col ? bias16[gcol] : bias16[grow]);
+    if (p.epi == EPI_BIAS_RESIDUAL && gcol < p.Nk)
+      z += to_f32(bf16, p.zaux[static_cast<long long>(grow) * p.ld_zaux + gcol]);
     const bool in = gcol < p.Nk;
-    if (in) p.D[static_cast<long long>(grow) * p.ldd + gcol] = __float2half_rn(apply_act(p.epi, z));
+    if (in)
+      reinterpret_cast<unsigned short*>(p.D)[static_cast<long long>(grow) * p.ldd + gcol] =
+          from_f32(bf16, apply_act(p.epi, z));
+    if (p.epi == EPI_GELU_AUX_BIAS && in)
+      p.zaux[static_cast<long long>(grow) * p.ld_zaux + gcol] = from_f32(bf16, z);
     if (p.epi == EPI_RELU_AUX_BIAS) {
       const uint32_t bits = __ballot_sync(0xffffffffu, in && z > 0.0f);
       if (lane == 0 && gcol0 < ((p.Nk + 127) & ~127))
@@ -711,14 +787,14 @@ cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len
 }
 
 cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmD, const GemmArgs& args, int grid,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args,
+                           int grid, cudaStream_t stream) {
   if (pair) {
-    if (block_n == 256) return launch_impl<256, true>(tmA, tmB, tmD, args, grid, stream);
-    return launch_impl<128, true>(tmA, tmB, tmD, args, grid, stream);
+    if (block_n == 256) return launch_impl<256, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    return launch_impl<128, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
   }
-  if (block_n == 256) return launch_impl<256, false>(tmA, tmB, tmD, args, grid, stream);
-  return launch_impl<128, false>(tmA, tmB, tmD, args, grid, stream);
+  if (block_n == 256) return launch_impl<256, false>(tmA, tmB, tmD, tmZ, args, grid, stream);
+  return launch_impl<128, false>(tmA, tmB, tmD, tmZ, args, grid, stream);
 }
 
 }  // namespace ge

@@ -32,20 +32,23 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+template <bool BF16>
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc) {
-  const __half2* ha = reinterpret_cast<const __half2*>(&a);
-  const __half2* hb = reinterpret_cast<const __half2*>(&b);
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 fa = __half22float2(ha[i]);
-    const float2 fb = __half22float2(hb[i]);
+    const float2 fa = to_f32x2(BF16, wa[i]);
+    const float2 fb = to_f32x2(BF16, wb[i]);
     acc = fmaf(fa.x, fb.x, acc);
     acc = fmaf(fa.y, fb.y, acc);
   }
   return acc;
 }
 
-template <int NT, int UNROLL>
+// BF16 picks the element type of A, B, bias and D at compile time so that the
+// fp16 and bf16 inner loops each decode with one instruction per pair.
+template <int NT, int UNROLL, bool BF16>
 __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
@@ -77,7 +80,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
           const __half* brow = p.B + n * p.ldb + k;
 #pragma unroll
           for (int u = 0; u < UNROLL; ++u)
-            acc[n] = dot8(a[u], __ldg(reinterpret_cast<const uint4*>(brow + u * SLAB)), acc[n]);
+            acc[n] = dot8<BF16>(a[u], __ldg(reinterpret_cast<const uint4*>(brow + u * SLAB)), acc[n]);
         }
       }
     }
@@ -85,13 +88,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
       const uint4 a = ld_stream(arow + k);
 #pragma unroll
       for (int n = 0; n < NT; ++n)
-        if (n < p.N) acc[n] = dot8(a, __ldg(reinterpret_cast<const uint4*>(p.B + n * p.ldb + k)), acc[n]);
+        if (n < p.N) acc[n] = dot8<BF16>(a, __ldg(reinterpret_cast<const uint4*>(p.B + n * p.ldb + k)), acc[n]);
     }
     for (int kk = K8 + lane; kk < p.K; kk += 32) {  // ragged K tail
-      const float av = __half2float(arow[kk]);
+      const float av = to_f32(BF16, reinterpret_cast<const unsigned short*>(arow)[kk]);
 #pragma unroll
       for (int n = 0; n < NT; ++n)
-        if (n < p.N) acc[n] = fmaf(av, __half2float(p.B[n * p.ldb + kk]), acc[n]);
+        if (n < p.N)
+          acc[n] = fmaf(av, to_f32(BF16, reinterpret_cast<const unsigned short*>(p.B)[n * p.ldb + kk]), acc[n]);
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
@@ -103,12 +107,15 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
     for (int n = 0; n < NT; ++n)
       if (n == lane) z = acc[n];
     if (lane < p.N) {
-      if (p.epi != EPI_NONE) z += __half2float(p.bias[m]);
+      if (p.epi != EPI_NONE) z += to_f32(BF16, reinterpret_cast<const unsigned short*>(p.bias)[m]);
+      if (p.epi == EPI_BIAS_RESIDUAL)
+        z += to_f32(BF16, p.res[m * p.ldd_m + static_cast<long long>(lane) * p.ldd_n]);
       float y = z;
       if (p.epi == EPI_RELU_BIAS) y = fmaxf(z, 0.0f);
       else if (p.epi == EPI_GELU_BIAS) y = gelu_tanh(z);
       else if (p.epi == EPI_GELU_ERF_BIAS) y = gelu_erf(z);
-      p.D[m * p.ldd_m + static_cast<long long>(lane) * p.ldd_n] = __float2half_rn(y);
+      reinterpret_cast<unsigned short*>(p.D)[m * p.ldd_m + static_cast<long long>(lane) * p.ldd_n] =
+          from_f32(BF16, y);
     }
   }
 }
@@ -131,7 +138,8 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL>, a);
+  cudaError_t e = a.bf16 ? cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL, true>, a)
+                         : cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL, false>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -10,7 +10,7 @@
 
 namespace ge {
 
-// Epilogue codes used by the kernels (forward only).
+// Epilogue codes used by the kernels.
 enum EpiCode : int {
   EPI_NONE = 0,
   EPI_BIAS = 1,
@@ -18,7 +18,10 @@ enum EpiCode : int {
   EPI_GELU_BIAS = 3,
   EPI_RELU_AUX_BIAS = 4,
   EPI_DRELU_BGRAD = 5,  // GEMM epilogue form: aux is the input mask
-  EPI_GELU_ERF_BIAS = 6
+  EPI_GELU_ERF_BIAS = 6,
+  EPI_GELU_AUX_BIAS = 7,  // tanh-GELU; the pre-activation z is a second output (zaux)
+  EPI_DGELU_BGRAD = 8,    // GEMM epilogue form: zaux is the input pre-activation
+  EPI_BIAS_RESIDUAL = 9   // h = A.B + bias + residual (zaux is the residual input)
 };
 
 // Device error word bits (the plan's workspace word 0).
@@ -38,6 +41,7 @@ struct GemmArgs {
   int a_mn;          // A' is M-major (1) or K-major (0)
   int b_mn;          // B' is N-major (1) or K-major (0)
   int epi;           // EpiCode
+  int bf16;          // element type of A, B, bias, D: bfloat16 (1) or fp16 (0)
   int bias_per_col;  // bias indexed by D' column (1) or row (0)
   const __half* bias;
   uint32_t* aux;     // mask words, rows of D', ld_aux words per row
@@ -58,6 +62,12 @@ struct GemmArgs {
   // is [num n-tiles][Mk]; column case: [ceil(Mk/32)][Nk].
   float* bg_partials;
   float* bgrad;
+  // GELU_AUX_BIAS: z of every element, written like D' (ld_zaux elements per
+  // row; through the zaux tensor map except on a ragged edge). DGELU_BGRAD:
+  // the stored z read back (same layout). BIAS_RESIDUAL: the residual input
+  // (same layout; it may be D itself).
+  unsigned short* zaux;
+  long long ld_zaux;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs
@@ -68,9 +78,10 @@ cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cu
 // out[i] = sum over j = 0..rows-1 (in order) of part[j * len + i], fp32.
 cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
                                 cudaStream_t stream);
+// tmZ: the zaux tensor map (GELU_AUX_BIAS; any valid map otherwise).
 cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmD, const GemmArgs& args, int grid,
-                           cudaStream_t stream);
+                           const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args,
+                           int grid, cudaStream_t stream);
 
 // Weight-streaming GEMV for N <= 16: A K-major [M, K] (lda), B K-major
 // (B[k,n] at B[n*ldb + k]), D[m,n] at m*ldd_m + n*ldd_n.
@@ -83,12 +94,15 @@ struct GemvArgs {
   __half* D;
   long long ldd_m, ldd_n;
   const __half* bias;
+  const unsigned short* res;  // BIAS_RESIDUAL: residual, strides as D (may be D)
   int epi;
+  int bf16;           // element type: bfloat16 (1) or fp16 (0)
   int static_a;       // launch with programmatic dependent launch (A never written upstream)
 };
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
 
-// DRELU_BGRAD on a stored matrix of R rows x C contiguous columns.
+// DRELU_BGRAD (gelu = 0: mask bits) or DGELU_BGRAD (gelu = 1: the stored
+// pre-activation zaux) on a stored matrix of R rows x C contiguous columns.
 // reduce_rows = 1: bgrad[c] = sum over rows r (D column-major case);
 // reduce_rows = 0: bgrad[r] = sum over columns c (D row-major case).
 struct DreluArgs {
@@ -102,15 +116,40 @@ struct DreluArgs {
   float* partials;    // [splits][C] workspace (reduce_rows only)
   unsigned int* counters;  // [ceil(C/256)] workspace (reduce_rows only)
   int splits;
+  int bf16;           // element type of dY / dZ: bfloat16 (1) or fp16 (0)
+  int gelu;           // DGELU_BGRAD: dZ = dY * gelu'(z) with z from zaux
+  const unsigned short* zaux;
+  long long ld_zaux;  // elements
 };
 cudaError_t launch_drelu_bgrad(const DreluArgs& args, int reduce_rows, cudaStream_t stream);
-int drelu_splits(long long R, long long C, int num_sms);
+int drelu_splits(long long R, long long C, int num_sms, int gelu);
 
 // Unfused baseline kernels, in place on D (R rows x C contiguous, ld).
 cudaError_t launch_bias_add(__half* D, long long R, long long C, long long ld, const __half* bias,
-                            int bias_per_row, cudaStream_t stream);
+                            int bias_per_row, int bf16, cudaStream_t stream);
+// GELU_AUX_BIAS also copies z to zaux (ld_zaux elements per row) first.
 cudaError_t launch_activation(__half* D, long long R, long long C, long long ld, int epi,
-                              uint32_t* aux, long long ld_aux, cudaStream_t stream);
+                              uint32_t* aux, long long ld_aux, unsigned short* zaux,
+                              long long ld_zaux, int bf16, cudaStream_t stream);
+
+// Normalisation of every row of H (R rows x C contiguous features, ld):
+// RMSNorm (layer = 0) y = h * rsqrt(mean(h^2) + eps) * gamma, or LayerNorm
+// (layer = 1) y = (h - mean) * rsqrt(var + eps) * gamma + beta (population
+// variance), written to Y (same layout; Y may be H).
+struct NormArgs {
+  long long R, C, ld;
+  const unsigned short* H;
+  unsigned short* Y;
+  const unsigned short* gamma;
+  const unsigned short* beta;
+  float eps;
+  int layer;
+  int bf16;
+};
+cudaError_t launch_norm(const NormArgs& args, int num_sms, cudaStream_t stream);
+// D[r, c] += res[r * ld + c] (unfused baseline of the residual add).
+cudaError_t launch_residual_add(__half* D, long long R, long long C, long long ld,
+                                const unsigned short* res, int bf16, cudaStream_t stream);
 
 // Bounded-wait probe (test hook).
 cudaError_t launch_wait_probe(unsigned int* err, long long budget, cudaStream_t stream);

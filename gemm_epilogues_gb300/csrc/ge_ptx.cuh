@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace ge {
@@ -277,13 +278,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, operand
+// Instruction descriptor, kind::f16: fp32 accumulator, fp16 or bf16 A and B
+// (both the same type), operand
 // majors (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n, uint32_t a_mn,
-                                                     uint32_t b_mn) {
+                                                     uint32_t b_mn, uint32_t bf16 = 0) {
   return (1u << 4)            // D format: f32
-         | (0u << 7)          // A format: f16
-         | (0u << 10)         // B format: f16
+         | (bf16 << 7)        // A format: f16 (0) or bf16 (1)
+         | (bf16 << 10)       // B format: same as A
          | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
@@ -308,9 +310,44 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
+// Derivative of the tanh-form GELU. With u = sqrt(2/pi) (z + 0.044715 z^3)
+// and t = tanh(u), the product and chain rules give
+//   0.5 (1 + t) + 0.5 z (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 z^2).
+// It uses CUDA's tanhf (a few ulp) rather than tanh.approx: bias gradients
+// sum these values over thousands of rows, where the approximation's error
+// would accumulate.
+__device__ __forceinline__ float gelu_tanh_grad(float z) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  const float k1 = 0.044715f;
+  const float z2 = z * z;
+  const float t = tanhf(k0 * fmaf(k1 * z, z2, z));
+  const float slope = (0.5f * z) * fmaf(-t, t, 1.0f) * k0 * fmaf(3.0f * k1, z2, 1.0f);
+  return fmaf(0.5f, t, 0.5f) + slope;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 16-bit element type of a kernel's operands, bias and output.
+__device__ __forceinline__ uint32_t pack2(bool bf16, float lo, float hi) {
+  return bf16 ? pack_bf162(lo, hi) : pack_half2(lo, hi);
+}
+__device__ __forceinline__ float to_f32(bool bf16, unsigned short bits) {
+  return bf16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+}
+__device__ __forceinline__ float2 to_f32x2(bool bf16, uint32_t w) {
+  if (bf16) return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+__device__ __forceinline__ unsigned short from_f32(bool bf16, float x) {
+  return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 
 }  // namespace ge

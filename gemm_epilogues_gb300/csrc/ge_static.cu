@@ -128,7 +128,7 @@ extern "C" ge_status_t ge_drelu_bgrad_static(int64_t M, int64_t N, ge_dlayout_t 
     const size_t ticket_bytes = (static_cast<size_t>(strips) * 4 + kTicketAlign - 1) / kTicketAlign * kTicketAlign;
     if (ticket_bytes + static_cast<size_t>(C) * 4 > kScratchBytes) return GE_ERR_UNSUPPORTED;
     int64_t max_splits = static_cast<int64_t>((kScratchBytes - ticket_bytes) / (static_cast<size_t>(C) * 4));
-    int splits = ge::drelu_splits(R, C, s.num_sms);
+    int splits = ge::drelu_splits(R, C, s.num_sms, 0);
     if (splits > max_splits) splits = static_cast<int>(max_splits);
     a.splits = splits;
     a.counters = reinterpret_cast<unsigned int*>(s.ptr);

@@ -15,7 +15,7 @@ namespace {
 
 __device__ __forceinline__ float act_of(int epi, float z) {
   if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
-  if (epi == EPI_GELU_BIAS) return gelu_tanh(z);
+  if (epi == EPI_GELU_BIAS || epi == EPI_GELU_AUX_BIAS) return gelu_tanh(z);
   if (epi == EPI_GELU_ERF_BIAS) return gelu_erf(z);
   return z;
 }
@@ -23,28 +23,29 @@ __device__ __forceinline__ float act_of(int epi, float z) {
 // D[r, c] += bias[r] (bias_per_row) or bias[c]; 8 contiguous fp16 per thread.
 __global__ void __launch_bounds__(256) bias_add_kernel(__half* D, long long R, long long C,
                                                         long long ld, const __half* bias,
-                                                        int bias_per_row) {
+                                                        int bias_per_row, int bf16_flag) {
+  const bool bf16 = bf16_flag != 0;
+  const unsigned short* b16 = reinterpret_cast<const unsigned short*>(bias);
   const long long vpr = (C + 7) / 8;  // 8-wide groups per row
   const long long total = R * vpr;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
     const long long r = i / vpr;
     const long long c0 = (i - r * vpr) * 8;
-    __half* row = D + r * ld;
+    unsigned short* row = reinterpret_cast<unsigned short*>(D) + r * ld;
     if (c0 + 8 <= C) {
       uint4 v = *reinterpret_cast<const uint4*>(row + c0);
-      __half2* h = reinterpret_cast<__half2*>(&v);
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        float2 f = __half22float2(h[t]);
-        f.x += __half2float(bias_per_row ? bias[r] : bias[c0 + 2 * t]);
-        f.y += __half2float(bias_per_row ? bias[r] : bias[c0 + 2 * t + 1]);
-        h[t] = __floats2half2_rn(f.x, f.y);
+        float2 f = to_f32x2(bf16, w[t]);
+        f.x += to_f32(bf16, bias_per_row ? b16[r] : b16[c0 + 2 * t]);
+        f.y += to_f32(bf16, bias_per_row ? b16[r] : b16[c0 + 2 * t + 1]);
+        w[t] = pack2(bf16, f.x, f.y);
       }
-      *reinterpret_cast<uint4*>(row + c0) = v;
+      *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
       for (long long c = c0; c < C; ++c)
-        row[c] = __float2half_rn(__half2float(row[c]) +
-                                 __half2float(bias_per_row ? bias[r] : bias[c]));
+        row[c] = from_f32(bf16, to_f32(bf16, row[c]) + to_f32(bf16, bias_per_row ? b16[r] : b16[c]));
     }
   }
 }
@@ -55,7 +56,9 @@ __global__ void __launch_bounds__(256) bias_add_kernel(__half* D, long long R, l
 // (padding words up to the row's 128-column boundary included).
 __global__ void __launch_bounds__(256) activation_kernel(__half* D, long long R, long long C,
                                                           long long ld, int epi, uint32_t* aux,
-                                                          long long ld_aux) {
+                                                          long long ld_aux, unsigned short* zaux,
+                                                          long long ld_zaux, int bf16_flag) {
+  const bool bf16 = bf16_flag != 0;
   const long long wpr = aux ? ld_aux : (C + 31) / 32;  // 32-element words per row
   const long long units = R * wpr * 4;                 // one unit = 8 elements
   const long long pad_cols = ((C + 127) / 128) * 128;
@@ -70,23 +73,25 @@ __global__ void __launch_bounds__(256) activation_kernel(__half* D, long long R,
       r = u / wpr;
       word = u - r * wpr;
       c0 = word * 32 + (i & 3) * 8;
-      __half* row = D + r * ld;
+      unsigned short* row = reinterpret_cast<unsigned short*>(D) + r * ld;
       if (c0 + 8 <= C) {
         uint4 v = *reinterpret_cast<const uint4*>(row + c0);
-        __half2* h = reinterpret_cast<__half2*>(&v);
+        if (zaux) *reinterpret_cast<uint4*>(zaux + r * ld_zaux + c0) = v;  // GELU_AUX_BIAS: keep z
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const float2 f = __half22float2(h[t]);
+          const float2 f = to_f32x2(bf16, w[t]);
           byte |= (f.x > 0.0f ? 1u : 0u) << (2 * t);
           byte |= (f.y > 0.0f ? 1u : 0u) << (2 * t + 1);
-          h[t] = __floats2half2_rn(act_of(epi, f.x), act_of(epi, f.y));
+          w[t] = pack2(bf16, act_of(epi, f.x), act_of(epi, f.y));
         }
-        *reinterpret_cast<uint4*>(row + c0) = v;
+        *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
         for (long long c = c0; c < C && c < c0 + 8; ++c) {
-          const float f = __half2float(row[c]);
+          if (zaux) zaux[r * ld_zaux + c] = row[c];
+          const float f = to_f32(bf16, row[c]);
           byte |= (f > 0.0f ? 1u : 0u) << (c - c0);
-          row[c] = __float2half_rn(act_of(epi, f));
+          row[c] = from_f32(bf16, act_of(epi, f));
         }
       }
     }
@@ -126,17 +131,19 @@ int grid_for(long long work, int per_block) {
 }  // namespace
 
 cudaError_t launch_bias_add(__half* D, long long R, long long C, long long ld, const __half* bias,
-                            int bias_per_row, cudaStream_t s) {
+                            int bias_per_row, int bf16, cudaStream_t s) {
   if (R == 0 || C == 0) return cudaSuccess;
-  bias_add_kernel<<<grid_for(R * ((C + 7) / 8), 256), 256, 0, s>>>(D, R, C, ld, bias, bias_per_row);
+  bias_add_kernel<<<grid_for(R * ((C + 7) / 8), 256), 256, 0, s>>>(D, R, C, ld, bias, bias_per_row, bf16);
   return cudaGetLastError();
 }
 
 cudaError_t launch_activation(__half* D, long long R, long long C, long long ld, int epi,
-                              uint32_t* aux, long long ld_aux, cudaStream_t s) {
+                              uint32_t* aux, long long ld_aux, unsigned short* zaux,
+                              long long ld_zaux, int bf16, cudaStream_t s) {
   if (R == 0 || C == 0) return cudaSuccess;
   const long long wpr = aux ? ld_aux : (C + 31) / 32;
-  activation_kernel<<<grid_for(R * wpr * 4, 256), 256, 0, s>>>(D, R, C, ld, epi, aux, ld_aux);
+  activation_kernel<<<grid_for(R * wpr * 4, 256), 256, 0, s>>>(D, R, C, ld, epi, aux, ld_aux, zaux,
+                                                               ld_zaux, bf16);
   return cudaGetLastError();
 }
 

@@ -1,10 +1,10 @@
 """Seeded synthetic inputs shared by the tests, the smoke check and the
 benchmark. Random numbers only: this module holds none of the method's
-arithmetic. Both the CUDA path and the CPU oracle are given the same fp16
-bit patterns generated here.
+arithmetic. Both the CUDA path and the CPU oracle are given the same fp16 (or
+bf16) bit patterns generated here.
 
 Recipe: ``torch.Generator(device).manual_seed(seed)``, draw fp32, scale,
-round once to fp16 (round to nearest even). Seeds are
+round once to fp16 or bf16 (round to nearest even). Seeds are
 ``config_index * 1000 + tensor_index`` (A = 1, B = 2, bias = 3, dY = 4).
 Large tensors are drawn on the GPU (the CPU generator would take minutes);
 small ones on the CPU. The workloads stand in for the pages' shapes: the
@@ -20,27 +20,33 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-# Largest fp16 value below 1: keeps uniform [0,1) draws below 1 after rounding.
-_F16_BELOW_ONE = 0.99951171875
+# Largest value below 1 of each 16-bit type: keeps uniform [0,1) draws below 1
+# after rounding.
+_BELOW_ONE = {torch.float16: 0.99951171875, torch.bfloat16: 0.99609375}
+
+TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
-def f16_tensor(shape, seed: int, dist: str = "normal", std: float = 1.0, device="cpu") -> torch.Tensor:
-    """fp16 tensor of `shape`: dist "normal" -> N(0, std^2); "uniform01" -> U[0,1)."""
+def f16_tensor(shape, seed: int, dist: str = "normal", std: float = 1.0, device="cpu",
+               dtype: torch.dtype = torch.float16) -> torch.Tensor:
+    """16-bit tensor of `shape` (fp16, or bf16 with dtype=torch.bfloat16):
+    dist "normal" -> N(0, std^2); "uniform01" -> U[0,1); "int" -> integers in
+    [-std, std]. The same seed gives the same fp32 draws for either type."""
     dev = torch.device(device)
     g = torch.Generator(device=dev)
     g.manual_seed(int(seed))
     if dist == "uniform01":
         x = torch.rand(shape, generator=g, device=dev, dtype=torch.float32)
-        return x.to(torch.float16).clamp_(max=_F16_BELOW_ONE)
+        return x.to(dtype).clamp_(max=_BELOW_ONE[dtype])
     if dist == "normal":
         x = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
         if std != 1.0:
             x.mul_(std)
-        return x.to(torch.float16)
+        return x.to(dtype)
     if dist == "int":  # integers in [-std, std] (exact-arithmetic cases)
         hi = int(std)
         x = torch.randint(-hi, hi + 1, shape, generator=g, device=dev, dtype=torch.int32)
-        return x.to(torch.float16)
+        return x.to(dtype)
     raise ValueError(dist)
 
 
@@ -68,6 +74,7 @@ class Workload:
     bias_dist: tuple = ("normal", 1.0)
     index: int = 0
     extra: dict = field(default_factory=dict)
+    dtype: str = "f16"  # element type of A, B, bias and D: "f16" | "bf16"
 
     def a_shape(self):
         return (self.M, self.K) if self.a_major == "k" else (self.K, self.M)
@@ -79,11 +86,12 @@ class Workload:
         return (self.M, self.N) if self.d_layout == "row" else (self.N, self.M)
 
     def make(self, device="cpu"):
-        """(A, B, bias) fp16 tensors in storage layout."""
+        """(A, B, bias) tensors of the workload's element type in storage layout."""
         i = self.index * 1000
-        A = f16_tensor(self.a_shape(), i + 1, self.a_dist[0], self.a_dist[1], device)
-        B = f16_tensor(self.b_shape(), i + 2, self.b_dist[0], self.b_dist[1], device)
-        bias = f16_tensor((self.M,), i + 3, self.bias_dist[0], self.bias_dist[1], device)
+        t = TORCH_DTYPE[self.dtype]
+        A = f16_tensor(self.a_shape(), i + 1, self.a_dist[0], self.a_dist[1], device, t)
+        B = f16_tensor(self.b_shape(), i + 2, self.b_dist[0], self.b_dist[1], device, t)
+        bias = f16_tensor((self.M,), i + 3, self.bias_dist[0], self.bias_dist[1], device, t)
         return A, B, bias
 
     @property

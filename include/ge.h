@@ -75,10 +75,17 @@ typedef enum {
   GE_EPI_GELU_BIAS = 3,     /* D = gelu_tanh(A.B + bias)                       */
   GE_EPI_RELU_AUX_BIAS = 4, /* RELU_BIAS plus the bit-packed mask (z > 0)      */
   GE_EPI_DRELU_BGRAD = 5,   /* backward: dZ = dY * mask, bgrad = sum_n dZ      */
-  GE_EPI_GELU_ERF_BIAS = 6  /* D = z * Phi(z), z = A.B + bias (exact erf GELU) */
+  GE_EPI_GELU_ERF_BIAS = 6, /* D = z * Phi(z), z = A.B + bias (exact erf GELU) */
+  GE_EPI_GELU_AUX_BIAS = 7, /* GELU_BIAS plus z = A.B + bias kept as aux       */
+  GE_EPI_DGELU_BGRAD = 8,   /* backward: dZ = dY * gelu'(z), bgrad = sum_n     */
+  /* MatMul + bias + residual + norm over the M features (ge_execute_norm): */
+  GE_EPI_BIAS_RESIDUAL_RMSNORM = 9,
+  GE_EPI_BIAS_RESIDUAL_LAYERNORM = 10
 } ge_epilogue_t;
 
-typedef enum { GE_F16 = 0, GE_F32 = 1 } ge_dtype_t;
+/* GE_BF16: bfloat16 (1 sign, 8 exponent, 7 fraction bits), the other 16-bit
+ * operand type of the tensor cores' f16 kind. */
+typedef enum { GE_F16 = 0, GE_F32 = 1, GE_BF16 = 2 } ge_dtype_t;
 
 /* Operand storage. A: K_MAJOR -> A[m,k] at A[m*lda + k]; MN_MAJOR -> A[k*lda + m].
  *                  B: K_MAJOR -> B[k,n] at B[n*ldb + k]; MN_MAJOR -> B[k*ldb + n]. */
@@ -87,10 +94,12 @@ typedef enum { GE_K_MAJOR = 0, GE_MN_MAJOR = 1 } ge_major_t;
 /* D storage: ROW -> D[m,n] at D[m*ldd + n]; COL -> D[m,n] at D[n*ldd + m]. */
 typedef enum { GE_D_ROW = 0, GE_D_COL = 1 } ge_dlayout_t;
 
-/* Leading dimensions in elements (ld_aux in 32-bit words); 0 selects the
- * packed default (K or M/N for the operands, the contiguous extent of D, and
- * ceil(len/128)*4 words for the mask). Every leading dimension must be a
- * multiple of 8 elements (16 bytes), ld_aux a multiple of 4 words. */
+/* Leading dimensions in elements (ld_aux of a mask in 32-bit words, of the
+ * GELU_AUX_BIAS / DGELU_BGRAD pre-activation in elements); 0 selects the
+ * packed default (K or M/N for the operands, the contiguous extent of D,
+ * ceil(len/128)*4 words for the mask, and the contiguous extent of D rounded
+ * up to 8 for the pre-activation). Every leading dimension must be a
+ * multiple of 8 elements (16 bytes), a mask's ld_aux a multiple of 4 words. */
 typedef struct {
   ge_major_t a;
   ge_major_t b;
@@ -109,10 +118,12 @@ typedef enum {
  * ge_plan_create: validate a problem and choose its kernel.
  *   out      : receives the plan (set to NULL on failure).
  *   M, N, K  : problem size. M, N >= 1. K >= 1 for the forward epilogues;
- *              with DRELU_BGRAD, K == 0 selects the standalone kernel on a
- *              stored dY and K >= 1 the GEMM-epilogue form (the mask is
- *              applied to the product A.B). M, N, K < 2^31.
- *   a, b, d  : operand and output dtypes; GE_F16 only.
+ *              with DRELU_BGRAD or DGELU_BGRAD, K == 0 selects the standalone
+ *              kernel on a stored dY and K >= 1 the GEMM-epilogue form (the
+ *              gradient factor is applied to the product A.B). M, N, K < 2^31.
+ *   a, b, d  : operand and output dtypes: all GE_F16 or all GE_BF16. The
+ *              bias (and the standalone DRELU_BGRAD's dY and dZ) has the
+ *              same type; the DRELU_BGRAD bias gradient stays fp32.
  *   compute  : accumulation dtype; GE_F32 only.
  *   epi      : epilogue.
  *   layout   : may be NULL = {A K_MAJOR, B MN_MAJOR, D ROW, packed lds}.
@@ -133,27 +144,38 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K,
  * NULL = the legacy default stream). All pointers are device pointers of
  * the plan's device (alignment rules at the end of this comment).
  * Forward epilogues:
- *   A, B  : fp16 operands in the planned layouts (read only).
- *   bias  : fp16 [M] (read only); required for every *_BIAS epilogue,
+ * (T below is the plan's element type, fp16 or bf16.)
+ *   A, B  : T operands in the planned layouts (read only).
+ *   bias  : T [M] (read only); required for every *_BIAS epilogue,
  *           ignored for NONE.
- *   D     : fp16 output, written once.
+ *   D     : T output, written once.
  *   aux   : RELU_AUX_BIAS only: uint32 mask words, ge_aux_bytes(plan) bytes.
  *           Bit (c % 32) of word aux[r*ld_aux + c/32] is 1 iff the fp32
  *           pre-activation of the element at stored row r, contiguous index c
  *           of D is > 0 ((r,c) = (m,n) for D ROW, (n,m) for D COL). Words up
  *           to ceil(len/128)*4 of each row are written; bits past the end of
  *           the row are 0.
+ *   aux   : GELU_AUX_BIAS: T [rows of D][ld_aux] (ge_aux_bytes(plan) bytes,
+ *           16-byte aligned), stored like D: z = A.B + bias rounded once to T
+ *           (the pre-activation DGELU_BGRAD differentiates at).
  * DRELU_BGRAD as a GEMM epilogue (K >= 1): the backward product dH = A.B
  * (fp32 accumulate) is masked before its single store:
- *   A, B  : fp16 operands as for the forward epilogues.
+ *   A, B  : T operands as for the forward epilogues.
  *   aux   : the forward mask (read only), same packing as RELU_AUX_BIAS.
- *   D     : dZ, fp16: dZ[m,n] = fp16(dH[m,n]) where the bit is set, else +0.
+ *   D     : dZ, T: dZ[m,n] = T(dH[m,n]) where the bit is set, else +0.
  *   bias  : OUTPUT, fp32 [M]: bgrad[m] = sum over n of the masked fp32 dH,
  *           reduced in a fixed order (per-tile partial sums in the plan
  *           workspace, then one ordered pass), 16-byte aligned.
+ * DGELU_BGRAD (tanh-GELU backward; GELU counterpart of DRELU_BGRAD): as
+ * DRELU_BGRAD in both forms, with aux = the forward's z (T, stored like D,
+ * ld_aux elements, 16-byte aligned, read only) in place of the mask:
+ *   dZ[m,n] = T(g[m,n]), g = (dH or dY)[m,n] * gelu'(z[m,n]) in fp32, where
+ *   gelu'(z) = 0.5 (1 + t) + 0.5 z (1 - t^2) sqrt(2/pi) (1 + 0.134145 z^2),
+ *   t = tanh(sqrt(2/pi) (z + 0.044715 z^3)); bgrad[m] = sum over n of the
+ *   unrounded fp32 g, in a fixed order. dZ may alias dY, not aux.
  * DRELU_BGRAD standalone (K == 0; dY and dZ are [M,N] in the planned D layout):
- *   A     : dY, fp16 (read only).        B : unused (may be NULL).
- *   aux   : the forward mask (read only). D : dZ, fp16; may alias A.
+ *   A     : dY, T (read only).           B : unused (may be NULL).
+ *   aux   : the forward mask (read only). D : dZ, T; may alias A.
  *   bias  : OUTPUT, fp32 [M]: bgrad[m] = sum over n of dZ[m,n], reduced in
  *           fp32 in a fixed order (deterministic run to run).
  *   dZ[m,n] = dY[m,n] where the mask bit is set, +0 elsewhere.
@@ -172,14 +194,56 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B,
  * ge_execute_unfused: the three-kernel baseline on the same inputs: the
  * plan's GEMM with no epilogue writes D, then one kernel reads D, adds the
  * bias and writes D, then one kernel reads D, applies the activation (and
- * writes the mask for RELU_AUX_BIAS, from the rounded fp16 z) and writes D
+ * writes the mask for RELU_AUX_BIAS, from the rounded z) and writes D
  * (ops-nn MatMul fusion, "ops-nn's MatMul fusion strategy", the unfused
- * three-step flow). Only for BIAS / RELU_BIAS / GELU_BIAS / RELU_AUX_BIAS
+ * three-step flow). Only for BIAS / RELU_BIAS / GELU_BIAS / RELU_AUX_BIAS / GELU_ERF_BIAS / GELU_AUX_BIAS
  * plans. Arguments and errors as ge_execute.
  */
 ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B,
                                const void* bias, void* D, void* aux,
                                void* stream);
+
+/*
+ * ge_execute_norm: MatMul + bias + residual + normalisation, the structural
+ * fusion of ops-nn MatMul fusion (codearts), "ops-nn's MatMul fusion
+ * strategy", second level (MatMul + LayerNorm / RMSNorm with the residual
+ * connection; the norm reduces across the channel dimension). For a plan
+ * created with GE_EPI_BIAS_RESIDUAL_RMSNORM or _LAYERNORM and a column-major
+ * D (D[m,n] at n*ldd + m: N tokens of M contiguous features; other layouts
+ * are GE_ERR_UNSUPPORTED at planning):
+ *   h[m,n] = sum_k A[m,k] B[k,n] + bias[m] + residual[m,n]   (fp32)
+ *   H      = h rounded to T (the new residual stream), stored like D
+ *   for every token n, over its M features (population statistics):
+ *     RMSNorm:   Y = h * rsqrt(mean(h^2) + eps) * gamma
+ *     LayerNorm: Y = (h - mu) * rsqrt(mean((h - mu)^2) + eps) * gamma + beta
+ *   Y is stored like D, rounded to T.
+ * The GEMM (or, for N <= 16, the GEMV) adds bias and residual in its
+ * epilogue and stores H once; one more pass reads each token's row of H
+ * once and writes Y (the statistics are taken from the stored H).
+ *   A, B              : T operands in the planned layouts (read only).
+ *   bias, gamma, beta : T [M] (read only); beta only for LayerNorm (may be
+ *                       NULL for RMSNorm). gamma, beta 16-byte aligned.
+ *   residual, H, Y    : T, laid out like D (ldd), 16-byte aligned. H may be
+ *                       the residual buffer (in-place update of the residual
+ *                       stream); Y may be H.
+ *   eps               : >= 0, added to the mean square / variance.
+ * Returns GE_OK, GE_ERR_UNSUPPORTED (not a norm plan), GE_ERR_INVALID_ARG,
+ * GE_ERR_ALIGNMENT, GE_ERR_DEVICE_MISMATCH or GE_ERR_CUDA. ge_execute on a
+ * norm plan returns GE_ERR_UNSUPPORTED.
+ */
+ge_status_t ge_execute_norm(ge_plan_t plan, const void* A, const void* B, const void* bias,
+                            const void* residual, const void* gamma, const void* beta,
+                            void* H, void* Y, float eps, void* stream);
+
+/*
+ * ge_execute_norm_unfused: the same result by separate kernels, the flow the
+ * fusion replaces: the GEMM writes A.B as H, then bias add, residual add and
+ * the norm pass each read and write H. H must not be the residual buffer.
+ */
+ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B,
+                                    const void* bias, const void* residual,
+                                    const void* gamma, const void* beta, void* H, void* Y,
+                                    float eps, void* stream);
 
 /* Plan attributes (ge_plan_set_attr). */
 typedef enum {
@@ -225,10 +289,12 @@ int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split);
  * must make sure no execute of the plan is still running on the GPU. */
 ge_status_t ge_plan_free(ge_plan_t plan);
 
-/* Bytes of mask the caller allocates for RELU_AUX_BIAS (0 otherwise). */
+/* Bytes of aux output the caller allocates: the mask of RELU_AUX_BIAS or
+ * the pre-activation of GELU_AUX_BIAS (0 otherwise). */
 size_t ge_aux_bytes(ge_plan_t plan);
 
-/* Mask row pitch in 32-bit words chosen by the plan (0 if no mask). */
+/* Row pitch of aux chosen by the plan: 32-bit words for a mask, elements for
+ * a pre-activation (GELU_AUX_BIAS, DGELU_BGRAD); 0 if the plan has no aux. */
 int64_t ge_aux_ld(ge_plan_t plan);
 
 /* The kernel path the plan selected, or -1 for a NULL plan. */

@@ -6,20 +6,22 @@ import numpy as np
 import torch
 
 import gemm_epilogues_gb300 as ge
-from gemm_epilogues_gb300.inputs import Workload
+from gemm_epilogues_gb300.inputs import TORCH_DTYPE, Workload
 
 MAJOR = {"k": ge.GE_K_MAJOR, "m": ge.GE_MN_MAJOR, "n": ge.GE_MN_MAJOR}
 DLAY = {"row": ge.GE_D_ROW, "col": ge.GE_D_COL}
+GE_DT = {"f16": ge.GE_F16, "bf16": ge.GE_BF16}
 
-# Tolerances (fp16 outputs: |err| <= 1e-2 * max(1, |ref|); mask bit-exact
-# where |pre-activation| > 1e-3; fp32 bias gradient: relative 1e-4).
+# Tolerances (16-bit outputs: |err| <= 1e-2 * max(1, |ref|); mask bit-exact
+# where |pre-activation| > 1e-3; fp32 bias gradient: relative 1e-4). For bf16
+# the same bound holds: one bf16 step is at most 2^-7 = 0.0078 of the value.
 F16_REL = 1e-2
 MASK_BAND = 1e-3
 BGRAD_REL = 1e-4
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """fp16 tensor (any device) -> numpy uint16 bit patterns (flat)."""
+    """fp16/bf16 tensor (any device) -> numpy uint16 bit patterns (flat)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1)
 
 
@@ -32,10 +34,10 @@ def gpu_forward(w: Workload, A, B, bias, *, unfused=False, ld=None, stream=None)
     CUDA fp16 tensors in storage layout. Returns (D, aux, plan path)."""
     ld = ld or {}
     L = layout_of(w, ld.get("lda", 0), ld.get("ldb", 0), ld.get("ldd", 0))
-    with ge.Plan(w.M, w.N, w.K, ge.EPILOGUE_BY_NAME[w.epilogue], L) as p:
+    with ge.Plan(w.M, w.N, w.K, ge.EPILOGUE_BY_NAME[w.epilogue], L, dtype=GE_DT[w.dtype]) as p:
         rows, cols = w.d_shape()
         ldd = ld.get("ldd", 0) or cols
-        D = torch.full((rows, ldd), float("nan"), dtype=torch.float16, device=A.device)
+        D = torch.full((rows, ldd), float("nan"), dtype=TORCH_DTYPE[w.dtype], device=A.device)
         aux = None
         if w.epilogue == "relu_aux_bias":
             aux = torch.full((p.aux_bytes // 4,), 0xA5A5A5A5 - 2**32, dtype=torch.int32, device=A.device)
@@ -54,7 +56,7 @@ def oracle_full(oracle, w: Workload, A, B, bias, ld=None):
     return oracle.linear_forward(bits(A), bits(B), bits(bias) if w.epilogue != "none" else None,
                                  w.epilogue, w.M, w.N, w.K, a_major=w.a_major, b_major=w.b_major,
                                  d_layout=w.d_layout, lda=ld.get("lda"), ldb=ld.get("ldb"),
-                                 ldd=ld.get("ldd"))
+                                 ldd=ld.get("ldd"), dtype=w.dtype)
 
 
 def oracle_rows(oracle, w: Workload, A, B, bias, rows: np.ndarray):
@@ -72,16 +74,21 @@ def oracle_rows(oracle, w: Workload, A, B, bias, rows: np.ndarray):
     return oracle.linear_forward(bits(sub["A"]), bits(sub["B"]),
                                  bits(sub["bias"]) if w.epilogue != "none" else None, w.epilogue,
                                  sub["M"], sub["N"], w.K, a_major=w.a_major, b_major=w.b_major,
-                                 d_layout=w.d_layout)
+                                 d_layout=w.d_layout, dtype=w.dtype)
 
 
-def check_f16(oracle, got_bits: np.ndarray, ref_bits: np.ndarray, what: str):
-    got = oracle.f16_decode(got_bits)
-    ref = oracle.f16_decode(ref_bits)
+def check_f16(oracle, got_bits: np.ndarray, ref_bits: np.ndarray, what: str, dtype: str = "f16",
+              extra_tol=None):
+    """16-bit output within F16_REL * max(1, |ref|), plus `extra_tol` (per
+    element) where a path rounds an intermediate to 16 bits."""
+    got = oracle.f16_decode(got_bits, dtype)
+    ref = oracle.f16_decode(ref_bits, dtype)
     assert got.shape == ref.shape
     assert np.isfinite(got).all(), f"{what}: non-finite output"
     err = np.abs(got - ref)
     tol = F16_REL * np.maximum(1.0, np.abs(ref))
+    if extra_tol is not None:
+        tol = tol + extra_tol
     bad = err > tol
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance, worst err "
                            f"{err.max():.4g} at {int(err.argmax())} (ref {ref[err.argmax()]:.6g})")
@@ -94,11 +101,13 @@ def mask_bits(words: np.ndarray, rows: int, ld_aux: int, cols: int) -> np.ndarra
     return b[:, :cols]
 
 
-def check_mask(got_words, ref_words, Z, rows, cols, ld_aux, what):
+def check_mask(got_words, ref_words, Z, rows, cols, ld_aux, what, band=None):
+    """Mask bits equal wherever |z| is outside the band (MASK_BAND, or a
+    per-element `band` [rows, cols] for a path that rounds z first)."""
     g = mask_bits(got_words, rows, ld_aux, cols)
     r = mask_bits(ref_words, rows, ld_aux, cols)
     z = Z.reshape(rows, -1)[:, :cols]
-    sure = np.abs(z) > MASK_BAND
+    sure = np.abs(z) > (MASK_BAND if band is None else band)
     assert np.array_equal(g[sure], r[sure]), f"{what}: mask differs outside the |z| <= 1e-3 band"
     # bits past the end of each row (up to the 128-column padding) are zero
     gw = got_words.reshape(rows, ld_aux)

@@ -51,9 +51,15 @@ def test_plan_validation_without_device(lib):
     assert _create(0, 8, 8) == E.GE_ERR_INVALID_ARG
     assert _create(8, -1, 8) == E.GE_ERR_INVALID_ARG
     assert _create(8, 8, 0, epi=E.GE_EPI_BIAS) == E.GE_ERR_INVALID_ARG
-    assert _create(8, 8, 8, epi=9) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 8, 8, epi=11) == E.GE_ERR_INVALID_ARG
+    # the norm epilogues need the features contiguous (D column-major)
+    assert _create(8, 8, 8, epi=E.GE_EPI_BIAS_RESIDUAL_RMSNORM) == E.GE_ERR_UNSUPPORTED
     assert _create(8, 8, 8, a=E.GE_F32) == E.GE_ERR_UNSUPPORTED
     assert _create(8, 8, 8, compute=E.GE_F16) == E.GE_ERR_UNSUPPORTED
+    # bf16 only when A, B and D are all bf16, and still with fp32 accumulation
+    assert _create(8, 8, 8, a=E.GE_BF16) == E.GE_ERR_UNSUPPORTED
+    assert _create(8, 8, 8, E.GE_BF16, E.GE_BF16, E.GE_F16) == E.GE_ERR_UNSUPPORTED
+    assert _create(8, 8, 8, E.GE_BF16, E.GE_BF16, E.GE_BF16, E.GE_BF16) == E.GE_ERR_UNSUPPORTED
     assert _create(8, 8, 0, epi=E.GE_EPI_BIAS) == E.GE_ERR_INVALID_ARG
     assert _create(2**31, 8, 8) == E.GE_ERR_INVALID_ARG
     # leading dimensions smaller than the extent, or not multiples of 8

@@ -8,9 +8,9 @@ import pytest
 import torch
 
 import gemm_epilogues_gb300 as ge
-from gemm_epilogues_gb300.inputs import f16_tensor
+from gemm_epilogues_gb300.inputs import TORCH_DTYPE, f16_tensor
 
-from _util import bits, check_bgrad, check_f16
+from _util import GE_DT, bits, check_bgrad, check_f16
 
 pytestmark = pytest.mark.gpu
 
@@ -21,14 +21,15 @@ def _pad8(x):
     return (x + 7) // 8 * 8
 
 
-def run_case(oracle, M, N, K, am, bm, dl, seed, dist=("normal", 1.0), exact=False):
+def run_case(oracle, M, N, K, am, bm, dl, seed, dist=("normal", 1.0), exact=False, dtype="f16"):
+    t = TORCH_DTYPE[dtype]
     rng = np.random.default_rng(seed)
     a_shape = (M, K) if am == "k" else (K, M)
     b_shape = (N, K) if bm == "k" else (K, N)
     rows, cols = (M, N) if dl == "row" else (N, M)
     lda, ldb, ldd = _pad8(a_shape[1]), _pad8(b_shape[1]), _pad8(cols)
-    A = f16_tensor((a_shape[0], lda), seed + 1, *dist).cuda()
-    B = f16_tensor((b_shape[0], ldb), seed + 2, *dist).cuda()
+    A = f16_tensor((a_shape[0], lda), seed + 1, *dist, dtype=t).cuda()
+    B = f16_tensor((b_shape[0], ldb), seed + 2, *dist, dtype=t).cuda()
     A[:, a_shape[1]:] = float("nan")
     B[:, b_shape[1]:] = float("nan")
     ld_aux = 4 * ((cols + 127) // 128)
@@ -38,23 +39,24 @@ def run_case(oracle, M, N, K, am, bm, dl, seed, dist=("normal", 1.0), exact=Fals
     aux_host = words.view(np.uint32).reshape(-1).copy()
     aux = torch.from_numpy(aux_host.view(np.int32)).cuda()
     L = ge.make_layout(MAJ[am], MAJ[bm], ge.GE_D_ROW if dl == "row" else ge.GE_D_COL, lda, ldb, ldd, ld_aux)
-    with ge.Plan(M, N, K, ge.GE_EPI_DRELU_BGRAD, L) as p:
+    with ge.Plan(M, N, K, ge.GE_EPI_DRELU_BGRAD, L, dtype=GE_DT[dtype]) as p:
         assert p.path == ge.GE_PATH_TC_GEMM
-        dZ = torch.full((rows, ldd), float("nan"), dtype=torch.float16, device="cuda")
+        dZ = torch.full((rows, ldd), float("nan"), dtype=t, device="cuda")
         bgrad = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda")
         p.execute(A, B, bgrad, dZ, aux)
         torch.cuda.synchronize()
         assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
     ref_dz, ref_bg = oracle.gemm_drelu_bgrad(bits(A), bits(B), aux_host, M, N, K, a_major=am, b_major=bm,
-                                             d_layout=dl, lda=lda, ldb=ldb, ldd=ldd, ld_aux=ld_aux)
+                                             d_layout=dl, lda=lda, ldb=ldb, ldd=ldd, ld_aux=ld_aux,
+                                             dtype=dtype)
     got = bits(dZ).reshape(rows, ldd)[:, :cols].reshape(-1)
     want = ref_dz.reshape(rows, ldd)[:, :cols].reshape(-1)
     if exact:
         assert np.array_equal(got, want)
     else:
-        check_f16(oracle, got, want, f"gemm drelu {M}x{N}x{K} {am}{bm}{dl}")
+        check_f16(oracle, got, want, f"gemm drelu {M}x{N}x{K} {am}{bm}{dl} {dtype}", dtype)
     assert torch.isnan(dZ[:, cols:].float()).all(), "wrote past the logical columns"
-    dzf = oracle.f16_decode(ref_dz).reshape(rows, ldd)[:, :cols]
+    dzf = oracle.f16_decode(ref_dz, dtype).reshape(rows, ldd)[:, :cols]
     abs_sum = np.abs(dzf).sum(axis=0 if dl == "col" else 1)
     check_bgrad(bgrad.cpu().numpy(), ref_bg, abs_sum, f"gemm drelu bgrad {M}x{N}x{K} {am}{bm}{dl}")
 

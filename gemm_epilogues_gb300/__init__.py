@@ -68,7 +68,8 @@ ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_
                  "ge_aux_bytes", "ge_aux_ld", "ge_plan_path", "ge_plan_tile_n",
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
                  "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr",
-                 "ge_plan_autotune", "ge_plan_config", "ge_execute_norm", "ge_execute_norm_unfused")
+                 "ge_plan_autotune", "ge_plan_config", "ge_execute_norm", "ge_execute_norm_unfused",
+                 "ge_autotune_cache_clear")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -105,6 +106,8 @@ def load_library():
         lib.ge_execute.restype = i32
         lib.ge_execute_unfused.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         lib.ge_execute_unfused.restype = i32
+        lib.ge_autotune_cache_clear.argtypes = []
+        lib.ge_autotune_cache_clear.restype = None
         for fn in (lib.ge_execute_norm, lib.ge_execute_norm_unfused):
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
             fn.restype = i32
@@ -187,6 +190,10 @@ def ge_execute(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool = False)
     if raw:
         return st
     _check(st, "ge_execute")
+
+
+def ge_autotune_cache_clear():
+    load_library().ge_autotune_cache_clear()
 
 
 def ge_execute_norm(plan, A, B, bias, residual, gamma, beta, H, Y, eps=1e-5, stream=None, *,

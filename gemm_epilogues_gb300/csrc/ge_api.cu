@@ -9,8 +9,10 @@
 // error; the plan must be freed).
 #include <cudaTypedefs.h>
 
+#include <array>
 #include <cstdint>
 #include <cstdlib>
+#include <map>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -35,11 +37,14 @@ struct Plan {
   bool swap = false;
   int block_n = 256;
   int pair = 0;  // 2-CTA (cta_group::2) tiles of 256 rows
+  int epi_warps = 4;  // epilogue warps of the tensor-core kernel (4 or 8)
   int tail_start = 0;  // split-K tail (see GemmArgs); `tail_ws` holds its pieces
   int split = 1;
   void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
   size_t tail_ws_bytes = 0;
   bool tc_allow_split = true;
+  float2* nstats = nullptr;    // norm plans, tensor-core path: per (n-tile, token) statistics
+  float2* rowstats = nullptr;  // ... and per token (mean, rstd)
   float* bg_partials = nullptr;  // DRELU_BGRAD GEMM epilogue: bias-gradient partials
   long long bg_rows = 0, bg_len = 0;
   int grid = 0;
@@ -129,6 +134,25 @@ struct TcConfig {
   int block_n = 256, pair = 0, split = 1, tail_start = 0, grid = 1, group_m = 1;
 };
 
+// Configurations chosen by ge_plan_autotune, per device, problem and layout:
+// a plan created later for the same key starts from the tuned choice.
+struct TunedChoice {
+  int block_n, pair, split;
+};
+using TuneKey = std::array<int64_t, 13>;
+std::map<TuneKey, TunedChoice>& tuned_cache() {
+  static std::map<TuneKey, TunedChoice> m;
+  return m;
+}
+std::mutex& tuned_mutex() {
+  static std::mutex mu;
+  return mu;
+}
+TuneKey tune_key(const Plan& pl) {
+  return {pl.device, pl.M, pl.N, pl.K, static_cast<int64_t>(pl.epi), pl.bf16, pl.L.a, pl.L.b, pl.L.d,
+          pl.L.lda, pl.L.ldb, pl.L.ldd, pl.L.ld_aux};
+}
+
 TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   TcConfig c;
   c.block_n = block_n;
@@ -138,7 +162,7 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   const int64_t tile_m = pair ? 256 : 128;
   const long long num_m = (Mk + tile_m - 1) / tile_m;
   const long long tiles = num_m * ((Nk + block_n - 1) / block_n);
-  const long long workers = pair ? tc_gemm_max_pairs(block_n, pl.num_sms) : pl.num_sms;
+  const long long workers = pair ? tc_gemm_max_pairs(block_n, pl.num_sms, pl.epi_warps) : pl.num_sms;
   c.group_m = static_cast<int>(num_m < (pair ? 8 : 16) ? num_m : (pair ? 8 : 16));
   // Split-K tail: when the last of several waves would leave most workers
   // idle, the tiles of that wave are split along K into just enough pieces
@@ -287,13 +311,15 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.partials = pl->partials;
     g.bg_partials = pl->bg_partials;
     g.bf16 = pl->bf16;
+    g.nstats = epi_code == EPI_BIAS_RESIDUAL ? pl->nstats : nullptr;
     const bool backward = epi_code == EPI_DRELU_BGRAD || epi_code == EPI_DGELU_BGRAD;
     g.bgrad = backward ? static_cast<float*>(const_cast<void*>(bias)) : nullptr;
     if (backward) g.bias = nullptr;
-    e = launch_tc_gemm(pl->block_n, pl->pair, pl->tmA, pl->tmB, pl->tmD, pl->tmZ, g, pl->grid, st);
+    e = launch_tc_gemm(pl->block_n, pl->pair, pl->epi_warps, pl->tmA, pl->tmB, pl->tmD, pl->tmZ, g, pl->grid, st);
     if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, st);
     if (e == cudaSuccess && backward) {
-      const long long rows = pl->swap ? pl->bg_rows : (g.Nk + pl->block_n - 1) / pl->block_n;
+      const long long rows =
+          pl->swap ? pl->bg_rows : (pl->epi_warps / 4) * static_cast<long long>((g.Nk + pl->block_n - 1) / pl->block_n);
       e = launch_bgrad_reduce(pl->bg_partials, rows, pl->bg_len, g.bgrad, st);
     }
   }
@@ -318,8 +344,9 @@ ge_status_t check_norm_args(Plan* pl, const void* A, const void* B, const void* 
   return GE_OK;
 }
 
+// stats_ready: the GEMM epilogue has written the per-tile statistics.
 ge_status_t launch_norm_pass(Plan* pl, const void* gamma, const void* beta, const void* H, void* Y, float eps,
-                             cudaStream_t st) {
+                             bool stats_ready, cudaStream_t st) {
   NormArgs n{};
   n.R = pl->N;  // tokens: rows of the column-major D
   n.C = pl->M;  // features
@@ -331,6 +358,13 @@ ge_status_t launch_norm_pass(Plan* pl, const void* gamma, const void* beta, cons
   n.eps = eps;
   n.layer = pl->epi == GE_EPI_BIAS_RESIDUAL_LAYERNORM ? 1 : 0;
   n.bf16 = pl->bf16;
+  if (stats_ready && pl->nstats) {
+    n.partials = pl->nstats;
+    n.tile_w = pl->block_n;
+    n.ntiles = static_cast<int>((pl->M + pl->block_n - 1) / pl->block_n);
+    n.halves = pl->epi_warps / 4;
+    n.rowstats = pl->rowstats;
+  }
   return launch_norm(n, pl->num_sms, st) == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 
@@ -472,6 +506,17 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (const char* env = std::getenv("GE_SPLIT_TAIL"))
       if (env[0] == '0') tc_split = false;
     if (backward) tc_split = false;  // their bias-gradient partials are per tile
+    if (epi_is_norm(epi)) tc_split = false;  // the norm statistics are taken per whole tile
+    // Eight epilogue warps for the GELU derivative, the heaviest epilogue:
+    // with four it lengthens the GEMM (11008x8192x4096 with DGELU_BGRAD:
+    // 0.555 ms with eight, 0.654 with four). Every other epilogue measured
+    // faster with four (NONE 0.452 vs 0.478 ms on the same shape; the norm
+    // fusion at 4096x8192x4096: 0.235 vs 0.241 ms).
+    tmp.epi_warps = epi == GE_EPI_DGELU_BGRAD ? 8 : 4;
+    if (const char* env = std::getenv("GE_EPI_WARPS")) {  // sweeps
+      if (env[0] == '4') tmp.epi_warps = 4;
+      if (env[0] == '8') tmp.epi_warps = 8;
+    }
   }
   size_t ws = 256;
   size_t bg_off = 0;
@@ -481,13 +526,24 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (tmp.swap) {  // bgrad indexes D' columns: partials per 32-row block
       tmp.bg_rows = (Mk + 31) / 32;
       tmp.bg_len = Nk;
-    } else {         // bgrad indexes D' rows: partials per n-tile (capacity: 128-wide tiles)
-      tmp.bg_rows = (Nk + 127) / 128;
+    } else {         // bgrad indexes D' rows: partials per n-tile and epilogue half (capacity: 128-wide tiles)
+      tmp.bg_rows = 2 * ((Nk + 127) / 128);
       tmp.bg_len = Mk;
     }
     ws = (ws + 255) / 256 * 256;
     bg_off = ws;
     ws += static_cast<size_t>(tmp.bg_rows) * static_cast<size_t>(tmp.bg_len) * 4;
+  }
+  size_t nstats_off = 0, rowstats_off = 0;
+  if (tmp.path == GE_PATH_TC_GEMM && epi_is_norm(epi)) {
+    // D is column-major here, so the kernel's rows are the N tokens and its
+    // columns the M features; capacity for the narrowest (128-wide) tiles.
+    ws = (ws + 255) / 256 * 256;
+    nstats_off = ws;
+    ws += 2 * static_cast<size_t>((M + 127) / 128) * static_cast<size_t>(N) * 8;
+    ws = (ws + 255) / 256 * 256;
+    rowstats_off = ws;
+    ws += static_cast<size_t>(N) * 8;
   }
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
     tmp.splits = drelu_splits(tmp.R, tmp.C, tmp.num_sms, epi == GE_EPI_DGELU_BGRAD ? 1 : 0);
@@ -508,6 +564,10 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   tmp.ws_bytes = ws;
   tmp.err = static_cast<unsigned int*>(tmp.ws);
   if (bg_off) tmp.bg_partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + bg_off);
+  if (nstats_off) {
+    tmp.nstats = reinterpret_cast<float2*>(static_cast<char*>(tmp.ws) + nstats_off);
+    tmp.rowstats = reinterpret_cast<float2*>(static_cast<char*>(tmp.ws) + rowstats_off);
+  }
   if (tmp.path == GE_PATH_DRELU && L.d == GE_D_COL) {
     tmp.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + 256);
     const int64_t strips = (tmp.C + 255) / 256;
@@ -522,7 +582,18 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   }
   if (pl->path == GE_PATH_TC_GEMM) {
     pl->tc_allow_split = tc_split;
-    ge_status_t st = apply_config(pl, tc_config(*pl, tc_block_n, tc_pair, tc_split));
+    bool split_on = tc_split;
+    const bool overridden = std::getenv("GE_TILE_N") || std::getenv("GE_PAIR") || std::getenv("GE_SPLIT_TAIL");
+    if (!overridden) {
+      std::lock_guard<std::mutex> lock(tuned_mutex());
+      auto it = tuned_cache().find(tune_key(*pl));
+      if (it != tuned_cache().end()) {
+        tc_block_n = it->second.block_n;
+        tc_pair = it->second.pair;
+        split_on = tc_split && it->second.split > 1;
+      }
+    }
+    ge_status_t st = apply_config(pl, tc_config(*pl, tc_block_n, tc_pair, split_on));
     if (st != GE_OK) {
       cudaFree(pl->ws);
       delete pl;
@@ -647,7 +718,7 @@ ge_status_t ge_execute_norm(ge_plan_t plan, const void* A, const void* B, const 
   // h = A.B + bias + residual in the GEMM (or GEMV) epilogue, stored once as H
   s = launch_forward(pl, A, B, bias, H, const_cast<void*>(residual), EPI_BIAS_RESIDUAL, st);
   if (s != GE_OK) return s;
-  return launch_norm_pass(pl, gamma, beta, H, Y, eps, st);
+  return launch_norm_pass(pl, gamma, beta, H, Y, eps, pl->path == GE_PATH_TC_GEMM, st);
 }
 
 ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B, const void* bias,
@@ -668,7 +739,12 @@ ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B
   if (launch_residual_add(Hh, pl->R, pl->C, pl->L.ldd, static_cast<const unsigned short*>(residual), pl->bf16,
                           st) != cudaSuccess)
     return GE_ERR_CUDA;
-  return launch_norm_pass(pl, gamma, beta, H, Y, eps, st);
+  return launch_norm_pass(pl, gamma, beta, H, Y, eps, false, st);
+}
+
+void ge_autotune_cache_clear(void) {
+  std::lock_guard<std::mutex> lock(tuned_mutex());
+  tuned_cache().clear();
 }
 
 ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const void* bias, void* D,
@@ -720,6 +796,10 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
   const ge_status_t s2 = apply_config(pl, best >= 0 ? cands[best] : current);
   if (s != GE_OK) return s;
   if (s2 != GE_OK) return s2;
+  {
+    std::lock_guard<std::mutex> lock(tuned_mutex());
+    tuned_cache()[tune_key(*pl)] = TunedChoice{cands[best].block_n, cands[best].pair, cands[best].split};
+  }
   return ge_execute(plan, A, B, bias, D, aux, stream);  // outputs of the chosen configuration
 }
 

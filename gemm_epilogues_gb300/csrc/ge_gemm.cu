@@ -12,16 +12,19 @@
 //    the intermediate WX never goes back to global memory; RELU_AUX_BIAS
 //    also keeps the auxiliary output the backward pass needs.
 //
-// Structure (one CTA per SM, 192 threads):
+// Structure (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: A and B k-slices (64 fp16 = one 128-byte
 //               swizzle row) into a STAGES-deep shared-memory ring.
 //   warp 1      owns TMEM (2 x BN fp32 columns: a double-buffered 128 x BN
 //               accumulator) and one lane issues tcgen05.mma 128 x BN x 16.
-//   warps 2..5  epilogue: tcgen05.ld a 32-row x 32-column slab of the
+//   warps 2..9  epilogue: tcgen05.ld a 32-row x 32-column slab of the
 //               accumulator, add the bias, apply the activation, build the
 //               mask word, round to fp16, stage in 64-byte-swizzled shared
 //               memory and TMA-store it; runs while the MMA warp already
-//               accumulates the next tile into the other TMEM buffer.
+//               accumulates the next tile into the other TMEM buffer. Two
+//               warps share each TMEM lane quarter (warp % 4) and take
+//               alternate slabs, so heavier epilogues (GELU derivative,
+//               residual, statistics) keep pace with the MMAs.
 // Pair mode (PAIR = true, clusters of 2 CTAs on 2 SMs): the tile is 256 x BN;
 // each CTA stages its own 128 rows of A and its own half of B's BN columns,
 // the even CTA issues tcgen05.mma.cta_group::2 (M = 256) which reads both
@@ -39,12 +42,16 @@ namespace {
 
 constexpr int BM = 128;            // accumulator rows = TMEM lanes
 constexpr int BK = 64;             // fp16 k-slice per stage (128 bytes)
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_WARPS = 4;
+
 constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 fp16 columns
 
-template <int BN, bool PAIR>
+// EPIW = epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
+// taking alternate 32-column slabs).
+template <int BN, bool PAIR, int EPIW>
 struct Cfg {
+  static constexpr int EPI_WARPS = EPIW;
+  static constexpr int NUM_THREADS = 64 + 32 * EPIW;
+  static constexpr int HALVES = EPIW / 4;  // warps per lane quarter
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns staged by one CTA
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
@@ -102,13 +109,11 @@ __device__ __forceinline__ float apply_act(int epi, float z) {
 
 // Epilogue of one 32-column slab held by this thread (one accumulator row).
 // Returns the 32 packed 16-bit values in `packed`, the mask bits, and for
-// GELU_AUX_BIAS the packed pre-activations in `zpacked`. BIAS_RESIDUAL adds
-// the slab's residual values `rw` (packed pairs) after the bias.
+// GELU_AUX_BIAS the packed pre-activations in `zpacked`.
 template <int EPI, bool BIAS_COL>
 __device__ __forceinline__ uint32_t epilogue_slab(const uint32_t (&v)[32], float brow,
-                                                  const float (&bcol)[32], const uint32_t (&rw)[16],
-                                                  uint32_t (&packed)[16], uint32_t (&zpacked)[16],
-                                                  bool bf16) {
+                                                  const float (&bcol)[32], uint32_t (&packed)[16],
+                                                  uint32_t (&zpacked)[16], bool bf16) {
   uint32_t bits = 0;
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
@@ -117,11 +122,6 @@ __device__ __forceinline__ uint32_t epilogue_slab(const uint32_t (&v)[32], float
     if (EPI != EPI_NONE) {
       z0 += BIAS_COL ? bcol[j] : brow;
       z1 += BIAS_COL ? bcol[j + 1] : brow;
-    }
-    if (EPI == EPI_BIAS_RESIDUAL) {
-      const float2 r = to_f32x2(bf16, rw[j / 2]);
-      z0 += r.x;
-      z1 += r.y;
     }
     if (EPI == EPI_RELU_AUX_BIAS) {
       bits |= (z0 > 0.0f ? 1u : 0u) << j;
@@ -135,22 +135,43 @@ __device__ __forceinline__ uint32_t epilogue_slab(const uint32_t (&v)[32], float
 
 template <bool BIAS_COL>
 __device__ __forceinline__ uint32_t epilogue_dispatch(int epi, const uint32_t (&v)[32], float brow,
-                                                      const float (&bcol)[32], const uint32_t (&rw)[16],
-                                                      uint32_t (&packed)[16], uint32_t (&zp)[16],
-                                                      bool bf16) {
+                                                      const float (&bcol)[32], uint32_t (&packed)[16],
+                                                      uint32_t (&zp)[16], bool bf16) {
   switch (epi) {
-    case EPI_BIAS: return epilogue_slab<EPI_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
-    case EPI_RELU_BIAS: return epilogue_slab<EPI_RELU_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
-    case EPI_GELU_BIAS: return epilogue_slab<EPI_GELU_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+    case EPI_BIAS: return epilogue_slab<EPI_BIAS, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
+    case EPI_RELU_BIAS: return epilogue_slab<EPI_RELU_BIAS, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
+    case EPI_GELU_BIAS: return epilogue_slab<EPI_GELU_BIAS, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
     case EPI_GELU_ERF_BIAS:
-      return epilogue_slab<EPI_GELU_ERF_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+      return epilogue_slab<EPI_GELU_ERF_BIAS, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
     case EPI_RELU_AUX_BIAS:
-      return epilogue_slab<EPI_RELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+      return epilogue_slab<EPI_RELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
     case EPI_GELU_AUX_BIAS:
-      return epilogue_slab<EPI_GELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
-    case EPI_BIAS_RESIDUAL:
-      return epilogue_slab<EPI_BIAS_RESIDUAL, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
-    default: return epilogue_slab<EPI_NONE, BIAS_COL>(v, brow, bcol, rw, packed, zp, bf16);
+      return epilogue_slab<EPI_GELU_AUX_BIAS, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
+    default: return epilogue_slab<EPI_NONE, BIAS_COL>(v, brow, bcol, packed, zp, bf16);
+  }
+}
+
+// This thread's 32 16-bit values of a row-major input laid out like D'
+// (DGELU_BGRAD's z, BIAS_RESIDUAL's residual) at row grow, columns gcol0..,
+// packed in pairs; 0 past the matrix.
+__device__ __forceinline__ void load_slab16(const GemmArgs& p, int grow, int gcol0, uint32_t (&zw)[16]) {
+  const unsigned short* zrow = p.zaux + static_cast<long long>(grow) * p.ld_zaux + gcol0;
+  if (grow < p.Mk && gcol0 + 32 <= p.Nk) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(zrow) + i);
+      zw[4 * i] = w.x;
+      zw[4 * i + 1] = w.y;
+      zw[4 * i + 2] = w.z;
+      zw[4 * i + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t lo = grow < p.Mk && gcol0 + 2 * j < p.Nk ? zrow[2 * j] : 0u;
+      const uint32_t hi = grow < p.Mk && gcol0 + 2 * j + 1 < p.Nk ? zrow[2 * j + 1] : 0u;
+      zw[j] = lo | (hi << 16);
+    }
   }
 }
 
@@ -199,12 +220,12 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
   }
 }
 
-template <int BN, bool PAIR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int BN, bool PAIR, int EPIW>
+__global__ void __launch_bounds__(64 + 32 * EPIW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
                    const GemmArgs p) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, EPIW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -410,7 +431,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // -------------------------------------------------- epilogue warps
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int hh = (warp - 2) >> 2;   // which of the quarter's warps: slabs hh, hh + HALVES, ...
     uint8_t* stg = smem + C::OFF_EPI + (warp - 2) * 2 * EPI_BUF_BYTES;
     const bool backward = p.epi == EPI_DRELU_BGRAD || p.epi == EPI_DGELU_BGRAD;
     const bool has_bias = p.epi != EPI_NONE && !backward;
@@ -425,6 +447,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
       int mt, nt;
       tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
+      const int rbase = mt * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // warp's first row of D'
+      const int grow = rbase + lane;                                          // this thread's row
+      // DGELU_BGRAD's z / BIAS_RESIDUAL's residual: the first slab is
+      // requested before the wait for the accumulator, each later one while
+      // the slab before it is processed.
+      const bool needs_z = v < 0 && (p.epi == EPI_DGELU_BGRAD || p.epi == EPI_BIAS_RESIDUAL);
+      // Ask L2 for this thread's row segment of the next unit's per-element
+      // input (z / residual / mask) now, a whole tile ahead of its use: the
+      // slab loads then hit L2 instead of waiting on DRAM.
+      // (A bulk prefetch needs a 16-byte aligned start: the row pitches are
+      // multiples of 16 bytes, so only the base pointer is checked.)
+      const void* pf_base = p.epi == EPI_DRELU_BGRAD ? static_cast<const void*>(p.aux) : p.zaux;
+      if ((p.epi == EPI_DGELU_BGRAD || p.epi == EPI_BIAS_RESIDUAL || p.epi == EPI_DRELU_BGRAD) &&
+          (reinterpret_cast<uintptr_t>(pf_base) & 15u) == 0) {
+        for (int k = (u == first_tile ? 0 : 1); k < 2 && hh == 0; ++k) {
+          const int un = u + k * tile_step;
+          if (un >= num_units) break;
+          int tn, kb0n, kb1n, vn, mtn, ntn;
+          unit_info(un, p.tail_start, p.split, num_kb, tn, kb0n, kb1n, vn);
+          if (vn >= 0) continue;
+          tile_coords(tn, num_m, num_n, p.group_m, mtn, ntn);
+          const int rown = mtn * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
+          const int c0 = ntn * BN;
+          const int ncols = min(BN, p.Nk - c0);
+          if (rown < p.Mk && ncols > 0) {
+            if (p.epi == EPI_DRELU_BGRAD)
+              bulk_prefetch_l2(p.aux + static_cast<long long>(rown) * p.ld_aux + (c0 >> 5),
+                               static_cast<uint32_t>((((ncols + 31) >> 5) * 4 + 15) & ~15));
+            else
+              bulk_prefetch_l2(p.zaux + static_cast<long long>(rown) * p.ld_zaux + c0,
+                               static_cast<uint32_t>((ncols * 2 + 15) & ~15));
+          }
+        }
+      }
+      uint32_t zw[16];
+      if (needs_z) load_slab16(p, grow, nt * BN + 32 * hh, zw);
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.budget) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -444,7 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = hh; c < BN / 32; c += C::HALVES) {
           uint32_t vv[32];
           tmem_ld_32x32b_x32(t_row + 32u * c, vv);
           tmem_ld_wait();
@@ -464,15 +522,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (acc == 0) acc_phase ^= 1u;
         continue;
       }
-      const int rbase = mt * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // warp's first row of D'
-      const int grow = rbase + lane;                                          // this thread's row
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = to_f32(bf16, bias16[grow]);
       float bg_row = 0.0f;  // D*_BGRAD, bias per D' row: this tile's row sum
+      float st_n = 0.0f, st_mean = 0.0f, st_m2 = 0.0f;  // BIAS_RESIDUAL statistics of this row
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = hh; c < BN / 32; c += C::HALVES) {
         const int gcol0 = nt * BN + c * 32;
         if (gcol0 >= p.Nk) {
           // Past the end of the row: only the mask's zero padding words
@@ -486,29 +543,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t mword = 0;
         if (p.epi == EPI_DRELU_BGRAD && grow < p.Mk)
           mword = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
-        // DGELU_BGRAD: the slab's 32 stored pre-activations, likewise early;
-        // BIAS_RESIDUAL: the slab's 32 residual values.
-        uint32_t zw[16];
-        if (p.epi == EPI_DGELU_BGRAD || p.epi == EPI_BIAS_RESIDUAL) {
-          const unsigned short* zrow = p.zaux + static_cast<long long>(grow) * p.ld_zaux + gcol0;
-          if (grow < p.Mk && gcol0 + 32 <= p.Nk) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 w = __ldg(reinterpret_cast<const uint4*>(zrow) + i);
-              zw[4 * i] = w.x;
-              zw[4 * i + 1] = w.y;
-              zw[4 * i + 2] = w.z;
-              zw[4 * i + 3] = w.w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t lo = grow < p.Mk && gcol0 + 2 * j < p.Nk ? zrow[2 * j] : 0u;
-              const uint32_t hi = grow < p.Mk && gcol0 + 2 * j + 1 < p.Nk ? zrow[2 * j + 1] : 0u;
-              zw[j] = lo | (hi << 16);
-            }
-          }
-        }
+        uint32_t znext[16];
+        if (needs_z && c + C::HALVES < BN / 32) load_slab16(p, grow, gcol0 + 32 * C::HALVES, znext);
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + 32u * c, v);
         tmem_ld_wait();
@@ -582,9 +618,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; j < 32; ++j) srow += zm[j];
             bg_row += srow;
           }
+        } else if (p.epi == EPI_BIAS_RESIDUAL) {
+          // h = acc + bias + residual, stored once; with nstats the slab's
+          // exact mean and squared deviations (two passes over registers)
+          // are merged into the tile's running pair by Chan's formula.
+          float hv[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 r = to_f32x2(bf16, zw[j]);
+            hv[2 * j] = __uint_as_float(v[2 * j]) + (p.bias_per_col ? bcol[2 * j] : brow) + r.x;
+            hv[2 * j + 1] = __uint_as_float(v[2 * j + 1]) + (p.bias_per_col ? bcol[2 * j + 1] : brow) + r.y;
+            packed[j] = pack2(bf16, hv[2 * j], hv[2 * j + 1]);
+          }
+          if (p.nstats) {
+            const int nvalid = p.Nk - gcol0 < 32 ? p.Nk - gcol0 : 32;
+            float s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s += j < nvalid ? hv[j] : 0.0f;
+            const float nb = static_cast<float>(nvalid);
+            const float m = s / nb;
+            float q = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float d = j < nvalid ? hv[j] - m : 0.0f;
+              q = fmaf(d, d, q);
+            }
+            const float nn = st_n + nb;
+            const float delta = m - st_mean;
+            st_mean = fmaf(delta, nb / nn, st_mean);
+            st_m2 += fmaf(delta * delta, st_n * nb / nn, q);
+            st_n = nn;
+          }
         } else {
-          bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, zw, packed, zpacked, bf16)
-                                : epilogue_dispatch<false>(p.epi, v, brow, bcol, zw, packed, zpacked, bf16);
+          bits = p.bias_per_col ? epilogue_dispatch<true>(p.epi, v, brow, bcol, packed, zpacked, bf16)
+                                : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed, zpacked, bf16);
         }
         store_slab(packed, &tmD, reinterpret_cast<unsigned short*>(p.D), p.ldd, gcol0, rbase, grow,
                    p.Mk, p.Nk, stg, nstore, lane);
@@ -594,9 +661,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (p.Nk - gcol0 < 32) bits &= (1u << (p.Nk - gcol0)) - 1u;
           p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;
         }
+        if (needs_z) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) zw[j] = znext[j];
+        }
       }
       if (backward && !p.bias_per_col && grow < p.Mk)
-        p.bg_partials[static_cast<long long>(nt) * p.Mk + grow] = bg_row;
+        p.bg_partials[static_cast<long long>(C::HALVES * nt + hh) * p.Mk + grow] = bg_row;
+      if (p.epi == EPI_BIAS_RESIDUAL && p.nstats && grow < p.Mk)
+        p.nstats[static_cast<long long>(C::HALVES * nt + hh) * p.Mk + grow] = make_float2(st_mean, st_m2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -630,7 +703,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int EPIW>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
   static bool configured[64] = {};  // the attribute is set once per device
@@ -638,19 +711,19 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<BN, PAIR>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<BN, PAIR, EPIW>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if constexpr (PAIR) {
-      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       cudaGetLastError();
     }
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<BN, PAIR>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cfg<BN, PAIR, EPIW>::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, PAIR, EPIW>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if constexpr (PAIR) {
@@ -661,7 +734,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR>, tmA, tmB, tmD, tmZ, args);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW>, tmA, tmB, tmD, tmZ, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -723,7 +796,7 @@ __global__ void __launch_bounds__(256) bgrad_reduce_kernel(const float* part, lo
 }
 
 // Largest number of 2-CTA clusters of the pair kernel that can be resident.
-template <int BN>
+template <int BN, int EPIW>
 int max_pairs(int num_sms) {
   static int cached[64] = {};
   int dev = 0;
@@ -732,12 +805,12 @@ int max_pairs(int num_sms) {
     return num_sms / 2;
   }
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  cudaFuncSetAttribute(tc_gemm_kernel<BN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       Cfg<BN, true>::SMEM_BYTES);
+  cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       Cfg<BN, true, EPIW>::SMEM_BYTES);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<BN, true>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cfg<BN, true, EPIW>::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, true, EPIW>::SMEM_BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -746,7 +819,7 @@ int max_pairs(int num_sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true, EPIW>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = num_sms / 2;
   }
@@ -756,13 +829,9 @@ int max_pairs(int num_sms) {
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes(int block_n, int pair) {
-  if (pair) return block_n == 256 ? Cfg<256, true>::SMEM_BYTES : Cfg<128, true>::SMEM_BYTES;
-  return block_n == 256 ? Cfg<256, false>::SMEM_BYTES : Cfg<128, false>::SMEM_BYTES;
-}
-
-int tc_gemm_max_pairs(int block_n, int num_sms) {
-  return block_n == 256 ? max_pairs<256>(num_sms) : max_pairs<128>(num_sms);
+int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps) {
+  if (epi_warps == 8) return block_n == 256 ? max_pairs<256, 8>(num_sms) : max_pairs<128, 8>(num_sms);
+  return block_n == 256 ? max_pairs<256, 4>(num_sms) : max_pairs<128, 4>(num_sms);
 }
 
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream) {
@@ -786,15 +855,25 @@ cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args,
-                           int grid, cudaStream_t stream) {
+namespace {
+template <int EPIW>
+cudaError_t launch_width(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                         const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args, int grid,
+                         cudaStream_t stream) {
   if (pair) {
-    if (block_n == 256) return launch_impl<256, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
-    return launch_impl<128, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    if (block_n == 256) return launch_impl<256, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    return launch_impl<128, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
   }
-  if (block_n == 256) return launch_impl<256, false>(tmA, tmB, tmD, tmZ, args, grid, stream);
-  return launch_impl<128, false>(tmA, tmB, tmD, tmZ, args, grid, stream);
+  if (block_n == 256) return launch_impl<256, false, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
+  return launch_impl<128, false, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
+}
+}  // namespace
+
+cudaError_t launch_tc_gemm(int block_n, int pair, int epi_warps, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const CUtensorMap& tmD, const CUtensorMap& tmZ,
+                           const GemmArgs& args, int grid, cudaStream_t stream) {
+  if (epi_warps == 8) return launch_width<8>(block_n, pair, tmA, tmB, tmD, tmZ, args, grid, stream);
+  return launch_width<4>(block_n, pair, tmA, tmB, tmD, tmZ, args, grid, stream);
 }
 
 }  // namespace ge

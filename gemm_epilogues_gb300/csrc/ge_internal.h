@@ -57,9 +57,11 @@ struct GemmArgs {
   int tail_start;
   int split;
   float* partials;
-  // DRELU_BGRAD epilogue: per-block bias-gradient partial sums, reduced by
+  // D*_BGRAD epilogue: per-block bias-gradient partial sums, reduced by
   // launch_bgrad_reduce into `bgrad`. Row case (bias per D' row): bg_partials
-  // is [num n-tiles][Mk]; column case: [ceil(Mk/32)][Nk].
+  // is [halves * num n-tiles][Mk] (per n-tile, one row for each epilogue
+  // warp of a lane quarter: halves = epi_warps / 4); column case:
+  // [ceil(Mk/32)][Nk].
   float* bg_partials;
   float* bgrad;
   // GELU_AUX_BIAS: z of every element, written like D' (ld_zaux elements per
@@ -68,20 +70,27 @@ struct GemmArgs {
   // (same layout; it may be D itself).
   unsigned short* zaux;
   long long ld_zaux;
+  // BIAS_RESIDUAL: statistics of h per (n-tile, D' row) over the columns of
+  // the tile's 32-column slabs c with c % halves == half: (mean, sum of
+  // squared deviations) as float2 at nstats[(halves * nt + half) * Mk + row];
+  // null = not wanted.
+  float2* nstats;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs
-// (even) and the B tensor map's box is BN/2 rows (K-major B).
-size_t tc_gemm_smem_bytes(int block_n, int pair);
-int tc_gemm_max_pairs(int block_n, int num_sms);
+// (even) and the B tensor map's box is BN/2 rows (K-major B). epi_warps = 4
+// or 8 epilogue warps (8: two per TMEM lane quarter on alternate slabs; the
+// D*_BGRAD row partials and the norm statistics then have two halves per
+// n-tile).
+int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps);
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream);
 // out[i] = sum over j = 0..rows-1 (in order) of part[j * len + i], fp32.
 cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
                                 cudaStream_t stream);
 // tmZ: the zaux tensor map (GELU_AUX_BIAS; any valid map otherwise).
-cudaError_t launch_tc_gemm(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args,
-                           int grid, cudaStream_t stream);
+cudaError_t launch_tc_gemm(int block_n, int pair, int epi_warps, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const CUtensorMap& tmD, const CUtensorMap& tmZ,
+                           const GemmArgs& args, int grid, cudaStream_t stream);
 
 // Weight-streaming GEMV for N <= 16: A K-major [M, K] (lda), B K-major
 // (B[k,n] at B[n*ldb + k]), D[m,n] at m*ldd_m + n*ldd_n.
@@ -145,6 +154,14 @@ struct NormArgs {
   float eps;
   int layer;
   int bf16;
+  // Statistics already taken by the GEMM epilogue (GemmArgs::nstats):
+  // partials [halves * ntiles][R] for tiles tile_w features wide (the
+  // 32-feature slabs c % halves == half of each tile); rowstats ([R],
+  // scratch) receives (mean, rstd). partials == null: the pass takes them
+  // itself.
+  const float2* partials;
+  int ntiles, tile_w, halves;
+  float2* rowstats;
 };
 cudaError_t launch_norm(const NormArgs& args, int num_sms, cudaStream_t stream);
 // D[r, c] += res[r * ld + c] (unfused baseline of the residual add).

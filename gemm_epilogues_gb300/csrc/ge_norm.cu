@@ -30,10 +30,30 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// No "memory" clobber: the compiler may then issue the read-only gamma /
+// beta loads of later groups before these stores. H is read through the
+// volatile ld_stream, which stays ordered with these volatile stores, so Y
+// may still be H.
 __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
+               "r"(v.z), "r"(v.w));
+}
+
+// Y's 8 values of group g from H's values v, with gamma / beta.
+__device__ __forceinline__ uint4 norm8(const uint4& v, const uint4& gm, const uint4& bt, float mu, float rstd,
+                                       bool layer, bool bf16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t gw[4] = {gm.x, gm.y, gm.z, gm.w};
+  const uint32_t bw[4] = {bt.x, bt.y, bt.z, bt.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 x = to_f32x2(bf16, w[k]);
+    const float2 gg = to_f32x2(bf16, gw[k]);
+    const float2 bb = layer ? to_f32x2(bf16, bw[k]) : make_float2(0.0f, 0.0f);
+    o[k] = pack2(bf16, fmaf((x.x - mu) * rstd, gg.x, bb.x), fmaf((x.y - mu) * rstd, gg.y, bb.y));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ float warp_sum(float s) {
@@ -55,13 +75,31 @@ __device__ __forceinline__ float sum8(const uint4& v, bool bf16, F f) {
   return s;
 }
 
+// gamma and beta are the same for every row: a block stages them in shared
+// memory once (rows up to SMEM_FEATURES), so the output pass reads them at
+// shared-memory latency instead of going to L2 for every row.
+constexpr int SMEM_FEATURES = 8192;
+
 __global__ void __launch_bounds__(256) norm_kernel(const NormArgs p) {
+  extern __shared__ __align__(16) unsigned short gb_smem[];  // [gamma | beta], 8 * ceil(C/8) each
   const bool bf16 = p.bf16 != 0;
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
   const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
   const long long G = p.C >> 3;  // whole 16-byte groups per row
   const float inv_c = 1.0f / static_cast<float>(p.C);
+  const bool staged = p.C <= SMEM_FEATURES;
+  const long long beta_off = 8 * ((p.C + 7) >> 3);  // beta's copy starts on a 16-byte boundary
+  if (staged) {
+    for (long long g = threadIdx.x; g < G; g += blockDim.x) {
+      reinterpret_cast<uint4*>(gb_smem)[g] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + g);
+      if (p.layer)
+        reinterpret_cast<uint4*>(gb_smem + beta_off)[g] = __ldg(reinterpret_cast<const uint4*>(p.beta) + g);
+    }
+    __syncthreads();
+  }
+  const unsigned short* gam = staged ? gb_smem : p.gamma;
+  const unsigned short* bet = staged ? gb_smem + beta_off : p.beta;
   for (long long r = blockIdx.x * wpb + (threadIdx.x >> 5); r < p.R; r += nwarps) {
     const unsigned short* h = p.H + r * p.ld;
     unsigned short* y = p.Y + r * p.ld;
@@ -99,28 +137,123 @@ __global__ void __launch_bounds__(256) norm_kernel(const NormArgs p) {
     });
     const float rstd = rsqrtf(warp_sum(ss) * inv_c + p.eps);
 
-    for_groups([&](const uint4& v, long long g) {
-      const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma + 8 * g));
-      uint4 bt = make_uint4(0, 0, 0, 0);
-      if (p.layer) bt = __ldg(reinterpret_cast<const uint4*>(p.beta + 8 * g));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      const uint32_t gw[4] = {gm.x, gm.y, gm.z, gm.w};
-      const uint32_t bw[4] = {bt.x, bt.y, bt.z, bt.w};
-      uint32_t o[4];
+    // Output: gamma / beta of a batch of groups are requested before the
+    // batch's stores, so their latencies overlap instead of adding up.
+    constexpr int BATCH = 4;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 x = to_f32x2(bf16, w[k]);
-        const float2 gg = to_f32x2(bf16, gw[k]);
-        const float2 bb = p.layer ? to_f32x2(bf16, bw[k]) : make_float2(0.0f, 0.0f);
-        o[k] = pack2(bf16, fmaf((x.x - mu) * rstd, gg.x, bb.x), fmaf((x.y - mu) * rstd, gg.y, bb.y));
+    for (int i0 = 0; i0 < CACHE; i0 += BATCH) {
+      uint4 gm[BATCH], bt[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const long long g = lane + 32LL * (i0 + k);
+        gm[k] = bt[k] = make_uint4(0, 0, 0, 0);
+        if (g < G) {
+          gm[k] = *reinterpret_cast<const uint4*>(gam + 8 * g);
+          if (p.layer) bt[k] = *reinterpret_cast<const uint4*>(bet + 8 * g);
+        }
       }
-      st_stream(y + 8 * g, make_uint4(o[0], o[1], o[2], o[3]));
-    });
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const long long g = lane + 32LL * (i0 + k);
+        if (g < G) st_stream(y + 8 * g, norm8(cache[i0 + k], gm[k], bt[k], mu, rstd, p.layer != 0, bf16));
+      }
+    }
+    for (long long g = lane + 32LL * CACHE; g < G; g += 32) {  // groups past the register cache
+      const uint4 v = ld_stream(h + 8 * g);
+      const uint4 gm = *reinterpret_cast<const uint4*>(gam + 8 * g);
+      const uint4 bt = p.layer ? *reinterpret_cast<const uint4*>(bet + 8 * g) : make_uint4(0, 0, 0, 0);
+      st_stream(y + 8 * g, norm8(v, gm, bt, mu, rstd, p.layer != 0, bf16));
+    }
     if (has_tail) {
       const float gg = to_f32(bf16, p.gamma[tail_c]);
       const float bb = p.layer ? to_f32(bf16, p.beta[tail_c]) : 0.0f;
       y[tail_c] = from_f32(bf16, fmaf((tail - mu) * rstd, gg, bb));
     }
+  }
+}
+
+// Features of tile t's 32-feature slabs c with c % halves == half.
+__device__ __forceinline__ int half_count(long long C, int tile_w, int t, int half, int halves) {
+  int n = 0;
+  for (int c = half; c < tile_w / 32; c += halves) {
+    const long long left = C - static_cast<long long>(t) * tile_w - 32LL * c;
+    n += left <= 0 ? 0 : (left < 32 ? static_cast<int>(left) : 32);
+  }
+  return n;
+}
+
+// Statistics taken by the GEMM epilogue: per row, merge the partial (mean,
+// sum of squared deviations) pairs in a fixed order by Chan's formula, then
+// (mean, rstd) of the row. The partials are requested in batches so their
+// latencies overlap.
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const NormArgs p) {
+  constexpr int B = 8;
+  const int np = p.halves * p.ntiles;
+  for (long long r = blockIdx.x * 256LL + threadIdx.x; r < p.R; r += gridDim.x * 256LL) {
+    float n = 0.0f, mean = 0.0f, m2 = 0.0f;
+    for (int k0 = 0; k0 < np; k0 += B) {
+      float2 s[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+        s[b] = k0 + b < np ? __ldcg(p.partials + static_cast<long long>(k0 + b) * p.R + r) : make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int k = k0 + b;
+        if (k >= np) break;
+        const int nbi = half_count(p.C, p.tile_w, k / p.halves, k % p.halves, p.halves);
+        if (nbi == 0) continue;
+        const float nb = static_cast<float>(nbi);
+        const float nn = n + nb;
+        const float delta = s[b].x - mean;
+        mean = fmaf(delta, nb / nn, mean);
+        m2 += fmaf(delta * delta, n * nb / nn, s[b].y);
+        n = nn;
+      }
+    }
+    const float inv_c = 1.0f / static_cast<float>(p.C);
+    // LayerNorm: variance about the mean; RMSNorm: mean square (M2 + C mean^2) / C
+    const float ms = p.layer ? m2 * inv_c : fmaf(mean, mean, m2 * inv_c);
+    p.rowstats[r] = make_float2(p.layer ? mean : 0.0f, rsqrtf(ms + p.eps));
+  }
+}
+
+// y = (h - mean) * rstd * gamma + beta for every element, 8 per thread-step,
+// four independent steps in flight: a plain stream at copy speed.
+__global__ void __launch_bounds__(256) norm_apply_kernel(const NormArgs p) {
+  const bool bf16 = p.bf16 != 0;
+  const bool layer = p.layer != 0;
+  const long long G = p.C >> 3;
+  const long long total = p.R * G;
+  const long long stride = static_cast<long long>(gridDim.x) * 256;
+  constexpr int U = 4;
+  for (long long i0 = blockIdx.x * 256LL + threadIdx.x; i0 < total; i0 += U * stride) {
+    uint4 v[U];
+    long long rr[U], gg[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + u * stride;
+      rr[u] = i < total ? i / G : 0;
+      gg[u] = i < total ? i - rr[u] * G : 0;
+      v[u] = i < total ? ld_stream(p.H + rr[u] * p.ld + 8 * gg[u]) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (i0 + u * stride >= total) break;
+      const float2 st = __ldg(p.rowstats + rr[u]);
+      const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma) + gg[u]);
+      const uint4 bt = layer ? __ldg(reinterpret_cast<const uint4*>(p.beta) + gg[u]) : make_uint4(0, 0, 0, 0);
+      st_stream(p.Y + rr[u] * p.ld + 8 * gg[u], norm8(v[u], gm, bt, st.x, st.y, layer, bf16));
+    }
+  }
+  // the C % 8 features past the last whole group, one thread each
+  const long long tail = p.C - 8 * G;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < p.R * tail; i += stride) {
+    const long long r = i / tail;
+    const long long c = 8 * G + (i - r * tail);
+    const float2 st = p.rowstats[r];
+    const float x = to_f32(bf16, p.H[r * p.ld + c]);
+    const float b = layer ? to_f32(bf16, p.beta[c]) : 0.0f;
+    p.Y[r * p.ld + c] = from_f32(bf16, fmaf((x - st.x) * st.y, to_f32(bf16, p.gamma[c]), b));
   }
 }
 
@@ -158,10 +291,27 @@ __global__ void __launch_bounds__(256) residual_add_kernel(unsigned short* D, lo
 
 cudaError_t launch_norm(const NormArgs& a, int num_sms, cudaStream_t s) {
   if (a.R == 0 || a.C == 0) return cudaSuccess;
+  if (a.partials) {
+    long long fb = (a.R + 255) / 256;
+    if (fb > 65535) fb = 65535;
+    norm_finalize_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(a);
+    const long long work = a.R * ((a.C + 7) / 8);
+    long long blocks = (work + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    norm_apply_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   long long blocks = (a.R + 7) / 8;  // one row per warp when the grid allows
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  norm_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  const size_t smem = a.C <= SMEM_FEATURES ? static_cast<size_t>((a.C + 7) / 8) * 16 * 2 : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  norm_kernel<<<static_cast<unsigned>(blocks), 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -273,12 +273,20 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
  * configuration, so D / aux / bias hold its results. It blocks the host until
  * the timing runs finish and may re-allocate the plan's tail workspace.
  * Plans of the other paths are left unchanged (GE_OK). reps in 1..1000.
+ * The choice is also remembered for the process (per device, M, N, K,
+ * epilogue, element type and layout): plans created later for the same
+ * problem start from it (unless GE_TILE_N / GE_PAIR / GE_SPLIT_TAIL are set
+ * in the environment).
  * Returns GE_OK or the first failing status (the plan then keeps a valid
  * configuration).
  */
 ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B,
                              const void* bias, void* D, void* aux, void* stream,
                              int reps);
+
+/* Forget every configuration remembered by ge_plan_autotune (existing plans
+ * keep theirs). */
+void ge_autotune_cache_clear(void);
 
 /* The plan's tensor-core configuration: tile width, 2-SM pair mode (0/1)
  * and split-K pieces of the tail (1 = none); zeros for other paths. Any

@@ -313,6 +313,14 @@ def test_autotune_picks_a_candidate_and_stays_correct(oracle):
         torch.cuda.synchronize()
         assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
         assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+        tuned = p.config
+    # a later plan for the same problem starts from the tuned configuration
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_MN_MAJOR, ge.GE_D_ROW)
+    with ge.Plan(M, N, K, ge.GE_EPI_RELU_AUX_BIAS, L) as p2:
+        assert p2.config == tuned
+    ge.ge_autotune_cache_clear()
+    with ge.Plan(M, N, K, ge.GE_EPI_RELU_AUX_BIAS, L) as p3:
+        assert p3.config[0] == ge.GE_PATH_TC_GEMM
 
 
 @pytest.mark.parametrize("epi", EPIS + ["gelu_erf_bias"])

@@ -27,6 +27,7 @@
 // last block of a column strip (an atomic ticket) adds the splits in order.
 // Row case (D row-major: bgrad is a sum along each storage row): one warp per
 // row, 16-byte loads along the row, a butterfly reduction.
+#include <atomic>
 #include <cstdlib>
 
 #include "ge_internal.h"
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(256) drelu_rows_kernel(const DreluArgs p) {
 // 62 us), at least 64 rows per split, at most 256 splits. GE_DRELU_SPLITS
 // overrides (sweeps).
 int drelu_splits(long long R, long long C, int num_sms, int gelu) {
-  static int occ[2] = {0, 0};
+  static std::atomic<int> occ[2] = {0, 0};
   if (occ[gelu ? 1 : 0] == 0) {
     int o = 0;
     const cudaError_t e =

@@ -34,6 +34,8 @@
 // Every wait is bounded; an expired wait records a bit in the error word,
 // raises a CTA-wide abort flag, and every role drains its in-flight copies
 // before the CTA frees TMEM and exits.
+#include <atomic>
+
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
@@ -706,7 +708,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
 template <int BN, bool PAIR, int EPIW>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
-  static bool configured[64] = {};  // the attribute is set once per device
+  static std::atomic<bool> configured[64] = {};  // the attribute is set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -798,7 +800,7 @@ __global__ void __launch_bounds__(256) bgrad_reduce_kernel(const float* part, lo
 // Largest number of 2-CTA clusters of the pair kernel that can be resident.
 template <int BN, int EPIW>
 int max_pairs(int num_sms) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();

@@ -3,24 +3,23 @@
 // fusion strategy", second level: the norm reduces across the channel
 // dimension, so it cannot be applied element by element in the GEMM's
 // epilogue). The GEMM epilogue has already written h = A.B + bias +
-// residual as H; this kernel reads every token's row of H once and writes
-// the normalised row:
+// residual as H:
 //
 //   RMSNorm:   y = h * rsqrt(mean(h^2) + eps) * gamma
 //   LayerNorm: y = (h - mu) * rsqrt(mean((h - mu)^2) + eps) * gamma + beta
 //
-// One warp per row. The row stays in registers (up to CACHE 16-byte groups
-// per lane, 4096 16-bit features), so the mean and the variance are two
-// exact passes over registers rather than a sum of squares minus a squared
-// mean; longer rows re-read their remainder (from L2) in each pass. Memory
-// traffic is one read of H and one write of Y: HBM-bound.
+// Tensor-core path: the GEMM epilogue also took each token's statistics
+// (per tile); norm_finalize_kernel merges them into (mean, rstd) per token
+// and norm_apply_kernel streams H -> Y elementwise (one read of H, one
+// write of Y: HBM-bound, no reductions on the way).
+// GEMV path and unfused flow: norm_kernel takes the statistics itself, one
+// block per token, the row in registers, two exact passes (mean, then
+// squared deviations) rather than a sum of squares minus a squared mean.
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
 namespace ge {
 namespace {
-
-constexpr int CACHE = 16;  // 16-byte groups per lane kept in registers
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
@@ -75,145 +74,142 @@ __device__ __forceinline__ float sum8(const uint4& v, bool bf16, F f) {
   return s;
 }
 
-// gamma and beta are the same for every row: a block stages them in shared
-// memory once (rows up to SMEM_FEATURES), so the output pass reads them at
-// shared-memory latency instead of going to L2 for every row.
-constexpr int SMEM_FEATURES = 8192;
+// Norm of whole rows of H when no statistics were taken upstream (the GEMV
+// path, N <= 16 tokens, and the unfused flow): one 256-thread block per row.
+// Thread t keeps the row's 16-byte groups t, t + 256, ... (up to BLOCK_CACHE
+// of them: 8192 features) in registers; two block reductions give the mean
+// and the variance exactly (two passes over registers); a third pass writes
+// Y. Longer rows re-read their remainder (from L2) in each pass.
+constexpr int BLOCK_CACHE = 4;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();  // red may still be read by the previous reduction
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t += red[i];  // fixed order: the same sum in every thread
+  return t;
+}
 
 __global__ void __launch_bounds__(256) norm_kernel(const NormArgs p) {
-  extern __shared__ __align__(16) unsigned short gb_smem[];  // [gamma | beta], 8 * ceil(C/8) each
+  __shared__ float red[8];
   const bool bf16 = p.bf16 != 0;
-  const int lane = threadIdx.x & 31;
-  const long long wpb = blockDim.x >> 5;
-  const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
+  const bool layer = p.layer != 0;
   const long long G = p.C >> 3;  // whole 16-byte groups per row
   const float inv_c = 1.0f / static_cast<float>(p.C);
-  const bool staged = p.C <= SMEM_FEATURES;
-  const long long beta_off = 8 * ((p.C + 7) >> 3);  // beta's copy starts on a 16-byte boundary
-  if (staged) {
-    for (long long g = threadIdx.x; g < G; g += blockDim.x) {
-      reinterpret_cast<uint4*>(gb_smem)[g] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + g);
-      if (p.layer)
-        reinterpret_cast<uint4*>(gb_smem + beta_off)[g] = __ldg(reinterpret_cast<const uint4*>(p.beta) + g);
-    }
-    __syncthreads();
-  }
-  const unsigned short* gam = staged ? gb_smem : p.gamma;
-  const unsigned short* bet = staged ? gb_smem + beta_off : p.beta;
-  for (long long r = blockIdx.x * wpb + (threadIdx.x >> 5); r < p.R; r += nwarps) {
+  const int t = threadIdx.x;
+  for (long long r = blockIdx.x; r < p.R; r += gridDim.x) {
     const unsigned short* h = p.H + r * p.ld;
     unsigned short* y = p.Y + r * p.ld;
-    uint4 cache[CACHE];
+    uint4 cache[BLOCK_CACHE];
 #pragma unroll
-    for (int i = 0; i < CACHE; ++i) {
-      const long long g = lane + 32LL * i;
+    for (int i = 0; i < BLOCK_CACHE; ++i) {
+      const long long g = t + 256LL * i;
       cache[i] = g < G ? ld_stream(h + 8 * g) : make_uint4(0, 0, 0, 0);
     }
-    // Visit every 16-byte group g of the row owned by this lane: the cached
-    // ones with static register indices, the rest (rows longer than
-    // 32 * CACHE groups) re-read.
-    auto for_groups = [&](auto&& fn) {
-#pragma unroll
-      for (int i = 0; i < CACHE; ++i) {
-        const long long g = lane + 32LL * i;
-        if (g < G) fn(cache[i], g);
-      }
-      for (long long g = lane + 32LL * CACHE; g < G; g += 32) fn(ld_stream(h + 8 * g), g);
-    };
-    // ragged tail (C % 8 elements): one element per lane
-    const long long tail_c = 8 * G + lane;
+    // the C % 8 features past the last whole group: one per thread
+    const long long tail_c = 8 * G + t;
     const bool has_tail = tail_c < p.C;
     const float tail = has_tail ? to_f32(bf16, h[tail_c]) : 0.0f;
-
+    auto for_groups = [&](auto&& fn) {
+#pragma unroll
+      for (int i = 0; i < BLOCK_CACHE; ++i) {
+        const long long g = t + 256LL * i;
+        if (g < G) fn(cache[i], g);
+      }
+      for (long long g = t + 256LL * BLOCK_CACHE; g < G; g += 256) fn(ld_stream(h + 8 * g), g);
+    };
     float mu = 0.0f;
-    if (p.layer) {
+    if (layer) {
       float s = tail;
       for_groups([&](const uint4& v, long long) { s += sum8(v, bf16, [](float x) { return x; }); });
-      mu = warp_sum(s) * inv_c;
+      mu = block_sum(s, red) * inv_c;
     }
     float ss = has_tail ? (tail - mu) * (tail - mu) : 0.0f;
     for_groups([&](const uint4& v, long long) {
       ss += sum8(v, bf16, [mu](float x) { return (x - mu) * (x - mu); });
     });
-    const float rstd = rsqrtf(warp_sum(ss) * inv_c + p.eps);
-
-    // Output: gamma / beta of a batch of groups are requested before the
-    // batch's stores, so their latencies overlap instead of adding up.
-    constexpr int BATCH = 4;
-#pragma unroll
-    for (int i0 = 0; i0 < CACHE; i0 += BATCH) {
-      uint4 gm[BATCH], bt[BATCH];
-#pragma unroll
-      for (int k = 0; k < BATCH; ++k) {
-        const long long g = lane + 32LL * (i0 + k);
-        gm[k] = bt[k] = make_uint4(0, 0, 0, 0);
-        if (g < G) {
-          gm[k] = *reinterpret_cast<const uint4*>(gam + 8 * g);
-          if (p.layer) bt[k] = *reinterpret_cast<const uint4*>(bet + 8 * g);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < BATCH; ++k) {
-        const long long g = lane + 32LL * (i0 + k);
-        if (g < G) st_stream(y + 8 * g, norm8(cache[i0 + k], gm[k], bt[k], mu, rstd, p.layer != 0, bf16));
-      }
-    }
-    for (long long g = lane + 32LL * CACHE; g < G; g += 32) {  // groups past the register cache
-      const uint4 v = ld_stream(h + 8 * g);
-      const uint4 gm = *reinterpret_cast<const uint4*>(gam + 8 * g);
-      const uint4 bt = p.layer ? *reinterpret_cast<const uint4*>(bet + 8 * g) : make_uint4(0, 0, 0, 0);
-      st_stream(y + 8 * g, norm8(v, gm, bt, mu, rstd, p.layer != 0, bf16));
-    }
+    const float rstd = rsqrtf(block_sum(ss, red) * inv_c + p.eps);
+    for_groups([&](const uint4& v, long long g) {
+      const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma) + g);
+      const uint4 bt = layer ? __ldg(reinterpret_cast<const uint4*>(p.beta) + g) : make_uint4(0, 0, 0, 0);
+      st_stream(y + 8 * g, norm8(v, gm, bt, mu, rstd, layer, bf16));
+    });
     if (has_tail) {
-      const float gg = to_f32(bf16, p.gamma[tail_c]);
-      const float bb = p.layer ? to_f32(bf16, p.beta[tail_c]) : 0.0f;
-      y[tail_c] = from_f32(bf16, fmaf((tail - mu) * rstd, gg, bb));
+      const float bb = layer ? to_f32(bf16, p.beta[tail_c]) : 0.0f;
+      y[tail_c] = from_f32(bf16, fmaf((tail - mu) * rstd, to_f32(bf16, p.gamma[tail_c]), bb));
     }
   }
 }
 
-// Features of tile t's 32-feature slabs c with c % halves == half.
-__device__ __forceinline__ int half_count(long long C, int tile_w, int t, int half, int halves) {
-  int n = 0;
-  for (int c = half; c < tile_w / 32; c += halves) {
-    const long long left = C - static_cast<long long>(t) * tile_w - 32LL * c;
-    n += left <= 0 ? 0 : (left < 32 ? static_cast<int>(left) : 32);
-  }
-  return n;
+// Features of tile t's 32-feature slabs c with c % halves == half: the tile
+// holds v = min(tile_w, C - t*tile_w) features, v / 32 whole slabs and one
+// slab of v % 32.
+__device__ __forceinline__ float half_count(long long C, int tile_w, int t, int half, int halves) {
+  const long long left = C - static_cast<long long>(t) * tile_w;
+  const int v = left < tile_w ? static_cast<int>(left) : tile_w;
+  const int full = v >> 5;
+  const int whole = (full + halves - 1 - half) / halves;  // whole slabs c < full with c % halves == half
+  return static_cast<float>(32 * whole + (full % halves == half ? (v & 31) : 0));
 }
 
-// Statistics taken by the GEMM epilogue: per row, merge the partial (mean,
-// sum of squared deviations) pairs in a fixed order by Chan's formula, then
-// (mean, rstd) of the row. The partials are requested in batches so their
-// latencies overlap.
+// Chan's merge of two (count, mean, sum of squared deviations) summaries.
+__device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, float nb, float mb, float m2b) {
+  const float nn = n + nb;
+  if (nn == 0.0f) return;
+  const float delta = mb - mean;
+  const float w = __fdividef(nb, nn);  // counts are integers below 2^24: a fast divide is exact enough
+  mean = fmaf(delta, w, mean);
+  m2 = m2 + m2b + delta * delta * (n * w);
+  n = nn;
+}
+
+// Statistics taken by the GEMM epilogue: one warp per row. Lane l merges
+// partials l, l + 32, ... in order, then a fixed shuffle tree merges the
+// lanes (lower lane on the left at every level), so the result does not
+// depend on timing. Writes (mean, rstd) of the row.
 __global__ void __launch_bounds__(256) norm_finalize_kernel(const NormArgs p) {
-  constexpr int B = 8;
+  const int lane = threadIdx.x & 31;
+  const long long wpb = blockDim.x >> 5;
+  const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
   const int np = p.halves * p.ntiles;
-  for (long long r = blockIdx.x * 256LL + threadIdx.x; r < p.R; r += gridDim.x * 256LL) {
+  for (long long r = blockIdx.x * wpb + (threadIdx.x >> 5); r < p.R; r += nwarps) {
     float n = 0.0f, mean = 0.0f, m2 = 0.0f;
-    for (int k0 = 0; k0 < np; k0 += B) {
-      float2 s[B];
+    for (int k = lane; k < np; k += 32) {
+      const float2 s = __ldcg(p.partials + static_cast<long long>(k) * p.R + r);
+      float nb;
+      if (p.halves == 1) {  // one partial per tile: its features
+        const long long left = p.C - static_cast<long long>(k) * p.tile_w;
+        nb = static_cast<float>(left < p.tile_w ? left : p.tile_w);
+      } else {
+        nb = half_count(p.C, p.tile_w, k / p.halves, k % p.halves, p.halves);
+      }
+      chan_merge(n, mean, m2, nb, s.x, s.y);
+    }
 #pragma unroll
-      for (int b = 0; b < B; ++b)
-        s[b] = k0 + b < np ? __ldcg(p.partials + static_cast<long long>(k0 + b) * p.R + r) : make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-        const int k = k0 + b;
-        if (k >= np) break;
-        const int nbi = half_count(p.C, p.tile_w, k / p.halves, k % p.halves, p.halves);
-        if (nbi == 0) continue;
-        const float nb = static_cast<float>(nbi);
-        const float nn = n + nb;
-        const float delta = s[b].x - mean;
-        mean = fmaf(delta, nb / nn, mean);
-        m2 += fmaf(delta * delta, n * nb / nn, s[b].y);
-        n = nn;
+    for (int off = 1; off < 32; off <<= 1) {
+      const float on = __shfl_xor_sync(0xffffffffu, n, off);
+      const float om = __shfl_xor_sync(0xffffffffu, mean, off);
+      const float o2 = __shfl_xor_sync(0xffffffffu, m2, off);
+      if (lane & off) {  // this lane holds the right operand: merge into the partner's (left) copy
+        float ln = on, lm = om, l2 = o2;
+        chan_merge(ln, lm, l2, n, mean, m2);
+        n = ln;
+        mean = lm;
+        m2 = l2;
+      } else {
+        chan_merge(n, mean, m2, on, om, o2);
       }
     }
-    const float inv_c = 1.0f / static_cast<float>(p.C);
-    // LayerNorm: variance about the mean; RMSNorm: mean square (M2 + C mean^2) / C
-    const float ms = p.layer ? m2 * inv_c : fmaf(mean, mean, m2 * inv_c);
-    p.rowstats[r] = make_float2(p.layer ? mean : 0.0f, rsqrtf(ms + p.eps));
+    if (lane == 0) {
+      const float inv_c = 1.0f / static_cast<float>(p.C);
+      // LayerNorm: variance about the mean; RMSNorm: mean square (M2 + C mean^2) / C
+      const float ms = p.layer ? m2 * inv_c : fmaf(mean, mean, m2 * inv_c);
+      p.rowstats[r] = make_float2(p.layer ? mean : 0.0f, rsqrtf(ms + p.eps));
+    }
   }
 }
 
@@ -292,8 +288,8 @@ __global__ void __launch_bounds__(256) residual_add_kernel(unsigned short* D, lo
 cudaError_t launch_norm(const NormArgs& a, int num_sms, cudaStream_t s) {
   if (a.R == 0 || a.C == 0) return cudaSuccess;
   if (a.partials) {
-    long long fb = (a.R + 255) / 256;
-    if (fb > 65535) fb = 65535;
+    long long fb = (a.R + 7) / 8;  // one row per warp
+    if (fb > static_cast<long long>(num_sms) * 16) fb = static_cast<long long>(num_sms) * 16;
     norm_finalize_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(a);
     const long long work = a.R * ((a.C + 7) / 8);
     long long blocks = (work + 255) / 256;
@@ -302,16 +298,10 @@ cudaError_t launch_norm(const NormArgs& a, int num_sms, cudaStream_t s) {
     norm_apply_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
     return cudaGetLastError();
   }
-  long long blocks = (a.R + 7) / 8;  // one row per warp when the grid allows
+  long long blocks = a.R;  // one row per block
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  const size_t smem = a.C <= SMEM_FEATURES ? static_cast<size_t>((a.C + 7) / 8) * 16 * 2 : 0;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  norm_kernel<<<static_cast<unsigned>(blocks), 256, smem, s>>>(a);
+  norm_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

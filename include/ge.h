@@ -35,11 +35,19 @@
  * Ownership and threading. The caller owns every device buffer (A, B, bias,
  * D, aux, and the DRELU_BGRAD outputs). A plan owns its host state and a
  * small device workspace allocated by ge_plan_create on the device current
- * at that time (an error word, and for DRELU_BGRAD the reduction partials
- * and counters). ge_execute never allocates and only enqueues work on the
- * given stream; the caller synchronises. Executes of one plan must be
- * ordered on one stream: two executes of the same plan that overlap on the
- * GPU race on its workspace. Distinct plans are independent.
+ * at that time (an error word; for DRELU_BGRAD / DGELU_BGRAD the reduction
+ * partials and counters; for the norm epilogues the per-token statistics;
+ * for a split-K tail its fp32 pieces). ge_execute never allocates and only
+ * enqueues work on the given stream; the caller synchronises. Executes of
+ * one plan must be ordered on one stream: two executes of the same plan that
+ * overlap on the GPU race on its workspace. Distinct plans are independent,
+ * and plans may be created, executed and freed from several host threads.
+ *
+ * Environment (read by ge_plan_create, for tuning sweeps; unset in normal
+ * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
+ * GE_SPLIT_TAIL = 0 disables the split-K tail; GE_EPI_WARPS = 4 | 8 forces the
+ * epilogue width; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row
+ * splits. They change speed, never results beyond rounding order.
  *
  * Errors. Every call returns a status and never aborts or prints. Arguments
  * are validated before anything is launched.

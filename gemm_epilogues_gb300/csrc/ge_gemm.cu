@@ -222,7 +222,12 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
   }
 }
 
-template <int BN, bool PAIR, int EPIW>
+// MCA (pairs only): clusters of 4 CTAs = two pairs on adjacent N-tiles of
+// one 256-row M-tile. Each CTA loads half of its 128 A rows and multicasts
+// them to the CTA holding the same rows in the other pair, so the A slice
+// crosses L2 once for both pairs; a stage is refilled only when both pairs'
+// MMAs have released it.
+template <int BN, bool PAIR, int EPIW, bool MCA = false>
 __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
@@ -244,13 +249,16 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // CTA within the pair
-  const bool leader = rank == 0;                         // issues the pair's MMAs
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // CTA within the cluster
+  const uint32_t pr = rank & 1u;                         // CTA within its pair
+  const uint32_t pp = MCA ? rank >> 1 : 0u;              // pair within the cluster
+  const uint32_t lead = rank & ~1u;                      // the pair's MMA-issuing CTA
+  const bool leader = pr == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), MCA ? 2 : 1);  // MCA: both pairs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -286,11 +294,19 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
 
   const int num_m = (p.Mk + C::TILE_M - 1) / C::TILE_M;
   const int num_n = (p.Nk + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
+  // MCA: a unit is one M-tile x two adjacent N-tiles; pair pp takes N-tile
+  // 2 * column + pp (past the last N-tile its outputs are simply not stored).
+  const int num_cols = MCA ? (num_n + 1) / 2 : num_n;
+  const int num_tiles = num_m * num_cols;
   const int num_kb = (p.K + BK - 1) / BK;
   const int num_units = p.tail_start + (num_tiles - p.tail_start) * p.split;
-  const int first_tile = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int CL = MCA ? 4 : (PAIR ? 2 : 1);  // CTAs per cluster
+  const int first_tile = static_cast<int>(blockIdx.x) / CL;
+  const int tile_step = static_cast<int>(gridDim.x) / CL;
+  auto coords = [&](int tile, int& mt, int& nt) {
+    tile_coords(tile, num_m, num_cols, p.group_m, mt, nt);
+    if (MCA) nt = 2 * nt + static_cast<int>(pp);
+  };
   bool aborted_here = false;
 
   if (warp == 0) {
@@ -304,9 +320,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         int tile, kb0, kb1, v;
         unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
         int mt, nt;
-        tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
-        const int row0 = mt * C::TILE_M + static_cast<int>(rank) * BM;     // this CTA's A rows
-        const int col0 = nt * BN + static_cast<int>(rank) * C::B_ROWS;     // this CTA's B columns
+        coords(tile, mt, nt);
+        const int row0 = mt * C::TILE_M + static_cast<int>(pr) * BM;     // this CTA's A rows
+        const int col0 = nt * BN + static_cast<int>(pr) * C::B_ROWS;     // this CTA's B columns
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.budget)) {
             if (!*abort_flag) atomicOr(p.err, ERR_PRODUCER_TIMEOUT);
@@ -316,7 +332,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
           }
           uint32_t fb = full_bar(stage);
           if (!PAIR || leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * C::STAGE_BYTES);
-          if constexpr (PAIR) fb = mapa_shared(fb, 0);  // completion counted by the leader
+          if constexpr (PAIR) fb = mapa_shared(fb, lead);  // completion counted by the pair's leader
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * BK;
@@ -326,7 +342,15 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
             else
               tma_load_2d(dst, map, fb, x, y);
           };
-          if (!p.a_mn) {
+          if constexpr (MCA) {
+            // this CTA's half of the A rows (64 of 128), for itself and the
+            // CTA with the same rows in the other pair
+            const uint16_t mask = static_cast<uint16_t>((1u << pr) | (1u << (pr + 2)));
+            if (!p.a_mn)
+              tma_load_2d_pair_mc(sa + 8192u * pp, &tmA, fb, k0, row0 + 64 * static_cast<int>(pp), mask);
+            else
+              tma_load_2d_pair_mc(sa + 8192u * pp, &tmA, fb, row0 + 64 * static_cast<int>(pp), k0, mask);
+          } else if (!p.a_mn) {
             load(sa, &tmA, k0, row0);
           } else {
             load(sa, &tmA, row0, k0);
@@ -405,9 +429,10 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
             else
               tc_mma_f16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
-          // frees the stage (in both CTAs of a pair) once these MMAs retire
+          // frees the stage (in both CTAs of a pair; MCA: in all four CTAs,
+          // whose A halves this pair also read) once these MMAs retire
           if constexpr (PAIR)
-            tc_commit_pair_mc(empty_bar(stage), 0x3);
+            tc_commit_pair_mc(empty_bar(stage), MCA ? 0xF : 0x3);
           else
             tc_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
@@ -418,7 +443,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         if (!ok) break;
         // accumulator ready for the epilogue (of both CTAs of a pair)
         if constexpr (PAIR)
-          tc_commit_pair_mc(tfull_bar(acc), 0x3);
+          tc_commit_pair_mc(tfull_bar(acc), static_cast<uint16_t>(0x3u << lead));
         else
           tc_commit(tfull_bar(acc));
         acc ^= 1;
@@ -426,7 +451,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
       }
       // Drain: all MMAs issued by this thread retire before TMEM is freed.
       if constexpr (PAIR)
-        tc_commit_pair_mc(drain_bar, 0x1);
+        tc_commit_pair_mc(drain_bar, static_cast<uint16_t>(0x1u << lead));
       else
         tc_commit(drain_bar);
       if (!mbar_wait_bounded(drain_bar, 0u, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
@@ -440,7 +465,6 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
     const bool has_bias = p.epi != EPI_NONE && !backward;
     const bool bf16 = p.bf16 != 0;
     const unsigned short* bias16 = reinterpret_cast<const unsigned short*>(p.bias);
-    const bool bias_vec_ok = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
@@ -448,8 +472,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
       int tile, kb0, kb1, v;
       unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
       int mt, nt;
-      tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
-      const int rbase = mt * C::TILE_M + static_cast<int>(rank) * BM + q * 32;  // warp's first row of D'
+      coords(tile, mt, nt);
+      const int rbase = mt * C::TILE_M + static_cast<int>(pr) * BM + q * 32;  // warp's first row of D'
       const int grow = rbase + lane;                                          // this thread's row
       // DGELU_BGRAD's z / BIAS_RESIDUAL's residual: the first slab is
       // requested before the wait for the accumulator, each later one while
@@ -469,8 +493,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
           int tn, kb0n, kb1n, vn, mtn, ntn;
           unit_info(un, p.tail_start, p.split, num_kb, tn, kb0n, kb1n, vn);
           if (vn >= 0) continue;
-          tile_coords(tn, num_m, num_n, p.group_m, mtn, ntn);
-          const int rown = mtn * C::TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
+          coords(tn, mtn, ntn);
+          const int rown = mtn * C::TILE_M + static_cast<int>(pr) * BM + q * 32 + lane;
           const int c0 = ntn * BN;
           const int ncols = min(BN, p.Nk - c0);
           if (rown < p.Mk && ncols > 0) {
@@ -485,6 +509,14 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
       }
       uint32_t zw[16];
       if (needs_z) load_slab16(p, grow, nt * BN + 32 * hh, zw);
+      // The bias is requested before the wait as well: per row, this
+      // thread's value; per column, one value per lane for each slab (lane l
+      // holds column 32c + l; the slab's 32 values are then broadcast by
+      // shuffles), the first now and each later one a slab ahead.
+      float brow = 0.0f;
+      if (has_bias && !p.bias_per_col && grow < p.Mk) brow = to_f32(bf16, bias16[grow]);
+      auto bias_lane = [&](int gc) { return has_bias && p.bias_per_col && gc < p.Nk ? to_f32(bf16, bias16[gc]) : 0.0f; };
+      float bl = bias_lane(nt * BN + 32 * hh + lane);
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.budget) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -499,7 +531,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
       if (v >= 0) {
         // Split-K unit: spill the fp32 accumulator rows to the workspace
         // (the fixup kernel adds the splits and applies the epilogue).
-        float* prow = p.partials + (static_cast<long long>(v) * C::TILE_M + static_cast<int>(rank) * BM +
+        float* prow = p.partials + (static_cast<long long>(v) * C::TILE_M + static_cast<int>(pr) * BM +
                                     q * 32 + lane) * BN;
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * BN);
@@ -516,7 +548,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         __syncwarp();
         if (lane == 0) {
           if (PAIR && !leader)
-            mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+            mbar_arrive_remote(mapa_shared(tempty_bar(acc), lead));
           else
             mbar_arrive(tempty_bar(acc));
         }
@@ -524,8 +556,6 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         if (acc == 0) acc_phase ^= 1u;
         continue;
       }
-      float brow = 0.0f;
-      if (has_bias && !p.bias_per_col && grow < p.Mk) brow = to_f32(bf16, bias16[grow]);
       float bg_row = 0.0f;  // D*_BGRAD, bias per D' row: this tile's row sum
       float st_n = 0.0f, st_mean = 0.0f, st_m2 = 0.0f;  // BIAS_RESIDUAL statistics of this row
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -547,33 +577,14 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
           mword = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
         uint32_t znext[16];
         if (needs_z && c + C::HALVES < BN / 32) load_slab16(p, grow, gcol0 + 32 * C::HALVES, znext);
+        const float bl_next = bias_lane(gcol0 + 32 * C::HALVES + lane);
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + 32u * c, v);
         tmem_ld_wait();
         float bcol[32];
-        if (has_bias && p.bias_per_col) {
-          if (bias_vec_ok && gcol0 + 32 <= p.Nk) {
-            const uint4* bp = reinterpret_cast<const uint4*>(p.bias + gcol0);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 w = __ldg(bp + i);
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const float2 f = to_f32x2(bf16, ww[t]);
-                bcol[8 * i + 2 * t] = f.x;
-                bcol[8 * i + 2 * t + 1] = f.y;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              bcol[j] = gcol0 + j < p.Nk ? to_f32(bf16, bias16[gcol0 + j]) : 0.0f;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) bcol[j] = 0.0f;
-        }
+        for (int j = 0; j < 32; ++j) bcol[j] = __shfl_sync(0xffffffffu, bl, j);
+        bl = bl_next;
         uint32_t packed[16];
         uint32_t zpacked[16];
         uint32_t bits = 0;
@@ -668,9 +679,10 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
           for (int j = 0; j < 16; ++j) zw[j] = znext[j];
         }
       }
-      if (backward && !p.bias_per_col && grow < p.Mk)
+      // (MCA: a pair whose N-tile lies past the last one has nothing to write)
+      if (backward && !p.bias_per_col && grow < p.Mk && nt < num_n)
         p.bg_partials[static_cast<long long>(C::HALVES * nt + hh) * p.Mk + grow] = bg_row;
-      if (p.epi == EPI_BIAS_RESIDUAL && p.nstats && grow < p.Mk)
+      if (p.epi == EPI_BIAS_RESIDUAL && p.nstats && grow < p.Mk && nt < num_n)
         p.nstats[static_cast<long long>(C::HALVES * nt + hh) * p.Mk + grow] = make_float2(st_mean, st_m2);
       tc_fence_before();
       __syncwarp();
@@ -678,14 +690,16 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         // this warp's share of the accumulator is free (the pair's MMA
         // issuer counts the arrivals of both CTAs' epilogue warps)
         if (PAIR && !leader)
-          mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+          mbar_arrive_remote(mapa_shared(tempty_bar(acc), lead));
         else
           mbar_arrive(tempty_bar(acc));
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group<0>();
+    // The stores must have read their staging buffers before the CTA's
+    // shared memory goes away; their global writes complete with the grid.
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
   (void)aborted_here;
@@ -705,7 +719,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
   }
 }
 
-template <int BN, bool PAIR, int EPIW>
+template <int BN, bool PAIR, int EPIW, bool MCA = false>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
   static std::atomic<bool> configured[64] = {};  // the attribute is set once per device
@@ -713,11 +727,11 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<BN, PAIR, EPIW>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if constexpr (PAIR) {
-      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       cudaGetLastError();
     }
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -730,13 +744,13 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   cudaLaunchAttribute attr[1];
   if constexpr (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = MCA ? 4 : 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW>, tmA, tmB, tmD, tmZ, args);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, MCA>, tmA, tmB, tmD, tmZ, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -797,8 +811,9 @@ __global__ void __launch_bounds__(256) bgrad_reduce_kernel(const float* part, lo
   }
 }
 
-// Largest number of 2-CTA clusters of the pair kernel that can be resident.
-template <int BN, int EPIW>
+// Largest number of CTA pairs of the pair kernel that can be resident (MCA:
+// in 4-CTA clusters).
+template <int BN, int EPIW, bool MCA>
 int max_pairs(int num_sms) {
   static std::atomic<int> cached[64] = {};
   int dev = 0;
@@ -807,33 +822,38 @@ int max_pairs(int num_sms) {
     return num_sms / 2;
   }
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW, MCA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        Cfg<BN, true, EPIW>::SMEM_BYTES);
+  if (MCA) cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW, MCA>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  cudaGetLastError();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(MCA ? (num_sms & ~3) : (num_sms & ~1)), 1, 1);
   cfg.blockDim = dim3(Cfg<BN, true, EPIW>::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg<BN, true, EPIW>::SMEM_BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = MCA ? 4 : 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true, EPIW>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true, EPIW, MCA>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
-    n = num_sms / 2;
+    n = MCA ? num_sms / 4 : num_sms / 2;
   }
+  n = MCA ? 2 * n : n;  // pairs
   if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
 
 }  // namespace
 
-int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps) {
-  if (epi_warps == 8) return block_n == 256 ? max_pairs<256, 8>(num_sms) : max_pairs<128, 8>(num_sms);
-  return block_n == 256 ? max_pairs<256, 4>(num_sms) : max_pairs<128, 4>(num_sms);
+int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps, int multicast) {
+  if (multicast && block_n == 256)
+    return epi_warps == 8 ? max_pairs<256, 8, true>(num_sms) : max_pairs<256, 4, true>(num_sms);
+  if (epi_warps == 8) return block_n == 256 ? max_pairs<256, 8, false>(num_sms) : max_pairs<128, 8, false>(num_sms);
+  return block_n == 256 ? max_pairs<256, 4, false>(num_sms) : max_pairs<128, 4, false>(num_sms);
 }
 
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream) {
@@ -862,6 +882,7 @@ template <int EPIW>
 cudaError_t launch_width(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args, int grid,
                          cudaStream_t stream) {
+  if (pair == 2 && block_n == 256) return launch_impl<256, true, EPIW, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
   if (pair) {
     if (block_n == 256) return launch_impl<256, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
     return launch_impl<128, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);

@@ -296,9 +296,11 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B,
  * keep theirs). */
 void ge_autotune_cache_clear(void);
 
-/* The plan's tensor-core configuration: tile width, 2-SM pair mode (0/1)
- * and split-K pieces of the tail (1 = none); zeros for other paths. Any
- * pointer may be NULL. Returns the path, or -1 for a NULL plan. */
+/* The plan's tensor-core configuration: tile width, 2-SM pair mode (0: one
+ * CTA per 128-row tile; 1: CTA pairs on 256-row tiles; 2: pairs in clusters
+ * of four that share A slices by multicast) and split-K pieces of the tail
+ * (1 = none); zeros for other paths. Any pointer may be NULL. Returns the
+ * path, or -1 for a NULL plan. */
 int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split);
 
 /* Release the plan and its device workspace (NULL is accepted). The caller

@@ -66,6 +66,7 @@ for _T in (1, 2048, 8192):
 ROW_CASES.update({
     "gelu_aux_fwd": ("gelu_aux", dict(unfused=False)), "gelu_aux_fwd_unfused": ("gelu_aux", dict(unfused=True)),
     "dgelu": ("dgelu", dict(K=0, unfused=False)),
+    "drelu_rows": ("drelu_rows", dict()),
     "bwd_gemm_dgelu": ("dgelu", dict(K=D_IN, unfused=False)),
     "bwd_gemm_dgelu_unfused": ("dgelu", dict(K=D_IN, unfused=True)),
 })
@@ -367,6 +368,23 @@ def run_row_case(args, rank):
         flops = 2.0 * M * N * K
         alg_bytes = 2 * (M * K + N * K + 2 * M * N) + 2 * M
         line["workload"] = f"MLP fwd GELU_AUX_BIAS {M}x{N}x{K}"
+    elif kind == "drelu_rows":
+        # DRELU_BGRAD with a row-major D: dY[11008 features][8192 tokens], the
+        # bias gradient a sum along each stored row
+        M, N = D_OUT, T_TOK
+        dY = f16_tensor((M, N), 7031, "normal", 1.0, dev)
+        ld_aux = (N + 127) // 128 * 4
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7032)
+        aux = torch.randint(-2**31, 2**31 - 1, (M * ld_aux,), generator=gen, device=dev, dtype=torch.int32)
+        dZ = torch.empty((M, N), dtype=torch.float16, device=dev)
+        bgrad = torch.empty(M, dtype=torch.float32, device=dev)
+        plan = ge.Plan(M, N, 0, ge.GE_EPI_DRELU_BGRAD, ge.make_layout(d=ge.GE_D_ROW))
+        run = lambda: plan.execute(dY, None, bgrad, dZ, aux, stream)
+        flops = 0.0
+        alg_bytes = 4 * M * N + 4 * M * ld_aux + 4 * M
+        line["workload"] = f"DRELU_BGRAD row-major dY[{M},{N}]"
+        drelu = None
     else:  # dgelu: standalone (K = 0) or as the backward GEMM's epilogue
         M, N = D_OUT, T_TOK
         K = prm["K"]
@@ -406,7 +424,7 @@ def run_row_case(args, rank):
     if flops:
         line.update({"tflops": flops / (ms * 1e-3) / 1e12, "frac_of_peak": flops / (ms * 1e-3) / 1e12 / peaks["tflops"]})
     plan.free()
-    if kind == "dgelu" and drelu is not None:
+    if kind in ("dgelu", "drelu_rows") and drelu is not None:
         drelu.free()
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -224,7 +224,28 @@ __global__ void __launch_bounds__(256) drelu_rows_kernel(const DreluArgs p) {
     const __half* src = p.dY + r * p.ld;
     __half* dst = p.dZ + r * p.ld;
     const uint32_t* mrow = p.mask + r * p.ld_aux;
-    for (long long c = lane * 8; c < C8; c += 256) {
+    // RU 16-byte steps of the row per round: all their loads are issued
+    // before any of their stores, so the round trips overlap.
+    constexpr int RU = GELU ? 2 : 4;
+    long long c = lane * 8;
+    for (; c + (RU - 1) * 256 < C8; c += RU * 256) {
+      uint4 v[RU], z[RU];
+      uint32_t w[RU];
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        const long long cc = c + u * 256;
+        v[u] = ld_stream(src + cc);
+        z[u] = make_uint4(0, 0, 0, 0);
+        w[u] = 0;
+        if constexpr (GELU)
+          z[u] = __ldg(reinterpret_cast<const uint4*>(p.zaux + r * p.ld_zaux + cc));
+        else
+          w[u] = __ldg(mrow + (cc >> 5)) >> (cc & 31);
+      }
+#pragma unroll
+      for (int u = 0; u < RU; ++u) st_stream(dst + c + u * 256, apply_group<GELU>(v[u], w[u], z[u], acc, bf16));
+    }
+    for (; c < C8; c += 256) {
       const uint4 v = ld_stream(src + c);
       uint32_t w = 0;
       uint4 z = make_uint4(0, 0, 0, 0);

@@ -275,12 +275,16 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
  * ge_plan_autotune: choose the plan's kernel configuration by timing.
  * Planning picks a configuration from the problem's shape; this call instead
  * runs every candidate of the tensor-core path (128- or 256-column tiles,
- * single-CTA or 2-SM pair tiles, with and without the split-K tail) `reps`
- * times on the caller's buffers (same meaning as ge_execute), keeps the
+ * single-CTA or 2-SM pair tiles, with and without the split-K tail, and pair
+ * clusters sharing A by multicast) `reps` times on the caller's buffers
+ * (same meaning as ge_execute), keeps the
  * fastest for every later execute, and finishes with one execute in that
  * configuration, so D / aux / bias hold its results. It blocks the host until
  * the timing runs finish and may re-allocate the plan's tail workspace.
- * Plans of the other paths are left unchanged (GE_OK). reps in 1..1000.
+ * Plans of the other paths are left unchanged (GE_OK). Norm plans
+ * (GE_EPI_BIAS_RESIDUAL_*) are not tuned: ge_execute does not run them, so
+ * the call returns GE_ERR_UNSUPPORTED and the plan keeps its configuration.
+ * reps in 1..1000.
  * The choice is also remembered for the process (per device, M, N, K,
  * epilogue, element type and layout): plans created later for the same
  * problem start from it (unless GE_TILE_N / GE_PAIR / GE_SPLIT_TAIL are set

@@ -15,6 +15,7 @@
 // GEMV path and unfused flow: norm_kernel takes the statistics itself, one
 // block per token, the row in registers, two exact passes (mean, then
 // squared deviations) rather than a sum of squares minus a squared mean.
+#include "ge_elem.cuh"
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
@@ -253,22 +254,40 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const NormArgs p) {
   }
 }
 
+// H += residual in place; units of 8 contiguous elements, two per thread
+// 256 apart inside the block's chunk, all loads issued before the stores.
+template <int F>
 __global__ void __launch_bounds__(256) residual_add_kernel(unsigned short* D, long long R, long long C,
                                                            long long ld, const unsigned short* res,
                                                            int bf16_flag) {
   const bool bf16 = bf16_flag != 0;
   const long long per_row = (C + 7) / 8;
   const long long total = R * per_row;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
-    const long long r = i / per_row;
-    const long long c0 = (i - r * per_row) * 8;
-    unsigned short* d = D + r * ld + c0;
-    const unsigned short* s = res + r * ld + c0;
-    if (c0 + 8 <= C) {
-      const uint4 a = *reinterpret_cast<const uint4*>(d);
-      const uint4 b = *reinterpret_cast<const uint4*>(s);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+  constexpr int U = 2;
+  const long long step = (F & F_BIG) ? static_cast<long long>(gridDim.x) * 256 * U : total;
+  for (long long i0 = blockIdx.x * (256LL * U) + threadIdx.x; i0 < total; i0 += step) {
+    uint4 va[U], vb[U];
+    long long off[U], cc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + u * 256;
+      cc[u] = C;
+      off[u] = 0;
+      va[u] = vb[u] = make_uint4(0, 0, 0, 0);
+      if (i < total) {
+        long long r, k;
+        split_index<F>(i, per_row, r, k);
+        cc[u] = k * 8;
+        off[u] = r * ld + cc[u];
+        va[u] = load_unit<F>(D + off[u], cc[u], C);
+        vb[u] = load_unit<F>(res + off[u], cc[u], C);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (cc[u] >= C) continue;
+      const uint32_t aw[4] = {va[u].x, va[u].y, va[u].z, va[u].w};
+      const uint32_t bw[4] = {vb[u].x, vb[u].y, vb[u].z, vb[u].w};
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -276,9 +295,7 @@ __global__ void __launch_bounds__(256) residual_add_kernel(unsigned short* D, lo
         const float2 z = to_f32x2(bf16, bw[k]);
         o[k] = pack2(bf16, x.x + z.x, x.y + z.y);
       }
-      *reinterpret_cast<uint4*>(d) = make_uint4(o[0], o[1], o[2], o[3]);
-    } else {
-      for (long long c = 0; c < C - c0; ++c) d[c] = from_f32(bf16, to_f32(bf16, d[c]) + to_f32(bf16, s[c]));
+      store_unit<F>(D + off[u], make_uint4(o[0], o[1], o[2], o[3]), cc[u], C);
     }
   }
 }
@@ -308,10 +325,19 @@ cudaError_t launch_norm(const NormArgs& a, int num_sms, cudaStream_t s) {
 cudaError_t launch_residual_add(__half* D, long long R, long long C, long long ld,
                                 const unsigned short* res, int bf16, cudaStream_t s) {
   if (R == 0 || C == 0) return cudaSuccess;
-  long long blocks = (R * ((C + 7) / 8) + 255) / 256;
+  const long long units = R * ((C + 7) / 8);
+  long long blocks = (units + 511) / 512;  // two units per thread
+  int f = C % 8 != 0 ? F_RAGGED : 0;
+  if (blocks > 65535LL * 8 || units > (1LL << 32)) f |= F_BIG;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  residual_add_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<unsigned short*>(D), R, C, ld,
-                                                                    res, bf16);
+  unsigned short* d = reinterpret_cast<unsigned short*>(D);
+  const unsigned g = static_cast<unsigned>(blocks);
+  switch (f) {
+    case 0: residual_add_kernel<0><<<g, 256, 0, s>>>(d, R, C, ld, res, bf16); break;
+    case F_RAGGED: residual_add_kernel<F_RAGGED><<<g, 256, 0, s>>>(d, R, C, ld, res, bf16); break;
+    case F_BIG: residual_add_kernel<F_BIG><<<g, 256, 0, s>>>(d, R, C, ld, res, bf16); break;
+    default: residual_add_kernel<F_RAGGED | F_BIG><<<g, 256, 0, s>>>(d, R, C, ld, res, bf16);
+  }
   return cudaGetLastError();
 }
 

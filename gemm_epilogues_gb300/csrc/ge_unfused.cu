@@ -7,101 +7,154 @@
 // again. These two kernels are those extra passes; with the GEMM's NONE
 // epilogue in front they form the three-kernel baseline the fused path is
 // measured against. Both work in place on D and are bound by HBM bandwidth.
+#include "ge_elem.cuh"
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
 namespace ge {
 namespace {
 
-__device__ __forceinline__ float act_of(int epi, float z) {
-  if (epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS) return fmaxf(z, 0.0f);
-  if (epi == EPI_GELU_BIAS || epi == EPI_GELU_AUX_BIAS) return gelu_tanh(z);
-  if (epi == EPI_GELU_ERF_BIAS) return gelu_erf(z);
-  return z;
+// The activation is a template parameter: with the choice made at run time
+// every unrolled element carried the erf and tanh GELU bodies, and the pass
+// ran at half the speed of one specialised per activation.
+enum Act : int { ACT_RELU = 0, ACT_GELU_TANH = 1, ACT_GELU_ERF = 2 };
+
+template <int ACT>
+__device__ __forceinline__ float act_of(float z) {
+  if constexpr (ACT == ACT_RELU) return fmaxf(z, 0.0f);
+  else if constexpr (ACT == ACT_GELU_TANH) return gelu_tanh(z);
+  else return gelu_erf(z);
 }
 
-// D[r, c] += bias[r] (bias_per_row) or bias[c]; 8 contiguous fp16 per thread.
+// Units of 8 contiguous elements. Each thread takes ELEM_U units 256 apart
+// inside its block's chunk of 256 * ELEM_U units and issues all their loads
+// before any store, so the round trips overlap. Measured on fp16
+// D[8192, 11008] with L2 flushed: bias add 59 us, ReLU 57 us, ReLU + mask
+// 68 us, GELU 62 us (5.5-6.3 TB/s; a plain copy of the same bytes takes
+// 57 us), against 74-88 us for one unit per thread or a persistent grid.
+constexpr int ELEM_U = 2;
+constexpr long long MAX_BLOCKS = 65535LL * 8;
+
+// D[r, c] += bias[r] (bias_per_row) or bias[c].
+template <int F>
 __global__ void __launch_bounds__(256) bias_add_kernel(__half* D, long long R, long long C,
                                                         long long ld, const __half* bias,
                                                         int bias_per_row, int bf16_flag) {
   const bool bf16 = bf16_flag != 0;
+  unsigned short* d16 = reinterpret_cast<unsigned short*>(D);
   const unsigned short* b16 = reinterpret_cast<const unsigned short*>(bias);
-  const long long vpr = (C + 7) / 8;  // 8-wide groups per row
+  const bool bvec = (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;  // 16-byte bias loads
+  const long long vpr = (C + 7) / 8;  // units per row
   const long long total = R * vpr;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
-    const long long r = i / vpr;
-    const long long c0 = (i - r * vpr) * 8;
-    unsigned short* row = reinterpret_cast<unsigned short*>(D) + r * ld;
-    if (c0 + 8 <= C) {
-      uint4 v = *reinterpret_cast<const uint4*>(row + c0);
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const long long step = (F & F_BIG) ? static_cast<long long>(gridDim.x) * 256 * ELEM_U : total;
+  for (long long i0 = blockIdx.x * (256LL * ELEM_U) + threadIdx.x; i0 < total; i0 += step) {
+    uint4 v[ELEM_U];
+    long long rr[ELEM_U], cc[ELEM_U];
+#pragma unroll
+    for (int u = 0; u < ELEM_U; ++u) {
+      const long long i = i0 + u * 256;
+      rr[u] = 0;
+      cc[u] = C;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (i < total) {
+        long long k;
+        split_index<F>(i, vpr, rr[u], k);
+        cc[u] = k * 8;
+        v[u] = load_unit<F>(d16 + rr[u] * ld + cc[u], cc[u], C);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < ELEM_U; ++u) {
+      const long long r = rr[u], c0 = cc[u];
+      if (c0 >= C) continue;
+      uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t bw[4];
+      if (bias_per_row) {
+        const uint32_t bb = b16[r];
+        bw[0] = bw[1] = bw[2] = bw[3] = bb | (bb << 16);
+      } else {
+        const uint4 bv = bvec ? load_unit<F>(b16 + c0, c0, C) : load_partial(b16 + c0, C - c0 < 8 ? static_cast<int>(C - c0) : 8);
+        bw[0] = bv.x, bw[1] = bv.y, bw[2] = bv.z, bw[3] = bv.w;
+      }
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        float2 f = to_f32x2(bf16, w[t]);
-        f.x += to_f32(bf16, bias_per_row ? b16[r] : b16[c0 + 2 * t]);
-        f.y += to_f32(bf16, bias_per_row ? b16[r] : b16[c0 + 2 * t + 1]);
-        w[t] = pack2(bf16, f.x, f.y);
+        const float2 f = to_f32x2(bf16, w[t]);
+        const float2 g = to_f32x2(bf16, bw[t]);
+        w[t] = pack2(bf16, f.x + g.x, f.y + g.y);
       }
-      *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-      for (long long c = c0; c < C; ++c)
-        row[c] = from_f32(bf16, to_f32(bf16, row[c]) + to_f32(bf16, bias_per_row ? b16[r] : b16[c]));
+      store_unit<F>(d16 + r * ld + c0, make_uint4(w[0], w[1], w[2], w[3]), c0, C);
     }
   }
 }
 
-// D = act(D) in place, 8 contiguous fp16 per lane (a warp reads 512
-// contiguous bytes). With a mask, four consecutive lanes cover one 32-element
-// mask word: each builds its byte and lane 0 of the four writes the word
-// (padding words up to the row's 128-column boundary included).
-__global__ void __launch_bounds__(256) activation_kernel(__half* D, long long R, long long C,
-                                                          long long ld, int epi, uint32_t* aux,
-                                                          long long ld_aux, unsigned short* zaux,
-                                                          long long ld_zaux, int bf16_flag) {
-  const bool bf16 = bf16_flag != 0;
-  const long long wpr = aux ? ld_aux : (C + 31) / 32;  // 32-element words per row
-  const long long units = R * wpr * 4;                 // one unit = 8 elements
+struct ActArgs {
+  __half* D;
+  long long R, C, ld;
+  uint32_t* aux;
+  long long ld_aux;
+  unsigned short* zaux;
+  long long ld_zaux;
+  int bf16;
+};
+
+// D = act(D) in place, 8 contiguous elements per unit (a warp reads 512
+// contiguous bytes). With F_MASK, four consecutive lanes cover one
+// 32-element mask word: each builds its byte and the first of the four writes
+// the word (padding words up to the row's 128-column boundary included).
+template <int ACT, int F>
+__global__ void __launch_bounds__(256) activation_kernel(const ActArgs a) {
+  const bool bf16 = a.bf16 != 0;
+  const long long C = a.C;
+  unsigned short* d16 = reinterpret_cast<unsigned short*>(a.D);
+  const long long wpr = (F & F_MASK) ? a.ld_aux : (C + 31) / 32;  // 32-element words per row
+  const long long units = a.R * wpr * 4;
   const long long pad_cols = ((C + 127) / 128) * 128;
-  // the loop bound is a multiple of 32 so whole warps iterate together
+  // the loop bound is a multiple of 32 so whole warps take the mask shuffles
   const long long total = (units + 31) & ~31LL;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
-    uint32_t byte = 0;
-    long long r = 0, word = 0, c0 = 0;
-    const bool live = i < units;
-    if (live) {
-      const long long u = i >> 2;
-      r = u / wpr;
-      word = u - r * wpr;
-      c0 = word * 32 + (i & 3) * 8;
-      unsigned short* row = reinterpret_cast<unsigned short*>(D) + r * ld;
-      if (c0 + 8 <= C) {
-        uint4 v = *reinterpret_cast<const uint4*>(row + c0);
-        if (zaux) *reinterpret_cast<uint4*>(zaux + r * ld_zaux + c0) = v;  // GELU_AUX_BIAS: keep z
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const long long step = (F & F_BIG) ? static_cast<long long>(gridDim.x) * 256 * ELEM_U : total;
+  for (long long i0 = blockIdx.x * (256LL * ELEM_U) + threadIdx.x; i0 < total; i0 += step) {
+    uint4 v[ELEM_U];
+    long long rr[ELEM_U], wd[ELEM_U];
+#pragma unroll
+    for (int u = 0; u < ELEM_U; ++u) {
+      const long long i = i0 + u * 256;
+      rr[u] = wd[u] = 0;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (i < units) {
+        split_index<F>(i >> 2, wpr, rr[u], wd[u]);
+        const long long cc = wd[u] * 32 + (i & 3) * 8;
+        if (cc < C) v[u] = load_unit<F>(d16 + rr[u] * a.ld + cc, cc, C);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < ELEM_U; ++u) {
+      const long long i = i0 + u * 256;
+      if (i >= total) break;  // uniform across the warp
+      uint32_t byte = 0;
+      const bool live = i < units;
+      const long long r = rr[u], word = wd[u], c0 = word * 32 + (i & 3) * 8;
+      if (live && c0 < C) {
+        if constexpr (F & F_ZAUX) store_unit<F>(a.zaux + r * a.ld_zaux + c0, v[u], c0, C);
+        uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float2 f = to_f32x2(bf16, w[t]);
-          byte |= (f.x > 0.0f ? 1u : 0u) << (2 * t);
-          byte |= (f.y > 0.0f ? 1u : 0u) << (2 * t + 1);
-          w[t] = pack2(bf16, act_of(epi, f.x), act_of(epi, f.y));
+          if constexpr (F & F_MASK) {
+            byte |= (f.x > 0.0f ? 1u : 0u) << (2 * t);
+            byte |= (f.y > 0.0f ? 1u : 0u) << (2 * t + 1);
+          }
+          w[t] = pack2(bf16, act_of<ACT>(f.x), act_of<ACT>(f.y));
         }
-        *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
-        for (long long c = c0; c < C && c < c0 + 8; ++c) {
-          if (zaux) zaux[r * ld_zaux + c] = row[c];
-          const float f = to_f32(bf16, row[c]);
-          byte |= (f > 0.0f ? 1u : 0u) << (c - c0);
-          row[c] = from_f32(bf16, act_of(epi, f));
-        }
+        store_unit<F>(d16 + r * a.ld + c0, make_uint4(w[0], w[1], w[2], w[3]), c0, C);
       }
-    }
-    if (aux && epi == EPI_RELU_AUX_BIAS) {
-      const int lane = threadIdx.x & 31;
-      const int base = lane & ~3;
-      uint32_t wv = 0;
+      if constexpr (F & F_MASK) {
+        const int lane = threadIdx.x & 31;
+        const int base = lane & ~3;
+        uint32_t wv = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) wv |= __shfl_sync(0xffffffffu, byte, base + q) << (8 * q);
-      if (live && (lane & 3) == 0 && word * 32 < pad_cols) aux[r * ld_aux + word] = wv;
+        for (int q = 0; q < 4; ++q) wv |= __shfl_sync(0xffffffffu, byte, base + q) << (8 * q);
+        if (live && (lane & 3) == 0 && word * 32 < pad_cols) a.aux[r * a.ld_aux + word] = wv;
+      }
     }
   }
 }
@@ -121,11 +174,28 @@ __global__ void wait_probe_kernel(unsigned int* err, long long budget) {
   }
 }
 
-int grid_for(long long work, int per_block) {
-  long long b = (work + per_block - 1) / per_block;
-  if (b > 65535LL * 8) b = 65535LL * 8;
-  if (b < 1) b = 1;
-  return static_cast<int>(b);
+// Blocks for `units` units and the F_BIG / F_RAGGED flags of the launch.
+int elem_grid(long long units, long long C, int& flags) {
+  long long b = (units + 256 * ELEM_U - 1) / (256 * ELEM_U);
+  flags = C % 8 != 0 ? F_RAGGED : 0;
+  if (b > MAX_BLOCKS || units > (1LL << 32)) flags |= F_BIG;
+  if (b > MAX_BLOCKS) b = MAX_BLOCKS;
+  return static_cast<int>(b < 1 ? 1 : b);
+}
+
+using ActLaunch = void (*)(const ActArgs&, int, cudaStream_t);
+
+template <int ACT, int F>
+void act_launch(const ActArgs& a, int blocks, cudaStream_t s) {
+  activation_kernel<ACT, F><<<blocks, 256, 0, s>>>(a);
+}
+
+// The instance for flags `f` (F_RAGGED | F_BIG bits) with X always set.
+template <int ACT, int X>
+ActLaunch act_pick(int f) {
+  static constexpr ActLaunch t[4] = {act_launch<ACT, X>, act_launch<ACT, X | F_RAGGED>, act_launch<ACT, X | F_BIG>,
+                                     act_launch<ACT, X | F_RAGGED | F_BIG>};
+  return t[f & 3];
 }
 
 }  // namespace
@@ -133,7 +203,15 @@ int grid_for(long long work, int per_block) {
 cudaError_t launch_bias_add(__half* D, long long R, long long C, long long ld, const __half* bias,
                             int bias_per_row, int bf16, cudaStream_t s) {
   if (R == 0 || C == 0) return cudaSuccess;
-  bias_add_kernel<<<grid_for(R * ((C + 7) / 8), 256), 256, 0, s>>>(D, R, C, ld, bias, bias_per_row, bf16);
+  int f = 0;
+  const int blocks = elem_grid(R * ((C + 7) / 8), C, f);
+  switch (f) {
+    case 0: bias_add_kernel<0><<<blocks, 256, 0, s>>>(D, R, C, ld, bias, bias_per_row, bf16); break;
+    case F_RAGGED: bias_add_kernel<F_RAGGED><<<blocks, 256, 0, s>>>(D, R, C, ld, bias, bias_per_row, bf16); break;
+    case F_BIG: bias_add_kernel<F_BIG><<<blocks, 256, 0, s>>>(D, R, C, ld, bias, bias_per_row, bf16); break;
+    default:
+      bias_add_kernel<F_RAGGED | F_BIG><<<blocks, 256, 0, s>>>(D, R, C, ld, bias, bias_per_row, bf16);
+  }
   return cudaGetLastError();
 }
 
@@ -141,9 +219,23 @@ cudaError_t launch_activation(__half* D, long long R, long long C, long long ld,
                               uint32_t* aux, long long ld_aux, unsigned short* zaux,
                               long long ld_zaux, int bf16, cudaStream_t s) {
   if (R == 0 || C == 0) return cudaSuccess;
-  const long long wpr = aux ? ld_aux : (C + 31) / 32;
-  activation_kernel<<<grid_for(R * wpr * 4, 256), 256, 0, s>>>(D, R, C, ld, epi, aux, ld_aux, zaux,
-                                                               ld_zaux, bf16);
+  const bool mask = aux && epi == EPI_RELU_AUX_BIAS;
+  const bool keep_z = zaux && epi == EPI_GELU_AUX_BIAS;
+  const long long wpr = mask ? ld_aux : (C + 31) / 32;
+  int f = 0;
+  const int blocks = elem_grid(R * wpr * 4, C, f);
+  ActLaunch fn = nullptr;
+  switch (epi) {
+    case EPI_RELU_BIAS:
+    case EPI_RELU_AUX_BIAS: fn = mask ? act_pick<ACT_RELU, F_MASK>(f) : act_pick<ACT_RELU, 0>(f); break;
+    case EPI_GELU_BIAS:
+    case EPI_GELU_AUX_BIAS:
+      fn = keep_z ? act_pick<ACT_GELU_TANH, F_ZAUX>(f) : act_pick<ACT_GELU_TANH, 0>(f);
+      break;
+    case EPI_GELU_ERF_BIAS: fn = act_pick<ACT_GELU_ERF, 0>(f); break;
+    default: return cudaErrorInvalidValue;
+  }
+  fn(ActArgs{D, R, C, ld, aux, ld_aux, zaux, ld_zaux, bf16}, blocks, s);
   return cudaGetLastError();
 }
 

@@ -133,6 +133,8 @@ def test_unfused_baseline(oracle, epi):
     the rounded fp16 z, which only differs inside the tolerance band)."""
     _run_case(oracle, 520, 264, 200, epi, "k", "n", "row", seed=8, unfused=True)
     _run_case(oracle, 520, 264, 200, epi, "k", "k", "col", seed=9, unfused=True)
+    _run_case(oracle, 301, 90, 64, epi, "k", "k", "col", seed=10, unfused=True)   # rows end 5 short of 8
+    _run_case(oracle, 96, 263, 64, epi, "m", "n", "row", seed=11, unfused=True)   # rows end 7 short of 8
 
 
 def test_repeat_is_deterministic():
@@ -303,7 +305,7 @@ def test_autotune_picks_a_candidate_and_stays_correct(oracle):
         p.autotune(A, B, bias, D, aux, reps=3)
         torch.cuda.synchronize()
         path, bn, pair, split = p.config
-        assert path == ge.GE_PATH_TC_GEMM and bn in (128, 256) and pair in (0, 1) and split >= 1
+        assert path == ge.GE_PATH_TC_GEMM and bn in (128, 256) and pair in (0, 1, 2) and split >= 1
         assert not (pair and bn != 256)
         ref = oracle_full(oracle, w, A.cpu(), B.cpu(), bias.cpu())
         check_f16(oracle, bits(D), ref["D"], "autotuned")

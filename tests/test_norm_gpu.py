@@ -98,6 +98,7 @@ def test_norm_layouts_bf16_inplace(oracle, norm):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_norm_unfused(oracle, norm, dtype):
     run_norm(oracle, 2048, 300, 256, norm, seed=430, dtype=dtype, unfused=True)
+    run_norm(oracle, 1003, 77, 96, norm, seed=431, dtype=dtype, unfused=True)  # ragged rows of H
 
 
 def test_norm_pair_tiles_split_tail(oracle, monkeypatch):

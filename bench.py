@@ -508,6 +508,12 @@ def run_ours(args, world, rank, local):
     assert dec.path == ge.GE_PATH_GEMV
     dec.set_attr(ge.GE_ATTR_STATIC_A, 1)  # decode weights are never written by earlier work
 
+    def _launches(p):  # kernels one execute launches: the GEMM, and the fixup of a split-K tail
+        path, _, _, split = p.config
+        return 2 if path == ge.GE_PATH_TC_GEMM and split > 1 else 1
+
+    launches_per_step = _launches(fwd) + 1 + _launches(dwp) + 1  # + DRELU_BGRAD + GEMV
+
     Y = torch.empty((T_TOK, D_OUT), dtype=torch.float16, device=dev)
     aux = torch.empty(fwd.aux_bytes // 4, dtype=torch.int32, device=dev)
     dZ = torch.empty_like(dY)
@@ -630,6 +636,22 @@ def run_ours(args, world, rank, local):
     kern["drelu_bgrad"]["algorithmic_bytes"] = bytes_bwd
     kern["dw_gemm"]["algorithmic_bytes"] = bytes_dw
     kern["decode_gemv_gelu_bias"]["algorithmic_bytes"] = bytes_dec
+    # What two events around one tiny launch (a one-element fill) read on
+    # this stream: the part of a single microsecond-scale launch's time that
+    # is launch and event overhead rather than the kernel's work.
+    tiny = torch.empty(1, dtype=torch.float32, device=dev)
+    floor = []
+    with torch.cuda.stream(stream):
+        for _ in range(25):
+            flush.zero_()
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            tiny.zero_()
+            f1.record(stream)
+            f1.synchronize()
+            floor.append(f0.elapsed_time(f1))
+    kern["decode_gemv_gelu_bias"]["event_launch_floor_ms"] = sorted(floor[5:])[len(floor[5:]) // 2]
     dominant = max(("fwd_gemm_relu_aux_bias", "dw_gemm"), key=lambda k: kern[k]["ms"])
     achieved = kern[dominant]["tflops"]
     # The GEMMs are timed inside the step loop (hundreds of back-to-back
@@ -787,6 +809,32 @@ def run_ours(args, world, rank, local):
     last = (e_steps - 1) & 1
     assert torch.equal(dWh[last], dWd[last].cpu()) and torch.equal(bgh[last], bgd[last].cpu())
 
+    # The same copies with no compute: the host link's own time per step
+    # (both directions at once), the floor under the end-to-end number.
+    def run_copies(nsteps):
+        h2d_s.wait_stream(stream)
+        d2h_s.wait_stream(stream)
+        for i in range(nsteps):
+            b = i & 1
+            with torch.cuda.stream(h2d_s):
+                Xd[b].copy_(Xh, non_blocking=True)
+                dYd[b].copy_(dYh, non_blocking=True)
+                x1d[b].copy_(x1h, non_blocking=True)
+            with torch.cuda.stream(d2h_s):
+                dWh[b].copy_(dWd[b], non_blocking=True)
+                bgh[b].copy_(bgd[b], non_blocking=True)
+                y1h[b].copy_(y1d[b], non_blocking=True)
+        stream.wait_stream(h2d_s)
+        stream.wait_stream(d2h_s)
+
+    run_copies(1)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    run_copies(e_steps)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    link_ms = reduce_max(ev0.elapsed_time(ev1) / e_steps, world)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rows = 4096
@@ -807,8 +855,9 @@ def run_ours(args, world, rank, local):
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "overlap": "inputs of step i+1 copied and results of step i read back on "
-                                   "their own streams while step i computes"},
-                "gpu_launches": 4 * args.steps,
+                                   "their own streams while step i computes",
+                        "copies_only_ms_per_step": link_ms},
+                "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk}
         print(json.dumps(line), flush=True)
     for p in (fwd, bwd, dwp, dec):

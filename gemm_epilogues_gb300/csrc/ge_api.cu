@@ -175,6 +175,10 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   const long long tiles = num_m * num_n;
   const long long workers = pair ? tc_gemm_max_pairs(block_n, pl.num_sms, pl.epi_warps, 0) : pl.num_sms;
   c.group_m = static_cast<int>(num_m < (pair ? 8 : 16) ? num_m : (pair ? 8 : 16));
+  if (const char* env = std::getenv("GE_GROUP_M")) {  // rasterisation sweeps
+    const long long g = std::atoll(env);
+    if (g >= 1) c.group_m = static_cast<int>(g < num_m ? g : num_m);
+  }
   // Split-K tail: when the last of several waves would leave most workers
   // idle, the tiles of that wave are split along K into just enough pieces
   // to occupy the workers (at least 4 k-blocks per piece, at most 16); a

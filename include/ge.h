@@ -46,8 +46,9 @@
  * Environment (read by ge_plan_create, for tuning sweeps; unset in normal
  * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
  * GE_SPLIT_TAIL = 0 disables the split-K tail; GE_EPI_WARPS = 4 | 8 forces the
- * epilogue width; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row
- * splits. They change speed, never results beyond rounding order.
+ * epilogue width; GE_GROUP_M = g sets how many M-tiles the tile order sweeps
+ * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits.
+ * They change speed, never results beyond rounding order.
  *
  * Errors. Every call returns a status and never aborts or prints. Arguments
  * are validated before anything is launched.

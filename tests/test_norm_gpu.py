@@ -121,3 +121,61 @@ def test_norm_rejects_bad_calls():
             ge.GE_ERR_INVALID_ARG  # H over the residual needs the fused path
         assert ge.ge_execute_norm(p.handle, A, B, v, H, v, v, H, H, raw=True) == ge.GE_OK
         torch.cuda.synchronize()
+
+
+def _norm_given(oracle, A, B, bias, res, gamma, beta, norm, M, N, K, what, unfused=False):
+    """Run the norm fusion on given fp16 inputs (A [M,K], B [N,K] K-major,
+    residual [N,M]) and compare H and Y with the oracle."""
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    with ge.Plan(M, N, K, EPI[norm], L) as p:
+        H = torch.full((N, M), float("nan"), dtype=torch.float16, device="cuda")
+        Y = torch.full((N, M), float("nan"), dtype=torch.float16, device="cuda")
+        p.execute_norm(A, B, bias, res, gamma, beta if norm == "layernorm" else None, H, Y, 1e-5, unfused=unfused)
+        torch.cuda.synchronize()
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+    refH, refY = oracle.linear_norm(bits(A), bits(B), bits(bias), bits(res), bits(gamma), bits(beta), norm, M, N, K,
+                                    eps=1e-5, d_layout="col")
+    check_f16(oracle, bits(H), refH, what + " H")
+    check_f16(oracle, bits(Y), refY, what + " Y")
+    return Y
+
+
+@pytest.mark.parametrize("norm", ["rmsnorm", "layernorm"])
+@pytest.mark.parametrize("N", [1, 5, 200])
+def test_norm_constant_tokens(oracle, norm, N):
+    """A = 0 and bias = 0, so h is the residual; each token's residual row is
+    one constant (one token all zeros). LayerNorm then gives beta (zero
+    deviation, rstd = 1/sqrt(eps) multiplies only rounding noise); RMSNorm
+    gives c/sqrt(c^2 + eps) times gamma."""
+    M, K = 1000, 64
+    A = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    B = f16_tensor((N, K), 450, device="cuda")
+    bias = torch.zeros(M, dtype=torch.float16, device="cuda")
+    c = f16_tensor((N, 1), 451, "normal", 3.0, "cuda")
+    c[0] = 0.0
+    res = c.expand(N, M).contiguous()
+    gamma = (1 + f16_tensor((M,), 452, "normal", 0.2, dtype=torch.float32)).half().cuda()
+    beta = f16_tensor((M,), 453, "normal", 0.2, "cuda")
+    for unfused in (False, True):
+        _norm_given(oracle, A, B, bias, res, gamma, beta, norm, M, N, K,
+                    f"{norm} constant tokens N={N}{' unfused' if unfused else ''}", unfused)
+
+
+@pytest.mark.parametrize("norm", ["rmsnorm", "layernorm"])
+@pytest.mark.parametrize("N", [3, 300])
+def test_norm_large_offset(oracle, norm, N):
+    """Residual rows around 1000 with a spread of a few units (A = 0 and bias
+    = 0, values on the fp16 grid there, so h is stored without rounding): the
+    mean is ~300 times the deviation, where a sum of squares less a squared
+    mean in fp32 would put an error of a few percent into the variance."""
+    M, K = 4096, 64
+    A = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    B = f16_tensor((N, K), 461, device="cuda")
+    bias = torch.zeros(M, dtype=torch.float16, device="cuda")
+    x = f16_tensor((N, M), 463, "normal", 3.0, dtype=torch.float32).clamp_(-20, 20)
+    res = (1000.0 + torch.round(2 * x) / 2).half().cuda()
+    gamma = (1 + f16_tensor((M,), 464, "normal", 0.2, dtype=torch.float32)).half().cuda()
+    beta = f16_tensor((M,), 465, "normal", 0.2, "cuda")
+    for unfused in (False, True):
+        _norm_given(oracle, A, B, bias, res, gamma, beta, norm, M, N, K,
+                    f"{norm} offset 1000 N={N}{' unfused' if unfused else ''}", unfused)

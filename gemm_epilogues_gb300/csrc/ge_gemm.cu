@@ -291,6 +291,10 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A dependent launched with programmatic serialization (the split-K fixup,
+  // a decode GEMV) may be scheduled from here on; it waits in the kernel
+  // for this grid to complete before it reads what this grid writes.
+  grid_launch_dependents();
 
   const int num_m = (p.Mk + C::TILE_M - 1) / C::TILE_M;
   const int num_n = (p.Nk + BN - 1) / BN;
@@ -759,6 +763,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
 // Adds the tile's split partials in split order, then bias, activation, mask
 // bit (ballot over the slab = one mask word) and the fp16 store.
 __global__ void __launch_bounds__(256) tc_gemm_fixup_kernel(const GemmArgs p, int tile_m, int bn) {
+  grid_dependency_wait();  // the GEMM's pieces are complete and visible
   const int lane = threadIdx.x & 31;
   const int num_m = (p.Mk + tile_m - 1) / tile_m;
   const int num_n = (p.Nk + bn - 1) / bn;
@@ -864,7 +869,19 @@ cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cu
   if (warps <= 0) return cudaSuccess;
   long long blocks = (warps + 7) / 8;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  tc_gemm_fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(args, tile_m, block_n);
+  // A programmatic dependent of the GEMM: it may be scheduled while the GEMM
+  // runs and waits in the kernel for the GEMM's completion.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_fixup_kernel, args, tile_m, block_n);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

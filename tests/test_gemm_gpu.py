@@ -220,6 +220,20 @@ def test_split_tail_pair_ragged(oracle, monkeypatch, epi):
     _run_case(oracle, 1000, 2056, 520, epi, "k", "k", "col", seed=33)
 
 
+@pytest.mark.parametrize("epi", ["bias", "relu_aux_bias", "gelu_bias"])
+def test_underfilled_problem_split_whole(oracle, epi):
+    """A single wave that leaves most SMs idle (config 2: 32 tiles of 128 x 128)
+    is split along K as a whole, 4 pieces per tile, and the fixup applies the
+    epilogue: bit-identical on integer data, within tolerance otherwise."""
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_MN_MAJOR, ge.GE_D_ROW)
+    with ge.Plan(1024, 512, 2048, ge.EPILOGUE_BY_NAME[epi], L) as p:
+        path, bn, pair, split = p.config
+        assert (path, bn, pair, split) == (ge.GE_PATH_TC_GEMM, 128, 0, 4)
+    if epi != "gelu_bias":
+        _run_case(oracle, 1024, 512, 2048, epi, "k", "n", "row", dist=("int", 1.0), seed=35, exact=True)
+    _run_case(oracle, 1024, 512, 2048, epi, "k", "n", "row", seed=36)
+
+
 def test_split_tail_matches_unsplit(oracle, monkeypatch):
     """The same problem with and without the split tail agrees with the oracle."""
     for flag in ("0", "1"):

@@ -276,6 +276,24 @@ def gelu_grad_f64(z: float) -> float:
     return _load().ora_gelu_grad_f64(float(z))
 
 
+def dw_drelu_bgrad(dY, aux, X, M: int, N: int, K: int, *, lda: int | None = None, ldb: int | None = None,
+                   ld_aux: int | None = None, dtype: str = "f16"):
+    """Weight gradient of a RELU_AUX_BIAS layer whose forward D was column-major
+    (nvmath-python cuBLASLt bias-fusion guide, "Advanced techniques", backward
+    item: the mask kept by the forward gates the incoming gradient). dY is
+    stored [K tokens][lda >= M features] and the mask [K][ld_aux] words along
+    the features. By definition, two pinned steps: dZ = dY where the mask bit
+    is set else +0 and bgrad[m] = sum over the K tokens of dZ (``drelu_bgrad``
+    on the column-major layout), then dW = dZ^T X (``linear_forward`` with no
+    epilogue: A = dZ read M-major, B = X [K][ldb >= N] read N-major, D
+    row-major [M][N]). Returns (dW bits, flat M*N; bgrad fp64 [M])."""
+    lda = lda or M
+    dZ, bgrad = drelu_bgrad(dY, aux, M, K, d_layout="col", ldd=lda, ld_aux=ld_aux, dtype=dtype)
+    out = linear_forward(dZ, X, None, "none", M, N, K, a_major="m", b_major="n", d_layout="row", lda=lda,
+                         ldb=ldb, dtype=dtype)
+    return out["D"], bgrad
+
+
 def dgelu_bgrad(dY, zaux, M: int, N: int, *, d_layout: str = "row", ldd: int | None = None,
                 ld_zaux: int | None = None, dtype: str = "f16"):
     """Backward epilogue of GELU_AUX_BIAS: g = dY * gelu'(z) with z the stored

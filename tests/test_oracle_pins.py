@@ -776,3 +776,31 @@ def test_norm_bf16(oracle):
     assert np.array_equal(H.reshape(N, M), oracle.bf16_encode(h.T))
     got = oracle.bf16_decode(Y).reshape(N, M)
     assert np.abs(got - y.T).max() <= np.abs(y).max() * 2 ** -8
+
+
+def test_dw_drelu_bgrad_brute_force(oracle):
+    """Weight gradient with the ReLU backward on its A operand: brute force
+    from an explicit bit array (dZ = dY where the bit is set, dW = dZ^T X,
+    bgrad = column sums of dZ over the tokens), padded pitches."""
+    rng = np.random.default_rng(97)
+    for (M, N, K) in [(1, 1, 1), (5, 3, 7), (40, 9, 33)]:
+        lda, ldx = M + 3, N + 2
+        ld_aux = (M + 127) // 128 * 4
+        dY = rng.standard_normal((K, lda)).astype(np.float16)
+        X = rng.standard_normal((K, ldx)).astype(np.float16)
+        keep = rng.random((K, M)) < 0.6
+        words = np.zeros((K, ld_aux), np.uint32)
+        for k in range(K):
+            for m in range(M):
+                if keep[k, m]:
+                    words[k, m // 32] |= np.uint32(1 << (m % 32))
+        dW, bgrad = oracle.dw_drelu_bgrad(dY.view(np.uint16).reshape(-1), words.reshape(-1),
+                                          X.view(np.uint16).reshape(-1), M, N, K, lda=lda, ldb=ldx,
+                                          ld_aux=ld_aux)
+        dZ = np.where(keep, dY[:, :M].astype(np.float64), 0.0)
+        want = np.zeros((M, N))
+        for m in range(M):
+            for n in range(N):
+                want[m, n] = math.fsum(dZ[k, m] * float(X[k, n]) for k in range(K))
+        assert np.array_equal(dW.reshape(M, N), want.astype(np.float16).view(np.uint16))
+        assert np.allclose(bgrad, [math.fsum(dZ[:, m]) for m in range(M)], rtol=1e-13, atol=1e-14)

@@ -40,6 +40,7 @@ GE_EPI_GELU_AUX_BIAS = 7
 GE_EPI_DGELU_BGRAD = 8
 GE_EPI_BIAS_RESIDUAL_RMSNORM = 9
 GE_EPI_BIAS_RESIDUAL_LAYERNORM = 10
+GE_EPI_DW_DRELU_BGRAD = 11
 # ge_dtype_t
 GE_F16 = 0
 GE_F32 = 1
@@ -61,7 +62,8 @@ EPILOGUE_BY_NAME = {"none": GE_EPI_NONE, "bias": GE_EPI_BIAS, "relu_bias": GE_EP
                     "gelu_bias": GE_EPI_GELU_BIAS, "relu_aux_bias": GE_EPI_RELU_AUX_BIAS,
                     "drelu_bgrad": GE_EPI_DRELU_BGRAD, "gelu_erf_bias": GE_EPI_GELU_ERF_BIAS,
                     "gelu_aux_bias": GE_EPI_GELU_AUX_BIAS, "dgelu_bgrad": GE_EPI_DGELU_BGRAD,
-                    "rmsnorm": GE_EPI_BIAS_RESIDUAL_RMSNORM, "layernorm": GE_EPI_BIAS_RESIDUAL_LAYERNORM}
+                    "rmsnorm": GE_EPI_BIAS_RESIDUAL_RMSNORM, "layernorm": GE_EPI_BIAS_RESIDUAL_LAYERNORM,
+                    "dw_drelu_bgrad": GE_EPI_DW_DRELU_BGRAD}
 
 # Every function the header declares (checked against include/ge.h by a test).
 ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_free",

@@ -251,6 +251,21 @@ ge_status_t apply_config(Plan* pl, const TcConfig& c) {
 // Tensor maps for the tensor-core path (kernel-level operands A', B', D' and,
 // for GELU_AUX_BIAS, the z output Z' stored like D'; otherwise tmZ repeats
 // D's map and is not used).
+// Mask words (DW_DRELU_BGRAD): rows of ld_aux uint32 words, K rows; a box of
+// 4 words (128 m) x 64 k-rows, no swizzle.
+bool make_mask_map(CUtensorMap* m, const void* base, uint64_t words, uint64_t rows, uint64_t ld_words) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {words, rows};
+  cuuint64_t strides[1] = {ld_words * 4};
+  cuuint32_t box[2] = {4, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D, void* Z) {
   if (!Z) Z = D;
   if (pl->mapA == A && pl->mapB == B && pl->mapD == D && pl->mapZ == Z) return GE_OK;
@@ -275,8 +290,11 @@ ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D, void* Z)
   else
     ok &= make_map(&pl->tmB, pl->bf16, Bk, Nk, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= make_map(&pl->tmD, pl->bf16, D, Nk, Mk, L.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok &= make_map(&pl->tmZ, pl->bf16, Z, Nk, Mk, Z == D ? L.ldd : L.ld_aux, 32, 32,
-                 CU_TENSOR_MAP_SWIZZLE_64B);
+  if (pl->epi == GE_EPI_DW_DRELU_BGRAD)  // the fourth map carries the mask words
+    ok &= make_mask_map(&pl->tmZ, Z, static_cast<uint64_t>(L.ld_aux), K, static_cast<uint64_t>(L.ld_aux));
+  else
+    ok &= make_map(&pl->tmZ, pl->bf16, Z, Nk, Mk, Z == D ? L.ldd : L.ld_aux, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) {
     pl->mapA = pl->mapB = pl->mapD = pl->mapZ = nullptr;
     return GE_ERR_CUDA;
@@ -311,7 +329,8 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     e = launch_gemv(g, pl->num_sms, st);
   } else {
     const bool zout = epi_code == EPI_GELU_AUX_BIAS;
-    ge_status_t s = build_maps(pl, A, B, D, zout ? aux : nullptr);
+    const bool mask_map = pl->epi == GE_EPI_DW_DRELU_BGRAD;
+    ge_status_t s = build_maps(pl, A, B, D, (zout || mask_map) ? aux : nullptr);
     if (s != GE_OK) return s;
     GemmArgs g{};
     g.Mk = static_cast<int>(pl->swap ? pl->N : pl->M);
@@ -342,8 +361,19 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     const bool backward = epi_code == EPI_DRELU_BGRAD || epi_code == EPI_DGELU_BGRAD;
     g.bgrad = backward ? static_cast<float*>(const_cast<void*>(bias)) : nullptr;
     if (backward) g.bias = nullptr;
+    const bool amask = pl->epi == GE_EPI_DW_DRELU_BGRAD;
+    if (amask) {  // D = (A masked) . B, no epilogue arithmetic; bgrad from the transform warps
+      g.epi = EPI_NONE;
+      g.amask = 1;
+      g.bias = nullptr;
+      g.aux = nullptr;
+      g.bgrad = static_cast<float*>(const_cast<void*>(bias));
+      g.bg_partials = g.bgrad ? pl->bg_partials : nullptr;
+    }
     e = launch_tc_gemm(pl->block_n, pl->pair, pl->epi_warps, pl->tmA, pl->tmB, pl->tmD, pl->tmZ, g, pl->grid, st);
     if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, st);
+    if (e == cudaSuccess && amask && g.bgrad)
+      e = launch_bgrad_reduce(pl->bg_partials, pl->split > 1 ? pl->split : 1, g.Mk, g.bgrad, st);
     if (e == cudaSuccess && backward) {
       const long long rows =
           pl->swap ? pl->bg_rows : (pl->epi_warps / 4) * static_cast<long long>((g.Nk + pl->block_n - 1) / pl->block_n);
@@ -420,7 +450,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
                            const ge_layout_t* layout) {
   if (!out) return GE_ERR_INVALID_ARG;
   *out = nullptr;
-  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_BIAS_RESIDUAL_LAYERNORM)
+  if (static_cast<int>(epi) < GE_EPI_NONE || static_cast<int>(epi) > GE_EPI_DW_DRELU_BGRAD)
     return GE_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 0) return GE_ERR_INVALID_ARG;
   const int64_t lim = (int64_t(1) << 31) - 1;
@@ -439,6 +469,10 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   // The norm runs over the M features of each token: they must be the
   // contiguous index of D (D column-major, i.e. Y[N tokens][M features]).
   if (epi_is_norm(epi) && L.d != GE_D_COL) return GE_ERR_UNSUPPORTED;
+  // The masked-operand weight gradient: A = dY read M-major ([K tokens][M]),
+  // its mask packed along M per token, D row-major (the kernel's own A').
+  const bool dw_mask = epi == GE_EPI_DW_DRELU_BGRAD;
+  if (dw_mask && (L.a != GE_MN_MAJOR || L.d != GE_D_ROW)) return GE_ERR_UNSUPPORTED;
 
   Plan tmp;
   tmp.M = M;
@@ -473,6 +507,12 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (L.ld_aux % 4 != 0) return GE_ERR_ALIGNMENT;
     tmp.aux_words = L.ld_aux;
   }
+  if (dw_mask) {  // mask rows are the K tokens, words along the M features
+    if (L.ld_aux == 0) L.ld_aux = (M + 127) / 128 * 4;
+    if (L.ld_aux < (M + 31) / 32) return GE_ERR_INVALID_ARG;
+    if (L.ld_aux % 4 != 0) return GE_ERR_ALIGNMENT;
+    tmp.aux_words = L.ld_aux;
+  }
   const bool has_zaux = epi == GE_EPI_GELU_AUX_BIAS || epi == GE_EPI_DGELU_BGRAD;
   if (epi_is_norm(epi)) tmp.aux_words = L.ldd;  // residual, H and Y share D's layout
   if (has_zaux) {  // 16-bit z stored like D: ld_aux in elements, 16-byte rows
@@ -487,7 +527,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     tmp.path = GE_PATH_DRELU;
     if (L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
   } else if (N <= 16 && L.a == GE_K_MAJOR && L.b == GE_K_MAJOR && epi != GE_EPI_RELU_AUX_BIAS &&
-             !has_zaux && !backward) {
+             !has_zaux && !backward && !dw_mask) {
     tmp.path = GE_PATH_GEMV;
     if (L.lda % 8 != 0 || L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
   } else {
@@ -532,7 +572,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     }
     // Pairs of pairs that share A slices by multicast: opt-in for now.
     if (const char* env = std::getenv("GE_MULTICAST"))
-      if (env[0] == '1' && tc_pair == 1 && tc_block_n == 256) tc_pair = 2;
+      if (env[0] == '1' && tc_pair == 1 && tc_block_n == 256 && !dw_mask) tc_pair = 2;
     if (const char* env = std::getenv("GE_SPLIT_TAIL"))
       if (env[0] == '0') tc_split = false;
     if (backward) tc_split = false;  // their bias-gradient partials are per tile
@@ -547,6 +587,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       if (env[0] == '4') tmp.epi_warps = 4;
       if (env[0] == '8') tmp.epi_warps = 8;
     }
+    if (dw_mask) tmp.epi_warps = 4;  // the masking warps take the place of four more
   }
   size_t ws = 256;
   size_t bg_off = 0;
@@ -563,6 +604,12 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     ws = (ws + 255) / 256 * 256;
     bg_off = ws;
     ws += static_cast<size_t>(tmp.bg_rows) * static_cast<size_t>(tmp.bg_len) * 4;
+  }
+  if (tmp.path == GE_PATH_TC_GEMM && dw_mask) {
+    // bias-gradient partials: one row per split-K piece (at most 16) over M
+    ws = (ws + 255) / 256 * 256;
+    bg_off = ws;
+    ws += 16 * static_cast<size_t>(M) * 4;
   }
   size_t nstats_off = 0, rowstats_off = 0;
   if (tmp.path == GE_PATH_TC_GEMM && epi_is_norm(epi)) {
@@ -684,6 +731,17 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B, const void*
       return s;
     return launch_forward(pl, A, B, bias, D, aux, static_cast<int>(pl->epi), st);
   }
+  if (pl->epi == GE_EPI_DW_DRELU_BGRAD) {
+    // A = dY, aux = the forward mask (input), bias = fp32 bgrad output or NULL.
+    if (!aux) return GE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(aux) || (bias && !aligned16(bias)))
+      return GE_ERR_ALIGNMENT;
+    if ((s = check_device(pl, 0, A)) != GE_OK || (s = check_device(pl, 1, B)) != GE_OK ||
+        (s = check_device(pl, 3, D)) != GE_OK || (s = check_device(pl, 4, aux)) != GE_OK ||
+        (bias && (s = check_device(pl, 2, bias)) != GE_OK))
+      return s;
+    return launch_forward(pl, A, B, bias, D, aux, EPI_NONE, st);
+  }
   if (epi_has_bias(pl->epi) && !bias) return GE_ERR_INVALID_ARG;
   const bool needs_aux = pl->epi == GE_EPI_RELU_AUX_BIAS || pl->epi == GE_EPI_GELU_AUX_BIAS;
   if (needs_aux && !aux) return GE_ERR_INVALID_ARG;
@@ -795,7 +853,7 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
         if (c.split > 1) cands[n++] = c;
       }
     }
-  cands[n++] = tc_config(*pl, 256, 2, false);  // pairs sharing A by multicast
+  if (pl->epi != GE_EPI_DW_DRELU_BGRAD) cands[n++] = tc_config(*pl, 256, 2, false);  // pairs sharing A by multicast
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
     cudaGetLastError();

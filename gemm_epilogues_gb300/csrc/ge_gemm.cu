@@ -48,11 +48,13 @@ constexpr int BK = 64;             // fp16 k-slice per stage (128 bytes)
 constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 fp16 columns
 
 // EPIW = epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
-// taking alternate 32-column slabs).
-template <int BN, bool PAIR, int EPIW>
+// taking alternate 32-column slabs). AM = the A operand is masked in shared
+// memory by four more warps before the MMA reads it (DW_DRELU_BGRAD).
+template <int BN, bool PAIR, int EPIW, bool AM = false>
 struct Cfg {
   static constexpr int EPI_WARPS = EPIW;
-  static constexpr int NUM_THREADS = 64 + 32 * EPIW;
+  static constexpr int XFORM_WARPS = AM ? 4 : 0;
+  static constexpr int NUM_THREADS = 64 + 32 * EPIW + 32 * XFORM_WARPS;
   static constexpr int HALVES = EPIW / 4;  // warps per lane quarter
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns staged by one CTA
   static constexpr int A_BYTES = BM * BK * 2;
@@ -61,8 +63,13 @@ struct Cfg {
   static constexpr int STAGES = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
   static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
-  static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // AM: per stage, the mask words of the stage's BK k-rows for this CTA's
+  // BM rows of A' (BK x BM/32 words = 1 KB), loaded with the operands.
+  static constexpr int MASK_SLOT = BK * (BM / 32) * 4;
+  static constexpr int OFF_MASK = OFF_EPI + EPI_BYTES;
+  static constexpr int MASK_BYTES = AM ? STAGES * MASK_SLOT : 0;
+  static constexpr int OFF_BAR = OFF_MASK + MASK_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + (AM ? STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB for base alignment
   static constexpr int TMEM_COLS = 2 * BN;
@@ -227,12 +234,12 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
 // them to the CTA holding the same rows in the other pair, so the A slice
 // crosses L2 once for both pairs; a stage is refilled only when both pairs'
 // MMAs have released it.
-template <int BN, bool PAIR, int EPIW, bool MCA = false>
-__global__ void __launch_bounds__(64 + 32 * EPIW, 1)
+template <int BN, bool PAIR, int EPIW, bool MCA = false, bool AM = false>
+__global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
                    const GemmArgs p) {
-  using C = Cfg<BN, PAIR, EPIW>;
+  using C = Cfg<BN, PAIR, EPIW, AM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -243,6 +250,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  // AM: stage s of A' has been masked (the MMA waits on this instead of the
+  // load's barrier); counted on the pair's leader for both CTAs' warps.
+  auto xform_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 5 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -265,6 +275,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
       mbar_init(tempty_bar(b), C::EPI_ARRIVALS);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (AM)
+      for (int s = 0; s < C::STAGES; ++s) mbar_init(xform_bar(s), (PAIR ? 2 : 1) * C::XFORM_WARPS);
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD);
-    if (p.epi == EPI_GELU_AUX_BIAS) tma_prefetch_desc(&tmZ);
+    if (p.epi == EPI_GELU_AUX_BIAS || AM) tma_prefetch_desc(&tmZ);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -335,17 +347,26 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
             break;
           }
           uint32_t fb = full_bar(stage);
-          if (!PAIR || leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * C::STAGE_BYTES);
-          if constexpr (PAIR) fb = mapa_shared(fb, lead);  // completion counted by the pair's leader
+          if constexpr (AM) {
+            // each CTA counts its own operands and mask slice: its transform
+            // warps wait for exactly these bytes
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES + C::MASK_SLOT);
+          } else {
+            if (!PAIR || leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * C::STAGE_BYTES);
+            if constexpr (PAIR) fb = mapa_shared(fb, lead);  // completion counted by the pair's leader
+          }
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * BK;
           auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
-            if constexpr (PAIR)
+            if constexpr (PAIR && !AM)
               tma_load_2d_pair(dst, map, fb, x, y);
             else
               tma_load_2d(dst, map, fb, x, y);
           };
+          // AM: the mask words of k-rows k0.. for this CTA's A' rows row0..
+          // (row0 is a multiple of 128, so the word coordinate is 16-byte aligned)
+          if constexpr (AM) load(sbase + C::OFF_MASK + stage * C::MASK_SLOT, &tmZ, row0 / 32, k0);
           if constexpr (MCA) {
             // this CTA's half of the A rows (64 of 128), for itself and the
             // CTA with the same rows in the other pair
@@ -374,7 +395,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         }
       }
       // Drain: every issued load must land before the CTA may exit.
-      if (!PAIR || leader) {
+      if (!PAIR || leader || AM) {
         for (int s = 0; s < C::STAGES; ++s) {
           if (fills > s) {
             const long long last = s + (long long)C::STAGES * ((fills - 1 - s) / C::STAGES);
@@ -411,7 +432,13 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.budget)) {
+          bool landed;
+          if constexpr (AM)  // masked by both CTAs' transform warps
+            landed = PAIR ? mbar_wait_bounded_cluster(xform_bar(stage), phase, abort_flag, p.budget)
+                          : mbar_wait_bounded(xform_bar(stage), phase, abort_flag, p.budget);
+          else
+            landed = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.budget);
+          if (!landed) {
             if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -459,6 +486,103 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
       else
         tc_commit(drain_bar);
       if (!mbar_wait_bounded(drain_bar, 0u, never, p.budget)) atomicOr(p.err, ERR_DRAIN_TIMEOUT);
+    }
+  } else if (AM && warp >= 2 + EPIW) {
+    // ------------------------------------------ A-operand mask (AM only)
+    // A' is M-major: a stage holds this CTA's BM = 128 rows as two 8 KB
+    // chunks of BK = 64 k-rows x 64 m (128 bytes, 128-byte swizzle: the
+    // 16-byte unit u of k-row r sits at unit u ^ (r & 7)). Thread t owns the
+    // 8 m of unit (t >> 3) on the k-rows r = (t & 7) + 8i, so its physical
+    // unit is the same on every row, and it keeps their masked fp32 sums.
+    const int xt = static_cast<int>(threadIdx.x) - 32 * (2 + EPIW);
+    const int xunit = xt >> 3, ph = xt & 7;
+    const int chunk = xunit >> 3, uu = xunit & 7;
+    const uint32_t a_off = 8192u * chunk + 16u * static_cast<uint32_t>(uu ^ ph);
+    const int wsel = 2 * chunk + (uu >> 2);  // mask word of these 8 m (of the row's 4)
+    const int bsh = 8 * (uu & 3);
+    const bool bf16 = p.bf16 != 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = first_tile; u < num_units && ok; u += tile_step) {
+      int tile, kb0, kb1, v;
+      unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
+      int mt, nt;
+      coords(tile, mt, nt);
+      const bool want_bg = p.bg_partials != nullptr && nt == 0;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.budget) ? 1 : 0;
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          if (lane == 0) {
+            if (!*abort_flag) atomicOr(p.err, ERR_XFORM_TIMEOUT);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        uint8_t* abase = smem + stage * C::STAGE_BYTES + a_off;
+        const uint32_t* mrow = reinterpret_cast<const uint32_t*>(smem + C::OFF_MASK + stage * C::MASK_SLOT) + wsel;
+#pragma unroll
+        for (int i = 0; i < BK / 8; ++i) {
+          const int r = ph + 8 * i;
+          const uint32_t bits = (mrow[4 * r] >> bsh) & 0xFFu;
+          uint4* cell = reinterpret_cast<uint4*>(abase + 128 * r);
+          const uint4 val = *cell;
+          uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t keep = ((bits >> (2 * t)) & 1u ? 0x0000FFFFu : 0u) |
+                                  ((bits >> (2 * t + 1)) & 1u ? 0xFFFF0000u : 0u);
+            w[t] &= keep;  // a cleared element is +0 in either type
+            if (want_bg) {
+              const float2 f = to_f32x2(bf16, w[t]);
+              acc[2 * t] += f.x;
+              acc[2 * t + 1] += f.y;
+            }
+          }
+          *cell = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        // the masked tile must be visible to the tensor core (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR && !leader)
+            mbar_arrive_remote(mapa_shared(xform_bar(stage), lead));
+          else
+            mbar_arrive(xform_bar(stage));
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (want_bg) {
+        // the 8 k-row phases of each unit are 8 adjacent lanes: a fixed tree
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 1);
+          acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 2);
+          acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 4);
+        }
+        if (ph == 0) {
+          const int m0 = mt * C::TILE_M + static_cast<int>(pr) * BM + 64 * chunk + 8 * uu;
+          const int piece = v >= 0 ? v % p.split : 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (m0 + e < p.Mk) {
+              p.bg_partials[static_cast<long long>(piece) * p.Mk + m0 + e] = acc[e];
+              if (v < 0)  // a whole tile: the other pieces' rows hold nothing
+                for (int sp = 1; sp < p.split; ++sp) p.bg_partials[static_cast<long long>(sp) * p.Mk + m0 + e] = 0.0f;
+            }
+          }
+        }
+      }
     }
   } else {
     // -------------------------------------------------- epilogue warps
@@ -723,27 +847,28 @@ __global__ void __launch_bounds__(64 + 32 * EPIW, 1)
   }
 }
 
-template <int BN, bool PAIR, int EPIW, bool MCA = false>
+template <int BN, bool PAIR, int EPIW, bool MCA = false, bool AM = false>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
+  using C = Cfg<BN, PAIR, EPIW, AM>;
   static std::atomic<bool> configured[64] = {};  // the attribute is set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<BN, PAIR, EPIW>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA, AM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if constexpr (PAIR) {
-      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA, AM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       cudaGetLastError();
     }
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(Cfg<BN, PAIR, EPIW>::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<BN, PAIR, EPIW>::SMEM_BYTES;
+  cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if constexpr (PAIR) {
@@ -754,7 +879,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, MCA>, tmA, tmB, tmD, tmZ, args);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, MCA, AM>, tmA, tmB, tmD, tmZ, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -899,6 +1024,18 @@ template <int EPIW>
 cudaError_t launch_width(int block_n, int pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args, int grid,
                          cudaStream_t stream) {
+  if constexpr (EPIW == 4) {
+    if (args.amask) {  // four epilogue warps, no multicast
+      if (pair) {
+        if (block_n == 256) return launch_impl<256, true, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+        return launch_impl<128, true, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+      }
+      if (block_n == 256) return launch_impl<256, false, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+      return launch_impl<128, false, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    }
+  } else {
+    if (args.amask) return cudaErrorInvalidValue;
+  }
   if (pair == 2 && block_n == 256) return launch_impl<256, true, EPIW, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
   if (pair) {
     if (block_n == 256) return launch_impl<256, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);

@@ -30,7 +30,8 @@ enum ErrBits : unsigned int {
   ERR_MMA_TIMEOUT = 2u,
   ERR_EPILOGUE_TIMEOUT = 4u,
   ERR_DRAIN_TIMEOUT = 8u,
-  ERR_PROBE_TIMEOUT = 16u
+  ERR_PROBE_TIMEOUT = 16u,
+  ERR_XFORM_TIMEOUT = 32u
 };
 
 // Kernel-level problem of the tensor-core GEMM: D'[Mk, Nk] (row-major, via
@@ -75,6 +76,12 @@ struct GemmArgs {
   // squared deviations) as float2 at nstats[(halves * nt + half) * Mk + row];
   // null = not wanted.
   float2* nstats;
+  // DW_DRELU_BGRAD (amask = 1): A' (M-major) is masked by the forward's ReLU
+  // mask as it is loaded (the mask arrives through the fourth tensor map);
+  // with bg_partials set, the masked A' is also summed over each unit's
+  // k-range into bg_partials[piece][Mk] (piece = split-K piece, 0 for whole
+  // tiles, whose other rows are zeroed), by the CTAs of the first N-tile.
+  int amask;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs

@@ -89,7 +89,10 @@ typedef enum {
   GE_EPI_DGELU_BGRAD = 8,   /* backward: dZ = dY * gelu'(z), bgrad = sum_n     */
   /* MatMul + bias + residual + norm over the M features (ge_execute_norm): */
   GE_EPI_BIAS_RESIDUAL_RMSNORM = 9,
-  GE_EPI_BIAS_RESIDUAL_LAYERNORM = 10
+  GE_EPI_BIAS_RESIDUAL_LAYERNORM = 10,
+  /* weight gradient of a RELU_AUX_BIAS layer, the ReLU backward applied to
+   * the A operand (dY) as it is loaded; bgrad from the same pass:          */
+  GE_EPI_DW_DRELU_BGRAD = 11
 } ge_epilogue_t;
 
 /* GE_BF16: bfloat16 (1 sign, 8 exponent, 7 fraction bits), the other 16-bit
@@ -182,6 +185,23 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K,
  *   gelu'(z) = 0.5 (1 + t) + 0.5 z (1 - t^2) sqrt(2/pi) (1 + 0.134145 z^2),
  *   t = tanh(sqrt(2/pi) (z + 0.044715 z^3)); bgrad[m] = sum over n of the
  *   unrounded fp32 g, in a fixed order. dZ may alias dY, not aux.
+ * DW_DRELU_BGRAD (weight gradient of a RELU_AUX_BIAS layer whose forward D
+ * was column-major, Y[tokens][features]; the ReLU backward is applied to the
+ * A operand as the GEMM loads it, so dZ = dY * mask is never stored and no
+ * separate DRELU_BGRAD pass runs. Plan: M = features, N = the other operand's
+ * width, K = tokens; layout a = MN_MAJOR, d = ROW; ld_aux in words, default
+ * ceil(M/128)*4):
+ *   A     : dY, T [K tokens][lda >= M] (read only).
+ *   B     : T operand in the planned layout (X: MN_MAJOR [K][ldb >= N]).
+ *   aux   : the forward mask (read only), [K][ld_aux] uint32 words packed
+ *           along the M features (the RELU_AUX_BIAS packing of a column-major
+ *           forward D), 16-byte aligned.
+ *   D     : dW, T: D[m,n] = T(sum over k of dZ[k,m] * B[k,n]) in fp32, with
+ *           dZ[k,m] = dY[k,m] where bit (m % 32) of aux[k*ld_aux + m/32] is
+ *           set, else +0.
+ *   bias  : OUTPUT, fp32 [M] or NULL (not wanted): bgrad[m] = sum over k of
+ *           dZ[k,m], in fp32 in a fixed order, 16-byte aligned.
+ *   A, B, D and aux 16-byte aligned; the tensor-core path only.
  * DRELU_BGRAD standalone (K == 0; dY and dZ are [M,N] in the planned D layout):
  *   A     : dY, T (read only).           B : unused (may be NULL).
  *   aux   : the forward mask (read only). D : dZ, T; may alias A.

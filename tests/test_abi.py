@@ -51,7 +51,14 @@ def test_plan_validation_without_device(lib):
     assert _create(0, 8, 8) == E.GE_ERR_INVALID_ARG
     assert _create(8, -1, 8) == E.GE_ERR_INVALID_ARG
     assert _create(8, 8, 0, epi=E.GE_EPI_BIAS) == E.GE_ERR_INVALID_ARG
-    assert _create(8, 8, 8, epi=11) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 8, 8, epi=12) == E.GE_ERR_INVALID_ARG
+    # the masked-operand weight gradient needs A read M-major and D row-major
+    assert _create(8, 8, 8, epi=E.GE_EPI_DW_DRELU_BGRAD,
+                   layout=ge.make_layout(E.GE_K_MAJOR, E.GE_MN_MAJOR, E.GE_D_ROW)) == E.GE_ERR_UNSUPPORTED
+    assert _create(8, 8, 8, epi=E.GE_EPI_DW_DRELU_BGRAD,
+                   layout=ge.make_layout(E.GE_MN_MAJOR, E.GE_MN_MAJOR, E.GE_D_COL)) == E.GE_ERR_UNSUPPORTED
+    assert _create(64, 64, 64, epi=E.GE_EPI_DW_DRELU_BGRAD,
+                   layout=ge.make_layout(E.GE_MN_MAJOR, E.GE_MN_MAJOR, E.GE_D_ROW, ld_aux=6)) == E.GE_ERR_ALIGNMENT
     # the norm epilogues need the features contiguous (D column-major)
     assert _create(8, 8, 8, epi=E.GE_EPI_BIAS_RESIDUAL_RMSNORM) == E.GE_ERR_UNSUPPORTED
     assert _create(8, 8, 8, a=E.GE_F32) == E.GE_ERR_UNSUPPORTED

@@ -67,6 +67,7 @@ ROW_CASES.update({
     "gelu_aux_fwd": ("gelu_aux", dict(unfused=False)), "gelu_aux_fwd_unfused": ("gelu_aux", dict(unfused=True)),
     "dgelu": ("dgelu", dict(K=0, unfused=False)),
     "drelu_rows": ("drelu_rows", dict()),
+    "dw_drelu": ("dw_drelu", dict(unfused=False)), "dw_drelu_unfused": ("dw_drelu", dict(unfused=True)),
     "bwd_gemm_dgelu": ("dgelu", dict(K=D_IN, unfused=False)),
     "bwd_gemm_dgelu_unfused": ("dgelu", dict(K=D_IN, unfused=True)),
 })
@@ -368,6 +369,36 @@ def run_row_case(args, rank):
         flops = 2.0 * M * N * K
         alg_bytes = 2 * (M * K + N * K + 2 * M * N) + 2 * M
         line["workload"] = f"MLP fwd GELU_AUX_BIAS {M}x{N}x{K}"
+    elif kind == "dw_drelu":
+        # Weight gradient of the MLP layer from the incoming dY: fused (the
+        # ReLU backward applied to the GEMM's A operand, bgrad in the same
+        # pass) or the two-kernel flow (standalone DRELU_BGRAD storing dZ,
+        # then the dW GEMM on it)
+        M, N, K = D_OUT, D_IN, T_TOK
+        dY = f16_tensor((K, M), 7041, "normal", 1.0, dev)
+        Xw = f16_tensor((K, N), 7042, "normal", 1.0, dev)
+        ld_aux = (M + 127) // 128 * 4
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7043)
+        aux = torch.randint(-2**31, 2**31 - 1, (K * ld_aux,), generator=gen, device=dev, dtype=torch.int32)
+        dW = torch.empty((M, N), dtype=torch.float16, device=dev)
+        bgrad = torch.empty(M, dtype=torch.float32, device=dev)
+        L = ge.make_layout(ge.GE_MN_MAJOR, ge.GE_MN_MAJOR, ge.GE_D_ROW)
+        if prm["unfused"]:
+            plan = ge.Plan(M, N, K, ge.GE_EPI_NONE, L)
+            drelu = ge.Plan(M, K, 0, ge.GE_EPI_DRELU_BGRAD, ge.make_layout(d=ge.GE_D_COL))
+            dZ = torch.empty_like(dY)
+
+            def run():
+                drelu.execute(dY, None, bgrad, dZ, aux, stream)
+                plan.execute(dZ, Xw, None, dW, None, stream)
+        else:
+            plan = ge.Plan(M, N, K, ge.GE_EPI_DW_DRELU_BGRAD, L)
+            drelu = None
+            run = lambda: plan.execute(dY, Xw, bgrad, dW, aux, stream)
+        flops = 2.0 * M * N * K
+        alg_bytes = 2 * (M * K + K * N + M * N) + 4 * K * ld_aux + 4 * M
+        line["workload"] = f"dW {M}x{N}x{K} from dY with the ReLU backward + bgrad"
     elif kind == "drelu_rows":
         # DRELU_BGRAD with a row-major D: dY[11008 features][8192 tokens], the
         # bias gradient a sum along each stored row
@@ -424,7 +455,7 @@ def run_row_case(args, rank):
     if flops:
         line.update({"tflops": flops / (ms * 1e-3) / 1e12, "frac_of_peak": flops / (ms * 1e-3) / 1e12 / peaks["tflops"]})
     plan.free()
-    if kind in ("dgelu", "drelu_rows") and drelu is not None:
+    if kind in ("dgelu", "drelu_rows", "dw_drelu") and drelu is not None:
         drelu.free()
     if rank == 0:
         print(json.dumps(line), flush=True)

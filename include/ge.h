@@ -201,7 +201,10 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K,
  *           set, else +0.
  *   bias  : OUTPUT, fp32 [M] or NULL (not wanted): bgrad[m] = sum over k of
  *           dZ[k,m], in fp32 in a fixed order, 16-byte aligned.
- *   A, B, D and aux 16-byte aligned; the tensor-core path only.
+ *   A, B, D and aux 16-byte aligned; the tensor-core path only. (Measured
+ *   slower than DRELU_BGRAD followed by a NONE GEMM on the stored dZ: it
+ *   saves the dZ round trip through HBM but adds a shared-memory pass per
+ *   operand stage.)
  * DRELU_BGRAD standalone (K == 0; dY and dZ are [M,N] in the planned D layout):
  *   A     : dY, T (read only).           B : unused (may be NULL).
  *   aux   : the forward mask (read only). D : dZ, T; may alias A.

@@ -214,39 +214,53 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const NormArgs p) {
   }
 }
 
-// y = (h - mean) * rstd * gamma + beta for every element, 8 per thread-step,
-// four independent steps in flight: a plain stream at copy speed.
+// y = (h - mean) * rstd * gamma + beta for every element: units of 8
+// features, two per thread 256 apart inside the block's chunk, both loads
+// issued before the stores (the layout of the other elementwise passes,
+// which run at copy speed).
+template <int F>
 __global__ void __launch_bounds__(256) norm_apply_kernel(const NormArgs p) {
   const bool bf16 = p.bf16 != 0;
   const bool layer = p.layer != 0;
   const long long G = p.C >> 3;
   const long long total = p.R * G;
-  const long long stride = static_cast<long long>(gridDim.x) * 256;
-  constexpr int U = 4;
-  for (long long i0 = blockIdx.x * 256LL + threadIdx.x; i0 < total; i0 += U * stride) {
+  constexpr int U = 2;
+  const long long step = (F & F_BIG) ? static_cast<long long>(gridDim.x) * 256 * U : total;
+  for (long long i0 = blockIdx.x * (256LL * U) + threadIdx.x; i0 < total; i0 += step) {
     uint4 v[U];
     long long rr[U], gg[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const long long i = i0 + u * stride;
-      rr[u] = i < total ? i / G : 0;
-      gg[u] = i < total ? i - rr[u] * G : 0;
-      v[u] = i < total ? ld_stream(p.H + rr[u] * p.ld + 8 * gg[u]) : make_uint4(0, 0, 0, 0);
+      const long long i = i0 + u * 256;
+      rr[u] = gg[u] = 0;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (i < total) {
+        split_index<F>(i, G, rr[u], gg[u]);
+        v[u] = ld_stream(p.H + rr[u] * p.ld + 8 * gg[u]);
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (i0 + u * stride >= total) break;
+      if (i0 + u * 256 >= total) continue;
       const float2 st = __ldg(p.rowstats + rr[u]);
       const uint4 gm = __ldg(reinterpret_cast<const uint4*>(p.gamma) + gg[u]);
       const uint4 bt = layer ? __ldg(reinterpret_cast<const uint4*>(p.beta) + gg[u]) : make_uint4(0, 0, 0, 0);
       st_stream(p.Y + rr[u] * p.ld + 8 * gg[u], norm8(v[u], gm, bt, st.x, st.y, layer, bf16));
     }
   }
-  // the C % 8 features past the last whole group, one thread each
-  const long long tail = p.C - 8 * G;
+}
+
+// The C % 8 features past the last whole group of every row, one thread
+// each (launched only when C is not a multiple of 8).
+__global__ void __launch_bounds__(256) norm_apply_tail_kernel(const NormArgs p) {
+  const bool bf16 = p.bf16 != 0;
+  const bool layer = p.layer != 0;
+  const long long c0 = p.C & ~7LL;
+  const long long tail = p.C - c0;
+  const long long stride = static_cast<long long>(gridDim.x) * 256;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < p.R * tail; i += stride) {
     const long long r = i / tail;
-    const long long c = 8 * G + (i - r * tail);
+    const long long c = c0 + (i - r * tail);
     const float2 st = p.rowstats[r];
     const float x = to_f32(bf16, p.H[r * p.ld + c]);
     const float b = layer ? to_f32(bf16, p.beta[c]) : 0.0f;
@@ -308,11 +322,21 @@ cudaError_t launch_norm(const NormArgs& a, int num_sms, cudaStream_t s) {
     long long fb = (a.R + 7) / 8;  // one row per warp
     if (fb > static_cast<long long>(num_sms) * 16) fb = static_cast<long long>(num_sms) * 16;
     norm_finalize_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(a);
-    const long long work = a.R * ((a.C + 7) / 8);
-    long long blocks = (work + 255) / 256;
-    const long long cap = static_cast<long long>(num_sms) * 16;
-    if (blocks > cap) blocks = cap;
-    norm_apply_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    const long long units = a.R * (a.C >> 3);
+    if (units > 0) {
+      long long blocks = (units + 511) / 512;  // two units per thread
+      const bool big = blocks > 65535LL * 8 || units > (1LL << 32);
+      if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+      if (big)
+        norm_apply_kernel<F_BIG><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+      else
+        norm_apply_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    }
+    if (a.C & 7) {
+      long long tb = (a.R * (a.C & 7) + 255) / 256;
+      if (tb > 65535LL * 8) tb = 65535LL * 8;
+      norm_apply_tail_kernel<<<static_cast<unsigned>(tb), 256, 0, s>>>(a);
+    }
     return cudaGetLastError();
   }
   long long blocks = a.R;  // one row per block

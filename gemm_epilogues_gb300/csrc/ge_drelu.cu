@@ -270,7 +270,56 @@ __global__ void __launch_bounds__(256) drelu_rows_kernel(const DreluArgs p) {
   }
 }
 
+// out[i] = the sum over j of part[j * len + i] (the bias-gradient partials
+// of a GEMM epilogue): a block takes 32 consecutive i, its 8 warps the rows
+// j = w, w + 8, ... in order, and the first warp adds their 8 sums in warp
+// order, so the result does not depend on timing. (A thread per i summing
+// every row in turn kept too few loads in flight: 256 partial rows of 11008
+// took tens of microseconds.)
+__global__ void __launch_bounds__(256) bgrad_reduce_kernel(const float* part, long long rows, long long len,
+                                                           float* out) {
+  __shared__ float red[8][32];
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  for (long long c0 = blockIdx.x * 32LL; c0 < len; c0 += gridDim.x * 32LL) {
+    const long long i = c0 + lane;
+    float s = 0.0f;
+    if (i < len) {
+      long long j = w;
+      for (; j + 24 < rows; j += 32) {  // four rows of this warp's share per step
+        const float a0 = __ldcg(part + j * len + i);
+        const float a1 = __ldcg(part + (j + 8) * len + i);
+        const float a2 = __ldcg(part + (j + 16) * len + i);
+        const float a3 = __ldcg(part + (j + 24) * len + i);
+        s += a0;
+        s += a1;
+        s += a2;
+        s += a3;
+      }
+      for (; j < rows; j += 8) s += __ldcg(part + j * len + i);
+    }
+    red[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && i < len) {
+      float t = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t += red[k][lane];
+      out[i] = t;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
+                                cudaStream_t stream) {
+  if (len <= 0) return cudaSuccess;
+  long long blocks = (len + 31) / 32;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  bgrad_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, rows, len, out);
+  return cudaGetLastError();
+}
 
 // Row splits for the column case: one wave of resident blocks (measured on
 // dY[8192, 11008], 43 strips, 3 blocks per SM: 8 or 10 splits (0.75 and 0.94

@@ -932,15 +932,6 @@ __global__ void __launch_bounds__(256) tc_gemm_fixup_kernel(const GemmArgs p, in
   }
 }
 
-__global__ void __launch_bounds__(256) bgrad_reduce_kernel(const float* part, long long rows,
-                                                           long long len, float* out) {
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < len; i += gridDim.x * 256LL) {
-    float s = 0.0f;
-    for (long long j = 0; j < rows; ++j) s += __ldcg(part + j * len + i);
-    out[i] = s;
-  }
-}
-
 // Largest number of CTA pairs of the pair kernel that can be resident (MCA:
 // in 4-CTA clusters).
 template <int BN, int EPIW, bool MCA>
@@ -1007,15 +998,6 @@ cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cu
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_fixup_kernel, args, tile_m, block_n);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
-                                cudaStream_t stream) {
-  if (len <= 0) return cudaSuccess;
-  long long blocks = (len + 255) / 256;
-  if (blocks > 65535) blocks = 65535;
-  bgrad_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, rows, len, out);
   return cudaGetLastError();
 }
 

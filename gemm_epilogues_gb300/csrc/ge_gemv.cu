@@ -14,10 +14,13 @@
 // butterfly warp reduction, then bias + activation + fp16 rounding per output.
 // With static weights the plan launches the kernel as a programmatic
 // dependent, so a chain of decode projections starts layer i+1's weight reads
-// while layer i drains. For N = 1 a warp issues a whole 4096-element row (16
-// slabs) at once, in 4-warp blocks; for larger N, with fewer slabs in flight
-// per warp, each warp first asks L2 for its first row with one bulk prefetch
-// (PF). Measured on a 4096 x 4096 fp16 weight, L2 flushed: 16 slabs, 4-warp
+// while layer i drains: for N = 1 (fp16) each warp loads the first half of
+// its row into registers before it waits for the previous grid (back to back
+// over 8 weights of 4096 x 4096: 9.8 -> 8.0 us a layer), then the rest in
+// one 8-slab round; for larger N, with fewer slabs in flight per warp, each
+// warp first asks L2 for its first row with one bulk prefetch (PF). For
+// N = 1 a warp issues a whole 4096-element row (16 slabs) at once, in 4-warp
+// blocks. Measured on a 4096 x 4096 fp16 weight, L2 flushed: 16 slabs, 4-warp
 // blocks, no prefetch 11.9 us single / 8.0 us back to back; 8 slabs, 8-warp
 // blocks, prefetch 14.5 / 8.8 us; 16 slabs with the prefetch 15.9 / 10.3 us.
 // (A variant that streamed rows through a shared-memory ring with bulk copies
@@ -52,7 +55,7 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
 
 // BF16 picks the element type of A, B, bias and D at compile time so that the
 // fp16 and bf16 inner loops each decode with one instruction per pair.
-template <int NT, int UNROLL, bool BF16, bool PF>
+template <int NT, int UNROLL, bool BF16, bool PF, bool PRE = false>
 __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
@@ -66,14 +69,47 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
     if (lane == 0 && m0 < p.M && (p.K & 7) == 0)
       bulk_prefetch_l2(p.A + m0 * p.lda, static_cast<uint32_t>(p.K) * 2u);
   }
+  // PRE (static weights): the first PRE_SLABS slabs of this warp's first
+  // row are requested before the wait on the previous grid, which may still
+  // be running, so a chain of decode projections streams weights across
+  // layer boundaries. fp16 only: the bf16 decode needs more registers per
+  // slab, and with the preload a 4096-row grid no longer fits at once
+  // (measured 13.2 -> 19.6 us for one launch).
+  constexpr bool PRELOAD = PRE && !BF16;
+  constexpr int PRE_SLABS = 8;
+  const long long m_first = blockIdx.x * wpb + (threadIdx.x >> 5);
+  uint4 pre[PRELOAD ? PRE_SLABS : 1];
+  bool have_pre = false;
+  if constexpr (PRELOAD) {
+    if (p.static_a && m_first < p.M && lane * 8 + (PRE_SLABS - 1) * SLAB < K8) {
+      const __half* arow = p.A + m_first * p.lda;
+#pragma unroll
+      for (int u = 0; u < PRE_SLABS; ++u) pre[u] = ld_stream(arow + lane * 8 + u * SLAB);
+      have_pre = true;
+    }
+  }
   grid_launch_dependents();
   grid_dependency_wait();  // B may come from, and D may be read by, the previous grid
-  for (long long m = blockIdx.x * wpb + (threadIdx.x >> 5); m < p.M; m += nwarps) {
+  for (long long m = m_first; m < p.M; m += nwarps) {
     const __half* arow = p.A + m * p.lda;
     float acc[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n] = 0.0f;
     int k = lane * 8;
+    if constexpr (PRELOAD) {
+      if (have_pre && m == m_first) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          if (n < p.N) {
+            const __half* brow = p.B + n * p.ldb + k;
+#pragma unroll
+            for (int u = 0; u < PRE_SLABS; ++u)
+              acc[n] = dot8<BF16>(pre[u], __ldg(reinterpret_cast<const uint4*>(brow + u * SLAB)), acc[n]);
+          }
+        }
+        k += PRE_SLABS * SLAB;
+      }
+    }
     for (; k + (UNROLL - 1) * SLAB < K8; k += UNROLL * SLAB) {
       uint4 a[UNROLL];
 #pragma unroll
@@ -88,17 +124,18 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
         }
       }
     }
-    if constexpr (UNROLL > 4) {  // what is left of the row, four slabs at a time
-      for (; k + 3 * SLAB < K8; k += 4 * SLAB) {
-        uint4 a[4];
+    if constexpr (UNROLL > 4) {  // what is left of the row, MID slabs at a time
+      constexpr int MID = UNROLL >= 16 ? 8 : 4;
+      for (; k + (MID - 1) * SLAB < K8; k += MID * SLAB) {
+        uint4 a[MID];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = ld_stream(arow + k + u * SLAB);
+        for (int u = 0; u < MID; ++u) a[u] = ld_stream(arow + k + u * SLAB);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           if (n < p.N) {
             const __half* brow = p.B + n * p.ldb + k;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < MID; ++u)
               acc[n] = dot8<BF16>(a[u], __ldg(reinterpret_cast<const uint4*>(brow + u * SLAB)), acc[n]);
           }
         }
@@ -140,7 +177,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   }
 }
 
-template <int NT, int UNROLL, int THREADS, bool PF>
+template <int NT, int UNROLL, int THREADS, bool PF, bool PRE = false>
 cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
   constexpr int warps = THREADS / 32;
   long long blocks = (a.M + warps - 1) / warps;  // one row per warp when the grid allows
@@ -158,8 +195,8 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = a.bf16 ? cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL, true, PF>, a)
-                         : cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL, false, PF>, a);
+  cudaError_t e = a.bf16 ? cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL, true, PF, PRE>, a)
+                         : cudaLaunchKernelEx(&cfg, gemv_kernel<NT, UNROLL, false, PF, PRE>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -167,7 +204,7 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
-  if (a.N <= 1) return launch_nt<1, 16, 128, false>(a, num_sms, s);
+  if (a.N <= 1) return launch_nt<1, 16, 128, false, true>(a, num_sms, s);
   if (a.N <= 2) return launch_nt<2, 8, 256, true>(a, num_sms, s);
   if (a.N <= 4) return launch_nt<4, 4, 256, true>(a, num_sms, s);
   if (a.N <= 8) return launch_nt<8, 4, 256, true>(a, num_sms, s);

@@ -248,6 +248,28 @@ def test_gemv_many_rows_per_warp(oracle, M, N, K):
     assert path == ge.GE_PATH_GEMV
 
 
+@pytest.mark.parametrize("M,K", [(4096, 4096), (12000, 4096), (1000, 4104), (700, 1000)])
+def test_gemv_static_weights_preload(oracle, M, K):
+    """One token with static weights: the first slabs of each warp's first row
+    are loaded before the wait on the previous grid; rows beyond the grid's
+    warps (12000), a ragged K (4104) and rows shorter than the preload (1000)."""
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    W = f16_tensor((M, K), 730 + M, "normal", K ** -0.5).cuda()
+    x = f16_tensor((1, K), 731).cuda()
+    b = f16_tensor((M,), 732, "normal", 0.1).cuda()
+    with ge.Plan(M, 1, K, ge.GE_EPI_GELU_BIAS, L) as p:
+        p.set_attr(ge.GE_ATTR_STATIC_A, 1)
+        assert p.path == ge.GE_PATH_GEMV
+        y = torch.full((1, M), float("nan"), dtype=torch.float16, device="cuda")
+        p.execute(W, x, b, y)
+        p.execute(W, x, b, y)  # a second launch depends on the first
+        torch.cuda.synchronize()
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+    r = oracle.linear_forward(bits(W), bits(x), bits(b), "gelu_bias", M, 1, K, a_major="k", b_major="k",
+                              d_layout="col")
+    check_f16(oracle, bits(y), r["D"], f"static gemv {M}x1x{K}")
+
+
 def test_gemv_chain_with_static_weights(oracle):
     """A chain of decode projections (each layer's output is the next one's
     input, ping-pong buffers) launched with programmatic dependent launch:

@@ -12,8 +12,10 @@
  *    fp16 operands with a 32-bit compute type and fp16 output.
  *  - same page, "Advanced techniques": RELU_BIAS and GELU_BIAS fuse the
  *    activation after the bias; DRELU_BGRAD fuses the ReLU-gradient mask with
- *    the bias-gradient accumulation in the backward pass; a plan is costly
- *    and is meant to be reused across many executes.
+ *    the bias-gradient accumulation in the backward pass (also the source of
+ *    DW_DRELU_BGRAD, which applies that mask to the weight-gradient GEMM's
+ *    operand); a plan is costly and is meant to be reused across many
+ *    executes.
  *  - Fusing bias addition with matrix multiplication using nvmath-python:
  *    Y = ReLU(WX + B); RELU_AUX_BIAS also writes an auxiliary output for the
  *    backward pass; planning is blocking and chooses the kernel; a plan must
@@ -35,9 +37,9 @@
  * Ownership and threading. The caller owns every device buffer (A, B, bias,
  * D, aux, and the DRELU_BGRAD outputs). A plan owns its host state and a
  * small device workspace allocated by ge_plan_create on the device current
- * at that time (an error word; for DRELU_BGRAD / DGELU_BGRAD the reduction
- * partials and counters; for the norm epilogues the per-token statistics;
- * for a split-K tail its fp32 pieces). ge_execute never allocates and only
+ * at that time (an error word; for DRELU_BGRAD / DGELU_BGRAD and
+ * DW_DRELU_BGRAD the reduction partials and counters; for the norm
+ * epilogues the per-token statistics; for a split-K tail its fp32 pieces). ge_execute never allocates and only
  * enqueues work on the given stream; the caller synchronises. Executes of
  * one plan must be ordered on one stream: two executes of the same plan that
  * overlap on the GPU race on its workspace. Distinct plans are independent,

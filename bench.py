@@ -75,11 +75,17 @@ ROW_CASES.update({
 
 def kernel_source_hash(files=("gemm_epilogues_gb300/csrc/ge_gemm.cu", "gemm_epilogues_gb300/csrc/ge_ptx.cuh",
                                "gemm_epilogues_gb300/csrc/ge_internal.h")) -> str:
+    """Hash of the GEMM kernel's code: comments and blank lines are left out,
+    so a change of wording alone does not invalidate a capture."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

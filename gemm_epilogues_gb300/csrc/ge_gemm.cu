@@ -12,19 +12,22 @@
 //    the intermediate WX never goes back to global memory; RELU_AUX_BIAS
 //    also keeps the auxiliary output the backward pass needs.
 //
-// Structure (one CTA per SM, 320 threads):
+// Structure (one CTA per SM, 64 + 32 * EPIW threads):
 //   warp 0      TMA producer: A and B k-slices (64 fp16 = one 128-byte
 //               swizzle row) into a STAGES-deep shared-memory ring.
 //   warp 1      owns TMEM (2 x BN fp32 columns: a double-buffered 128 x BN
 //               accumulator) and one lane issues tcgen05.mma 128 x BN x 16.
-//   warps 2..9  epilogue: tcgen05.ld a 32-row x 32-column slab of the
-//               accumulator, add the bias, apply the activation, build the
-//               mask word, round to fp16, stage in 64-byte-swizzled shared
-//               memory and TMA-store it; runs while the MMA warp already
-//               accumulates the next tile into the other TMEM buffer. Two
-//               warps share each TMEM lane quarter (warp % 4) and take
-//               alternate slabs, so heavier epilogues (GELU derivative,
-//               residual, statistics) keep pace with the MMAs.
+//   warps 2..   EPIW = 4 or 8 epilogue warps: tcgen05.ld a 32-row x
+//               32-column slab of the accumulator, add the bias, apply the
+//               activation, build the mask word, round to fp16, stage in
+//               64-byte-swizzled shared memory and TMA-store it; runs while
+//               the MMA warp already accumulates the next tile into the
+//               other TMEM buffer. With 8, two warps share each TMEM lane
+//               quarter (warp % 4) and take alternate slabs, so the heaviest
+//               epilogue (the GELU derivative) keeps pace with the MMAs.
+//   (AM)        four more warps clear the masked elements of each stage's A
+//               tile in shared memory before the MMA reads it (the weight
+//               gradient with the ReLU backward on its operand).
 // Pair mode (PAIR = true, clusters of 2 CTAs on 2 SMs): the tile is 256 x BN;
 // each CTA stages its own 128 rows of A and its own half of B's BN columns,
 // the even CTA issues tcgen05.mma.cta_group::2 (M = 256) which reads both

@@ -831,16 +831,21 @@ def run_ours(args, world, rank, local):
     d2h = dWh[0].numel() * 2 + bgh[0].numel() * 4 + y1h[0].numel() * 2
     run_e2e(2)
     torch.cuda.synchronize()
+    # three timed runs of e_steps steps each; the median is reported, so one
+    # host-side stall (the copies are issued from Python) does not decide it
+    e2e_runs = []
+    for _ in range(3):
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_e2e(e_steps)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        e2e_runs.append(ev0.elapsed_time(ev1) / e_steps)
     barrier(world)
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    run_e2e(e_steps)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = reduce_max(ev0.elapsed_time(ev1) / e_steps, world)
+    e2e_ms = reduce_max(sorted(e2e_runs)[1], world)
     e2e_value = flops_step * world / (e2e_ms * 1e-3) / 1e12
     # results of the last step reached the host and equal the device values
     last = (e_steps - 1) & 1
@@ -893,7 +898,8 @@ def run_ours(args, world, rank, local):
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "overlap": "inputs of step i+1 copied and results of step i read back on "
                                    "their own streams while step i computes",
-                        "copies_only_ms_per_step": link_ms},
+                        "copies_only_ms_per_step": link_ms,
+                        "runs_ms_per_step": e2e_runs, "of_runs": "median"},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk}
         print(json.dumps(line), flush=True)

@@ -47,6 +47,8 @@
  *
  * Environment (read by ge_plan_create, for tuning sweeps; unset in normal
  * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
+ * GE_MULTICAST = 1 turns 2-SM pairs of 256-wide tiles into clusters of four
+ * that share their A slices by TMA multicast (not for DW_DRELU_BGRAD);
  * GE_SPLIT_TAIL = 0 disables the split-K tail; GE_EPI_WARPS = 4 | 8 forces the
  * epilogue width; GE_GROUP_M = g sets how many M-tiles the tile order sweeps
  * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits.

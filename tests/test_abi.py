@@ -100,3 +100,15 @@ def test_null_handles(lib):
     assert ge.load_library().ge_plan_free(None) == ge.GE_OK
     assert ge.ge_aux_bytes(None) == 0
     assert ge.ge_plan_path(None) == -1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises: there is no fallback."""
+    monkeypatch.setattr(ge, "_lib", None)
+    monkeypatch.setattr(ge, "LIB_PATH", str(tmp_path / "libgemm_epilogues.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        ge.load_library()
+    with pytest.raises(RuntimeError, match="not built"):
+        ge.Plan(64, 64, 64, ge.GE_EPI_BIAS)
+    with pytest.raises(RuntimeError, match="not built"):
+        ge.ge_status_string(ge.GE_OK)

@@ -50,6 +50,14 @@ def test_plan_validation_without_device(lib):
     E = ge
     assert _create(0, 8, 8) == E.GE_ERR_INVALID_ARG
     assert _create(8, -1, 8) == E.GE_ERR_INVALID_ARG
+    # empty problems are rejected on every path before the device is touched
+    assert _create(8, 0, 8) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 0, 8, epi=E.GE_EPI_RELU_AUX_BIAS) == E.GE_ERR_INVALID_ARG
+    assert _create(0, 8, 0, epi=E.GE_EPI_DRELU_BGRAD) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 0, 0, epi=E.GE_EPI_DRELU_BGRAD) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 0, 0, epi=E.GE_EPI_DGELU_BGRAD) == E.GE_ERR_INVALID_ARG
+    assert _create(8, 8, 0, epi=E.GE_EPI_DW_DRELU_BGRAD,
+                   layout=ge.make_layout(E.GE_MN_MAJOR, E.GE_MN_MAJOR, E.GE_D_ROW)) == E.GE_ERR_INVALID_ARG
     assert _create(8, 8, 0, epi=E.GE_EPI_BIAS) == E.GE_ERR_INVALID_ARG
     assert _create(8, 8, 8, epi=12) == E.GE_ERR_INVALID_ARG
     # the masked-operand weight gradient needs A read M-major and D row-major

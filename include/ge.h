@@ -39,11 +39,12 @@
  * small device workspace allocated by ge_plan_create on the device current
  * at that time (an error word; for DRELU_BGRAD / DGELU_BGRAD and
  * DW_DRELU_BGRAD the reduction partials and counters; for the norm
- * epilogues the per-token statistics; for a split-K tail its fp32 pieces). ge_execute never allocates and only
- * enqueues work on the given stream; the caller synchronises. Executes of
- * one plan must be ordered on one stream: two executes of the same plan that
- * overlap on the GPU race on its workspace. Distinct plans are independent,
- * and plans may be created, executed and freed from several host threads.
+ * epilogues the per-token statistics; for a split-K tail its fp32 pieces).
+ * ge_execute never allocates and only enqueues work on the given stream;
+ * the caller synchronises. Executes of one plan must be ordered on one
+ * stream: two executes of the same plan that overlap on the GPU race on its
+ * workspace. Distinct plans are independent, and plans may be created,
+ * executed and freed from several host threads.
  *
  * Environment (read by ge_plan_create, for tuning sweeps; unset in normal
  * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
@@ -232,8 +233,8 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B,
  * bias and writes D, then one kernel reads D, applies the activation (and
  * writes the mask for RELU_AUX_BIAS, from the rounded z) and writes D
  * (ops-nn MatMul fusion, "ops-nn's MatMul fusion strategy", the unfused
- * three-step flow). Only for BIAS / RELU_BIAS / GELU_BIAS / RELU_AUX_BIAS / GELU_ERF_BIAS / GELU_AUX_BIAS
- * plans. Arguments and errors as ge_execute.
+ * three-step flow). Only for BIAS / RELU_BIAS / GELU_BIAS / RELU_AUX_BIAS /
+ * GELU_ERF_BIAS / GELU_AUX_BIAS plans. Arguments and errors as ge_execute.
  */
 ge_status_t ge_execute_unfused(ge_plan_t plan, const void* A, const void* B,
                                const void* bias, void* D, void* aux,
@@ -305,9 +306,9 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
  * runs every candidate of the tensor-core path (128- or 256-column tiles,
  * single-CTA or 2-SM pair tiles, with and without the split-K tail, and pair
  * clusters sharing A by multicast) `reps` times on the caller's buffers
- * (same meaning as ge_execute), keeps the
- * fastest for every later execute, and finishes with one execute in that
- * configuration, so D / aux / bias hold its results. It blocks the host until
+ * (same meaning as ge_execute), keeps the fastest for every later execute,
+ * and finishes with one execute in that configuration, so D / aux / bias
+ * hold its results. It blocks the host until
  * the timing runs finish and may re-allocate the plan's tail workspace.
  * Plans of the other paths are left unchanged (GE_OK). Norm plans
  * (GE_EPI_BIAS_RESIDUAL_*) are not tuned: ge_execute does not run them, so

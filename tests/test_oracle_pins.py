@@ -759,6 +759,28 @@ def test_norm_brute_force(oracle, norm, dl):
         assert (np.abs(Y - y) <= half_step * (1 + 1e-9) + 1e-300).all(), "Y differs from the brute force"
 
 
+@pytest.mark.parametrize("norm", ["rmsnorm", "layernorm"])
+def test_norm_matches_library_norms(oracle, norm):
+    """Against torch's own LayerNorm / RMSNorm in fp64 over each token's M
+    features (h from the library matmul): Y is their result rounded once."""
+    import torch.nn.functional as F
+    rng = np.random.default_rng(98 + (norm == "layernorm"))
+    M, N, K = 96, 7, 24
+    A, B, bias, res, gamma, beta = _norm_inputs(rng, M, N, K)
+    eps = 1e-5
+    H, Y = _run_norm(oracle, A, B, bias, res, gamma, beta if norm == "layernorm" else None, norm, eps)
+    h = torch.from_numpy(A.astype(np.float64)) @ torch.from_numpy(B.astype(np.float64)) \
+        + torch.from_numpy(bias.astype(np.float64))[:, None] + torch.from_numpy(res.astype(np.float64))
+    g = torch.from_numpy(gamma.astype(np.float64))
+    if norm == "layernorm":
+        y = F.layer_norm(h.T, (M,), g, torch.from_numpy(beta.astype(np.float64)), eps).T
+    else:
+        y = F.rms_norm(h.T, (M,), g, eps).T
+    y = y.numpy()
+    half_step = np.spacing(np.abs(y).astype(np.float16)).astype(np.float64) / 2
+    assert (np.abs(Y - y) <= half_step * (1 + 1e-6)).all(), "Y differs from the library norm"
+
+
 def test_norm_bf16(oracle):
     rng = np.random.default_rng(99)
     M, N, K = 16, 3, 5

@@ -94,7 +94,9 @@ struct GemmArgs {
 // split-K tail). multicast: the occupancy of that variant.
 int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps, int multicast);
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream);
-// out[i] = sum over j = 0..rows-1 (in order) of part[j * len + i], fp32.
+// out[i] = sum over j = 0..rows-1 of part[j * len + i] in fp32, in a fixed
+// order: for each w = 0..7 the rows j = w, w + 8, w + 16, ... are added in
+// turn, then the eight sums are added in w order (the same result every run).
 cudaError_t launch_bgrad_reduce(const float* part, long long rows, long long len, float* out,
                                 cudaStream_t stream);
 // tmZ: the zaux tensor map (GELU_AUX_BIAS; any valid map otherwise).

@@ -162,18 +162,8 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   const int64_t tile_m = pair ? 256 : 128;
   const long long num_m = (Mk + tile_m - 1) / tile_m;
   const long long num_n = (Nk + block_n - 1) / block_n;
-  if (pair == 2) {
-    // Multicast pairs: a unit is an M-tile x two N-tiles, run by a cluster
-    // of two pairs; no split-K tail.
-    const long long units = num_m * ((num_n + 1) / 2);
-    const long long clusters = tc_gemm_max_pairs(block_n, pl.num_sms, pl.epi_warps, 1) / 2;
-    c.group_m = static_cast<int>(num_m < 8 ? num_m : 8);
-    c.tail_start = static_cast<int>(units);
-    c.grid = static_cast<int>(4 * (units < clusters ? units : clusters));
-    return c;
-  }
   const long long tiles = num_m * num_n;
-  const long long workers = pair ? tc_gemm_max_pairs(block_n, pl.num_sms, pl.epi_warps, 0) : pl.num_sms;
+  const long long workers = pair ? tc_gemm_max_pairs(block_n, pl.num_sms, pl.epi_warps) : pl.num_sms;
   c.group_m = static_cast<int>(num_m < (pair ? 8 : 16) ? num_m : (pair ? 8 : 16));
   if (const char* env = std::getenv("GE_GROUP_M")) {  // rasterisation sweeps
     const long long g = std::atoll(env);
@@ -280,8 +270,8 @@ ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D, void* Z)
   const uint64_t Nk = pl->swap ? pl->M : pl->N;
   const uint64_t K = pl->K;
   bool ok = true;
-  if (!a_mn)  // multicast pairs load 64 of a CTA's 128 A rows each
-    ok &= make_map(&pl->tmA, pl->bf16, Ak, K, Mk, lda, 64, pl->pair == 2 ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!a_mn)
+    ok &= make_map(&pl->tmA, pl->bf16, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     ok &= make_map(&pl->tmA, pl->bf16, Ak, Mk, K, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!b_mn)
@@ -570,9 +560,6 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       if (env[0] == '0') tc_pair = 0;
       if (env[0] == '1') tc_pair = 1;
     }
-    // Pairs of pairs that share A slices by multicast: opt-in for now.
-    if (const char* env = std::getenv("GE_MULTICAST"))
-      if (env[0] == '1' && tc_pair == 1 && tc_block_n == 256 && !dw_mask) tc_pair = 2;
     if (const char* env = std::getenv("GE_SPLIT_TAIL"))
       if (env[0] == '0') tc_split = false;
     if (backward) tc_split = false;  // their bias-gradient partials are per tile
@@ -853,7 +840,6 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
         if (c.split > 1) cands[n++] = c;
       }
     }
-  if (pl->epi != GE_EPI_DW_DRELU_BGRAD) cands[n++] = tc_config(*pl, 256, 2, false);  // pairs sharing A by multicast
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
     cudaGetLastError();

@@ -232,12 +232,7 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
   }
 }
 
-// MCA (pairs only): clusters of 4 CTAs = two pairs on adjacent N-tiles of
-// one 256-row M-tile. Each CTA loads half of its 128 A rows and multicasts
-// them to the CTA holding the same rows in the other pair, so the A slice
-// crosses L2 once for both pairs; a stage is refilled only when both pairs'
-// MMAs have released it.
-template <int BN, bool PAIR, int EPIW, bool MCA = false, bool AM = false>
+template <int BN, bool PAIR, int EPIW, bool AM = false>
 __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
@@ -264,14 +259,13 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // CTA within the cluster
   const uint32_t pr = rank & 1u;                         // CTA within its pair
-  const uint32_t pp = MCA ? rank >> 1 : 0u;              // pair within the cluster
   const uint32_t lead = rank & ~1u;                      // the pair's MMA-issuing CTA
   const bool leader = pr == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), MCA ? 2 : 1);  // MCA: both pairs release a stage
+      mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -313,19 +307,13 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
 
   const int num_m = (p.Mk + C::TILE_M - 1) / C::TILE_M;
   const int num_n = (p.Nk + BN - 1) / BN;
-  // MCA: a unit is one M-tile x two adjacent N-tiles; pair pp takes N-tile
-  // 2 * column + pp (past the last N-tile its outputs are simply not stored).
-  const int num_cols = MCA ? (num_n + 1) / 2 : num_n;
-  const int num_tiles = num_m * num_cols;
+  const int num_tiles = num_m * num_n;
   const int num_kb = (p.K + BK - 1) / BK;
   const int num_units = p.tail_start + (num_tiles - p.tail_start) * p.split;
-  constexpr int CL = MCA ? 4 : (PAIR ? 2 : 1);  // CTAs per cluster
+  constexpr int CL = PAIR ? 2 : 1;  // CTAs per cluster
   const int first_tile = static_cast<int>(blockIdx.x) / CL;
   const int tile_step = static_cast<int>(gridDim.x) / CL;
-  auto coords = [&](int tile, int& mt, int& nt) {
-    tile_coords(tile, num_m, num_cols, p.group_m, mt, nt);
-    if (MCA) nt = 2 * nt + static_cast<int>(pp);
-  };
+  auto coords = [&](int tile, int& mt, int& nt) { tile_coords(tile, num_m, num_n, p.group_m, mt, nt); };
   bool aborted_here = false;
 
   if (warp == 0) {
@@ -370,15 +358,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           // AM: the mask words of k-rows k0.. for this CTA's A' rows row0..
           // (row0 is a multiple of 128, so the word coordinate is 16-byte aligned)
           if constexpr (AM) load(sbase + C::OFF_MASK + stage * C::MASK_SLOT, &tmZ, row0 / 32, k0);
-          if constexpr (MCA) {
-            // this CTA's half of the A rows (64 of 128), for itself and the
-            // CTA with the same rows in the other pair
-            const uint16_t mask = static_cast<uint16_t>((1u << pr) | (1u << (pr + 2)));
-            if (!p.a_mn)
-              tma_load_2d_pair_mc(sa + 8192u * pp, &tmA, fb, k0, row0 + 64 * static_cast<int>(pp), mask);
-            else
-              tma_load_2d_pair_mc(sa + 8192u * pp, &tmA, fb, row0 + 64 * static_cast<int>(pp), k0, mask);
-          } else if (!p.a_mn) {
+          if (!p.a_mn) {
             load(sa, &tmA, k0, row0);
           } else {
             load(sa, &tmA, row0, k0);
@@ -463,10 +443,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             else
               tc_mma_f16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
-          // frees the stage (in both CTAs of a pair; MCA: in all four CTAs,
-          // whose A halves this pair also read) once these MMAs retire
+          // frees the stage (in both CTAs of a pair) once these MMAs retire
           if constexpr (PAIR)
-            tc_commit_pair_mc(empty_bar(stage), MCA ? 0xF : 0x3);
+            tc_commit_pair_mc(empty_bar(stage), 0x3);
           else
             tc_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
@@ -810,10 +789,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           for (int j = 0; j < 16; ++j) zw[j] = znext[j];
         }
       }
-      // (MCA: a pair whose N-tile lies past the last one has nothing to write)
-      if (backward && !p.bias_per_col && grow < p.Mk && nt < num_n)
+      if (backward && !p.bias_per_col && grow < p.Mk)
         p.bg_partials[static_cast<long long>(C::HALVES * nt + hh) * p.Mk + grow] = bg_row;
-      if (p.epi == EPI_BIAS_RESIDUAL && p.nstats && grow < p.Mk && nt < num_n)
+      if (p.epi == EPI_BIAS_RESIDUAL && p.nstats && grow < p.Mk)
         p.nstats[static_cast<long long>(C::HALVES * nt + hh) * p.Mk + grow] = make_float2(st_mean, st_m2);
       tc_fence_before();
       __syncwarp();
@@ -850,7 +828,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   }
 }
 
-template <int BN, bool PAIR, int EPIW, bool MCA = false, bool AM = false>
+template <int BN, bool PAIR, int EPIW, bool AM = false>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
   using C = Cfg<BN, PAIR, EPIW, AM>;
@@ -859,11 +837,11 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA, AM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, AM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if constexpr (PAIR) {
-      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, MCA, AM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, AM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       cudaGetLastError();
     }
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -876,13 +854,13 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   cudaLaunchAttribute attr[1];
   if constexpr (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = MCA ? 4 : 2;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, MCA, AM>, tmA, tmB, tmD, tmZ, args);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, AM>, tmA, tmB, tmD, tmZ, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -935,9 +913,8 @@ __global__ void __launch_bounds__(256) tc_gemm_fixup_kernel(const GemmArgs p, in
   }
 }
 
-// Largest number of CTA pairs of the pair kernel that can be resident (MCA:
-// in 4-CTA clusters).
-template <int BN, int EPIW, bool MCA>
+// Largest number of CTA pairs of the pair kernel that can be resident.
+template <int BN, int EPIW>
 int max_pairs(int num_sms) {
   static std::atomic<int> cached[64] = {};
   int dev = 0;
@@ -946,38 +923,34 @@ int max_pairs(int num_sms) {
     return num_sms / 2;
   }
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW, MCA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        Cfg<BN, true, EPIW>::SMEM_BYTES);
-  if (MCA) cudaFuncSetAttribute(tc_gemm_kernel<BN, true, EPIW, MCA>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   cudaGetLastError();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(MCA ? (num_sms & ~3) : (num_sms & ~1)), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
   cfg.blockDim = dim3(Cfg<BN, true, EPIW>::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg<BN, true, EPIW>::SMEM_BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = MCA ? 4 : 2;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true, EPIW, MCA>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, true, EPIW>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
-    n = MCA ? num_sms / 4 : num_sms / 2;
+    n = num_sms / 2;
   }
-  n = MCA ? 2 * n : n;  // pairs
   if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
 
 }  // namespace
 
-int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps, int multicast) {
-  if (multicast && block_n == 256)
-    return epi_warps == 8 ? max_pairs<256, 8, true>(num_sms) : max_pairs<256, 4, true>(num_sms);
-  if (epi_warps == 8) return block_n == 256 ? max_pairs<256, 8, false>(num_sms) : max_pairs<128, 8, false>(num_sms);
-  return block_n == 256 ? max_pairs<256, 4, false>(num_sms) : max_pairs<128, 4, false>(num_sms);
+int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps) {
+  if (epi_warps == 8) return block_n == 256 ? max_pairs<256, 8>(num_sms) : max_pairs<128, 8>(num_sms);
+  return block_n == 256 ? max_pairs<256, 4>(num_sms) : max_pairs<128, 4>(num_sms);
 }
 
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream) {
@@ -1010,18 +983,17 @@ cudaError_t launch_width(int block_n, int pair, const CUtensorMap& tmA, const CU
                          const CUtensorMap& tmD, const CUtensorMap& tmZ, const GemmArgs& args, int grid,
                          cudaStream_t stream) {
   if constexpr (EPIW == 4) {
-    if (args.amask) {  // four epilogue warps, no multicast
+    if (args.amask) {  // four epilogue warps
       if (pair) {
-        if (block_n == 256) return launch_impl<256, true, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
-        return launch_impl<128, true, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+        if (block_n == 256) return launch_impl<256, true, 4, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+        return launch_impl<128, true, 4, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
       }
-      if (block_n == 256) return launch_impl<256, false, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
-      return launch_impl<128, false, 4, false, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+      if (block_n == 256) return launch_impl<256, false, 4, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
+      return launch_impl<128, false, 4, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
     }
   } else {
     if (args.amask) return cudaErrorInvalidValue;
   }
-  if (pair == 2 && block_n == 256) return launch_impl<256, true, EPIW, true>(tmA, tmB, tmD, tmZ, args, grid, stream);
   if (pair) {
     if (block_n == 256) return launch_impl<256, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
     return launch_impl<128, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);

@@ -89,10 +89,7 @@ struct GemmArgs {
 // or 8 epilogue warps (8: two per TMEM lane quarter on alternate slabs; the
 // D*_BGRAD row partials and the norm statistics then have two halves per
 // n-tile).
-// pair = 2 (block_n 256 only): pairs in clusters of 4 that multicast their A
-// slices to each other (the unit is one 256-row M-tile x two N-tiles; no
-// split-K tail). multicast: the occupancy of that variant.
-int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps, int multicast);
+int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps);
 cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream);
 // out[i] = sum over j = 0..rows-1 of part[j * len + i] in fp32, in a fixed
 // order: for each w = 0..7 the rows j = w, w + 8, w + 16, ... are added in

@@ -210,18 +210,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 
 // Pair (cta_group::2) forms: one warp of each CTA of the pair executes the
 // alloc / relinquish / dealloc together.
-// Pair load multicast: the box lands at the same shared-memory offset in
-// every CTA of cta_mask, and each destination's bytes are counted on the
-// barrier at offset `bar` of that destination's pair-leader CTA.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* desc, uint32_t bar,
-                                                    int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
                "r"(ncols)
@@ -250,7 +238,8 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
 }
 
 // Arrive once on the barrier at offset `bar` in every CTA of `cta_mask` when
-// the pair's tcgen05 operations issued so far by this thread have completed.
+// the pair's tcgen05 operations issued so far by this thread have completed
+// (a completion signal to the pair's own barriers; it moves no data).
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

@@ -48,8 +48,6 @@
  *
  * Environment (read by ge_plan_create, for tuning sweeps; unset in normal
  * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
- * GE_MULTICAST = 1 turns 2-SM pairs of 256-wide tiles into clusters of four
- * that share their A slices by TMA multicast (not for DW_DRELU_BGRAD);
  * GE_SPLIT_TAIL = 0 disables the split-K tail; GE_EPI_WARPS = 4 | 8 forces the
  * epilogue width; GE_GROUP_M = g sets how many M-tiles the tile order sweeps
  * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits.
@@ -304,8 +302,7 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
  * ge_plan_autotune: choose the plan's kernel configuration by timing.
  * Planning picks a configuration from the problem's shape; this call instead
  * runs every candidate of the tensor-core path (128- or 256-column tiles,
- * single-CTA or 2-SM pair tiles, with and without the split-K tail, and pair
- * clusters sharing A by multicast) `reps` times on the caller's buffers
+ * single-CTA or 2-SM pair tiles, with and without the split-K tail) `reps` times on the caller's buffers
  * (same meaning as ge_execute), keeps the fastest for every later execute,
  * and finishes with one execute in that configuration, so D / aux / bias
  * hold its results. It blocks the host until
@@ -330,8 +327,7 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B,
 void ge_autotune_cache_clear(void);
 
 /* The plan's tensor-core configuration: tile width, 2-SM pair mode (0: one
- * CTA per 128-row tile; 1: CTA pairs on 256-row tiles; 2: pairs in clusters
- * of four that share A slices by multicast) and split-K pieces of the tail
+ * CTA per 128-row tile; 1: CTA pairs on 256-row tiles) and split-K pieces of the tail
  * (1 = none); zeros for other paths. Any pointer may be NULL. Returns the
  * path, or -1 for a NULL plan. */
 int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split);

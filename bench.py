@@ -115,6 +115,17 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def choose_tensor_peak(peaks, timed_s: float, clocks):
+    """The measured tensor peak a kernel timed in a region of `timed_s`
+    seconds is held to: the sustained figure (a seconds-long loop under the
+    power cap) only when the region lasted at least a second and the clock
+    record saw the power cap; otherwise the burst figure.
+    Returns (peak, sustained?, power cap seen?)."""
+    capped = bool(clocks) and "sw_power_cap" in (clocks.get("reasons") or [])
+    sustained = timed_s >= 1.0 and capped
+    return (peaks["tflops_sustained"] if sustained else peaks["tflops"]), sustained, capped
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
 
@@ -518,6 +529,230 @@ def run_bwd_gemm_drelu(args, rank, unfused):
         print(json.dumps(line), flush=True)
 
 
+# Every workload config, timed alone: key -> (workload key, dtype)
+CONFIG_TABLE = (("cfg_c1", "c1"), ("cfg_c2_bias", "c2_bias"), ("cfg_c2_relu_bias", "c2_relu_bias"),
+                ("cfg_c2_gelu_bias", "c2_gelu_bias"), ("cfg_c3_T1", "c3_T1"), ("cfg_c3_T512", "c3_T512"),
+                ("cfg_c3_T2048", "c3_T2048"), ("cfg_c4_fwd", "c4_fwd"), ("cfg_c4_bwd", "c4_bwd"),
+                ("cfg_c4_dw", "c4_dw"), ("cfg_c5", "c5"))
+# configs whose launch lasts microseconds: their per-launch event time holds
+# the launch and event overhead, so the device time is also taken from CUDA
+# graph replays
+_MICRO = ("cfg_c1", "cfg_c2_bias", "cfg_c2_relu_bias", "cfg_c2_gelu_bias", "cfg_c3_T1", "cfg_c3_T512",
+          "cfg_c3_T2048")
+
+
+def _pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, max(0, int(math.ceil(q * len(xs))) - 1))]
+
+
+def _graph_device_ms(run, flush_fn, reps, rounds=5):
+    """Device time of one `run()` from CUDA graph replays: a graph of `reps`
+    (flush, run) pairs minus a graph of `reps` flushes, per run; the median of
+    `rounds` replays. None if capture fails."""
+    import torch
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):  # warm the captured calls outside capture
+            flush_fn()
+            run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g_both, g_flush = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_both):
+            for _ in range(reps):
+                flush_fn()
+                run()
+        with torch.cuda.graph(g_flush):
+            for _ in range(reps):
+                flush_fn()
+        torch.cuda.synchronize()
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+    stream = torch.cuda.current_stream()
+    out = []
+    for _ in range(rounds):
+        t = []
+        for g in (g_both, g_flush):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g.replay()  # warm
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        out.append((t[0] - t[1]) / reps)
+    del g_both, g_flush
+    return statistics.median(out)
+
+
+def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
+    """Every workload config alone on this GPU: per-launch CUDA-event times
+    after a read-only L2 flush (median and p90 over >= 50 launches after 10
+    warm-ups; the 17.6-TFLOP config 5 over 10), the roofline of each config
+    (the faster of the tensor peak and its bytes at the copy rate), the same
+    engine's unfused three-kernel sequence, and for microsecond launches the
+    device time from graph replays. Returns (entries, cpu_inputs) where
+    cpu_inputs are host copies of the inputs the oracle baselines use."""
+    import torch
+    import gemm_epilogues_gb300 as ge
+    from gemm_epilogues_gb300.inputs import f16_tensor, pages_workloads, sample_rows
+    stream = torch.cuda.current_stream()
+    works = pages_workloads()
+    major = {"k": ge.GE_K_MAJOR, "m": ge.GE_MN_MAJOR, "n": ge.GE_MN_MAJOR}
+    tpk = peaks["tflops"] * 1e12  # burst: each config is timed alone, briefly
+    hbm = peaks["hbm_gbs"] * 1e9
+    out, cpu_in = {}, {}
+
+    def timed(fn, warm, reps):
+        ts = []
+        for i in range(warm + reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= warm:
+                ts.append(e0.elapsed_time(e1))
+        return ts
+
+    for key, wk in CONFIG_TABLE:
+        big = key == "cfg_c5"
+        warm, reps = (3, 10) if big else (10, 50)
+        if wk == "c4_bwd":
+            # DRELU_BGRAD on dY[8192 tokens, 11008]: mask words drawn at random
+            M, N = D_OUT, T_TOK
+            dY = f16_tensor((N, M), 3004, "normal", 1.0, dev)
+            ld_aux = (M + 127) // 128 * 4
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(3005)
+            aux = torch.randint(-2**31, 2**31 - 1, (N * ld_aux,), generator=gen, device=dev, dtype=torch.int32)
+            dZ = torch.empty_like(dY)
+            bgrad = torch.empty(M, dtype=torch.float32, device=dev)
+            plan = ge.Plan(M, N, 0, ge.GE_EPI_DRELU_BGRAD, ge.make_layout(d=ge.GE_D_COL))
+            run = lambda: plan.execute(dY, None, bgrad, dZ, aux, stream)
+            ts = timed(run, warm, reps)
+            assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
+            nbytes = 2 * N * M * 2 + 4 * N * ld_aux + 4 * M
+            med = statistics.median(ts)
+            out[key] = {"workload": f"DRELU_BGRAD dY[{N},{M}] + mask -> dZ, fp32 bgrad[{M}]", "path": "drelu",
+                        "ms": med, "p90_ms": _pct(ts, 0.9), "reps": reps, "gbs": nbytes / (med * 1e-3) / 1e9,
+                        "algorithmic_bytes": nbytes, "bound": "hbm",
+                        "frac_of_roofline": nbytes / hbm / (med * 1e-3), "roofline_gbs": peaks["hbm_gbs"]}
+            if keep_cpu_inputs:
+                cpu_in[key] = (dY.cpu(), aux.cpu(), M, N, ld_aux)
+            plan.free()
+            del dY, aux, dZ, bgrad
+            continue
+        w = works[wk]
+        A, B, bias = w.make(dev)
+        L = ge.make_layout(major[w.a_major], major[w.b_major],
+                           ge.GE_D_ROW if w.d_layout == "row" else ge.GE_D_COL)
+        plan = ge.Plan(w.M, w.N, w.K, ge.EPILOGUE_BY_NAME[w.epilogue], L)
+        if plan.path == ge.GE_PATH_GEMV:
+            plan.set_attr(ge.GE_ATTR_STATIC_A, 1)  # decode weights: never written upstream
+        D = torch.empty(w.d_shape(), dtype=A.dtype, device=dev)
+        aux = torch.empty(max(plan.aux_bytes // 4, 1), dtype=torch.int32, device=dev)
+        bias_arg = bias if w.epilogue != "none" else None
+        aux_arg = aux if w.epilogue == "relu_aux_bias" else None
+        # (the stream is looked up at each call: graph capture runs on its own)
+        run = lambda: plan.execute(A, B, bias_arg, D, aux_arg, torch.cuda.current_stream())
+        ts = timed(run, warm, reps)
+        assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
+        med = statistics.median(ts)
+        flops, nbytes = w.flops, w.algorithmic_bytes()
+        t_roof = max(flops / tpk, nbytes / hbm)
+        path, tile_n, pair, split = plan.config
+        e = {"workload": w.name, "path": {ge.GE_PATH_GEMV: "gemv", ge.GE_PATH_TC_GEMM: "tcgen05"}.get(path, path),
+             "tile_n": tile_n, "pair": pair, "split": split,
+             "ms": med, "p90_ms": _pct(ts, 0.9), "min_ms": min(ts), "reps": reps,
+             "tflops": flops / (med * 1e-3) / 1e12, "gbs": nbytes / (med * 1e-3) / 1e9,
+             "flops": flops, "algorithmic_bytes": nbytes,
+             "bound": "hbm" if nbytes / hbm > flops / tpk else "tensor",
+             "roofline_tflops": flops / t_roof / 1e12, "frac_of_roofline": t_roof / (med * 1e-3),
+             "frac_of_tensor_peak": flops / (med * 1e-3) / tpk}
+        if key in _MICRO:
+            g = _graph_device_ms(run, flush.zero_, 20)
+            if g is not None and g > 0:
+                e["graph_device_ms"] = g
+                e["graph_frac_of_roofline"] = t_roof / (g * 1e-3)
+        if w.epilogue != "none":
+            urun = lambda: plan.execute_unfused(A, B, bias_arg, D, aux_arg, torch.cuda.current_stream())
+            uts = timed(urun, 2 if big else 5, 5 if big else 30)
+            assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
+            e["unfused_ms"] = statistics.median(uts)
+            e["fused_speedup"] = e["unfused_ms"] / med
+        out[key] = e
+        if keep_cpu_inputs:
+            # inputs of the oracle baseline: whole problems up to config 3,
+            # 256 sampled stored rows of D for the others
+            if wk in ("c4_fwd", "c4_dw", "c5"):
+                rows_total = w.N if w.d_layout == "col" else w.M
+                idx = torch.as_tensor(sample_rows(rows_total, 256), device=dev)
+                if wk == "c4_fwd":  # stored rows = tokens = rows of X
+                    cpu_in[key] = ("sample", A.cpu(), B.index_select(0, idx).cpu(), bias.cpu(), w, rows_total)
+                elif wk == "c4_dw":  # stored rows = features = columns of the M-major A
+                    cpu_in[key] = ("sample", A.index_select(1, idx).contiguous().cpu(), B.cpu(),
+                                   None, w, rows_total)
+                else:  # stored rows = rows of A
+                    cpu_in[key] = ("sample", A.index_select(0, idx).cpu(), B.cpu(),
+                                   bias.index_select(0, idx).cpu(), w, rows_total)
+            else:
+                cpu_in[key] = ("full", A.cpu(), B.cpu(), bias.cpu(), w, None)
+        plan.free()
+        del A, B, bias, D, aux
+        torch.cuda.empty_cache()
+    return out, cpu_in
+
+
+def oracle_config_baselines(cpu_in):
+    """The oracle (fp64, the host's cores) on each config: whole problems for
+    configs 1-3 and the DRELU_BGRAD pass, 256 sampled rows of D for the
+    config-4 GEMMs and config 5 (the rate scaled to the whole problem by the
+    ratio of rows, which the oracle's row-parallel loop makes linear)."""
+    import numpy as np
+    import torch
+    from oracle import oracle
+    oracle.build()
+    thr = os.cpu_count() or 1
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    out = {}
+    for key, v in cpu_in.items():
+        if key == "cfg_c4_bwd":
+            dY, aux, M, N, ld_aux = v
+            dyb, auxw = bits(dY), aux.numpy().view(np.uint32)
+            t0 = time.perf_counter()
+            oracle.drelu_bgrad(dyb, auxw, M, N, d_layout="col", ld_aux=ld_aux)
+            dt = time.perf_counter() - t0
+            nbytes = 2 * N * M * 2 + 4 * N * ld_aux + 4 * M
+            out[key] = {"gbs": nbytes / dt / 1e9, "s": dt, "sample": "whole problem", "threads": 1}
+            continue
+        kind, A, B, bias, w, rows_total = v
+        Ab, Bb = bits(A), bits(B)
+        bb = None if bias is None else bits(bias)
+        M, N = w.M, w.N
+        if kind == "sample":  # the sampled stored rows of D
+            if w.d_layout == "col":
+                N = B.shape[0] if w.b_major == "k" else B.shape[1]
+            else:
+                M = A.shape[1] if w.a_major == "m" else A.shape[0]
+        n_s = N if w.d_layout == "col" else M
+        t0 = time.perf_counter()
+        oracle.linear_forward(Ab, Bb, bb, w.epilogue, M, N, w.K, a_major=w.a_major, b_major=w.b_major,
+                              d_layout=w.d_layout, threads=thr)
+        dt = time.perf_counter() - t0
+        flops = 2.0 * M * N * w.K
+        e = {"tflops": flops / dt / 1e12, "s": dt, "threads": thr,
+             "sample": "whole problem" if kind == "full" else f"{n_s} of {rows_total} stored rows of D"}
+        if kind == "sample":
+            e["extrapolated_s"] = dt * rows_total / n_s
+        out[key] = e
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     import gemm_epilogues_gb300 as ge
@@ -691,15 +926,24 @@ def run_ours(args, world, rank, local):
     kern["decode_gemv_gelu_bias"]["event_launch_floor_ms"] = sorted(floor[5:])[len(floor[5:]) // 2]
     dominant = max(("fwd_gemm_relu_aux_bias", "dw_gemm"), key=lambda k: kern[k]["ms"])
     achieved = kern[dominant]["tflops"]
-    # The GEMMs are timed inside the step loop (hundreds of back-to-back
-    # steps under the power cap), so the sustained measured peak applies; the
-    # burst figure is kept beside it.
-    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peaks["tflops_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["tflops_sustained"],
-                "traffic": captured_traffic(dominant),
-                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside the step loop; "
-                               "fp16 tensor rate = bf16)",
-                "burst_peak": peaks["tflops"], "frac_of_burst": achieved / peaks["tflops"]}
+    # Which measured peak applies follows from this run's own clock record:
+    # the sustained figure (a seconds-long loop under the power cap) only
+    # when the timed region itself lasted seconds and the power cap was seen
+    # in it; otherwise the burst figure.
+    timed_s = sum(tot) * 1e-3
+    peak, sustained, capped = choose_tensor_peak(peaks, timed_s, clk)
+    traffic = captured_traffic(dominant)
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the "
+                                   "committed capture of the same kernel source" if traffic else
+                                   "none: the kernel source changed since the last capture"),
+                "peak_source": (f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'} "
+                                f"(fp16 tensor rate = bf16; timed region {timed_s:.3f} s, "
+                                f"sw_power_cap {'seen' if capped else 'not seen'})"),
+                "burst_peak": peaks["tflops"], "sustained_peak": peaks["tflops_sustained"],
+                "frac_of_burst": achieved / peaks["tflops"],
+                "frac_of_sustained": achieved / peaks["tflops_sustained"]}
 
     # ---- baselines and the back-to-back decode measurement (outside the step)
     # (1) the unfused three-kernel sequence on the forward's inputs
@@ -877,6 +1121,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     link_ms = reduce_max(ev0.elapsed_time(ev1) / e_steps, world)
 
+    # ---- every workload config alone (one GPU; replicas skip it)
+    configs, cfg_cpu_in = None, {}
+    if world == 1 and not args.no_configs:
+        configs, cfg_cpu_in = run_config_table(dev, peaks, flush, keep_cpu_inputs=not args.no_cpu_baseline)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rows = 4096
@@ -884,6 +1133,9 @@ def run_ours(args, world, rank, local):
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                "sample": f"forward GEMM on {rows} of {T_TOK} tokens (all 11008 outputs, K=4096), "
                          f"{dt:.1f} s wall"}
+        if cfg_cpu_in:
+            cpu["configs"] = oracle_config_baselines(cfg_cpu_in)
+            cfg_cpu_in = None
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -893,7 +1145,7 @@ def run_ours(args, world, rank, local):
                 "config": {"workload": WORKLOAD, "tokens": T_TOK, "d_in": D_IN, "d_out": D_OUT,
                            "decode_hidden": D_DEC, "l2": "flushed between timed steps (read-only pass over 2x L2)",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-                "kernels": kern, "roofline": roofline, "cpu_baseline": cpu,
+                "kernels": kern, "configs": configs, "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "overlap": "inputs of step i+1 copied and results of step i read back on "
@@ -914,6 +1166,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the table of every workload config")
     ap.add_argument("--case", default="step",
                     choices=["step", "fwd", "bwd", "dw", "gemv", "fwd_unfused"] + sorted(CONFIG_CASES)
                     + sorted(ROW_CASES),

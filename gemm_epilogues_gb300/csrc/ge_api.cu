@@ -67,8 +67,10 @@ struct Plan {
   const void* mapD = nullptr;
   const void* mapZ = nullptr;
   CUtensorMap tmA{}, tmB{}, tmD{}, tmZ{};
-  // last pointers whose device was verified
+  // last pointers whose device was verified, and the driver's id of the
+  // allocation each one was in at the time
   const void* checked[6] = {};
+  unsigned long long checked_id[6] = {};
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -112,9 +114,36 @@ bool epi_has_bias(ge_epilogue_t e) {
          e == GE_EPI_RELU_AUX_BIAS || e == GE_EPI_GELU_ERF_BIAS || e == GE_EPI_GELU_AUX_BIAS;
 }
 
-// Verify that `p` is device memory of the plan's device (cached per slot).
+// The driver's unique id of the allocation holding `p` (0 if unknown): a
+// pointer value freed and handed out again, possibly on another device of
+// the same address space, gets a new id.
+using PFN_pointerGetAttribute = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+unsigned long long buffer_id(const void* p) {
+  static PFN_pointerGetAttribute fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_pointerGetAttribute>(f);
+  });
+  unsigned long long id = 0;
+  if (!fn || fn(&id, CU_POINTER_ATTRIBUTE_BUFFER_ID, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) {
+    cudaGetLastError();
+    return 0;
+  }
+  return id;
+}
+
+// Verify that `p` is device memory of the plan's device. The result is
+// cached per slot for the same pointer in the same allocation; a pointer
+// whose allocation changed (freed and reallocated) is verified again.
 ge_status_t check_device(Plan* pl, int slot, const void* p) {
-  if (!p || pl->checked[slot] == p) return GE_OK;
+  if (!p) return GE_OK;
+  const unsigned long long id = buffer_id(p);
+  if (pl->checked[slot] == p && id != 0 && pl->checked_id[slot] == id) return GE_OK;
   cudaPointerAttributes at;
   cudaError_t e = cudaPointerGetAttributes(&at, p);
   if (e != cudaSuccess) {
@@ -125,6 +154,7 @@ ge_status_t check_device(Plan* pl, int slot, const void* p) {
     return GE_ERR_DEVICE_MISMATCH;
   if (at.device != pl->device) return GE_ERR_DEVICE_MISMATCH;
   pl->checked[slot] = p;
+  pl->checked_id[slot] = id;
   return GE_OK;
 }
 

@@ -369,3 +369,28 @@ def linear_norm(A, B, bias, res, gamma, beta, norm: str, M: int, N: int, K: int,
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return H, Y
+
+
+def decode_chain(As, biases, X, epilogue: str, M: int, N: int, *, dtype: str = "f16",
+                 threads: int | None = None):
+    """A stack of decode projections, each layer's stored output the next
+    layer's input (ops-nn MatMul fusion, "Why MatMul is the inference
+    bottleneck": a decode step carries one token's activations through one
+    weight matrix after another, each read once):
+
+        Y_0 = act(A_0 . X + b_0),   Y_l = act(A_l . Y_(l-1) + b_l),
+
+    every layer square (K = M) and computed by ``linear_forward`` (fp64,
+    rounded once to the element type), so layer l reads exactly the rounded
+    Y_(l-1). X is N tokens x M (a K-major B); each Y_l is stored like a
+    column-major D, N rows of M. ``As`` and ``biases`` list the layers' bit
+    patterns (a bias may be None for "none"). Returns the layers' outputs,
+    flat uint16 arrays of N*M."""
+    prev = _u16(X)
+    outs = []
+    for A, b in zip(As, biases):
+        r = linear_forward(A, prev, b, epilogue, M, N, M, a_major="k", b_major="k", d_layout="col",
+                           dtype=dtype, threads=threads)
+        outs.append(r["D"])
+        prev = r["D"]
+    return outs

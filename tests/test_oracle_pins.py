@@ -826,3 +826,68 @@ def test_dw_drelu_bgrad_brute_force(oracle):
                 want[m, n] = math.fsum(dZ[k, m] * float(X[k, n]) for k in range(K))
         assert np.array_equal(dW.reshape(M, N), want.astype(np.float16).view(np.uint16))
         assert np.allclose(bgrad, [math.fsum(dZ[:, m]) for m in range(M)], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- decode chain
+def _f16_bits(x):
+    return np.asarray(x, np.float16).view(np.uint16).reshape(-1)
+
+
+def test_decode_chain_permutation_then_its_transpose_is_identity(oracle):
+    """W0 = P (a permutation, not symmetric), W1 = P^T: layer 0 permutes the
+    token's features, layer 1 undoes it, exactly. A transposed weight, a
+    swapped layer order or a lost intermediate would fail."""
+    M, N = 7, 2
+    perm = np.array([3, 0, 6, 1, 5, 2, 4])
+    P = np.zeros((M, M))
+    P[np.arange(M), perm] = 1.0  # (P x)[i] = x[perm[i]]
+    X = np.arange(N * M, dtype=np.float64).reshape(N, M) - 5.0
+    y0, y1 = oracle.decode_chain([_f16_bits(P), _f16_bits(P.T)], [None, None], _f16_bits(X), "none", M, N)
+    assert np.array_equal(oracle.f16_decode(y0).reshape(N, M), X[:, perm])
+    assert np.array_equal(y1, _f16_bits(X))
+
+
+def test_decode_chain_bias_accumulates_through_identity_layers(oracle):
+    """W = I with a BIAS epilogue: Y_l = X + b_0 + ... + b_l (small integers,
+    exact in fp16)."""
+    M, N, L = 9, 3, 4
+    I = _f16_bits(np.eye(M))
+    rng = np.random.default_rng(5)
+    X = rng.integers(-4, 5, (N, M)).astype(np.float64)
+    bs = [rng.integers(-3, 4, M).astype(np.float64) for _ in range(L)]
+    outs = oracle.decode_chain([I] * L, [_f16_bits(b) for b in bs], _f16_bits(X), "bias", M, N)
+    acc = X.copy()
+    for l in range(L):
+        acc = acc + bs[l][None, :]
+        assert np.array_equal(oracle.f16_decode(outs[l]).reshape(N, M), acc)
+
+
+def test_decode_chain_relu_closed_form(oracle):
+    """W = I, bias -1, ReLU: Y_l = max(X - (l + 1), 0)."""
+    M, N, L = 6, 2, 3
+    X = np.array([[0, 1, 2, 3, 4, -2], [5, 6, -1, 2, 0, 9]], np.float64)
+    outs = oracle.decode_chain([_f16_bits(np.eye(M))] * L, [_f16_bits(-np.ones(M))] * L, _f16_bits(X),
+                               "relu_bias", M, N)
+    for l in range(L):
+        assert np.array_equal(oracle.f16_decode(outs[l]).reshape(N, M), np.maximum(X - (l + 1), 0))
+
+
+def test_decode_chain_matches_numpy_layer_by_layer(oracle):
+    """Random chain with tanh-GELU against an independent numpy computation:
+    fp64 product and bias, the tanh form of GELU, then numpy's own round to
+    nearest even fp16 before the next layer."""
+    M, N, L = 24, 2, 3
+    rng = np.random.default_rng(11)
+    Ws = [rng.standard_normal((M, M)).astype(np.float16) / np.float16(4) for _ in range(L)]
+    bs = [(rng.standard_normal(M) * 0.3).astype(np.float16) for _ in range(L)]
+    X = rng.standard_normal((N, M)).astype(np.float16)
+    outs = oracle.decode_chain([w.view(np.uint16).reshape(-1) for w in Ws],
+                               [b.view(np.uint16) for b in bs], X.view(np.uint16).reshape(-1),
+                               "gelu_bias", M, N)
+    x = X.astype(np.float64)
+    for l in range(L):
+        z = x @ Ws[l].astype(np.float64).T + bs[l].astype(np.float64)[None, :]
+        y = 0.5 * z * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (z + 0.044715 * z ** 3)))
+        y16 = y.astype(np.float16)
+        assert np.array_equal(outs[l], y16.view(np.uint16).reshape(-1)), f"layer {l}"
+        x = y16.astype(np.float64)

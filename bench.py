@@ -828,7 +828,13 @@ def run_ours(args, world, rank, local):
     if args.case != "step":
         # Profiling mode: only one kernel of the step, `steps` times after
         # `warmup` launches (each launch preceded by the L2 flush).
+        if args.case == "chain":  # the 32-layer decode stack of the bench line
+            Wc = [f16_tensor((D_DEC, D_DEC), 2200 + i, "normal", 1 / 64, dev) for i in range(32)]
+            bc = [f16_tensor((D_DEC,), 2300 + i, "normal", math.sqrt(0.02), dev) for i in range(32)]
+            Yc = torch.empty((32, 1, D_DEC), dtype=torch.float16, device=dev)
+            chain = ge.Plan(D_DEC, 1, D_DEC, ge.GE_EPI_GELU_BIAS, ge.make_layout(K_, K_, ge.GE_D_COL))
         one = {"fwd": lambda: fwd.execute(W, X, b, Y, aux, stream),
+               "chain": lambda: chain.execute_chain(Wc, bc, x1, Yc, stream),
                "fwd_unfused": lambda: fwd.execute_unfused(W, X, b, Y, aux, stream),
                "bwd": lambda: bwd.execute(dY, None, bgrad, dZ, aux, stream),
                "dw": lambda: dwp.execute(dZ, X, None, dW, None, stream),
@@ -1005,6 +1011,24 @@ def run_ours(args, world, rank, local):
                                         "launches": rounds * len(W2s), "weights": "8 x 33.5 MB rotating",
                                         "cuda_graph": graph_ok}
     del W2s
+    # (3) a stack of decode projections in one launch (ge_execute_chain):
+    # 32 layers of 4096 x 4096 (1.07 GB of weights, far more than L2), each
+    # layer's output the next layer's input, L2 flushed before each launch
+    CH = 32
+    Wc = [f16_tensor((D_DEC, D_DEC), 2200 + i, "normal", 1 / 64, dev) for i in range(CH)]
+    bc = [f16_tensor((D_DEC,), 2300 + i, "normal", math.sqrt(0.02), dev) for i in range(CH)]
+    Yc = torch.empty((CH, 1, D_DEC), dtype=torch.float16, device=dev)
+    chain = ge.Plan(D_DEC, 1, D_DEC, ge.GE_EPI_GELU_BIAS, ge.make_layout(K_, K_, ge.GE_D_COL))
+    ct = _time_flushed(lambda: chain.execute_chain(Wc, bc, x1, Yc, stream), 10, 3, dev)
+    assert ge.ge_get_last_device_error(chain.handle) == ge.GE_OK
+    chain.free()
+    ch_ms = statistics.median(ct) / CH
+    kern["decode_gemv_chain"] = {"ms": ch_ms, "gbs": bytes_dec / ch_ms / 1e6,
+                                 "frac_of_peak": bytes_dec / ch_ms / 1e6 / peaks["hbm_gbs"],
+                                 "layers_per_launch": CH, "launches": len(ct),
+                                 "launch_ms_median": statistics.median(ct),
+                                 "weights": f"{CH} x 33.5 MB, one cooperative launch, L2 flushed before each"}
+    del Wc, bc, Yc
     assert ge.ge_get_last_device_error(dec.handle) == ge.GE_OK
     assert ge.ge_get_last_device_error(fwd.handle) == ge.GE_OK
 
@@ -1168,7 +1192,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the table of every workload config")
     ap.add_argument("--case", default="step",
-                    choices=["step", "fwd", "bwd", "dw", "gemv", "fwd_unfused"] + sorted(CONFIG_CASES)
+                    choices=["step", "fwd", "bwd", "dw", "gemv", "fwd_unfused", "chain"] + sorted(CONFIG_CASES)
                     + sorted(ROW_CASES),
                     help="time one kernel of the step alone, or one of the workload configs")
     args = ap.parse_args()

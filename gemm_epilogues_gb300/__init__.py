@@ -71,7 +71,7 @@ ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
                  "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr",
                  "ge_plan_autotune", "ge_plan_config", "ge_execute_norm", "ge_execute_norm_unfused",
-                 "ge_autotune_cache_clear")
+                 "ge_autotune_cache_clear", "ge_execute_chain")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -137,6 +137,8 @@ def load_library():
         lib.ge_plan_autotune.restype = i32
         lib.ge_plan_config.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.ge_plan_config.restype = i32
+        lib.ge_execute_chain.argtypes = [vp, i64, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp, vp]
+        lib.ge_execute_chain.restype = i32
         lib.ge_version.argtypes = []
         lib.ge_version.restype = ctypes.c_char_p
         _lib = lib
@@ -217,6 +219,20 @@ def ge_execute_unfused(plan, A, B, bias, D, aux=None, stream=None, *, raw: bool 
     if raw:
         return st
     _check(st, "ge_execute_unfused")
+
+
+def ge_execute_chain(plan, As, biases, X, Y, stream=None, *, raw: bool = False):
+    """A stack of len(As) decode projections in one launch (see include/ge.h);
+    ``biases`` may be None for a NONE plan."""
+    n = len(As)
+    arr_a = (ctypes.c_void_p * max(n, 1))(*[_ptr(a) for a in As])
+    arr_b = None
+    if biases is not None:
+        arr_b = (ctypes.c_void_p * max(n, 1))(*[_ptr(b) for b in biases])
+    st = load_library().ge_execute_chain(plan, n, arr_a, arr_b, _ptr(X), _ptr(Y), _stream(stream))
+    if raw:
+        return st
+    _check(st, "ge_execute_chain")
 
 
 def ge_plan_set_attr(plan, attr: int, value: int, *, raw: bool = False):
@@ -305,6 +321,9 @@ class Plan:
     @property
     def config(self):
         return ge_plan_config(self.handle)
+
+    def execute_chain(self, As, biases, X, Y, stream=None):
+        ge_execute_chain(self.handle, As, biases, X, Y, stream)
 
     def execute_unfused(self, A, B, bias, D, aux=None, stream=None):
         ge_execute_unfused(self.handle, A, B, bias, D, aux, stream)

@@ -71,6 +71,9 @@ struct Plan {
   // allocation each one was in at the time
   const void* checked[6] = {};
   unsigned long long checked_id[6] = {};
+  // ge_execute_chain: the weight and bias pointers verified so far, with
+  // their allocations' ids
+  std::map<const void*, unsigned long long> chain_checked;
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -607,6 +610,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (dw_mask) tmp.epi_warps = 4;  // the masking warps take the place of four more
   }
   size_t ws = 256;
+  if (tmp.path == GE_PATH_GEMV) ws += static_cast<size_t>(kChainSyncWords) * 4;  // ge_execute_chain
   size_t bg_off = 0;
   if (tmp.path == GE_PATH_TC_GEMM && backward) {
     const int64_t Mk = tmp.swap ? N : M;
@@ -845,6 +849,61 @@ ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B
                           st) != cudaSuccess)
     return GE_ERR_CUDA;
   return launch_norm_pass(pl, gamma, beta, H, Y, eps, false, st);
+}
+
+ge_status_t ge_execute_chain(ge_plan_t plan, int64_t layers, const void* const* A, const void* const* bias,
+                             const void* X, void* Y, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_ERR_INVALID_ARG;
+  // a decode-sized plan whose layers can feed one another: square, the
+  // output stored like the next layer's input (D column-major: N rows of M)
+  if (pl->path != GE_PATH_GEMV || epi_is_norm(pl->epi) || pl->M != pl->K || pl->L.d != GE_D_COL)
+    return GE_ERR_UNSUPPORTED;
+  if (pl->K % 8 != 0 || pl->L.ldd % 8 != 0 || pl->L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
+  const int ring = gemv_chain_ring(static_cast<int>(pl->K), static_cast<int>(pl->N));
+  if (ring < 1) return GE_ERR_UNSUPPORTED;  // one weight row per warp does not fit in shared memory
+  if (layers < 1 || layers > kChainMaxLayers) return GE_ERR_INVALID_ARG;
+  const bool has_bias = pl->epi != GE_EPI_NONE;
+  if (!A || !X || !Y || (has_bias && !bias)) return GE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Y)) return GE_ERR_ALIGNMENT;
+  for (int64_t l = 0; l < layers; ++l) {
+    if (!A[l] || (has_bias && !bias[l])) return GE_ERR_INVALID_ARG;
+    if (!aligned16(A[l]) || (has_bias && (reinterpret_cast<uintptr_t>(bias[l]) & 1u))) return GE_ERR_ALIGNMENT;
+  }
+  ge_status_t s;
+  if ((s = check_device(pl, 1, X)) != GE_OK || (s = check_device(pl, 3, Y)) != GE_OK) return s;
+  for (int64_t l = 0; l < 2 * layers; ++l) {
+    const void* p = l < layers ? A[l] : (has_bias ? bias[l - layers] : nullptr);
+    if (!p) continue;
+    const unsigned long long id = buffer_id(p);
+    auto it = pl->chain_checked.find(p);
+    if (it != pl->chain_checked.end() && id != 0 && it->second == id) continue;
+    if ((s = check_device(pl, 5, p)) != GE_OK) return s;
+    if (pl->chain_checked.size() > 4096) pl->chain_checked.clear();
+    pl->chain_checked[p] = id;
+  }
+  ChainArgs c{};
+  c.layers = static_cast<int>(layers);
+  c.M = static_cast<int>(pl->M);
+  c.K = static_cast<int>(pl->K);
+  c.N = static_cast<int>(pl->N);
+  for (int64_t l = 0; l < layers; ++l) {
+    c.A[l] = static_cast<const unsigned short*>(A[l]);
+    c.bias[l] = has_bias ? static_cast<const unsigned short*>(bias[l]) : nullptr;
+  }
+  c.lda = pl->L.lda;
+  c.X = static_cast<const unsigned short*>(X);
+  c.ldx = pl->L.ldb;
+  c.Y = static_cast<unsigned short*>(Y);
+  c.ldy = pl->L.ldd;
+  c.epi = static_cast<int>(pl->epi);
+  c.bf16 = pl->bf16;
+  c.ring = ring;
+  c.err = pl->err;
+  c.sync = reinterpret_cast<unsigned int*>(static_cast<char*>(pl->ws) + 256);
+  c.budget = kWaitBudgetCycles;
+  const cudaError_t e = launch_gemv_chain(c, pl->num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 
 void ge_autotune_cache_clear(void) {

@@ -39,20 +39,6 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
-template <bool BF16>
-__device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc) {
-  const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-  const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 fa = to_f32x2(BF16, wa[i]);
-    const float2 fb = to_f32x2(BF16, wb[i]);
-    acc = fmaf(fa.x, fb.x, acc);
-    acc = fmaf(fa.y, fb.y, acc);
-  }
-  return acc;
-}
-
 // BF16 picks the element type of A, B, bias and D at compile time so that the
 // fp16 and bf16 inner loops each decode with one instruction per pair.
 template <int NT, int UNROLL, bool BF16, bool PF, bool PRE = false>

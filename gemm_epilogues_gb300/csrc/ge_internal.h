@@ -31,7 +31,8 @@ enum ErrBits : unsigned int {
   ERR_EPILOGUE_TIMEOUT = 4u,
   ERR_DRAIN_TIMEOUT = 8u,
   ERR_PROBE_TIMEOUT = 16u,
-  ERR_XFORM_TIMEOUT = 32u
+  ERR_XFORM_TIMEOUT = 32u,
+  ERR_CHAIN_TIMEOUT = 64u
 };
 
 // Kernel-level problem of the tensor-core GEMM: D'[Mk, Nk] (row-major, via
@@ -118,6 +119,36 @@ struct GemvArgs {
   int static_a;       // launch with programmatic dependent launch (A never written upstream)
 };
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
+
+// A stack of `layers` square decode projections in one cooperative launch:
+// Y_0 = act(A_0 . X + bias_0), Y_l = act(A_l . Y_(l-1) + bias_l), each Y_l
+// rounded to the element type. X is [N][ldx], layer l's output is
+// Y + l * N * ldy, [N][ldy] (N tokens of M = K features).
+constexpr int kChainMaxLayers = 64;
+// Synchronisation words of a chain in the plan workspace: one arrival
+// counter per layer, then the finished-block count and the abort flag; all
+// zero between launches (the last block to finish clears them).
+constexpr int kChainSyncWords = kChainMaxLayers + 2;
+struct ChainArgs {
+  int layers, M, K, N;
+  const unsigned short* A[kChainMaxLayers];     // [M][lda] each
+  const unsigned short* bias[kChainMaxLayers];  // [M] each; unused for EPI_NONE
+  long long lda;
+  const unsigned short* X;
+  long long ldx;
+  unsigned short* Y;
+  long long ldy;
+  int epi;
+  int bf16;
+  int ring;                 // weight-row slots per warp in shared memory
+  unsigned int* err;        // device error word
+  unsigned int* sync;       // kChainSyncWords words
+  long long budget;         // bounded-wait budget in SM clock cycles
+};
+// Weight-row slots per warp that fit in shared memory beside the staged
+// activations (0: a row of K elements does not fit).
+int gemv_chain_ring(int K, int N);
+cudaError_t launch_gemv_chain(const ChainArgs& args, int num_sms, cudaStream_t stream);
 
 // DRELU_BGRAD (gelu = 0: mask bits) or DGELU_BGRAD (gelu = 1: the stored
 // pre-activation zaux) on a stored matrix of R rows x C contiguous columns.

@@ -280,6 +280,41 @@ ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B
                                     const void* gamma, const void* beta, void* H, void* Y,
                                     float eps, void* stream);
 
+/*
+ * ge_execute_chain: a stack of decode projections in one launch (ops-nn
+ * MatMul fusion (codearts), "Why MatMul is the inference bottleneck": a
+ * decode step carries one token's activations through one weight matrix
+ * after another, and each costs the time to read its weights once from HBM).
+ * For a decode-sized plan (GE_PATH_GEMV: N <= 16, A and B K-major) that is
+ * square (M == K) with a column-major D (N rows of M features, the layout of
+ * the next layer's K-major B), and an epilogue in NONE / BIAS / RELU_BIAS /
+ * GELU_BIAS / GELU_ERF_BIAS:
+ *   Y_0 = act(A_0 . X + bias_0),   Y_l = act(A_l . Y_(l-1) + bias_l),
+ * every Y_l rounded to T and stored, and layer l reading exactly the stored
+ * Y_(l-1).
+ *   layers : 1 .. 64.
+ *   A      : host array of `layers` device pointers, T [M][lda] each (the
+ *            plan's A layout), 16-byte aligned (read only).
+ *   bias   : host array of `layers` device pointers, T [M] each, 2-byte
+ *            aligned (read only); may be NULL for NONE.
+ *   X      : T, N rows of K with the plan's ldb (read only), 16-byte aligned.
+ *   Y      : T, layer l's output at Y + l * N * ldd elements, N rows of M with
+ *            the plan's ldd; 16-byte aligned. Must not overlap X or weights.
+ * K, ldb and ldd must be multiples of 8. One cooperative launch runs every
+ * layer: each SM keeps its next weight rows -- of this layer and the
+ * following ones -- streaming into shared memory while the grid waits for
+ * the previous layer's outputs. The launch needs every SM of the device free
+ * of other work to start. Executes of one plan must be ordered on one stream
+ * (they share the plan's synchronisation words).
+ * Returns GE_OK, GE_ERR_UNSUPPORTED (plan not of this form, or K too large
+ * for one weight row per warp in shared memory: about 13,000 elements),
+ * GE_ERR_INVALID_ARG (layers out of range, a required pointer NULL),
+ * GE_ERR_ALIGNMENT, GE_ERR_DEVICE_MISMATCH or GE_ERR_CUDA. Device waits are
+ * bounded; an expired wait is reported by ge_get_last_device_error.
+ */
+ge_status_t ge_execute_chain(ge_plan_t plan, int64_t layers, const void* const* A,
+                             const void* const* bias, const void* X, void* Y, void* stream);
+
 /* Plan attributes (ge_plan_set_attr). */
 typedef enum {
   /* value 1: A is never written by work queued earlier on the execute's

@@ -394,7 +394,7 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
       g.bg_partials = g.bgrad ? pl->bg_partials : nullptr;
     }
     e = launch_tc_gemm(pl->block_n, pl->pair, pl->epi_warps, pl->tmA, pl->tmB, pl->tmD, pl->tmZ, g, pl->grid, st);
-    if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, st);
+    if (e == cudaSuccess && pl->split > 1) e = launch_tc_gemm_fixup(pl->block_n, pl->pair, g, pl->num_sms, st);
     if (e == cudaSuccess && amask && g.bgrad)
       e = launch_bgrad_reduce(pl->bg_partials, pl->split > 1 ? pl->split : 1, g.Mk, g.bgrad, st);
     if (e == cudaSuccess && backward) {

@@ -91,7 +91,7 @@ struct GemmArgs {
 // D*_BGRAD row partials and the norm statistics then have two halves per
 // n-tile).
 int tc_gemm_max_pairs(int block_n, int num_sms, int epi_warps);
-cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, cudaStream_t stream);
+cudaError_t launch_tc_gemm_fixup(int block_n, int pair, const GemmArgs& args, int num_sms, cudaStream_t stream);
 // out[i] = sum over j = 0..rows-1 of part[j * len + i] in fp32, in a fixed
 // order: for each w = 0..7 the rows j = w, w + 8, w + 16, ... are added in
 // turn, then the eight sums are added in w order (the same result every run).

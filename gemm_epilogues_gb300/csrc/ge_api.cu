@@ -603,6 +603,15 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     // faster with four (NONE 0.452 vs 0.478 ms on the same shape; the norm
     // fusion at 4096x8192x4096: 0.235 vs 0.241 ms).
     tmp.epi_warps = epi == GE_EPI_DGELU_BGRAD ? 8 : 4;
+    // A problem of at most one wave gives each CTA one tile: its epilogue
+    // cannot overlap another tile's MMAs and is on the critical path, so
+    // eight warps take it in half the time.
+    {
+      const long long tm = tc_pair ? 256 : 128;
+      const long long tiles = ((Mk + tm - 1) / tm) * ((Nk + tc_block_n - 1) / tc_block_n);
+      const long long workers = tc_pair ? tmp.num_sms / 2 : tmp.num_sms;
+      if (tiles <= workers) tmp.epi_warps = 8;
+    }
     if (const char* env = std::getenv("GE_EPI_WARPS")) {  // sweeps
       if (env[0] == '4') tmp.epi_warps = 4;
       if (env[0] == '8') tmp.epi_warps = 8;

@@ -625,8 +625,12 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
       // shuffles), the first now and each later one a slab ahead.
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = to_f32(bf16, bias16[grow]);
-      auto bias_lane = [&](int gc) { return has_bias && p.bias_per_col && gc < p.Nk ? to_f32(bf16, bias16[gc]) : 0.0f; };
-      float bl = bias_lane(nt * BN + 32 * hh + lane);
+      // (kept as loaded: converted when the slab uses it, so the load of
+      // the next slab's value does not stall this one)
+      auto bias_lane = [&](int gc) -> unsigned short {
+        return has_bias && p.bias_per_col && gc < p.Nk ? bias16[gc] : static_cast<unsigned short>(0);
+      };
+      unsigned short bl = bias_lane(nt * BN + 32 * hh + lane);
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.budget) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -687,13 +691,14 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           mword = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
         uint32_t znext[16];
         if (needs_z && c + C::HALVES < BN / 32) load_slab16(p, grow, gcol0 + 32 * C::HALVES, znext);
-        const float bl_next = bias_lane(gcol0 + 32 * C::HALVES + lane);
+        const unsigned short bl_next = bias_lane(gcol0 + 32 * C::HALVES + lane);
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_row + 32u * c, v);
         tmem_ld_wait();
         float bcol[32];
+        const float blf = to_f32(bf16, bl);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) bcol[j] = __shfl_sync(0xffffffffu, bl, j);
+        for (int j = 0; j < 32; ++j) bcol[j] = __shfl_sync(0xffffffffu, blf, j);
         bl = bl_next;
         uint32_t packed[16];
         uint32_t zpacked[16];

@@ -38,6 +38,7 @@ struct Plan {
   int block_n = 256;
   int pair = 0;  // 2-CTA (cta_group::2) tiles of 256 rows
   int epi_warps = 4;  // epilogue warps of the tensor-core kernel (4 or 8)
+  int kb = 64;        // k-values per pipeline stage (64 or 128)
   int tail_start = 0;  // split-K tail (see GemmArgs); `tail_ws` holds its pieces
   int split = 1;
   void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
@@ -106,6 +107,25 @@ bool make_map(CUtensorMap* m, int bf16, const void* base, uint64_t d0, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+// K-major 16-bit operand of `rows` rows with K = 64 * panels contiguous
+// elements (row pitch ld) seen as 3-D: 64 elements x rows x panels, so that
+// one box (64 x box_rows x box_panels, 128-byte swizzle) fetches several
+// 64-wide panels at once. Only for K a multiple of 64: a panel never runs
+// past the end of a row.
+bool make_map_panels(CUtensorMap* m, int bf16, const void* base, uint64_t rows, uint64_t panels, uint64_t ld,
+                     uint32_t box_rows, uint32_t box_panels) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, panels};
+  cuuint64_t strides[2] = {ld * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_panels};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool epi_is_norm(ge_epilogue_t e) {
@@ -164,8 +184,19 @@ ge_status_t check_device(Plan* pl, int slot, const void* p) {
 // Tensor-core launch configuration for a tile width and pair mode: work
 // units, grid, rasterisation group and the split-K tail.
 struct TcConfig {
-  int block_n = 256, pair = 0, split = 1, tail_start = 0, grid = 1, group_m = 1;
+  int block_n = 256, pair = 0, split = 1, tail_start = 0, grid = 1, group_m = 1, kb = 64;
 };
+
+// k-values per pipeline stage for a tile shape: 128 (two 64-wide panels per
+// operand box) when K is a multiple of 128 and a stage stays within 64 KB
+// (2-SM pairs, or 128-wide single-CTA tiles); 64 otherwise, and always for
+// the masked-operand weight gradient. GE_KB = 64 | 128 forces it (sweeps).
+int kb_for(const Plan& pl, int block_n, int pair) {
+  const bool fits = pl.K % 128 == 0 && (pair || block_n == 128) && pl.epi != GE_EPI_DW_DRELU_BGRAD;
+  if (const char* env = std::getenv("GE_KB"))
+    if (env[0] == '6') return 64;
+  return fits ? 128 : 64;
+}
 
 // Configurations chosen by ge_plan_autotune, per device, problem and layout:
 // a plan created later for the same key starts from the tuned choice.
@@ -190,6 +221,7 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   TcConfig c;
   c.block_n = block_n;
   c.pair = pair;
+  c.kb = kb_for(pl, block_n, pair);
   const int64_t Mk = pl.swap ? pl.N : pl.M;
   const int64_t Nk = pl.swap ? pl.M : pl.N;
   const int64_t tile_m = pair ? 256 : 128;
@@ -211,7 +243,7 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   // way: the fixup is launched as a programmatic dependent of the GEMM, so
   // its launch overlaps the GEMM (1024x512x2048 GELU_BIAS, 32 tiles: 25.0 ->
   // 21.9 us; 4096x128x4096: 34.0 -> 25.5 us).
-  const long long num_kb = (pl.K + 63) / 64;
+  const long long num_kb = (pl.K + c.kb - 1) / c.kb;
   const long long rem = tiles % workers;
   auto pieces = [&](long long t) {
     long long S = workers / t;
@@ -262,6 +294,7 @@ ge_status_t apply_config(Plan* pl, const TcConfig& c) {
   }
   pl->block_n = c.block_n;
   pl->pair = c.pair;
+  pl->kb = c.kb;
   pl->split = c.split;
   pl->tail_start = c.tail_start;
   pl->grid = c.grid;
@@ -303,15 +336,18 @@ ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D, void* Z)
   const uint64_t Nk = pl->swap ? pl->M : pl->N;
   const uint64_t K = pl->K;
   bool ok = true;
+  const uint32_t b_rows = static_cast<uint32_t>(pl->pair ? pl->block_n / 2 : pl->block_n);
+  const uint32_t kb = static_cast<uint32_t>(pl->kb);
   if (!a_mn)
-    ok &= make_map(&pl->tmA, pl->bf16, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= kb == 128 ? make_map_panels(&pl->tmA, pl->bf16, Ak, Mk, K / 64, lda, 128, 2)
+                    : make_map(&pl->tmA, pl->bf16, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   else
-    ok &= make_map(&pl->tmA, pl->bf16, Ak, Mk, K, lda, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&pl->tmA, pl->bf16, Ak, Mk, K, lda, 64, kb, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!b_mn)
-    ok &= make_map(&pl->tmB, pl->bf16, Bk, K, Nk, ldb, 64, pl->pair ? pl->block_n / 2 : pl->block_n,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= kb == 128 ? make_map_panels(&pl->tmB, pl->bf16, Bk, Nk, K / 64, ldb, b_rows, 2)
+                    : make_map(&pl->tmB, pl->bf16, Bk, K, Nk, ldb, 64, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   else
-    ok &= make_map(&pl->tmB, pl->bf16, Bk, Nk, K, ldb, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&pl->tmB, pl->bf16, Bk, Nk, K, ldb, 64, kb, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= make_map(&pl->tmD, pl->bf16, D, Nk, Mk, L.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (pl->epi == GE_EPI_DW_DRELU_BGRAD)  // the fourth map carries the mask words
     ok &= make_mask_map(&pl->tmZ, Z, static_cast<uint64_t>(L.ld_aux), K, static_cast<uint64_t>(L.ld_aux));
@@ -381,6 +417,7 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.bg_partials = pl->bg_partials;
     g.bf16 = pl->bf16;
     g.nstats = epi_code == EPI_BIAS_RESIDUAL ? pl->nstats : nullptr;
+    g.kb = pl->kb;
     const bool backward = epi_code == EPI_DRELU_BGRAD || epi_code == EPI_DGELU_BGRAD;
     g.bgrad = backward ? static_cast<float*>(const_cast<void*>(bias)) : nullptr;
     if (backward) g.bias = nullptr;

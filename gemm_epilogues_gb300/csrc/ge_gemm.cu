@@ -46,22 +46,27 @@ namespace ge {
 namespace {
 
 constexpr int BM = 128;            // accumulator rows = TMEM lanes
-constexpr int BK = 64;             // fp16 k-slice per stage (128 bytes)
+constexpr int BK = 64;             // 16-bit k-values in one 128-byte swizzle row (one panel)
 
 constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 fp16 columns
 
 // EPIW = epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
 // taking alternate 32-column slabs). AM = the A operand is masked in shared
 // memory by four more warps before the MMA reads it (DW_DRELU_BGRAD).
-template <int BN, bool PAIR, int EPIW, bool AM = false>
+// KB = k-values per stage: 64 (one panel) or 128 (two panels, each operand
+// fetched in one box of up to 32 KB: the TMA unit moves large boxes at a
+// higher rate than several small ones).
+template <int BN, bool PAIR, int EPIW, bool AM = false, int KB = 64>
 struct Cfg {
   static constexpr int EPI_WARPS = EPIW;
   static constexpr int XFORM_WARPS = AM ? 4 : 0;
   static constexpr int NUM_THREADS = 64 + 32 * EPIW + 32 * XFORM_WARPS;
   static constexpr int HALVES = EPIW / 4;  // warps per lane quarter
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns staged by one CTA
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static_assert(KB == 64 || (KB == 128 && !AM), "k-values per stage");
+  static constexpr int PANELS = KB / BK;
+  static constexpr int A_BYTES = BM * KB * 2;
+  static constexpr int B_BYTES = B_ROWS * KB * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
   static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
@@ -232,12 +237,12 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
   }
 }
 
-template <int BN, bool PAIR, int EPIW, bool AM = false>
+template <int BN, bool PAIR, int EPIW, bool AM = false, int KB = 64>
 __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
                    const GemmArgs p) {
-  using C = Cfg<BN, PAIR, EPIW, AM>;
+  using C = Cfg<BN, PAIR, EPIW, AM, KB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   const int num_m = (p.Mk + C::TILE_M - 1) / C::TILE_M;
   const int num_n = (p.Nk + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
-  const int num_kb = (p.K + BK - 1) / BK;
+  const int num_kb = (p.K + KB - 1) / KB;
   const int num_units = p.tail_start + (num_tiles - p.tail_start) * p.split;
   constexpr int CL = PAIR ? 2 : 1;  // CTAs per cluster
   const int first_tile = static_cast<int>(blockIdx.x) / CL;
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           }
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
-          const int k0 = kb * BK;
+          const int k0 = kb * KB;
           auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
             if constexpr (PAIR && !AM)
               tma_load_2d_pair(dst, map, fb, x, y);
@@ -358,17 +363,33 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           // AM: the mask words of k-rows k0.. for this CTA's A' rows row0..
           // (row0 is a multiple of 128, so the word coordinate is 16-byte aligned)
           if constexpr (AM) load(sbase + C::OFF_MASK + stage * C::MASK_SLOT, &tmZ, row0 / 32, k0);
+          // K-major with two panels: one 3-D box (64 k x rows x 2 panels)
+          // of a panel-indexed view of the operand.
+          auto load3 = [&](uint32_t dst, const CUtensorMap* map, int y, int z) {
+            if constexpr (PAIR && !AM)
+              tma_load_3d_pair(dst, map, fb, 0, y, z);
+            else
+              tma_load_3d(dst, map, fb, 0, y, z);
+          };
+          // M/N-major: 64-wide chunks of KB k-rows (KB x 128 bytes each)
+          constexpr uint32_t MN_CHUNK = KB * 128;
           if (!p.a_mn) {
-            load(sa, &tmA, k0, row0);
+            if constexpr (C::PANELS == 2)
+              load3(sa, &tmA, row0, 2 * kb);
+            else
+              load(sa, &tmA, k0, row0);
           } else {
             load(sa, &tmA, row0, k0);
-            load(sa + 8192, &tmA, row0 + 64, k0);
+            load(sa + MN_CHUNK, &tmA, row0 + 64, k0);
           }
           if (!p.b_mn) {
-            load(sb, &tmB, k0, col0);
+            if constexpr (C::PANELS == 2)
+              load3(sb, &tmB, col0, 2 * kb);
+            else
+              load(sb, &tmB, k0, col0);
           } else {
 #pragma unroll
-            for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + 8192 * j, &tmB, col0 + 64 * j, k0);
+            for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + MN_CHUNK * j, &tmB, col0 + 64 * j, k0);
           }
           ++fills;
           if (++stage == C::STAGES) {
@@ -431,13 +452,16 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+          for (int k = 0; k < KB / 16; ++k) {
             // K-major: the 16-wide k step is 32 bytes inside the 128-byte
-            // swizzle row; MN-major: 16 k-rows of 128 bytes = 2 KB.
-            const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                       : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-            const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                       : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+            // swizzle row of its panel (panels of rows x 128 bytes follow
+            // one another); MN-major: 16 k-rows of 128 bytes = 2 KB, the
+            // 64-wide chunks KB x 128 bytes apart.
+            const uint32_t pk = static_cast<uint32_t>(k >> 2), wk = static_cast<uint32_t>(k & 3);
+            const uint64_t ad = p.a_mn ? smem_desc_sw128(sa + 2048u * k, KB * 128u, 1024u)
+                                       : smem_desc_sw128(sa + pk * (BM * 128u) + 32u * wk, 16u, 1024u);
+            const uint64_t bd = p.b_mn ? smem_desc_sw128(sb + 2048u * k, KB * 128u, 1024u)
+                                       : smem_desc_sw128(sb + pk * (C::B_ROWS * 128u) + 32u * wk, 16u, 1024u);
             if constexpr (PAIR)
               tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
             else
@@ -833,20 +857,20 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   }
 }
 
-template <int BN, bool PAIR, int EPIW, bool AM = false>
+template <int BN, bool PAIR, int EPIW, bool AM = false, int KB = 64>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                         const CUtensorMap& tmZ, const GemmArgs& args, int grid, cudaStream_t stream) {
-  using C = Cfg<BN, PAIR, EPIW, AM>;
+  using C = Cfg<BN, PAIR, EPIW, AM, KB>;
   static std::atomic<bool> configured[64] = {};  // the attribute is set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, AM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, AM, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if constexpr (PAIR) {
-      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, AM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      e = cudaFuncSetAttribute(tc_gemm_kernel<BN, PAIR, EPIW, AM, KB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       cudaGetLastError();
     }
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -865,7 +889,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, AM>, tmA, tmB, tmD, tmZ, args);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, PAIR, EPIW, AM, KB>, tmA, tmB, tmD, tmZ, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1041,6 +1065,14 @@ cudaError_t launch_width(int block_n, int pair, const CUtensorMap& tmA, const CU
     }
   } else {
     if (args.amask) return cudaErrorInvalidValue;
+  }
+  if (args.kb == 128) {  // stages of two panels (64 KB at most a stage)
+    if (pair) {
+      if (block_n == 256) return launch_impl<256, true, EPIW, false, 128>(tmA, tmB, tmD, tmZ, args, grid, stream);
+      return launch_impl<128, true, EPIW, false, 128>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    }
+    if (block_n == 128) return launch_impl<128, false, EPIW, false, 128>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    return cudaErrorInvalidValue;
   }
   if (pair) {
     if (block_n == 256) return launch_impl<256, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);

@@ -83,6 +83,10 @@ struct GemmArgs {
   // k-range into bg_partials[piece][Mk] (piece = split-K piece, 0 for whole
   // tiles, whose other rows are zeroed), by the CTAs of the first N-tile.
   int amask;
+  // k-values per pipeline stage: 64, or 128 (two 64-wide panels per operand
+  // box; K-major operands then come through 3-D tensor maps that index the
+  // panels, so K must be a multiple of 128)
+  int kb;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs

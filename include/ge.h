@@ -50,7 +50,9 @@
  * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
  * GE_SPLIT_TAIL = 0 disables the split-K tail; GE_EPI_WARPS = 4 | 8 forces the
  * epilogue width; GE_GROUP_M = g sets how many M-tiles the tile order sweeps
- * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits.
+ * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits;
+ * GE_KB = 64 forces one 64-wide k panel per pipeline stage (the default is
+ * two, in one TMA box per operand, when K is a multiple of 128).
  * They change speed, never results beyond rounding order.
  *
  * Errors. Every call returns a status and never aborts or prints. Arguments

@@ -203,6 +203,30 @@ def test_pair_tiles_exact_integer(oracle, monkeypatch, epi):
     _run_case(oracle, 520, 776, 128, epi, "m", "k", "col", dist=("int", 2.0), seed=22, exact=True)
 
 
+@pytest.mark.parametrize("am,bm,dl", [("k", "n", "row"), ("k", "k", "col"), ("m", "n", "row"),
+                                      ("m", "k", "col")])
+def test_pair_tiles_128_wide(oracle, monkeypatch, am, bm, dl):
+    """2-CTA pairs of 256 x 128 tiles (each CTA stages 64 columns of B):
+    K a multiple of 128 (two panels a stage) and a ragged K (one)."""
+    monkeypatch.setenv("GE_PAIR", "1")
+    monkeypatch.setenv("GE_TILE_N", "128")
+    for M, N, K, seed in ((520, 776, 1024, 40), (300, 264, 520, 41)):
+        _run_case(oracle, M, N, K, EPIS[seed % len(EPIS)], am, bm, dl, seed=seed)
+
+
+@pytest.mark.parametrize("kb", ["64", "128"])
+@pytest.mark.parametrize("epi", ["none", "relu_aux_bias"])
+def test_stage_panels_exact_integer(oracle, monkeypatch, kb, epi):
+    """One or two 64-wide k panels per pipeline stage (GE_KB) on a K that is
+    a multiple of 128, single-CTA and pair tiles, integer data: bit-identical
+    to the oracle either way."""
+    monkeypatch.setenv("GE_KB", kb)
+    for pair in ("0", "1"):
+        monkeypatch.setenv("GE_PAIR", pair)
+        _run_case(oracle, 520, 776, 384, epi, "k", "n", "row", dist=("int", 2.0), seed=42, exact=True)
+        _run_case(oracle, 520, 776, 384, epi, "m", "k", "col", dist=("int", 2.0), seed=43, exact=True)
+
+
 @pytest.mark.parametrize("epi", ["none", "bias", "relu_aux_bias"])
 def test_split_tail_exact_integer(oracle, epi):
     """Split-K tail (4 tiles split 4 ways, then the fixup kernel): integer

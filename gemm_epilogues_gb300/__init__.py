@@ -17,7 +17,11 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libgemm_epilogues.so")
+# GE_DEBUG_LIB=1 selects the checking build (build.build(debug=True)): the
+# same kernels compiled with GE_DEBUG, whose index, offset and mbarrier-phase
+# checks report GE_ERR_DEVICE_CHECK through ge_get_last_device_error.
+LIB_PATH = os.path.join(_HERE, "_build_debug" if os.environ.get("GE_DEBUG_LIB") == "1" else "_build",
+                        "libgemm_epilogues.so")
 
 # ge_status_t
 GE_OK = 0
@@ -28,6 +32,7 @@ GE_ERR_DEVICE_MISMATCH = 4
 GE_ERR_CUDA = 5
 GE_ERR_TIMEOUT = 6
 GE_ERR_OOM = 7
+GE_ERR_DEVICE_CHECK = 8
 # ge_epilogue_t
 GE_EPI_NONE = 0
 GE_EPI_BIAS = 1
@@ -71,7 +76,7 @@ ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
                  "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr",
                  "ge_plan_autotune", "ge_plan_config", "ge_execute_norm", "ge_execute_norm_unfused",
-                 "ge_autotune_cache_clear", "ge_execute_chain")
+                 "ge_autotune_cache_clear", "ge_execute_chain", "ge_debug_checks", "ge_debug_check_probe")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -139,6 +144,10 @@ def load_library():
         lib.ge_plan_config.restype = i32
         lib.ge_execute_chain.argtypes = [vp, i64, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp, vp]
         lib.ge_execute_chain.restype = i32
+        lib.ge_debug_checks.argtypes = []
+        lib.ge_debug_checks.restype = i32
+        lib.ge_debug_check_probe.argtypes = [vp, vp]
+        lib.ge_debug_check_probe.restype = i32
         lib.ge_version.argtypes = []
         lib.ge_version.restype = ctypes.c_char_p
         _lib = lib
@@ -283,6 +292,14 @@ def ge_get_last_device_error(plan) -> int:
 
 def ge_debug_wait_timeout(plan, budget_cycles: int, stream=None) -> int:
     return int(load_library().ge_debug_wait_timeout(plan, int(budget_cycles), _stream(stream)))
+
+
+def ge_debug_checks() -> bool:
+    return bool(load_library().ge_debug_checks())
+
+
+def ge_debug_check_probe(plan, stream=None) -> int:
+    return int(load_library().ge_debug_check_probe(plan, _stream(stream)))
 
 
 def ge_drelu_bgrad_static(M: int, N: int, d: int, ldd: int, ld_aux: int, dY, aux, dZ, bgrad,

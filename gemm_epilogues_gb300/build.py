@@ -1,6 +1,9 @@
 """Build step of the CUDA library: compiles ``csrc/*.cu`` for sm_103a with
 nvcc (one process per translation unit, in parallel) and links
-``_build/libgemm_epilogues.so`` in the package directory."""
+``_build/libgemm_epilogues.so`` in the package directory. ``debug=True``
+builds the checking variant (``-DGE_DEBUG``: device-side index, offset and
+mbarrier-phase checks that report through the plan's error word) into
+``_build_debug/``."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -13,6 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libgemm_epilogues.so")
+OUT_DEBUG = os.path.join(HERE, "_build_debug")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,19 +45,22 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
     """Compile and link the library if any source or header changed."""
-    os.makedirs(OUT, exist_ok=True)
+    out = OUT_DEBUG if debug else OUT
+    lib = os.path.join(out, "libgemm_epilogues.so")
+    extra = ["-DGE_DEBUG"] if debug else []
+    os.makedirs(out, exist_ok=True)
     srcs = _sources()
     hdrs = _headers()
     nvcc = _nvcc()
     objs = []
     jobs = []
     for src in srcs:
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
-            cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
+            cmd = [nvcc] + NVCC_FLAGS + extra + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
             jobs.append(cmd)
 
     def run(cmd):
@@ -68,17 +75,18 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     print(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             print(r.stdout + r.stderr)
             raise RuntimeError("link of libgemm_epilogues.so failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

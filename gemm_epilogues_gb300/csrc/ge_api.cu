@@ -385,6 +385,7 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.epi = epi_code;
     g.static_a = pl->static_a;
     g.bf16 = pl->bf16;
+    g.err = pl->err;
     e = launch_gemv(g, pl->num_sms, st);
   } else {
     const bool zout = epi_code == EPI_GELU_AUX_BIAS;
@@ -501,6 +502,7 @@ const char* ge_status_string(ge_status_t s) {
     case GE_ERR_CUDA: return "GE_ERR_CUDA: CUDA call or launch failed";
     case GE_ERR_TIMEOUT: return "GE_ERR_TIMEOUT: a bounded device wait expired";
     case GE_ERR_OOM: return "GE_ERR_OOM: workspace allocation failed";
+    case GE_ERR_DEVICE_CHECK: return "GE_ERR_DEVICE_CHECK: a device-side index or phase check failed (debug build)";
   }
   return "unknown ge_status_t";
 }
@@ -1085,6 +1087,7 @@ ge_status_t ge_get_last_device_error(ge_plan_t plan) {
     cudaGetLastError();
     return GE_ERR_CUDA;
   }
+  if (w & ERR_DEBUG_CHECK) return GE_ERR_DEVICE_CHECK;
   return w ? GE_ERR_TIMEOUT : GE_OK;
 }
 
@@ -1092,6 +1095,21 @@ ge_status_t ge_debug_wait_timeout(ge_plan_t plan, int64_t budget_cycles, void* s
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl || budget_cycles < 1 || budget_cycles > (int64_t(1) << 31)) return GE_ERR_INVALID_ARG;
   cudaError_t e = launch_wait_probe(pl->err, budget_cycles, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+int ge_debug_checks(void) {
+#ifdef GE_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+ge_status_t ge_debug_check_probe(ge_plan_t plan, void* stream) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return GE_ERR_INVALID_ARG;
+  const cudaError_t e = launch_check_probe(pl->err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 

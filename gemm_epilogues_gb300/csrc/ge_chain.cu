@@ -149,6 +149,10 @@ __global__ void __launch_bounds__(32 * CW, 1) gemv_chain_kernel(const __grid_con
     const long long row = r0 + warp + CW * (q / SEG);
     const int s = static_cast<int>(t % p.ring);
     const uint32_t bar = bar0 + 8u * s;
+    // (GE_DEBUG) the item lies in this warp's sequence, its row in the
+    // block's range, its slot in the warp's ring; a skipped copy ends in
+    // the consumer's bounded wait
+    if (!GE_DCHECK(t >= 0 && t < total && l < p.layers && row < r1 && s < p.ring, p.err)) return;
     mbar_arrive_expect_tx(bar, seg_bytes);
     bulk_load_1d(ring_s + static_cast<uint32_t>(s) * seg_bytes,
                  reinterpret_cast<const uint8_t*>(p.A[l] + row * p.lda) + (q % SEG) * seg_bytes, seg_bytes, bar);
@@ -203,6 +207,9 @@ __global__ void __launch_bounds__(32 * CW, 1) gemv_chain_kernel(const __grid_con
       if (__any_sync(0xffffffffu, *abort_s != 0)) break;  // the same decision in every lane
       const int j = q / SEG, h = q % SEG;
       const int s = static_cast<int>(t % p.ring);
+      // (GE_DEBUG) lane 0 issues at most `ring` items ahead of the ones
+      // consumed: a slot's barrier is never a phase ahead of its waiter
+      if (lane == 0) (void)GE_DCHECK(issued - t <= p.ring && issued >= t, p.err);
       const uint32_t par = static_cast<uint32_t>((t / p.ring) & 1);
       const bool landed = mbar_wait_bounded(bar0 + 8u * s, par, abort_s, p.budget);
       if (!__all_sync(0xffffffffu, landed)) {

@@ -79,7 +79,9 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_MASK + MASK_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5 + (AM ? STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB for base alignment
+  // misc: TMEM address, abort flag, a flag that is never set, then (GE_DEBUG)
+  // the producer's fill count of each stage
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 4 * 8 + 1024;  // + 1 KB for base alignment
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;
   static constexpr int EPI_ARRIVALS = PAIR ? 2 * EPI_WARPS : EPI_WARPS;
@@ -204,7 +206,8 @@ __device__ __forceinline__ void load_slab16(const GemmArgs& p, int grow, int gco
 __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const CUtensorMap* map,
                                            unsigned short* dst, long long ld, int gcol0, int rbase,
                                            int grow, int Mk, int Nk, uint8_t* stg, int& nstore,
-                                           int lane) {
+                                           int lane, unsigned int* dbg_err) {
+  (void)dbg_err;
   if (gcol0 + 32 > Nk && (Nk & 7) != 0) {
     if (grow < Mk) {
       unsigned short* drow = dst + static_cast<long long>(grow) * ld + gcol0;
@@ -219,6 +222,9 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
     }
   } else if (rbase < Mk) {
     uint8_t* buf = stg + (nstore & 1) * EPI_BUF_BYTES;
+#ifdef GE_DEBUG
+    if (lane == 0 && (gcol0 < 0 || gcol0 % 8 != 0 || rbase < 0)) atomicOr(dbg_err, ERR_DEBUG_CHECK);
+#endif
     if (lane == 0 && nstore >= 2) bulk_wait_group_read<1>();
     __syncwarp();
 #pragma unroll
@@ -259,6 +265,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  // GE_DEBUG: fills issued into each stage (the MMA warp checks that the
+  // producer is never more than one phase of a stage ahead of it)
+  volatile unsigned int* dbg_fills = reinterpret_cast<volatile unsigned int*>(smem + C::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -281,6 +290,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
       for (int s = 0; s < C::STAGES; ++s) mbar_init(xform_bar(s), (PAIR ? 2 : 1) * C::XFORM_WARPS);
     *abort_flag = 0;
     *never = 0;
+    for (int s = 0; s < C::STAGES && s < 8; ++s) dbg_fills[s] = 0u;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -354,6 +364,15 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * KB;
+          // TMA: the innermost coordinate of every box is a multiple of 64
+          // elements (128 bytes); the stage lies below the epilogue buffers
+          if (!GE_DCHECK(k0 >= 0 && k0 % 64 == 0 && row0 >= 0 && row0 % 64 == 0 && col0 >= 0 && col0 % 64 == 0 &&
+                             (stage + 1) * C::STAGE_BYTES <= C::OFF_EPI && kb < num_kb,
+                         p.err)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
           auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
             if constexpr (PAIR && !AM)
               tma_load_2d_pair(dst, map, fb, x, y);
@@ -392,6 +411,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + MN_CHUNK * j, &tmB, col0 + 64 * j, k0);
           }
           ++fills;
+#ifdef GE_DEBUG
+          if (stage < 8) dbg_fills[stage] = dbg_fills[stage] + 1u;
+#endif
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -425,9 +447,16 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+#ifdef GE_DEBUG
+      unsigned int uses[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // stages consumed so far
+#endif
       for (int u = first_tile; u < num_units && ok; u += tile_step) {
         int tile, kb0, kb1, v;
         unit_info(u, p.tail_start, p.split, num_kb, tile, kb0, kb1, v);
+        if (!GE_DCHECK(acc * BN + BN <= C::TMEM_COLS, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.budget)) {
           if (!*abort_flag) atomicOr(p.err, ERR_MMA_TIMEOUT);
           *abort_flag = 1;
@@ -436,6 +465,20 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
+#ifdef GE_DEBUG
+          // the fills of this stage the producer issued so far, less the
+          // uses: 0 (not yet refilled) or 1; 2 would be a phase the parity
+          // wait cannot tell from the one it waits for
+          if (stage < 8) {  // (pairs: the leader's own producer's fills)
+            const unsigned int ahead = dbg_fills[stage] - uses[stage];
+            if (!GE_DCHECK(ahead <= 1u, p.err)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (stage < 8) ++uses[stage];
+#endif
           bool landed;
           if constexpr (AM)  // masked by both CTAs' transform warps
             landed = PAIR ? mbar_wait_bounded_cluster(xform_bar(stage), phase, abort_flag, p.budget)
@@ -717,6 +760,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
         if (needs_z && c + C::HALVES < BN / 32) load_slab16(p, grow, gcol0 + 32 * C::HALVES, znext);
         const unsigned short bl_next = bias_lane(gcol0 + 32 * C::HALVES + lane);
         uint32_t v[32];
+        (void)GE_DCHECK(acc * BN + 32 * c + 32 <= C::TMEM_COLS && gcol0 % 32 == 0 && rbase % 32 == 0 &&
+                      (p.aux == nullptr || (gcol0 >> 5) < p.ld_aux),
+                  p.err);
         tmem_ld_32x32b_x32(t_row + 32u * c, v);
         tmem_ld_wait();
         float bcol[32];
@@ -806,9 +852,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
                                 : epilogue_dispatch<false>(p.epi, v, brow, bcol, packed, zpacked, bf16);
         }
         store_slab(packed, &tmD, reinterpret_cast<unsigned short*>(p.D), p.ldd, gcol0, rbase, grow,
-                   p.Mk, p.Nk, stg, nstore, lane);
+                   p.Mk, p.Nk, stg, nstore, lane, p.err);
         if (p.epi == EPI_GELU_AUX_BIAS)
-          store_slab(zpacked, &tmZ, p.zaux, p.ld_zaux, gcol0, rbase, grow, p.Mk, p.Nk, stg, nstore, lane);
+          store_slab(zpacked, &tmZ, p.zaux, p.ld_zaux, gcol0, rbase, grow, p.Mk, p.Nk, stg, nstore, lane, p.err);
         if (p.epi == EPI_RELU_AUX_BIAS && grow < p.Mk) {
           if (p.Nk - gcol0 < 32) bits &= (1u << (p.Nk - gcol0)) - 1u;
           p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)] = bits;

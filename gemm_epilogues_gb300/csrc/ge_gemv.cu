@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   grid_dependency_wait();  // B may come from, and D may be read by, the previous grid
   for (long long m = m_first; m < p.M; m += nwarps) {
     const __half* arow = p.A + m * p.lda;
+    if (lane == 0 && p.err) (void)GE_DCHECK(m >= 0 && p.K <= p.lda && p.N <= NT, p.err);
     float acc[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n] = 0.0f;

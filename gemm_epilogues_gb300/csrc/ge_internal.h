@@ -32,8 +32,19 @@ enum ErrBits : unsigned int {
   ERR_DRAIN_TIMEOUT = 8u,
   ERR_PROBE_TIMEOUT = 16u,
   ERR_XFORM_TIMEOUT = 32u,
-  ERR_CHAIN_TIMEOUT = 64u
+  ERR_CHAIN_TIMEOUT = 64u,
+  ERR_DEBUG_CHECK = 128u  // a GE_DEBUG build's index / offset / phase check failed
 };
+
+// Checks of the GE_DEBUG build: a failed check records ERR_DEBUG_CHECK in
+// the error word and evaluates to false, so the caller skips the access (a
+// skipped copy then ends in a bounded wait that aborts the kernel). No trap,
+// no assert: the context stays usable. Without GE_DEBUG it is `true`.
+#ifdef GE_DEBUG
+#define GE_DCHECK(cond, errp) ((cond) ? true : (atomicOr((errp), ::ge::ERR_DEBUG_CHECK), false))
+#else
+#define GE_DCHECK(cond, errp) true
+#endif
 
 // Kernel-level problem of the tensor-core GEMM: D'[Mk, Nk] (row-major, via
 // the D tensor map) = act(A'[Mk, K] . B'[K, Nk] + bias), where the planner
@@ -121,6 +132,7 @@ struct GemvArgs {
   int epi;
   int bf16;           // element type: bfloat16 (1) or fp16 (0)
   int static_a;       // launch with programmatic dependent launch (A never written upstream)
+  unsigned int* err;  // device error word (GE_DEBUG checks)
 };
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
 
@@ -214,5 +226,7 @@ cudaError_t launch_residual_add(__half* D, long long R, long long C, long long l
 
 // Bounded-wait probe (test hook).
 cudaError_t launch_wait_probe(unsigned int* err, long long budget, cudaStream_t stream);
+// Debug-check probe (test hook): records ERR_DEBUG_CHECK in a GE_DEBUG build.
+cudaError_t launch_check_probe(unsigned int* err, cudaStream_t stream);
 
 }  // namespace ge

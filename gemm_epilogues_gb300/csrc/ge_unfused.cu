@@ -174,6 +174,16 @@ __global__ void wait_probe_kernel(unsigned int* err, long long budget) {
   }
 }
 
+// A check that fails by construction and guards nothing: a GE_DEBUG build
+// records ERR_DEBUG_CHECK in the error word; the normal build does nothing.
+__global__ void check_probe_kernel(unsigned int* err) {
+#ifdef GE_DEBUG
+  if (threadIdx.x == 0) (void)GE_DCHECK(threadIdx.x != 0, err);
+#else
+  (void)err;
+#endif
+}
+
 // Blocks for `units` units and the F_BIG / F_RAGGED flags of the launch.
 int elem_grid(long long units, long long C, int& flags) {
   long long b = (units + 256 * ELEM_U - 1) / (256 * ELEM_U);
@@ -236,6 +246,11 @@ cudaError_t launch_activation(__half* D, long long R, long long C, long long ld,
     default: return cudaErrorInvalidValue;
   }
   fn(ActArgs{D, R, C, ld, aux, ld_aux, zaux, ld_zaux, bf16}, blocks, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_check_probe(unsigned int* err, cudaStream_t s) {
+  check_probe_kernel<<<1, 32, 0, s>>>(err);
   return cudaGetLastError();
 }
 

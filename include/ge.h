@@ -78,7 +78,9 @@ typedef enum {
   GE_ERR_DEVICE_MISMATCH = 4, /* a buffer is not on the plan's device          */
   GE_ERR_CUDA = 5,            /* a CUDA runtime call or a launch failed        */
   GE_ERR_TIMEOUT = 6,         /* a bounded device-side wait expired            */
-  GE_ERR_OOM = 7              /* plan workspace allocation failed              */
+  GE_ERR_OOM = 7,             /* plan workspace allocation failed              */
+  GE_ERR_DEVICE_CHECK = 8     /* a device-side index, offset or mbarrier-phase
+                                 check of a debug build (GE_DEBUG) failed      */
 } ge_status_t;
 
 /* Epilogues (nvmath-python MatmulEpilog names). NONE is D = A.B. */
@@ -391,7 +393,9 @@ int ge_plan_tile_n(ge_plan_t plan);
  * Read and clear the plan's device error word. Synchronises the device.
  * Returns GE_OK when no device-side wait of this plan has expired since the
  * last read, GE_ERR_TIMEOUT when one has (the kernel then stopped early and
- * its outputs are undefined), GE_ERR_CUDA if the read itself failed.
+ * its outputs are undefined), GE_ERR_DEVICE_CHECK when a check of a debug
+ * build (compiled with GE_DEBUG) failed (the access was skipped; outputs
+ * undefined), GE_ERR_CUDA if the read itself failed.
  */
 ge_status_t ge_get_last_device_error(ge_plan_t plan);
 
@@ -445,6 +449,19 @@ ge_status_t ge_drelu_bgrad_static(int64_t M, int64_t N, ge_dlayout_t d,
                                   int64_t ldd, int64_t ld_aux, const void* dY,
                                   const void* aux, void* dZ, void* bgrad,
                                   void* stream);
+
+/* 1 if this library was compiled with the device-side checks (GE_DEBUG),
+ * else 0. */
+int ge_debug_checks(void);
+
+/*
+ * Test hook for the checking build: launches one thread whose GE_DEBUG
+ * check fails by construction (it guards no memory access). In a build with
+ * the checks, ge_get_last_device_error then returns GE_ERR_DEVICE_CHECK; in
+ * the normal build the kernel does nothing and it returns GE_OK. Returns
+ * the launch status.
+ */
+ge_status_t ge_debug_check_probe(ge_plan_t plan, void* stream);
 
 /* Library version, "major.minor.patch". */
 const char* ge_version(void);

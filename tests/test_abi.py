@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for s in range(8):
+    for s in range(9):
         assert ge.ge_status_string(s).startswith("GE_")
     assert ge.ge_status_string(99) == "unknown ge_status_t"
     assert re.match(r"\d+\.\d+\.\d+", ge.ge_version())

@@ -76,7 +76,8 @@ ABI_FUNCTIONS = ("ge_plan_create", "ge_execute", "ge_execute_unfused", "ge_plan_
                  "ge_get_last_device_error", "ge_status_string", "ge_debug_wait_timeout",
                  "ge_version", "ge_drelu_bgrad_static", "ge_plan_set_attr",
                  "ge_plan_autotune", "ge_plan_config", "ge_execute_norm", "ge_execute_norm_unfused",
-                 "ge_autotune_cache_clear", "ge_execute_chain", "ge_debug_checks", "ge_debug_check_probe")
+                 "ge_autotune_cache_clear", "ge_execute_chain", "ge_debug_checks", "ge_debug_check_probe",
+                 "ge_plan_stream_k_tiles")
 
 
 class ge_layout_t(ctypes.Structure):
@@ -142,6 +143,8 @@ def load_library():
         lib.ge_plan_autotune.restype = i32
         lib.ge_plan_config.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.ge_plan_config.restype = i32
+        lib.ge_plan_stream_k_tiles.argtypes = [vp]
+        lib.ge_plan_stream_k_tiles.restype = i32
         lib.ge_execute_chain.argtypes = [vp, i64, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp, vp]
         lib.ge_execute_chain.restype = i32
         lib.ge_debug_checks.argtypes = []
@@ -266,6 +269,11 @@ def ge_plan_config(plan):
     return path, bn.value, pr.value, sp.value
 
 
+def ge_plan_stream_k_tiles(plan) -> int:
+    """Tiles the plan computes stream-K (0: none)."""
+    return int(load_library().ge_plan_stream_k_tiles(plan))
+
+
 def ge_plan_free(plan):
     _check(load_library().ge_plan_free(plan), "ge_plan_free")
 
@@ -338,6 +346,10 @@ class Plan:
     @property
     def config(self):
         return ge_plan_config(self.handle)
+
+    @property
+    def stream_k_tiles(self) -> int:
+        return ge_plan_stream_k_tiles(self.handle)
 
     def execute_chain(self, As, biases, X, Y, stream=None):
         ge_execute_chain(self.handle, As, biases, X, Y, stream)

@@ -41,6 +41,8 @@ struct Plan {
   int kb = 64;        // k-values per pipeline stage (64 or 128)
   int tail_start = 0;  // split-K tail (see GemmArgs); `tail_ws` holds its pieces
   int split = 1;
+  int sk_tiles = 0;    // stream-K tiles (see GemmArgs); `tail_ws` holds the workers' slots
+  unsigned int* sk_sync = nullptr;  // stream-K epoch, counter and flags (in `ws`)
   void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
   size_t tail_ws_bytes = 0;
   bool tc_allow_split = true;
@@ -184,7 +186,7 @@ ge_status_t check_device(Plan* pl, int slot, const void* p) {
 // Tensor-core launch configuration for a tile width and pair mode: work
 // units, grid, rasterisation group and the split-K tail.
 struct TcConfig {
-  int block_n = 256, pair = 0, split = 1, tail_start = 0, grid = 1, group_m = 1, kb = 64;
+  int block_n = 256, pair = 0, split = 1, tail_start = 0, grid = 1, group_m = 1, kb = 64, sk_tiles = 0;
 };
 
 // k-values per pipeline stage for a tile shape: 128 (two 64-wide panels per
@@ -201,7 +203,7 @@ int kb_for(const Plan& pl, int block_n, int pair) {
 // Configurations chosen by ge_plan_autotune, per device, problem and layout:
 // a plan created later for the same key starts from the tuned choice.
 struct TunedChoice {
-  int block_n, pair, split;
+  int block_n, pair, split, sk;
 };
 using TuneKey = std::array<int64_t, 13>;
 std::map<TuneKey, TunedChoice>& tuned_cache() {
@@ -243,6 +245,14 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
   // way: the fixup is launched as a programmatic dependent of the GEMM, so
   // its launch overlaps the GEMM (1024x512x2048 GELU_BIAS, 32 tiles: 25.0 ->
   // 21.9 us; 4096x128x4096: 34.0 -> 25.5 us).
+  // Stream-K (GE_STREAM_K = 1, for any ragged last wave): the last one or
+  // two waves' tiles are shared out as equal ranges of k-block iterations
+  // (each tile then in about W / sk_tiles + 1 pieces) and every tile is
+  // finished inside the GEMM by the worker that starts it. Not the default:
+  // measured slower than the plain waves on the shapes it is for (FFN up
+  // 4096x2048x4096: 73 vs 58 us; 4096x512x4096: 36 vs 30 us), because the
+  // finisher's epilogue (a whole tile's, plus adding the pieces) lands at
+  // the very end of every worker's range.
   const long long num_kb = (pl.K + c.kb - 1) / c.kb;
   const long long rem = tiles % workers;
   auto pieces = [&](long long t) {
@@ -250,7 +260,14 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
     if (S > num_kb / 4) S = num_kb / 4;
     return S > 16 ? 16LL : S;
   };
-  if (allow_split && tiles > workers && rem != 0 && rem * 2 <= workers) {
+  int sk_env = -1;
+  if (const char* env = std::getenv("GE_STREAM_K")) sk_env = env[0] == '0' ? 0 : (env[0] == '1' ? 1 : -1);
+  // (not for the masked-operand weight gradient: its bias-gradient partials
+  // are per split-K piece)
+  const bool sk_ok = allow_split && rem != 0 && sk_env != 0 && pl.epi != GE_EPI_DW_DRELU_BGRAD;
+  if (sk_ok && sk_env == 1) {
+    c.sk_tiles = static_cast<int>(tiles < 2 * workers ? tiles : rem + workers);
+  } else if (allow_split && tiles > workers && rem != 0 && rem * 2 <= workers) {
     const long long S = pieces(rem);
     if (S >= 2) {
       c.split = static_cast<int>(S);
@@ -264,13 +281,22 @@ TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
     }
   }
   if (c.split == 1) c.tail_start = static_cast<int>(tiles);
-  const long long units = c.tail_start + (tiles - c.tail_start) * c.split;
-  const long long g = units < workers ? units : workers;
-  c.grid = static_cast<int>(pair ? 2 * g : g);
+  if (c.sk_tiles > 0) {
+    c.grid = static_cast<int>(pair ? 2 * workers : workers);  // every worker has a range
+  } else {
+    const long long units = c.tail_start + (tiles - c.tail_start) * c.split;
+    const long long g = units < workers ? units : workers;
+    c.grid = static_cast<int>(pair ? 2 * g : g);
+  }
   return c;
 }
 
 size_t tc_tail_bytes(const Plan& pl, const TcConfig& c) {
+  if (c.sk_tiles > 0) {  // one slot per worker
+    const int64_t tile_m = c.pair ? 256 : 128;
+    const int64_t workers = c.pair ? c.grid / 2 : c.grid;
+    return static_cast<size_t>(workers) * tile_m * c.block_n * 4;
+  }
   if (c.split <= 1) return 0;
   const int64_t Mk = pl.swap ? pl.N : pl.M;
   const int64_t Nk = pl.swap ? pl.M : pl.N;
@@ -297,6 +323,7 @@ ge_status_t apply_config(Plan* pl, const TcConfig& c) {
   pl->kb = c.kb;
   pl->split = c.split;
   pl->tail_start = c.tail_start;
+  pl->sk_tiles = c.sk_tiles;
   pl->grid = c.grid;
   pl->group_m = c.group_m;
   pl->partials = static_cast<float*>(pl->tail_ws);
@@ -415,6 +442,8 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.tail_start = pl->tail_start;
     g.split = pl->split;
     g.partials = pl->partials;
+    g.sk_tiles = pl->sk_tiles;
+    g.sk_sync = pl->sk_sync;
     g.bg_partials = pl->bg_partials;
     g.bf16 = pl->bf16;
     g.nstats = epi_code == EPI_BIAS_RESIDUAL ? pl->nstats : nullptr;
@@ -659,6 +688,12 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   }
   size_t ws = 256;
   if (tmp.path == GE_PATH_GEMV) ws += static_cast<size_t>(kChainSyncWords) * 4;  // ge_execute_chain
+  size_t sk_off = 0;
+  if (tmp.path == GE_PATH_TC_GEMM) {
+    // stream-K: epoch, finished-CTA count, one flag per (CTA, epilogue warp)
+    sk_off = ws;
+    ws += (2 + 8 * static_cast<size_t>(tmp.num_sms)) * 4;
+  }
   size_t bg_off = 0;
   if (tmp.path == GE_PATH_TC_GEMM && backward) {
     const int64_t Mk = tmp.swap ? N : M;
@@ -710,6 +745,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   tmp.ws_bytes = ws;
   tmp.err = static_cast<unsigned int*>(tmp.ws);
   if (bg_off) tmp.bg_partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + bg_off);
+  if (sk_off) tmp.sk_sync = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + sk_off);
   if (nstats_off) {
     tmp.nstats = reinterpret_cast<float2*>(static_cast<char*>(tmp.ws) + nstats_off);
     tmp.rowstats = reinterpret_cast<float2*>(static_cast<char*>(tmp.ws) + rowstats_off);
@@ -729,14 +765,15 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   if (pl->path == GE_PATH_TC_GEMM) {
     pl->tc_allow_split = tc_split;
     bool split_on = tc_split;
-    const bool overridden = std::getenv("GE_TILE_N") || std::getenv("GE_PAIR") || std::getenv("GE_SPLIT_TAIL");
+    const bool overridden = std::getenv("GE_TILE_N") || std::getenv("GE_PAIR") || std::getenv("GE_SPLIT_TAIL") ||
+                            std::getenv("GE_STREAM_K");
     if (!overridden) {
       std::lock_guard<std::mutex> lock(tuned_mutex());
       auto it = tuned_cache().find(tune_key(*pl));
       if (it != tuned_cache().end()) {
         tc_block_n = it->second.block_n;
         tc_pair = it->second.pair;
-        split_on = tc_split && it->second.split > 1;
+        split_on = tc_split && (it->second.split > 1 || it->second.sk);
       }
     }
     ge_status_t st = apply_config(pl, tc_config(*pl, tc_block_n, tc_pair, split_on));
@@ -974,7 +1011,7 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
       cands[n++] = tc_config(*pl, bn, pair, false);
       if (pl->tc_allow_split) {
         const TcConfig c = tc_config(*pl, bn, pair, true);
-        if (c.split > 1) cands[n++] = c;
+        if (c.split > 1 || c.sk_tiles > 0) cands[n++] = c;
       }
     }
   cudaEvent_t e0, e1;
@@ -1010,7 +1047,8 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
   if (s2 != GE_OK) return s2;
   {
     std::lock_guard<std::mutex> lock(tuned_mutex());
-    tuned_cache()[tune_key(*pl)] = TunedChoice{cands[best].block_n, cands[best].pair, cands[best].split};
+    tuned_cache()[tune_key(*pl)] =
+        TunedChoice{cands[best].block_n, cands[best].pair, cands[best].split, cands[best].sk_tiles > 0 ? 1 : 0};
   }
   return ge_execute(plan, A, B, bias, D, aux, stream);  // outputs of the chosen configuration
 }
@@ -1022,6 +1060,12 @@ int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split) {
   if (pair) *pair = pl->path == GE_PATH_TC_GEMM ? pl->pair : 0;
   if (split) *split = pl->path == GE_PATH_TC_GEMM ? pl->split : 0;
   return static_cast<int>(pl->path);
+}
+
+int ge_plan_stream_k_tiles(ge_plan_t plan) {
+  Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (!pl) return -1;
+  return pl->path == GE_PATH_TC_GEMM ? pl->sk_tiles : 0;
 }
 
 ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value) {

@@ -50,27 +50,6 @@ namespace {
 constexpr int kSmemMax = 232448;        // dynamic shared memory per block
 constexpr int kSmemSlack = 128 + 16;    // base alignment + the block's flags
 
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void red_release_gpu_add(unsigned int* p, unsigned int v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// 16 bytes from L2 (the activations of the previous layer were written by
-// other SMs during this launch: they must not come from this SM's L1).
-__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
-
 __device__ __forceinline__ float chain_act(int epi, float z) {
   if (epi == EPI_RELU_BIAS) return fmaxf(z, 0.0f);
   if (epi == EPI_GELU_BIAS) return gelu_tanh(z);

@@ -1,0 +1,9 @@
+// ge_gemm_epi_relu_aux.cu -- the tensor-core GEMM kernels with the bias + ReLU + mask epilogue.
+#include "ge_gemm_kernel.cuh"
+
+namespace ge {
+
+template cudaError_t launch_tc_gemm_epi<EPI_RELU_AUX_BIAS>(int, int, int, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                   const GemmArgs&, int, cudaStream_t);
+
+}  // namespace ge

@@ -33,7 +33,8 @@ enum ErrBits : unsigned int {
   ERR_PROBE_TIMEOUT = 16u,
   ERR_XFORM_TIMEOUT = 32u,
   ERR_CHAIN_TIMEOUT = 64u,
-  ERR_DEBUG_CHECK = 128u  // a GE_DEBUG build's index / offset / phase check failed
+  ERR_DEBUG_CHECK = 128u,  // a GE_DEBUG build's index / offset / phase check failed
+  ERR_PEER_TIMEOUT = 256u  // a stream-K tile's finisher waited too long for a peer's piece
 };
 
 // Checks of the GE_DEBUG build: a failed check records ERR_DEBUG_CHECK in
@@ -98,6 +99,19 @@ struct GemmArgs {
   // box; K-major operands then come through 3-D tensor maps that index the
   // panels, so K must be a multiple of 128)
   int kb;
+  // Stream-K (sk_tiles > 0; then split = 1 and there is no split-K tail):
+  // the last sk_tiles tiles are cut into I = sk_tiles * ceil(K / kb)
+  // k-block iterations, and worker w of the W = grid / (pair ? 2 : 1)
+  // workers computes iterations [w * I / W, (w + 1) * I / W) after its
+  // share of the other tiles. A worker's first stream-K segment, when it
+  // starts inside a tile, goes as fp32 to slot w of `partials`
+  // ([W][TILE_M][BN]); the worker whose segment starts the tile adds the
+  // slots of the tile's other segments in k order in its epilogue.
+  // sk_sync: [0] launch epoch, [1] finished-CTA count, [2 + cta * epi_warps
+  // + warp] the epoch + 1 at which that epilogue warp's rows of the CTA's
+  // slot are complete. Zeroed once; every launch leaves it consistent.
+  int sk_tiles;
+  unsigned int* sk_sync;
 };
 
 // pair = 1: 2-CTA clusters (cta_group::2, 256-row tiles); grid counts CTAs

@@ -39,7 +39,9 @@
  * small device workspace allocated by ge_plan_create on the device current
  * at that time (an error word; for DRELU_BGRAD / DGELU_BGRAD and
  * DW_DRELU_BGRAD the reduction partials and counters; for the norm
- * epilogues the per-token statistics; for a split-K tail its fp32 pieces).
+ * epilogues the per-token statistics; for a split-K tail its fp32 pieces;
+ * for stream-K tiles the workers' fp32 pieces and the flags that order
+ * them).
  * ge_execute never allocates and only enqueues work on the given stream;
  * the caller synchronises. Executes of one plan must be ordered on one
  * stream: two executes of the same plan that overlap on the GPU race on its
@@ -52,7 +54,10 @@
  * epilogue width; GE_GROUP_M = g sets how many M-tiles the tile order sweeps
  * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits;
  * GE_KB = 64 forces one 64-wide k panel per pipeline stage (the default is
- * two, in one TMA box per operand, when K is a multiple of 128).
+ * two, in one TMA box per operand, when K is a multiple of 128);
+ * GE_STREAM_K = 0 never shares the last waves' tiles out as stream-K k-ranges,
+ * 1 does so whenever the last wave is ragged (the default: when it is more
+ * than half full).
  * They change speed, never results beyond rounding order.
  *
  * Errors. Every call returns a status and never aborts or prints. Arguments
@@ -341,7 +346,8 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
  * ge_plan_autotune: choose the plan's kernel configuration by timing.
  * Planning picks a configuration from the problem's shape; this call instead
  * runs every candidate of the tensor-core path (128- or 256-column tiles,
- * single-CTA or 2-SM pair tiles, with and without the split-K tail) `reps` times on the caller's buffers
+ * single-CTA or 2-SM pair tiles, with and without the split-K tail or the
+ * stream-K last waves) `reps` times on the caller's buffers
  * (same meaning as ge_execute), keeps the fastest for every later execute,
  * and finishes with one execute in that configuration, so D / aux / bias
  * hold its results. It blocks the host until
@@ -352,8 +358,8 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
  * reps in 1..1000.
  * The choice is also remembered for the process (per device, M, N, K,
  * epilogue, element type and layout): plans created later for the same
- * problem start from it (unless GE_TILE_N / GE_PAIR / GE_SPLIT_TAIL are set
- * in the environment).
+ * problem start from it (unless GE_TILE_N / GE_PAIR / GE_SPLIT_TAIL /
+ * GE_STREAM_K are set in the environment).
  * Returns GE_OK or the first failing status (the plan then keeps a valid
  * configuration).
  */
@@ -370,6 +376,17 @@ void ge_autotune_cache_clear(void);
  * (1 = none); zeros for other paths. Any pointer may be NULL. Returns the
  * path, or -1 for a NULL plan. */
 int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split);
+
+/* Stream-K (tensor-core path). When the last wave of output tiles would
+ * leave workers (SMs, or SM pairs) idle, the planner may give the last
+ * `n` tiles' k-block iterations out in equal contiguous ranges, one per
+ * worker; a tile cut between workers is finished inside the GEMM by the
+ * worker whose range starts it, which adds the others' fp32 pieces in k
+ * order (bounded waits on flags in the plan workspace; an expired one
+ * reports GE_ERR_TIMEOUT through ge_get_last_device_error). Every worker of
+ * the launch has to be resident at once: the grid is the number that fits.
+ * Returns n (0: none, or not a tensor-core plan), or -1 for a NULL plan. */
+int ge_plan_stream_k_tiles(ge_plan_t plan);
 
 /* Release the plan and its device workspace (NULL is accepted). The caller
  * must make sure no execute of the plan is still running on the GPU. */

@@ -101,6 +101,7 @@ def test_plan_attr_validation(lib):
     assert ge.ge_plan_set_attr(None, ge.GE_ATTR_STATIC_A, 1, raw=True) == ge.GE_ERR_INVALID_ARG
     assert ge.ge_plan_autotune(None, None, None, None, None, raw=True) == ge.GE_ERR_INVALID_ARG
     assert ge.ge_plan_config(None)[0] == -1
+    assert ge.ge_plan_stream_k_tiles(None) == -1
 
 
 def test_null_handles(lib):

@@ -5,7 +5,7 @@ invariant (a producer never more than one phase of a stage ahead of its
 consumer). A failed check records a bit in the plan's error word and skips
 the access, so the context stays usable; ge_get_last_device_error reports
 GE_ERR_DEVICE_CHECK. The ragged, odd-shape and pair-tile GEMM tests, the
-split-K tests and the decode-stack tests run against it in a child process
+split-K and stream-K tests and the decode-stack tests run against it in a child process
 (the binding picks the library when it is first loaded)."""
 import os
 import subprocess
@@ -57,11 +57,11 @@ def test_ragged_pair_split_and_chain_tests_pass_under_checks(debug_lib):
     """Every case checks ge_get_last_device_error, so a failed device check
     fails the case."""
     sel = ("ragged or pair_tiles or 128_wide or stage_panels or split or whole or exact_integer "
-           "or every_epilogue or gemv or chain")
+           "or every_epilogue or gemv or chain or stream_k")
     out = _child(
         "import sys, pytest\n"
         "import gemm_epilogues_gb300 as ge\n"
         "assert ge.ge_debug_checks()\n"
         f"sys.exit(pytest.main(['-q', '-m', 'gpu', '-p', 'no:cacheprovider', '-k', {sel!r}, "
-        "'tests/test_gemm_gpu.py', 'tests/test_chain_gpu.py']))\n")
+        "'tests/test_gemm_gpu.py', 'tests/test_chain_gpu.py', 'tests/test_stream_k_gpu.py']))\n")
     assert " passed" in out and " failed" not in out, out[-2000:]

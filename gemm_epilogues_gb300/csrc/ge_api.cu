@@ -192,7 +192,9 @@ struct TcConfig {
 // k-values per pipeline stage for a tile shape: 128 (two 64-wide panels per
 // operand box) when K is a multiple of 128 and a stage stays within 64 KB
 // (2-SM pairs, or 128-wide single-CTA tiles); 64 otherwise, and always for
-// the masked-operand weight gradient. GE_KB = 64 | 128 forces it (sweeps).
+// the masked-operand weight gradient. GE_KB = 64 forces one panel (sweeps).
+// (Four panels, 96 KB stages, on 256 x 128 pair tiles measured slower:
+// 4096 x 512 x 4096 GELU_BIAS 26.8 vs 25.5 us.)
 int kb_for(const Plan& pl, int block_n, int pair) {
   const bool fits = pl.K % 128 == 0 && (pair || block_n == 128) && pl.epi != GE_EPI_DW_DRELU_BGRAD;
   if (const char* env = std::getenv("GE_KB"))
@@ -366,12 +368,12 @@ ge_status_t build_maps(Plan* pl, const void* A, const void* B, void* D, void* Z)
   const uint32_t b_rows = static_cast<uint32_t>(pl->pair ? pl->block_n / 2 : pl->block_n);
   const uint32_t kb = static_cast<uint32_t>(pl->kb);
   if (!a_mn)
-    ok &= kb == 128 ? make_map_panels(&pl->tmA, pl->bf16, Ak, Mk, K / 64, lda, 128, 2)
+    ok &= kb >= 128 ? make_map_panels(&pl->tmA, pl->bf16, Ak, Mk, K / 64, lda, 128, kb / 64)
                     : make_map(&pl->tmA, pl->bf16, Ak, K, Mk, lda, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     ok &= make_map(&pl->tmA, pl->bf16, Ak, Mk, K, lda, 64, kb, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!b_mn)
-    ok &= kb == 128 ? make_map_panels(&pl->tmB, pl->bf16, Bk, Nk, K / 64, ldb, b_rows, 2)
+    ok &= kb >= 128 ? make_map_panels(&pl->tmB, pl->bf16, Bk, Nk, K / 64, ldb, b_rows, kb / 64)
                     : make_map(&pl->tmB, pl->bf16, Bk, K, Nk, ldb, 64, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     ok &= make_map(&pl->tmB, pl->bf16, Bk, Nk, K, ldb, 64, kb, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -671,14 +673,16 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     // faster with four (NONE 0.452 vs 0.478 ms on the same shape; the norm
     // fusion at 4096x8192x4096: 0.235 vs 0.241 ms).
     tmp.epi_warps = epi == GE_EPI_DGELU_BGRAD ? 8 : 4;
-    // A problem of at most one wave gives each CTA one tile: its epilogue
-    // cannot overlap another tile's MMAs and is on the critical path, so
-    // eight warps take it in half the time.
+    // A problem of at most two waves has the epilogue of a CTA's last (or
+    // only) tile on its critical path, overlapped with no MMA: eight warps
+    // take it in about two thirds of the time (4096x2048x4096 GELU_BIAS:
+    // 53.5 vs 55.1 us). With more waves four are faster (11008x8192x4096:
+    // 425 vs 441 us).
     {
       const long long tm = tc_pair ? 256 : 128;
       const long long tiles = ((Mk + tm - 1) / tm) * ((Nk + tc_block_n - 1) / tc_block_n);
       const long long workers = tc_pair ? tmp.num_sms / 2 : tmp.num_sms;
-      if (tiles <= workers) tmp.epi_warps = 8;
+      if (tiles <= 2 * workers) tmp.epi_warps = 8;
     }
     if (const char* env = std::getenv("GE_EPI_WARPS")) {  // sweeps
       if (env[0] == '4') tmp.epi_warps = 4;

@@ -445,8 +445,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           // M/N-major: 64-wide chunks of KB k-rows (KB x 128 bytes each)
           constexpr uint32_t MN_CHUNK = KB * 128;
           if (!p.a_mn) {
-            if constexpr (C::PANELS == 2)
-              load3(sa, &tmA, row0, 2 * kb);
+            if constexpr (C::PANELS >= 2)
+              load3(sa, &tmA, row0, C::PANELS * kb);
             else
               load(sa, &tmA, k0, row0);
           } else {
@@ -454,8 +454,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             load(sa + MN_CHUNK, &tmA, row0 + 64, k0);
           }
           if (!p.b_mn) {
-            if constexpr (C::PANELS == 2)
-              load3(sb, &tmB, col0, 2 * kb);
+            if constexpr (C::PANELS >= 2)
+              load3(sb, &tmB, col0, C::PANELS * kb);
             else
               load(sb, &tmB, k0, col0);
           } else {
@@ -742,24 +742,34 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
       }
       uint32_t zw[16];
       if (needs_z) load_slab16(p, grow, nt * BN + 32 * hh, zw);
-      // The bias is requested before the wait as well: per row, this
-      // thread's value; per column, one value per lane for each slab (lane l
-      // holds column 32c + l; the slab's 32 values are then broadcast by
-      // shuffles), the first now and each later one a slab ahead.
+      // The bias is requested before the wait as well, the first slab's now
+      // and each later one's a slab ahead, and kept as loaded (converted at
+      // use, so a load in flight stalls nothing): per row, this thread's
+      // value; per column, with a 16-byte aligned bias, the slab's 32 raw
+      // values in every lane (four 16-byte loads of one address, a
+      // broadcast); otherwise, and for a slab that runs past Nk, lane l
+      // holds column 32c + l and the 32 values are broadcast by shuffles.
       float brow = 0.0f;
       if (has_bias && !p.bias_per_col && grow < p.Mk) brow = to_f32(bf16, bias16[grow]);
-      // Per column, with a 16-byte aligned bias: the slab's 64-byte run is
-      // asked into L1 a slab ahead and read at use by every lane with four
-      // 16-byte loads of one address (a broadcast). Otherwise (and for a
-      // slab that runs past Nk) lane l holds column 32c + l, broadcast by
-      // shuffles; the lane value is kept as loaded and converted at use, so
-      // the next slab's load does not stall this one.
       const bool bias_cols = has_bias && p.bias_per_col;
       const bool bias_vec = bias_cols && (reinterpret_cast<uintptr_t>(bias16) & 15u) == 0;
       auto bias_lane = [&](int gc) -> unsigned short {
         return bias_cols && !bias_vec && gc < p.Nk ? bias16[gc] : static_cast<unsigned short>(0);
       };
-      if (bias_vec && lane == 0 && nt * BN + 32 * hh < p.Nk) prefetch_l1(bias16 + nt * BN + 32 * hh);
+      auto bias_run = [&](int gc, uint4 (&b)[4]) {
+        if (bias_vec && gc + 32 <= p.Nk) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) b[i] = __ldg(reinterpret_cast<const uint4*>(bias16 + gc) + i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) b[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      // (with eight epilogue warps a thread has 168 registers: the slab's
+      // run is then loaded at the slab's start, behind its TMEM load)
+      constexpr bool kBiasAhead = EPIW == 4;
+      uint4 bq[4];
+      if constexpr (kBiasAhead) bias_run(nt * BN + 32 * hh, bq);
       unsigned short bl = bias_lane(nt * BN + 32 * hh + lane);
       // Stream-K finisher: the workers sk_w0 .. sk_w1 - 1 hold the rest of
       // this tile's k-range (their first segments, spilled early in their
@@ -794,7 +804,25 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
         }
         fok = __shfl_sync(0xffffffffu, fok, 0);
         if (!fok) break;
+        // every lane acquires the flags too (its loads of the pieces come
+        // after), then asks the first slab's pieces into L1
+        for (int wq = sk_w0; wq < sk_w1; ++wq)
+          if (sk_begin(wq + 1, sk_iters, tile_step) != sk_begin(wq, sk_iters, tile_step))
+            (void)ld_acquire_gpu(p.sk_sync + 2 + (static_cast<long long>(wq) * CL + static_cast<int>(pr)) * EPIW + (warp - 2));
       }
+      // The pieces of slab c of this warp: 4 KB per worker slot (8 chunks of
+      // 512 bytes); lane l asks line l of each into L1 a slab ahead of use.
+      auto piece_chunks = [&](int wq, int c) -> const uint4* {
+        return reinterpret_cast<const uint4*>(
+                   p.partials + (static_cast<long long>(wq) * C::TILE_M + static_cast<int>(pr) * BM) * BN) +
+               static_cast<long long>((q * (BN / 32) + c) * 8) * 32;
+      };
+      auto piece_prefetch = [&](int c) {
+        for (int wq = sk_w0; wq < sk_w1; ++wq)
+          if (sk_begin(wq + 1, sk_iters, tile_step) != sk_begin(wq, sk_iters, tile_step))
+            prefetch_l1(piece_chunks(wq, c) + 8 * lane);
+      };
+      if (finish) piece_prefetch(hh);
       // The worker's first tile epilogue (v < 0) is preceded by a dry pass
       // over its first slab while the accumulator is still being computed:
       // the same instructions (the pass loop is not unrolled) without TMEM
@@ -893,7 +921,12 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             mword = p.aux[static_cast<long long>(grow) * p.ld_aux + (gcol0 >> 5)];
           uint32_t znext[16];
           if (!dry && needs_z && c + C::HALVES < BN / 32) load_slab16(p, grow, gcol0 + 32 * C::HALVES, znext);
-          if (bias_vec && lane == 0 && gcol0 + 32 * C::HALVES < p.Nk) prefetch_l1(bias16 + gcol0 + 32 * C::HALVES);
+          uint4 bq_next[4];
+          if constexpr (kBiasAhead)
+            bias_run(gcol0 + 32 * C::HALVES, bq_next);
+          else
+            bias_run(gcol0, bq);
+          if (finish && !dry && c + C::HALVES < BN / 32) piece_prefetch(c + C::HALVES);
           const unsigned short bl_next = bias_lane(gcol0 + 32 * C::HALVES + lane);
           uint32_t v[32];
           (void)GE_DCHECK(acc * BN + 32 * c + 32 <= C::TMEM_COLS && gcol0 % 32 == 0 && rbase % 32 == 0 &&
@@ -911,12 +944,10 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
 #pragma unroll 1
             for (int wq = sk_w0; wq < sk_w1; ++wq) {
               if (sk_begin(wq + 1, sk_iters, tile_step) == sk_begin(wq, sk_iters, tile_step)) continue;
-              const uint4* src = reinterpret_cast<const uint4*>(
-                                     p.partials + (static_cast<long long>(wq) * C::TILE_M + static_cast<int>(pr) * BM) * BN) +
-                                 static_cast<long long>((q * (BN / 32) + c) * 8) * 32 + lane;
+              const uint4* src = piece_chunks(wq, c) + lane;
               uint4 pv[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) pv[i] = ld_cg_u4(src + 32 * i);
+              for (int i = 0; i < 8; ++i) pv[i] = src[32 * i];  // (in L1: asked for a slab ahead)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + __uint_as_float(pv[i].x));
@@ -928,10 +959,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           }
           float bcol[32];
           if (bias_vec && gcol0 + 32 <= p.Nk) {
-            const uint4* bsrc = reinterpret_cast<const uint4*>(bias16 + gcol0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint4 b = __ldg(bsrc + i);
+              const uint4 b = bq[i];
               const float2 f0 = to_f32x2(bf16, b.x), f1 = to_f32x2(bf16, b.y);
               const float2 f2 = to_f32x2(bf16, b.z), f3 = to_f32x2(bf16, b.w);
               bcol[8 * i] = f0.x;
@@ -953,7 +983,13 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) bcol[j] = brow;  // the row's bias (0 without one)
           }
-          if (!dry) bl = bl_next;
+          if (!dry) {
+            bl = bl_next;
+            if constexpr (kBiasAhead) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) bq[i] = bq_next[i];
+            }
+          }
           uint32_t packed[16];
           uint32_t zpacked[16];
           uint32_t bits = 0;

@@ -153,7 +153,7 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
 }
 
 // Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
-// One line into this SM's L1 (a later load of it then hits).
+// One line into this SM's L1 (a later cached load of it then hits).
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }

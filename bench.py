@@ -73,8 +73,8 @@ ROW_CASES.update({
 })
 
 
-def kernel_source_hash(files=("gemm_epilogues_gb300/csrc/ge_gemm.cu", "gemm_epilogues_gb300/csrc/ge_ptx.cuh",
-                               "gemm_epilogues_gb300/csrc/ge_internal.h")) -> str:
+def kernel_source_hash(files=("gemm_epilogues_gb300/csrc/ge_gemm.cu", "gemm_epilogues_gb300/csrc/ge_gemm_kernel.cuh",
+                               "gemm_epilogues_gb300/csrc/ge_ptx.cuh", "gemm_epilogues_gb300/csrc/ge_internal.h")) -> str:
     """Hash of the GEMM kernel's code: comments and blank lines are left out,
     so a change of wording alone does not invalidate a capture."""
     import hashlib
@@ -133,8 +133,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
 
@@ -142,7 +143,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -588,13 +589,15 @@ def _graph_device_ms(run, flush_fn, reps, rounds=5):
     return statistics.median(out)
 
 
-def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
+def run_config_table(dev, peaks, flush, keep_cpu_inputs=False, gpu_index=0):
     """Every workload config alone on this GPU: per-launch CUDA-event times
-    after a read-only L2 flush (median and p90 over >= 50 launches after 10
-    warm-ups; the 17.6-TFLOP config 5 over 10), the roofline of each config
-    (the faster of the tensor peak and its bytes at the copy rate), the same
-    engine's unfused three-kernel sequence, and for microsecond launches the
-    device time from graph replays. Returns (entries, cpu_inputs) where
+    after an L2 flush (median and p90 over >= 50 launches after 10 warm-ups;
+    the 17.6-TFLOP config 5 over 10), the SM clock and throttle reasons
+    sampled during each config's timed launches, the roofline of each config
+    (the faster of the burst tensor peak and its bytes at the copy rate; a
+    tensor-bound config also gets its fraction of the sustained peak), the
+    same engine's unfused three-kernel sequence, and for microsecond launches
+    the device time from graph replays. Returns (entries, cpu_inputs) where
     cpu_inputs are host copies of the inputs the oracle baselines use."""
     import torch
     import gemm_epilogues_gb300 as ge
@@ -606,9 +609,14 @@ def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
     hbm = peaks["hbm_gbs"] * 1e9
     out, cpu_in = {}, {}
 
-    def timed(fn, warm, reps):
+    last_clocks = {}
+
+    def timed(fn, warm, reps, sample=False):
         ts = []
+        cs = ClockSampler(gpu_index, 20) if sample else None
         for i in range(warm + reps):
+            if cs is not None and i == warm:
+                cs.start()
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -617,6 +625,9 @@ def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
             torch.cuda.synchronize()
             if i >= warm:
                 ts.append(e0.elapsed_time(e1))
+        if cs is not None:
+            last_clocks.clear()
+            last_clocks.update(cs.stop())
         return ts
 
     for key, wk in CONFIG_TABLE:
@@ -634,14 +645,15 @@ def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
             bgrad = torch.empty(M, dtype=torch.float32, device=dev)
             plan = ge.Plan(M, N, 0, ge.GE_EPI_DRELU_BGRAD, ge.make_layout(d=ge.GE_D_COL))
             run = lambda: plan.execute(dY, None, bgrad, dZ, aux, stream)
-            ts = timed(run, warm, reps)
+            ts = timed(run, warm, reps, sample=True)
             assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
             nbytes = 2 * N * M * 2 + 4 * N * ld_aux + 4 * M
             med = statistics.median(ts)
             out[key] = {"workload": f"DRELU_BGRAD dY[{N},{M}] + mask -> dZ, fp32 bgrad[{M}]", "path": "drelu",
                         "ms": med, "p90_ms": _pct(ts, 0.9), "reps": reps, "gbs": nbytes / (med * 1e-3) / 1e9,
                         "algorithmic_bytes": nbytes, "bound": "hbm",
-                        "frac_of_roofline": nbytes / hbm / (med * 1e-3), "roofline_gbs": peaks["hbm_gbs"]}
+                        "frac_of_roofline": nbytes / hbm / (med * 1e-3), "roofline_gbs": peaks["hbm_gbs"],
+                        "clocks": dict(last_clocks)}
             if keep_cpu_inputs:
                 cpu_in[key] = (dY.cpu(), aux.cpu(), M, N, ld_aux)
             plan.free()
@@ -660,7 +672,7 @@ def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
         aux_arg = aux if w.epilogue == "relu_aux_bias" else None
         # (the stream is looked up at each call: graph capture runs on its own)
         run = lambda: plan.execute(A, B, bias_arg, D, aux_arg, torch.cuda.current_stream())
-        ts = timed(run, warm, reps)
+        ts = timed(run, warm, reps, sample=True)
         assert ge.ge_get_last_device_error(plan.handle) == ge.GE_OK
         med = statistics.median(ts)
         flops, nbytes = w.flops, w.algorithmic_bytes()
@@ -673,7 +685,10 @@ def run_config_table(dev, peaks, flush, keep_cpu_inputs=False):
              "flops": flops, "algorithmic_bytes": nbytes,
              "bound": "hbm" if nbytes / hbm > flops / tpk else "tensor",
              "roofline_tflops": flops / t_roof / 1e12, "frac_of_roofline": t_roof / (med * 1e-3),
-             "frac_of_tensor_peak": flops / (med * 1e-3) / tpk}
+             "frac_of_tensor_peak": flops / (med * 1e-3) / tpk,
+             "clocks": dict(last_clocks)}
+        if e["bound"] == "tensor":
+            e["frac_of_sustained_peak"] = flops / (med * 1e-3) / (peaks["tflops_sustained"] * 1e12)
         if key in _MICRO:
             g = _graph_device_ms(run, flush.zero_, 20)
             if g is not None and g > 0:
@@ -1148,7 +1163,8 @@ def run_ours(args, world, rank, local):
     # ---- every workload config alone (one GPU; replicas skip it)
     configs, cfg_cpu_in = None, {}
     if world == 1 and not args.no_configs:
-        configs, cfg_cpu_in = run_config_table(dev, peaks, flush, keep_cpu_inputs=not args.no_cpu_baseline)
+        configs, cfg_cpu_in = run_config_table(dev, peaks, flush, keep_cpu_inputs=not args.no_cpu_baseline,
+                                               gpu_index=local)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -77,6 +77,13 @@ struct Plan {
   // ge_execute_chain: the weight and bias pointers verified so far, with
   // their allocations' ids
   std::map<const void*, unsigned long long> chain_checked;
+  // DW_DRELU_BGRAD run as two launches (the default): the standalone
+  // DRELU_BGRAD pass into dz_ws ([K][lda] elements), then the NONE GEMM on
+  // it; bg_scratch takes the bias gradient when the caller wants none.
+  Plan* sub_drelu = nullptr;
+  Plan* sub_gemm = nullptr;
+  void* dz_ws = nullptr;
+  float* bg_scratch = nullptr;
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -787,6 +794,35 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       return st;
     }
   }
+  // DW_DRELU_BGRAD as two launches unless GE_DW_MASK = gemm asks for the
+  // mask applied inside the GEMM (measured at 11008 x 4096 x 8192: 0.46 ms
+  // for the two launches, 1.74 ms in one: the masking warps' shared-memory
+  // pass and their hand-off to the MMA cost more than the dZ round trip).
+  const char* dw_env = std::getenv("GE_DW_MASK");
+  if (pl->path == GE_PATH_TC_GEMM && dw_mask && !(dw_env && dw_env[0] == 'g')) {
+    const ge_layout_t Ld{GE_K_MAJOR, GE_MN_MAJOR, GE_D_COL, 0, 0, L.lda, L.ld_aux};
+    const ge_layout_t Lg{GE_MN_MAJOR, L.b, GE_D_ROW, L.lda, L.ldb, L.ldd, 0};
+    ge_plan_t hd = nullptr, hg = nullptr;
+    ge_status_t st = ge_plan_create(&hd, M, K, 0, a, b, d, compute, GE_EPI_DRELU_BGRAD, &Ld);
+    if (st == GE_OK) st = ge_plan_create(&hg, M, N, K, a, b, d, compute, GE_EPI_NONE, &Lg);
+    const size_t dz_bytes = static_cast<size_t>(K) * static_cast<size_t>(L.lda) * 2;
+    const size_t bg_off = (dz_bytes + 255) / 256 * 256;
+    void* dz = nullptr;
+    if (st == GE_OK && cudaMalloc(&dz, bg_off + static_cast<size_t>(M) * 4) != cudaSuccess) {
+      cudaGetLastError();
+      st = GE_ERR_OOM;
+    }
+    if (st != GE_OK) {
+      ge_plan_free(hd);
+      ge_plan_free(hg);
+      ge_plan_free(reinterpret_cast<ge_plan_t>(pl));
+      return st;
+    }
+    pl->sub_drelu = reinterpret_cast<Plan*>(hd);
+    pl->sub_gemm = reinterpret_cast<Plan*>(hg);
+    pl->dz_ws = dz;
+    pl->bg_scratch = reinterpret_cast<float*>(static_cast<char*>(dz) + bg_off);
+  }
   *out = reinterpret_cast<ge_plan_t>(pl);
   return GE_OK;
 }
@@ -795,6 +831,14 @@ ge_status_t ge_execute(ge_plan_t plan, const void* A, const void* B, const void*
                        void* aux, void* stream) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl) return GE_ERR_INVALID_ARG;
+  if (pl->sub_gemm) {
+    // DW_DRELU_BGRAD as two launches: dZ = dY * mask (+ bgrad), then dW = dZ^T . B
+    if (!A || !B || !D || !aux) return GE_ERR_INVALID_ARG;
+    void* bg = bias ? const_cast<void*>(bias) : static_cast<void*>(pl->bg_scratch);
+    ge_status_t s1 = ge_execute(reinterpret_cast<ge_plan_t>(pl->sub_drelu), A, nullptr, bg, pl->dz_ws, aux, stream);
+    if (s1 != GE_OK) return s1;
+    return ge_execute(reinterpret_cast<ge_plan_t>(pl->sub_gemm), pl->dz_ws, B, nullptr, D, nullptr, stream);
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ge_status_t s;
   if (epi_is_norm(pl->epi)) return GE_ERR_UNSUPPORTED;  // ge_execute_norm
@@ -1005,6 +1049,14 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl || reps < 1 || reps > 1000) return GE_ERR_INVALID_ARG;
   if (pl->path != GE_PATH_TC_GEMM) return GE_OK;  // nothing to choose
+  if (pl->sub_gemm) {  // two launches: tune the GEMM on this call's dZ
+    if (!A || !B || !D || !aux) return GE_ERR_INVALID_ARG;
+    void* bg = bias ? const_cast<void*>(bias) : static_cast<void*>(pl->bg_scratch);
+    ge_status_t s1 = ge_execute(reinterpret_cast<ge_plan_t>(pl->sub_drelu), A, nullptr, bg, pl->dz_ws, aux, stream);
+    if (s1 != GE_OK) return s1;
+    return ge_plan_autotune(reinterpret_cast<ge_plan_t>(pl->sub_gemm), pl->dz_ws, B, nullptr, D, nullptr, stream,
+                            reps);
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const TcConfig current = tc_config(*pl, pl->block_n, pl->pair, pl->split > 1 || pl->tc_allow_split);
   TcConfig cands[8];
@@ -1060,6 +1112,7 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
 int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl) return -1;
+  if (pl->sub_gemm) return ge_plan_config(reinterpret_cast<ge_plan_t>(pl->sub_gemm), block_n, pair, split);
   if (block_n) *block_n = pl->path == GE_PATH_TC_GEMM ? pl->block_n : 0;
   if (pair) *pair = pl->path == GE_PATH_TC_GEMM ? pl->pair : 0;
   if (split) *split = pl->path == GE_PATH_TC_GEMM ? pl->split : 0;
@@ -1069,6 +1122,7 @@ int ge_plan_config(ge_plan_t plan, int* block_n, int* pair, int* split) {
 int ge_plan_stream_k_tiles(ge_plan_t plan) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
   if (!pl) return -1;
+  if (pl->sub_gemm) return ge_plan_stream_k_tiles(reinterpret_cast<ge_plan_t>(pl->sub_gemm));
   return pl->path == GE_PATH_TC_GEMM ? pl->sk_tiles : 0;
 }
 
@@ -1096,8 +1150,14 @@ ge_status_t ge_plan_free(ge_plan_t plan) {
     cudaGetLastError();
     s = GE_ERR_CUDA;
   }
+  if (pl->dz_ws && cudaFree(pl->dz_ws) != cudaSuccess) {
+    cudaGetLastError();
+    s = GE_ERR_CUDA;
+  }
+  const ge_status_t s1 = ge_plan_free(reinterpret_cast<ge_plan_t>(pl->sub_drelu));
+  const ge_status_t s2 = ge_plan_free(reinterpret_cast<ge_plan_t>(pl->sub_gemm));
   delete pl;
-  return s;
+  return s != GE_OK ? s : (s1 != GE_OK ? s1 : s2);
 }
 
 size_t ge_aux_bytes(ge_plan_t plan) {
@@ -1122,6 +1182,7 @@ int ge_plan_path(ge_plan_t plan) {
 
 int ge_plan_tile_n(ge_plan_t plan) {
   Plan* pl = reinterpret_cast<Plan*>(plan);
+  if (pl && pl->sub_gemm) return ge_plan_tile_n(reinterpret_cast<ge_plan_t>(pl->sub_gemm));
   return (pl && pl->path == GE_PATH_TC_GEMM) ? pl->block_n : 0;
 }
 
@@ -1135,8 +1196,16 @@ ge_status_t ge_get_last_device_error(ge_plan_t plan) {
     cudaGetLastError();
     return GE_ERR_CUDA;
   }
-  if (w & ERR_DEBUG_CHECK) return GE_ERR_DEVICE_CHECK;
-  return w ? GE_ERR_TIMEOUT : GE_OK;
+  ge_status_t s = (w & ERR_DEBUG_CHECK) ? GE_ERR_DEVICE_CHECK : (w ? GE_ERR_TIMEOUT : GE_OK);
+  // a plan run as two launches: their own words too (the gravest status wins:
+  // a failed read, then a failed check, then an expired wait)
+  auto rank = [](ge_status_t x) { return x == GE_ERR_CUDA ? 3 : x == GE_ERR_DEVICE_CHECK ? 2 : x == GE_ERR_TIMEOUT ? 1 : 0; };
+  for (Plan* sub : {pl->sub_drelu, pl->sub_gemm}) {
+    if (!sub) continue;
+    const ge_status_t t = ge_get_last_device_error(reinterpret_cast<ge_plan_t>(sub));
+    if (rank(t) > rank(s)) s = t;
+  }
+  return s;
 }
 
 ge_status_t ge_debug_wait_timeout(ge_plan_t plan, int64_t budget_cycles, void* stream) {

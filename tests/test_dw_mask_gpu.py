@@ -1,10 +1,13 @@
 """DW_DRELU_BGRAD: the weight-gradient GEMM of a RELU_AUX_BIAS layer with the
-ReLU backward applied to its A operand (dY) as the kernel loads it, and the
-bias gradient reduced in the same pass. Against the oracle (the pinned
-DRELU_BGRAD and GEMM steps composed): ragged extents and pitches, 1-CTA and
-2-SM tiles, split-K pieces, bf16, no bias-gradient output; at the MLP size
-on sampled features, and bit-identical to the unfused flow (standalone
-DRELU_BGRAD, then the same GEMM on the stored dZ)."""
+ReLU backward applied to its A operand (dY), and the bias gradient. Every
+test runs in both forms of the plan: the default two launches (the
+standalone DRELU_BGRAD pass into the plan's dZ buffer, then the NONE GEMM on
+it) and, with GE_DW_MASK=gemm, the mask applied inside the GEMM as the
+kernel loads its operand (bias gradient reduced in the same pass). Against
+the oracle (the pinned DRELU_BGRAD and GEMM steps composed): ragged extents
+and pitches, 1-CTA and 2-SM tiles, split-K pieces, bf16, no bias-gradient
+output; at the MLP size on sampled features, and bit-identical to the
+unfused flow run by hand."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +20,15 @@ from _util import GE_DT, bits, check_bgrad, check_f16
 pytestmark = pytest.mark.gpu
 
 MN, ROW = ge.GE_MN_MAJOR, ge.GE_D_ROW
+
+
+@pytest.fixture(autouse=True, params=["two_launches", "in_gemm"])
+def dw_mask_form(request, monkeypatch):
+    if request.param == "in_gemm":
+        monkeypatch.setenv("GE_DW_MASK", "gemm")
+    else:
+        monkeypatch.delenv("GE_DW_MASK", raising=False)
+    return request.param
 
 
 def _pad8(x):

@@ -74,9 +74,11 @@ ROW_CASES.update({
 
 
 def kernel_source_hash(files=("gemm_epilogues_gb300/csrc/ge_gemm.cu", "gemm_epilogues_gb300/csrc/ge_gemm_kernel.cuh",
-                               "gemm_epilogues_gb300/csrc/ge_ptx.cuh", "gemm_epilogues_gb300/csrc/ge_internal.h")) -> str:
-    """Hash of the GEMM kernel's code: comments and blank lines are left out,
-    so a change of wording alone does not invalidate a capture."""
+                               "gemm_epilogues_gb300/csrc/ge_ptx.cuh", "gemm_epilogues_gb300/csrc/ge_internal.h",
+                               "gemm_epilogues_gb300/csrc/ge_api.cu")) -> str:
+    """Hash of the GEMM kernel's code and of the planner that picks its tile
+    order (which moves its DRAM traffic): comments and blank lines are left
+    out, so a change of wording alone does not invalidate a capture."""
     import hashlib
     import re
     h = hashlib.sha256()

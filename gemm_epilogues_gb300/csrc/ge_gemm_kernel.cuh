@@ -847,19 +847,26 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           }
           tc_fence_after();
           if (v >= 0) {
-            // Split-K unit: spill the fp32 accumulator rows to the workspace
-            // (the fixup kernel adds the splits and applies the epilogue); a
-            // stream-K segment (u < 0): to the worker's slot, for the finisher.
-            // A stream-K slot holds each warp's slabs lane-interleaved (16-byte
-            // chunk i of lane l of slab c at ((q * BN / 32 + c) * 8 + i) * 32 + l
-            // in the CTA's half), so every store and the finisher's every load
-            // covers 512 contiguous bytes; the split-K pieces keep rows of BN
-            // values for the fixup kernel.
+            // Split-K unit: spill the fp32 accumulator rows to its piece of
+            // the workspace ([TILE_M][BN], read row-wise by the fixup kernel,
+            // which adds the pieces and applies the epilogue). Each 32 x 32
+            // slab goes through the warp's staging buffer (4 KB: 16-byte
+            // chunk j of row r at chunk j ^ (r & 7)) so that every global
+            // store covers 4 rows x 128 bytes; written straight from the
+            // lanes (a row each, 16 bytes 1 KB apart) the spill of a 256 x
+            // 256 tile took ~9 us. A stream-K segment (u < 0) goes to the
+            // worker's slot, which holds each warp's slabs lane-interleaved
+            // (chunk i of lane l of slab c at ((q * BN / 32 + c) * 8 + i) *
+            // 32 + l in the CTA's half): every store and the finisher's every
+            // load covers 512 contiguous bytes.
             (void)GE_DCHECK(u >= 0 || v == first_tile, p.err);
-            float* prow = p.partials + (static_cast<long long>(v) * C::TILE_M + static_cast<int>(pr) * BM +
-                                        q * 32 + lane) * BN;
+            float* prow0 = p.partials + (static_cast<long long>(v) * C::TILE_M + static_cast<int>(pr) * BM + q * 32) * BN;
             uint4* slot = reinterpret_cast<uint4*>(p.partials + (static_cast<long long>(v) * C::TILE_M +
                                                                  static_cast<int>(pr) * BM) * BN);
+            if (u >= 0) {  // the staging buffer is free once this warp's stores have read it
+              if (lane == 0) bulk_wait_group_read<0>();
+              __syncwarp();
+            }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -873,10 +880,19 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
                 for (int i = 0; i < 8; ++i)
                   dst[32 * i] = make_uint4(vv[4 * i], vv[4 * i + 1], vv[4 * i + 2], vv[4 * i + 3]);
               } else {
-                uint4* dst = reinterpret_cast<uint4*>(prow + c * 32);
+                uint4* st4 = reinterpret_cast<uint4*>(stg);
+                __syncwarp();  // the previous slab has been read back
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  dst[i] = make_uint4(vv[4 * i], vv[4 * i + 1], vv[4 * i + 2], vv[4 * i + 3]);
+                for (int j = 0; j < 8; ++j)
+                  st4[lane * 8 + (j ^ (lane & 7))] = make_uint4(vv[4 * j], vv[4 * j + 1], vv[4 * j + 2], vv[4 * j + 3]);
+                __syncwarp();
+                // lane l: chunk l & 7 of rows 4i + l / 8
+                const int ch = lane & 7;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const int r = 4 * i + (lane >> 3);
+                  reinterpret_cast<uint4*>(prow0 + static_cast<long long>(r) * BN + c * 32)[ch] = st4[r * 8 + (ch ^ (r & 7))];
+                }
               }
             }
             if (u < 0) {

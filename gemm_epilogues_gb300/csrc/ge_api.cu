@@ -229,6 +229,7 @@ TuneKey tune_key(const Plan& pl) {
 }
 
 TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
+  if (block_n == 224) allow_split = false;  // the fixup reads 128-column groups
   TcConfig c;
   c.block_n = block_n;
   c.pair = pair;
@@ -663,9 +664,11 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     // with them), so 128-wide tiles are used only when 256-wide ones would
     // leave more than half of the SMs without a tile.
     tc_block_n = (Nk <= 128 || t256 * 2 < tmp.num_sms) ? 128 : 256;
+    int want_n = 0;
     if (const char* env = std::getenv("GE_TILE_N")) {  // tile-width sweeps
-      const int want = std::atoi(env);
-      if (want == 128 || want == 256) tc_block_n = want;
+      want_n = std::atoi(env);
+      if (want_n == 128 || want_n == 256) tc_block_n = want_n;
+      if (want_n == 224) tc_block_n = 256;  // (narrowed below when the layout allows)
     }
     // 2-CTA pairs (256-row tiles) once there are enough of them to give
     // every pair of SMs at least one tile.
@@ -674,6 +677,22 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (const char* env = std::getenv("GE_PAIR")) {
       if (env[0] == '0') tc_pair = 0;
       if (env[0] == '1') tc_pair = 1;
+    }
+    // 256 x 224 pair tiles when 256-wide ones end in a last wave too full
+    // for the split-K tail and the narrower tiles make the waves come out
+    // shorter: e.g. 4096 x 2048 x 4096 (D column-major): 128 tiles of 256 x
+    // 256 on 76 pairs (two waves, the second 68 % full) or 152 of 256 x 224
+    // (two full waves of tiles an eighth shorter). K-major B' only (its 112
+    // rows a CTA are staged in 128-byte swizzle rows), no split-K tail.
+    const bool bmn_k = tmp.swap ? (L.a == GE_MN_MAJOR) : (L.b == GE_MN_MAJOR);
+    if (tc_pair && tc_block_n == 256 && !bmn_k && !dw_mask) {
+      const long long W = tmp.num_sms / 2;
+      const long long m_t = (Mk + 255) / 256;
+      const long long t256p = m_t * ((Nk + 255) / 256), t224p = m_t * ((Nk + 223) / 224);
+      const long long rem = t256p % W;
+      const bool ragged = rem != 0 && rem * 2 > W;
+      const long long cost256 = (t256p + W - 1) / W * 256, cost224 = (t224p + W - 1) / W * 224;
+      if (want_n == 224 || (want_n == 0 && ragged && cost224 * 100 < cost256 * 95)) tc_block_n = 224;
     }
     if (const char* env = std::getenv("GE_SPLIT_TAIL"))
       if (env[0] == '0') tc_split = false;
@@ -1066,9 +1085,11 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
   const TcConfig current = tc_config(*pl, pl->block_n, pl->pair, pl->split > 1 || pl->tc_allow_split);
   TcConfig cands[8];
   int n = 0;
-  for (int bn : {128, 256})
+  const bool b_mn_k = pl->swap ? (pl->L.a == GE_MN_MAJOR) : (pl->L.b == GE_MN_MAJOR);
+  for (int bn : {128, 256, 224})
     for (int pair : {0, 1}) {
-      if (pair && bn != 256) continue;
+      if (pair && bn == 128) continue;
+      if (bn == 224 && (!pair || b_mn_k || pl->epi == GE_EPI_DW_DRELU_BGRAD)) continue;
       cands[n++] = tc_config(*pl, bn, pair, false);
       if (pl->tc_allow_split) {
         const TcConfig c = tc_config(*pl, bn, pair, true);

@@ -91,7 +91,11 @@ struct Cfg {
   // misc: TMEM address, abort flag, a flag that is never set, then (GE_DEBUG)
   // the producer's fill count of each stage
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 4 * 8 + 1024;  // + 1 KB for base alignment
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = 2 * BN;  // columns in use (two accumulators)
+  // the allocation: a power of two of at least 32 columns
+  static constexpr int TMEM_ALLOC = TMEM_COLS <= 32 ? 32 : TMEM_COLS <= 64 ? 64 : TMEM_COLS <= 128 ? 128
+                                  : TMEM_COLS <= 256 ? 256 : 512;
+  static_assert(TMEM_COLS <= 512 && B_ROWS % 8 == 0, "tile width");
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;
   static constexpr int EPI_ARRIVALS = PAIR ? 2 * EPI_WARPS : EPI_WARPS;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -337,10 +341,10 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   }
   if (warp == 1) {
     if constexpr (PAIR) {
-      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_ALLOC);
       tmem_relinquish_pair();
     } else {
-      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_ALLOC);
       tmem_relinquish();
     }
   }
@@ -459,8 +463,11 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             else
               load(sb, &tmB, k0, col0);
           } else {
+            // (an N-major B is staged in 64-wide chunks: B_ROWS a multiple of 64)
+            if constexpr (C::B_ROWS % 64 == 0) {
 #pragma unroll
-            for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + MN_CHUNK * j, &tmB, col0 + 64 * j, k0);
+              for (int j = 0; j < C::B_ROWS / 64; ++j) load(sb + MN_CHUNK * j, &tmB, col0 + 64 * j, k0);
+            }
           }
           ++fills;
 #ifdef GE_DEBUG
@@ -919,8 +926,14 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
         float st_n = 0.0f, st_mean = 0.0f, st_m2 = 0.0f;  // BIAS_RESIDUAL statistics of this row
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * BN);
+        // the last n-tile also writes the mask's zero padding words up to
+        // the next multiple of 128 columns (a tile narrower than 128 -- 224
+        // wide -- can end before it)
+        const int c_end = (EPI == EPI_RELU_AUX_BIAS && nt == num_n - 1)
+                              ? max(BN / 32, ((((p.Nk + 127) & ~127) - nt * BN) + 31) / 32)
+                              : BN / 32;
 #pragma unroll 1
-        for (int c = hh; c < BN / 32; c += C::HALVES) {
+        for (int c = hh; c < c_end; c += C::HALVES) {
           if (dry && c != hh) break;
           const int gcol0 = nt * BN + c * 32;
           if (gcol0 >= p.Nk) {
@@ -1138,9 +1151,9 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   if (warp == 1) {
     tc_fence_after();
     if constexpr (PAIR)
-      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+      tmem_dealloc_pair(tmem_base, C::TMEM_ALLOC);
     else
-      tmem_dealloc(tmem_base, C::TMEM_COLS);
+      tmem_dealloc(tmem_base, C::TMEM_ALLOC);
   }
   if (p.sk_tiles > 0 && threadIdx.x == 0) {
     // The last CTA of the launch to get here moves the epoch on, so the
@@ -1207,6 +1220,11 @@ cudaError_t launch_width(int block_n, int pair, const CUtensorMap& tmA, const CU
     }
   } else {
     if (args.amask) return cudaErrorInvalidValue;
+  }
+  if (block_n == 224) {  // 256 x 224 pair tiles, K-major B' only (112 rows a CTA)
+    if (!pair || args.b_mn) return cudaErrorInvalidValue;
+    if (args.kb == 128) return launch_impl<EPI, 224, true, EPIW, false, 128>(tmA, tmB, tmD, tmZ, args, grid, stream);
+    return launch_impl<EPI, 224, true, EPIW>(tmA, tmB, tmD, tmZ, args, grid, stream);
   }
   if (args.kb == 128) {  // stages of two panels (64 KB at most a stage)
     if (pair) {

@@ -227,6 +227,36 @@ def test_stage_panels_exact_integer(oracle, monkeypatch, kb, epi):
         _run_case(oracle, 520, 776, 384, epi, "m", "k", "col", dist=("int", 2.0), seed=43, exact=True)
 
 
+@pytest.mark.parametrize("epi", EPIS + ["gelu_erf_bias"])
+def test_pair_tiles_224_wide(oracle, monkeypatch, epi):
+    """256 x 224 pair tiles (112 B' rows a CTA, 448 of 512 TMEM columns):
+    K-major B' only; N a multiple of 224, ragged (a last tile 64 wide, and
+    odd), integer data bit-identical, normal data in tolerance."""
+    monkeypatch.setenv("GE_TILE_N", "224")
+    monkeypatch.setenv("GE_PAIR", "1")
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    with ge.Plan(1344, 512, 512, ge.EPILOGUE_BY_NAME[epi], L) as p:
+        assert p.config[1:4] == (224, 1, 1)
+    exact = epi not in ("gelu_bias", "gelu_erf_bias")
+    dist = ("int", 2.0) if exact else ("normal", 1.0)
+    # D column-major: the kernel's N is M (1344 = 6 x 224; 1000; 4096 = 18 x 224 + 64)
+    _run_case(oracle, 1344, 512, 512, epi, "k", "k", "col", dist=dist, seed=80, exact=exact)
+    _run_case(oracle, 1000, 300, 640, epi, "k", "k", "col", dist=dist, seed=81, exact=exact)
+    _run_case(oracle, 520, 776, 384, epi, "m", "k", "row", dist=dist, seed=82, exact=exact)
+
+
+def test_pair_tiles_224_chosen_for_two_ragged_waves():
+    """The planner takes 256 x 224 pair tiles where 256 x 256 ones leave a
+    second wave too full for the split tail (FFN up-projection, T = 2048),
+    and never for an N-major B'."""
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    with ge.Plan(4096, 2048, 4096, ge.GE_EPI_GELU_BIAS, L) as p:
+        assert p.config[1:4] == (224, 1, 1), p.config
+    Ln = ge.make_layout(ge.GE_K_MAJOR, ge.GE_MN_MAJOR, ge.GE_D_ROW)
+    with ge.Plan(2048, 4096, 4096, ge.GE_EPI_GELU_BIAS, Ln) as p:
+        assert p.config[1] != 224, p.config
+
+
 @pytest.mark.parametrize("epi", ["none", "bias", "relu_aux_bias"])
 def test_split_tail_exact_integer(oracle, epi):
     """Split-K tail (4 tiles split 4 ways, then the fixup kernel): integer

@@ -30,8 +30,10 @@ def _sk_tiles(M, N, K, epi="bias", am=ge.GE_K_MAJOR, bm=ge.GE_MN_MAJOR, dl=ge.GE
 
 
 def test_planner_takes_stream_k_only_when_asked(monkeypatch):
-    # FFN up-projection T = 2048: 128 pair tiles on the pairs of SMs; by
+    # FFN up-projection T = 2048 in 256-wide pair tiles (left alone the
+    # planner takes 224-wide ones there): 128 tiles on the pairs of SMs; by
     # default two plain waves, with GE_STREAM_K = 1 stream-K over all of them
+    monkeypatch.setenv("GE_TILE_N", "256")
     n, cfg = _sk_tiles(4096, 2048, 4096, "gelu_bias", ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
     assert n == 0 and cfg[3] == 1, (n, cfg)
     monkeypatch.setenv("GE_STREAM_K", "1")

@@ -421,9 +421,13 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * KB;
           // TMA: the innermost coordinate of every box is a multiple of 64
-          // elements (128 bytes); the stage lies below the epilogue buffers
-          if (!GE_DCHECK(k0 >= 0 && k0 % 64 == 0 && row0 >= 0 && row0 % 64 == 0 && col0 >= 0 && col0 % 64 == 0 &&
-                             (stage + 1) * C::STAGE_BYTES <= C::OFF_EPI && kb < num_kb,
+          // elements (128 bytes): k0 for a K-major operand, row0 / col0 for
+          // an M/N-major one (a K-major operand's rows are the box's outer
+          // coordinate, any value: 224-wide pair tiles start B' at 112 r);
+          // the stage lies below the epilogue buffers
+          if (!GE_DCHECK(k0 >= 0 && k0 % 64 == 0 && row0 >= 0 && (!p.a_mn || row0 % 64 == 0) && col0 >= 0 &&
+                             (!p.b_mn || col0 % 64 == 0) && (stage + 1) * C::STAGE_BYTES <= C::OFF_EPI &&
+                             kb < num_kb,
                          p.err)) {
             *abort_flag = 1;
             ok = false;

@@ -212,7 +212,7 @@ int kb_for(const Plan& pl, int block_n, int pair) {
 // Configurations chosen by ge_plan_autotune, per device, problem and layout:
 // a plan created later for the same key starts from the tuned choice.
 struct TunedChoice {
-  int block_n, pair, split, sk;
+  int block_n, pair, split, sk, kb;
 };
 using TuneKey = std::array<int64_t, 13>;
 std::map<TuneKey, TunedChoice>& tuned_cache() {
@@ -228,12 +228,14 @@ TuneKey tune_key(const Plan& pl) {
           pl.L.lda, pl.L.ldb, pl.L.ldd, pl.L.ld_aux};
 }
 
-TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split) {
+// kb64: stages of one 64-wide k panel even where two would fit (an autotune
+// candidate).
+TcConfig tc_config(const Plan& pl, int block_n, int pair, bool allow_split, bool kb64 = false) {
   if (block_n == 224) allow_split = false;  // the fixup reads 128-column groups
   TcConfig c;
   c.block_n = block_n;
   c.pair = pair;
-  c.kb = kb_for(pl, block_n, pair);
+  c.kb = kb64 ? 64 : kb_for(pl, block_n, pair);
   const int64_t Mk = pl.swap ? pl.N : pl.M;
   const int64_t Nk = pl.swap ? pl.M : pl.N;
   const int64_t tile_m = pair ? 256 : 128;
@@ -800,6 +802,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   if (pl->path == GE_PATH_TC_GEMM) {
     pl->tc_allow_split = tc_split;
     bool split_on = tc_split;
+    bool tuned_kb64 = false;
     const bool overridden = std::getenv("GE_TILE_N") || std::getenv("GE_PAIR") || std::getenv("GE_SPLIT_TAIL") ||
                             std::getenv("GE_STREAM_K");
     if (!overridden) {
@@ -809,9 +812,10 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
         tc_block_n = it->second.block_n;
         tc_pair = it->second.pair;
         split_on = tc_split && (it->second.split > 1 || it->second.sk);
+        tuned_kb64 = it->second.kb == 64;
       }
     }
-    ge_status_t st = apply_config(pl, tc_config(*pl, tc_block_n, tc_pair, split_on));
+    ge_status_t st = apply_config(pl, tc_config(*pl, tc_block_n, tc_pair, split_on, tuned_kb64));
     if (st != GE_OK) {
       cudaFree(pl->ws);
       delete pl;
@@ -1082,18 +1086,24 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
                             reps);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const TcConfig current = tc_config(*pl, pl->block_n, pl->pair, pl->split > 1 || pl->tc_allow_split);
-  TcConfig cands[8];
+  const TcConfig current = tc_config(*pl, pl->block_n, pl->pair, pl->split > 1 || pl->tc_allow_split, pl->kb == 64);
+  // tile width x pair mode x split tail (or stream-K) on / off x stage
+  // shape (two 64-wide k panels a stage where they fit, or one)
+  TcConfig cands[16];
   int n = 0;
   const bool b_mn_k = pl->swap ? (pl->L.a == GE_MN_MAJOR) : (pl->L.b == GE_MN_MAJOR);
   for (int bn : {128, 256, 224})
     for (int pair : {0, 1}) {
       if (pair && bn == 128) continue;
       if (bn == 224 && (!pair || b_mn_k || pl->epi == GE_EPI_DW_DRELU_BGRAD)) continue;
-      cands[n++] = tc_config(*pl, bn, pair, false);
-      if (pl->tc_allow_split) {
-        const TcConfig c = tc_config(*pl, bn, pair, true);
-        if (c.split > 1 || c.sk_tiles > 0) cands[n++] = c;
+      for (bool kb64 : {false, true}) {
+        const TcConfig c0 = tc_config(*pl, bn, pair, false, kb64);
+        if (kb64 && c0.kb == tc_config(*pl, bn, pair, false).kb) continue;  // one panel already
+        cands[n++] = c0;
+        if (pl->tc_allow_split) {
+          const TcConfig c = tc_config(*pl, bn, pair, true, kb64);
+          if (c.split > 1 || c.sk_tiles > 0) cands[n++] = c;
+        }
       }
     }
   cudaEvent_t e0, e1;
@@ -1130,7 +1140,8 @@ ge_status_t ge_plan_autotune(ge_plan_t plan, const void* A, const void* B, const
   {
     std::lock_guard<std::mutex> lock(tuned_mutex());
     tuned_cache()[tune_key(*pl)] =
-        TunedChoice{cands[best].block_n, cands[best].pair, cands[best].split, cands[best].sk_tiles > 0 ? 1 : 0};
+        TunedChoice{cands[best].block_n, cands[best].pair, cands[best].split, cands[best].sk_tiles > 0 ? 1 : 0,
+                    cands[best].kb};
   }
   return ge_execute(plan, A, B, bias, D, aux, stream);  // outputs of the chosen configuration
 }

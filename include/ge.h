@@ -50,7 +50,8 @@
  * executed and freed from several host threads.
  *
  * Environment (read by ge_plan_create, for tuning sweeps; unset in normal
- * use): GE_TILE_N = 128 | 256 and GE_PAIR = 0 | 1 force the tensor-core tile;
+ * use): GE_TILE_N = 128 | 256 | 224 (224: 2-SM pairs, K-major B' only) and
+ * GE_PAIR = 0 | 1 force the tensor-core tile;
  * GE_SPLIT_TAIL = 0 disables the split-K tail; GE_EPI_WARPS = 4 | 8 forces the
  * epilogue width; GE_GROUP_M = g sets how many M-tiles the tile order sweeps
  * together; GE_DRELU_SPLITS = n sets the standalone D*_BGRAD row splits;
@@ -350,9 +351,10 @@ ge_status_t ge_plan_set_attr(ge_plan_t plan, ge_plan_attr_t attr, int64_t value)
 /*
  * ge_plan_autotune: choose the plan's kernel configuration by timing.
  * Planning picks a configuration from the problem's shape; this call instead
- * runs every candidate of the tensor-core path (128- or 256-column tiles,
- * single-CTA or 2-SM pair tiles, with and without the split-K tail or the
- * stream-K last waves) `reps` times on the caller's buffers
+ * runs every candidate of the tensor-core path (128-, 256- or (2-SM pairs,
+ * K-major B') 224-column tiles, single-CTA or 2-SM pair tiles, with and
+ * without the split-K tail or the stream-K last waves, pipeline stages of
+ * one or two 64-wide k panels) `reps` times on the caller's buffers
  * (same meaning as ge_execute), keeps the fastest for every later execute,
  * and finishes with one execute in that configuration, so D / aux / bias
  * hold its results. It blocks the host until

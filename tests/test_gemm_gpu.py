@@ -415,6 +415,30 @@ def test_autotune_picks_a_candidate_and_stays_correct(oracle):
         assert p3.config[0] == ge.GE_PATH_TC_GEMM
 
 
+def test_autotune_k_major_candidates_stay_correct(oracle):
+    """With a K-major B' the candidates also hold 224-wide pair tiles and
+    stages of one or two k panels; whichever wins, the outputs it leaves
+    match the oracle and a later plan for the problem starts from it."""
+    M, N, K = 1344, 600, 1024
+    w = Workload("autotune k-major", M, N, K, "gelu_bias", "k", "k", "col")
+    A, B, bias = w.make("cuda")
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_COL)
+    with ge.Plan(M, N, K, ge.GE_EPI_GELU_BIAS, L) as p:
+        D = torch.empty(w.d_shape(), dtype=torch.float16, device="cuda")
+        p.autotune(A, B, bias, D, None, reps=2)
+        torch.cuda.synchronize()
+        path, bn, pair, split = p.config
+        assert path == ge.GE_PATH_TC_GEMM and bn in (128, 224, 256)
+        assert not (bn == 224 and (not pair or split != 1))
+        ref = oracle_full(oracle, w, A.cpu(), B.cpu(), bias.cpu())
+        check_f16(oracle, bits(D), ref["D"], "autotuned k-major")
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+        tuned = p.config
+    with ge.Plan(M, N, K, ge.GE_EPI_GELU_BIAS, L) as p2:
+        assert p2.config == tuned
+    ge.ge_autotune_cache_clear()
+
+
 @pytest.mark.parametrize("epi", EPIS + ["gelu_erf_bias"])
 @pytest.mark.parametrize("kind", ["zeros", "overflow", "nan"])
 def test_degenerate_values(oracle, epi, kind):

@@ -43,6 +43,7 @@ struct Plan {
   int split = 1;
   int sk_tiles = 0;    // stream-K tiles (see GemmArgs); `tail_ws` holds the workers' slots
   unsigned int* sk_sync = nullptr;  // stream-K epoch, counter and flags (in `ws`)
+  unsigned int* chain_x = nullptr;  // ge_execute_chain's exchange words (in `ws`)
   void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
   size_t tail_ws_bytes = 0;
   bool tc_allow_split = true;
@@ -724,7 +725,15 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     if (dw_mask) tmp.epi_warps = 4;  // the masking warps take the place of four more
   }
   size_t ws = 256;
-  if (tmp.path == GE_PATH_GEMV) ws += static_cast<size_t>(kChainSyncWords) * 4;  // ge_execute_chain
+  size_t chain_x_off = 0;
+  if (tmp.path == GE_PATH_GEMV) {
+    ws += static_cast<size_t>(kChainSyncWords) * 4;  // ge_execute_chain
+    if (M == K && L.d == GE_D_COL && !epi_is_norm(epi)) {  // a plan a chain can run on: its exchange words
+      ws = (ws + 255) / 256 * 256;
+      chain_x_off = ws;
+      ws += chain_xbuf_words(M, N) * 4;
+    }
+  }
   size_t sk_off = 0;
   if (tmp.path == GE_PATH_TC_GEMM) {
     // stream-K: epoch, finished-CTA count, one flag per (CTA, epilogue warp)
@@ -783,6 +792,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   tmp.err = static_cast<unsigned int*>(tmp.ws);
   if (bg_off) tmp.bg_partials = reinterpret_cast<float*>(static_cast<char*>(tmp.ws) + bg_off);
   if (sk_off) tmp.sk_sync = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + sk_off);
+  if (chain_x_off) tmp.chain_x = reinterpret_cast<unsigned int*>(static_cast<char*>(tmp.ws) + chain_x_off);
   if (nstats_off) {
     tmp.nstats = reinterpret_cast<float2*>(static_cast<char*>(tmp.ws) + nstats_off);
     tmp.rowstats = reinterpret_cast<float2*>(static_cast<char*>(tmp.ws) + rowstats_off);
@@ -1021,8 +1031,8 @@ ge_status_t ge_execute_chain(ge_plan_t plan, int64_t layers, const void* const* 
   if (pl->path != GE_PATH_GEMV || epi_is_norm(pl->epi) || pl->M != pl->K || pl->L.d != GE_D_COL)
     return GE_ERR_UNSUPPORTED;
   if (pl->K % 8 != 0 || pl->L.ldd % 8 != 0 || pl->L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
-  const int ring = gemv_chain_ring(static_cast<int>(pl->K), static_cast<int>(pl->N));
-  if (ring < 1) return GE_ERR_UNSUPPORTED;  // one weight row per warp does not fit in shared memory
+  // the activations and one weight-row segment must fit in shared memory
+  if (gemv_chain_slots(static_cast<int>(pl->K), static_cast<int>(pl->N)) < 1) return GE_ERR_UNSUPPORTED;
   if (layers < 1 || layers > kChainMaxLayers) return GE_ERR_INVALID_ARG;
   const bool has_bias = pl->epi != GE_EPI_NONE;
   if (!A || !X || !Y || (has_bias && !bias)) return GE_ERR_INVALID_ARG;
@@ -1059,9 +1069,10 @@ ge_status_t ge_execute_chain(ge_plan_t plan, int64_t layers, const void* const* 
   c.ldy = pl->L.ldd;
   c.epi = static_cast<int>(pl->epi);
   c.bf16 = pl->bf16;
-  c.ring = ring;
   c.err = pl->err;
   c.sync = reinterpret_cast<unsigned int*>(static_cast<char*>(pl->ws) + 256);
+  c.xbuf = pl->chain_x;
+  if (!c.xbuf) return GE_ERR_UNSUPPORTED;
   c.budget = kWaitBudgetCycles;
   const cudaError_t e = launch_gemv_chain(c, pl->num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;

@@ -155,10 +155,15 @@ cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
 // rounded to the element type. X is [N][ldx], layer l's output is
 // Y + l * N * ldy, [N][ldy] (N tokens of M = K features).
 constexpr int kChainMaxLayers = 64;
-// Synchronisation words of a chain in the plan workspace: one arrival
-// counter per layer, then the finished-block count and the abort flag; all
-// zero between launches (the last block to finish clears them).
-constexpr int kChainSyncWords = kChainMaxLayers + 2;
+// Synchronisation words of a chain in the plan workspace: the launch epoch
+// (advanced by the last block of every launch), the finished-block count,
+// the abort flag and one arrival count per layer (all but the epoch zero
+// between launches).
+constexpr int kChainSyncWords = 3 + kChainMaxLayers;
+// Exchange words of a chain (2 x N x M, in the workspace of plans a chain
+// can run on): each layer's outputs, 16-bit value in the low half and a
+// (launch, layer) tag in the high half, double-buffered by layer parity.
+inline size_t chain_xbuf_words(long long M, long long N) { return 2ull * static_cast<size_t>(M * N); }
 struct ChainArgs {
   int layers, M, K, N;
   const unsigned short* A[kChainMaxLayers];     // [M][lda] each
@@ -170,14 +175,17 @@ struct ChainArgs {
   long long ldy;
   int epi;
   int bf16;
-  int ring;                 // weight-row slots per warp in shared memory
+  int slots;                // (set by the launcher) weight-segment slots per block
+  int producers;            // (set by the launcher) producer warps per block
+  int inflight;             // (set by the launcher) bulk copies in flight per block
   unsigned int* err;        // device error word
   unsigned int* sync;       // kChainSyncWords words
+  unsigned int* xbuf;       // 2 x N x M tagged activation words (the layers' exchange)
   long long budget;         // bounded-wait budget in SM clock cycles
 };
-// Weight-row slots per warp that fit in shared memory beside the staged
-// activations (0: a row of K elements does not fit).
-int gemv_chain_ring(int K, int N);
+// Weight-segment slots per block that fit in shared memory beside the
+// staged activations (0: not even one).
+int gemv_chain_slots(int K, int N);
 cudaError_t launch_gemv_chain(const ChainArgs& args, int num_sms, cudaStream_t stream);
 
 // DRELU_BGRAD (gelu = 0: mask bits) or DGELU_BGRAD (gelu = 1: the stored

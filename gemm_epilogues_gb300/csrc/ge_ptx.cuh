@@ -92,6 +92,28 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
 }
 
 // ------------------------------------------------- flags between CTAs (L2)
+// Relaxed gpu-scope accesses (coherent in L2, single-copy atomic per 32-bit
+// element): for data words that carry their own validity tag.
+__device__ __forceinline__ uint4 ld_relaxed_gpu_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu_u32(void* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_relaxed_gpu_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_relaxed_gpu_add(unsigned int* p, unsigned int v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
   unsigned int v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -467,5 +489,46 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
   }
   return acc;
 }
+
+// The same sum with mixed-precision fused multiply-adds: the 16-bit inputs
+// are multiplied and added in fp32 with one rounding -- the result of
+// widening both (exact) and one fp32 fma -- without the conversions. Fewer
+// instructions (the decode chain's shared-memory loop gains), more
+// registers (the register-streaming GEMV, which needs its occupancy, keeps
+// dot8).
+#define GE_DOT8_ASM(T)                                   \
+  "{\n"                                                  \
+  ".reg .b16 a<8>, b<8>;\n"                              \
+  "mov.b32 {a0, a1}, %1;\n"                              \
+  "mov.b32 {a2, a3}, %2;\n"                              \
+  "mov.b32 {a4, a5}, %3;\n"                              \
+  "mov.b32 {a6, a7}, %4;\n"                              \
+  "mov.b32 {b0, b1}, %5;\n"                              \
+  "mov.b32 {b2, b3}, %6;\n"                              \
+  "mov.b32 {b4, b5}, %7;\n"                              \
+  "mov.b32 {b6, b7}, %8;\n"                              \
+  "fma.rn.f32." T " %0, a0, b0, %0;\n"                   \
+  "fma.rn.f32." T " %0, a1, b1, %0;\n"                   \
+  "fma.rn.f32." T " %0, a2, b2, %0;\n"                   \
+  "fma.rn.f32." T " %0, a3, b3, %0;\n"                   \
+  "fma.rn.f32." T " %0, a4, b4, %0;\n"                   \
+  "fma.rn.f32." T " %0, a5, b5, %0;\n"                   \
+  "fma.rn.f32." T " %0, a6, b6, %0;\n"                   \
+  "fma.rn.f32." T " %0, a7, b7, %0;\n"                   \
+  "}\n"
+template <bool BF16>
+__device__ __forceinline__ float dot8_mixed(const uint4& a, const uint4& b, float acc) {
+  if constexpr (BF16) {
+    asm(GE_DOT8_ASM("bf16")
+        : "+f"(acc)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+  } else {
+    asm(GE_DOT8_ASM("f16")
+        : "+f"(acc)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+  }
+  return acc;
+}
+#undef GE_DOT8_ASM
 
 }  // namespace ge

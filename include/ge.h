@@ -59,7 +59,10 @@
  * two, in one TMA box per operand, when K is a multiple of 128);
  * GE_STREAM_K = 1 shares the last waves' tiles out as stream-K k-ranges
  * whenever the last wave is ragged (default off); GE_DW_MASK = gemm selects
- * the in-GEMM form of DW_DRELU_BGRAD (default: two launches).
+ * the in-GEMM form of DW_DRELU_BGRAD (default: two launches). Read by
+ * ge_execute_chain: GE_CHAIN_PRODUCERS = 1 | 2 | 3 producer warps per block
+ * (default 3) and GE_CHAIN_INFLIGHT = n bulk copies in flight per block
+ * (default half the ring).
  * They change speed, never results beyond rounding order.
  *
  * Errors. Every call returns a status and never aborts or prints. Arguments
@@ -318,11 +321,15 @@ ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B
  * K, ldb and ldd must be multiples of 8. One cooperative launch runs every
  * layer: each SM keeps its next weight rows -- of this layer and the
  * following ones -- streaming into shared memory while the grid waits for
- * the previous layer's outputs. The launch needs every SM of the device free
- * of other work to start. Executes of one plan must be ordered on one stream
- * (they share the plan's synchronisation words).
- * Returns GE_OK, GE_ERR_UNSUPPORTED (plan not of this form, or K too large
- * for one weight row per warp in shared memory: about 13,000 elements),
+ * the previous layer's outputs, which pass between the SMs as tagged words
+ * in the plan's workspace (2 x N x M x 4 bytes, allocated by ge_plan_create
+ * for every plan of this form). The launch needs every SM of the device
+ * free of other work to start. Executes of one plan must be ordered on one
+ * stream (they share the plan's synchronisation and exchange words).
+ * Returns GE_OK, GE_ERR_UNSUPPORTED (plan not of this form, or the N
+ * activation rows and one weight row segment do not fit in shared memory
+ * together: K above about 77,000 for one token, 25,800 for four, 6,800
+ * for 16),
  * GE_ERR_INVALID_ARG (layers out of range, a required pointer NULL),
  * GE_ERR_ALIGNMENT, GE_ERR_DEVICE_MISMATCH or GE_ERR_CUDA. Device waits are
  * bounded; an expired wait is reported by ge_get_last_device_error.

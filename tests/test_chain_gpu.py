@@ -64,8 +64,9 @@ def test_chain_bf16(oracle, N):
 
 
 def test_chain_one_token_longer_rows(oracle):
-    """K = 6144 > 4096: one token with the activations staged in shared
-    memory instead of registers."""
+    """K = 6144: one layer of a block's rows (41 rows of 12 KB) does not fit
+    in shared memory, so each warp streams through a ring of a few half
+    rows."""
     run_chain(oracle, 6144, 1, 3, "gelu_bias", seed=9150)
 
 
@@ -75,9 +76,10 @@ def test_chain_decode_size(oracle):
 
 
 def test_chain_full_depth_and_repeat(oracle):
-    """64 layers (the limit) twice in a row: the per-layer counters are
-    cleared by each launch for the next; both launches give the same bits,
-    and the last layer still matches the oracle on its stored input."""
+    """64 layers (the limit) twice in a row: the second launch waits for its
+    own layers' tagged exchange words, not the first launch's; both launches
+    give the same bits, and the last layer still matches the oracle on its
+    stored input."""
     M, N, L = 512, 1, 64
     Ws, bs = _layers(M, L, "gelu_bias", 9300, "f16")
     X = f16_tensor((N, M), 9399, "normal", 1.0, "cuda")
@@ -92,6 +94,28 @@ def test_chain_full_depth_and_repeat(oracle):
     ref = oracle.linear_forward(bits(Ws[-1]), bits(Y1[-2]), bits(bs[-1]), "gelu_bias", M, N, M,
                                 a_major="k", b_major="k", d_layout="col")
     check_f16(oracle, bits(Y1[-1]), ref["D"], "layer 64")
+
+
+def test_chain_depths_in_turn_on_one_plan(oracle):
+    """One plan running chains of 3, 1, 2, 5, 1, 3 layers in turn, each with
+    new weights and input: the exchange words a launch leaves behind (its
+    tags, in both halves of the exchange) never pass for the next launch's,
+    whatever the depths; every layer of every launch against the oracle."""
+    M, N = 776, 2
+    with ge.Plan(M, N, M, ge.GE_EPI_RELU_BIAS, ge.make_layout(KK, KK, ge.GE_D_COL)) as p:
+        for r, L in enumerate((3, 1, 2, 5, 1, 3)):
+            Ws, bs = _layers(M, L, "relu_bias", 9500 + 100 * r, "f16")
+            X = f16_tensor((N, M), 9550 + 100 * r, "normal", 1.0, "cuda")
+            Y = torch.full((L, N, M), float("nan"), dtype=torch.float16, device="cuda")
+            p.execute_chain(Ws, bs, X, Y)
+            torch.cuda.synchronize()
+            assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+            prev = X
+            for l in range(L):
+                ref = oracle.linear_forward(bits(Ws[l]), bits(prev), bits(bs[l]), "relu_bias", M, N, M,
+                                            a_major="k", b_major="k", d_layout="col")
+                check_f16(oracle, bits(Y[l]), ref["D"], f"launch {r} layer {l} of {L}")
+                prev = Y[l]
 
 
 def test_chain_first_layer_equals_single_gemv(oracle):
@@ -134,3 +158,18 @@ def test_chain_rejects():
         assert ge.ge_execute_chain(p.handle, [W], [b], X, Y, raw=True) == ge.GE_ERR_UNSUPPORTED
     with ge.Plan(M, 32, M, ge.GE_EPI_BIAS, col) as p:  # tensor-core path
         assert ge.ge_execute_chain(p.handle, [W], [b], X, Y, raw=True) == ge.GE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("producers", ["1", "2"])
+@pytest.mark.parametrize("M,N,L,epi", [
+    (4096, 1, 4, "gelu_bias"),
+    (6144, 1, 2, "gelu_bias"),     # the ring shorter than a layer: slots shared by several warps' items
+    (1000, 3, 5, "relu_bias"),
+    (520, 16, 2, "bias"),
+])
+def test_chain_producer_warps(oracle, monkeypatch, producers, M, N, L, epi):
+    """One, two or 32 producer lanes sharing out a block's bulk copies (by
+    default the count from 8 to 32 that keeps the most ring slots): the
+    ring's slots cut to a multiple of their number."""
+    monkeypatch.setenv("GE_CHAIN_PRODUCERS", producers)
+    run_chain(oracle, M, N, L, epi, seed=9300 + M + 31 * N)

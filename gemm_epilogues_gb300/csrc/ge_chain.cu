@@ -52,8 +52,14 @@
 // latency-bound): one producer gave 16.9 us a layer, three 7.2; 27 lanes of
 // one warp as producers were slower (8.8), so were whole-row items (7.6),
 // requesting the next layers into L2 ahead of the ring (+11-25 %), and
-// pacing the issue. Capping the copies in flight at half the ring gained a
-// little over none (6.77 against 7.00).
+// pacing the issue; four or six producer warps were slower than three (7.25,
+// 7.41: their waits take issue slots from the consumer warps). Capping the
+// copies in flight at half the ring gained a little over none (6.77
+// against 7.00). Stamps of the tagged form, per layer: ~0.5 us until the
+// count shows every block's stores issued, ~1.2 us until every word of the
+// previous layer has arrived and is staged, ~3.5 us until the last weight
+// segment of the layer has landed (a quarter of them are issued after the
+// staging), ~0.8 us for the last rows' dot products and stores.
 #include <atomic>
 #include <cstdlib>
 

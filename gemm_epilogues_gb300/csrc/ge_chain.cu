@@ -51,8 +51,8 @@
 // only every ~400 SM cycles (its mbarrier probes and the copy are
 // latency-bound): one producer gave 16.9 us a layer, three 7.2; 27 lanes of
 // one warp as producers were slower (8.8), so were whole-row items (7.6),
-// requesting the next layers into L2 ahead of the ring (+11-25 %), and
-// pacing the issue; four or six producer warps were slower than three (7.25,
+// requesting the next layers into L2 ahead of the ring (+11-25 %) or just
+// the items whose slots are still busy (+21 %), and pacing the issue; four or six producer warps were slower than three (7.25,
 // 7.41: their waits take issue slots from the consumer warps). Capping the
 // copies in flight at half the ring gained a little over none (6.77
 // against 7.00). Stamps of the tagged form, per layer: ~0.5 us until the

@@ -44,6 +44,7 @@ struct Plan {
   int sk_tiles = 0;    // stream-K tiles (see GemmArgs); `tail_ws` holds the workers' slots
   unsigned int* sk_sync = nullptr;  // stream-K epoch, counter and flags (in `ws`)
   unsigned int* chain_x = nullptr;  // ge_execute_chain's exchange words (in `ws`)
+  int two_producers = -1;           // tensor-core GEMM: a second producer warp issues B (-1: by layout)
   void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
   size_t tail_ws_bytes = 0;
   bool tc_allow_split = true;
@@ -456,6 +457,11 @@ ge_status_t launch_forward(Plan* pl, const void* A, const void* B, const void* b
     g.ldd = pl->L.ldd;
     g.err = pl->err;
     g.group_m = pl->group_m;
+    // a second producer warp issues B when an operand is M/N-major (its
+    // stage is then three or four TMA boxes, more than one thread issues in
+    // step with the MMAs: dW 11008x4096x8192 365 -> 356 us); K-major stages
+    // are two boxes and gain nothing (GE_TWO_PRODUCERS = 0 | 1 overrides)
+    g.two_producers = pl->two_producers >= 0 ? pl->two_producers : (g.a_mn || g.b_mn ? 1 : 0);
     g.budget = kWaitBudgetCycles;
     g.tail_start = pl->tail_start;
     g.split = pl->split;
@@ -718,6 +724,7 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       const long long workers = tc_pair ? tmp.num_sms / 2 : tmp.num_sms;
       if (tiles <= 2 * workers) tmp.epi_warps = 8;
     }
+    if (const char* env = std::getenv("GE_TWO_PRODUCERS")) tmp.two_producers = env[0] == '1' ? 1 : 0;
     if (const char* env = std::getenv("GE_EPI_WARPS")) {  // sweeps
       if (env[0] == '4') tmp.epi_warps = 4;
       if (env[0] == '8') tmp.epi_warps = 8;

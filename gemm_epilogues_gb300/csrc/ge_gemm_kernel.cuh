@@ -19,7 +19,7 @@
 //    the intermediate WX never goes back to global memory; RELU_AUX_BIAS
 //    also keeps the auxiliary output the backward pass needs.
 //
-// Structure (one CTA per SM, 64 + 32 * EPIW threads):
+// Structure (one CTA per SM, 96 + 32 * EPIW threads; 192 + 32 * EPIW with AM):
 //   warp 0      TMA producer: A and B k-slices (64 fp16 = one 128-byte
 //               swizzle row) into a STAGES-deep shared-memory ring.
 //   warp 1      owns TMEM (2 x BN fp32 columns: a double-buffered 128 x BN
@@ -35,6 +35,10 @@
 //   (AM)        four more warps clear the masked elements of each stage's A
 //               tile in shared memory before the MMA reads it (the weight
 //               gradient with the ReLU backward on its operand).
+//   (else)      one more warp: a second producer that issues the B loads
+//               when asked (p.two_producers: an M/N-major operand makes a
+//               stage three or four boxes, and one thread issues a box only
+//               every few hundred cycles); otherwise it idles.
 // Pair mode (PAIR = true, clusters of 2 CTAs on 2 SMs): the tile is 256 x BN;
 // each CTA stages its own 128 rows of A and its own half of B's BN columns,
 // the even CTA issues tcgen05.mma.cta_group::2 (M = 256) which reads both
@@ -69,7 +73,8 @@ template <int BN, bool PAIR, int EPIW, bool AM = false, int KB = 64>
 struct Cfg {
   static constexpr int EPI_WARPS = EPIW;
   static constexpr int XFORM_WARPS = AM ? 4 : 0;
-  static constexpr int NUM_THREADS = 64 + 32 * EPIW + 32 * XFORM_WARPS;
+  // (+1 warp without AM: the second producer, issuing B, when asked)
+  static constexpr int NUM_THREADS = 64 + 32 * EPIW + 32 * XFORM_WARPS + (AM ? 0 : 32);
   static constexpr int HALVES = EPIW / 4;  // warps per lane quarter
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns staged by one CTA
   static_assert(KB == 64 || (KB == 128 && !AM), "k-values per stage");
@@ -284,7 +289,7 @@ __device__ __forceinline__ void store_slab(const uint32_t (&packed)[16], const C
 }
 
 template <int EPI, int BN, bool PAIR, int EPIW, bool AM = false, int KB = 64>
-__global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
+__global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 32), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmZ,
                    const GemmArgs p) {
@@ -387,9 +392,16 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
   auto coords = [&](int tile, int& mt, int& nt) { tile_coords(tile, num_m, num_n, p.group_m, mt, nt); };
   bool aborted_here = false;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer
+  // ------------------------------------------------ TMA producer
+  // role_a: the CTA's producer (warp 0): the stage's expected bytes, A (and
+  // B unless a second producer takes it), the fill count and the drain.
+  // !role_a: the second producer (warp 2 + EPIW, p.two_producers): B only,
+  // on the same barriers -- a thread issues a TMA box only every few
+  // hundred cycles, so two threads keep narrow tiles fed.
+  auto run_producer = [&](bool role_a) {
+    {
+      const bool do_a = role_a;
+      const bool do_b = !role_a || AM || !p.two_producers;  // (AM: no second producer warp)
       int stage = 0;
       uint32_t phase = 0;
       long long fills = 0;
@@ -414,7 +426,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             // warps wait for exactly these bytes
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES + C::MASK_SLOT);
           } else {
-            if (!PAIR || leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * C::STAGE_BYTES);
+            if (role_a && (!PAIR || leader)) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * C::STAGE_BYTES);
             if constexpr (PAIR) fb = mapa_shared(fb, lead);  // completion counted by the pair's leader
           }
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
@@ -452,7 +464,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           };
           // M/N-major: 64-wide chunks of KB k-rows (KB x 128 bytes each)
           constexpr uint32_t MN_CHUNK = KB * 128;
-          if (!p.a_mn) {
+          if (!do_a) {
+          } else if (!p.a_mn) {
             if constexpr (C::PANELS >= 2)
               load3(sa, &tmA, row0, C::PANELS * kb);
             else
@@ -461,7 +474,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
             load(sa, &tmA, row0, k0);
             load(sa + MN_CHUNK, &tmA, row0 + 64, k0);
           }
-          if (!p.b_mn) {
+          if (!do_b) {
+          } else if (!p.b_mn) {
             if constexpr (C::PANELS >= 2)
               load3(sb, &tmB, col0, C::PANELS * kb);
             else
@@ -475,7 +489,7 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           }
           ++fills;
 #ifdef GE_DEBUG
-          if (stage < 8) dbg_fills[stage] = dbg_fills[stage] + 1u;
+          if (role_a && stage < 8) dbg_fills[stage] = dbg_fills[stage] + 1u;
 #endif
           if (++stage == C::STAGES) {
             stage = 0;
@@ -483,8 +497,15 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
           }
         }
       }
-      // Drain: every issued load must land before the CTA may exit.
-      if (!PAIR || leader || AM) {
+      // Drain: every issued load must land before the CTA may exit (the
+      // second producer's loads land on the same barriers).
+      if (!role_a) {
+        if (!ok) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < 100000LL) {
+          }
+        }
+      } else if (!PAIR || leader || AM) {
         for (int s = 0; s < C::STAGES; ++s) {
           if (fills > s) {
             const long long last = s + (long long)C::STAGES * ((fills - 1 - s) / C::STAGES);
@@ -499,8 +520,13 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 0), 1)
         while (clock64() - t0 < 100000LL) {
         }
       }
-      aborted_here = !ok;
+      if (role_a) aborted_here = !ok;
     }
+  };
+  if (warp == 0) {
+    if (lane == 0) run_producer(true);
+  } else if (!AM && warp == 2 + EPIW) {
+    if (lane == 0 && p.two_producers) run_producer(false);
   } else if (warp == 1) {
     if (lane == 0 && (!PAIR || leader)) {
       // ------------------------------------------------ MMA issuer

@@ -64,6 +64,7 @@ struct GemmArgs {
   long long ldd;
   unsigned int* err; // device error word
   int group_m;       // tile rasterisation group (m-tiles per group)
+  int two_producers;  // 1: a second producer warp issues the B loads
   long long budget;  // bounded-wait budget in SM clock cycles
   // Split-K tail: tiles >= tail_start are computed as `split` k-ranges whose
   // fp32 accumulators go to `partials` ([tile - tail_start][split][TILE_M][BN]);

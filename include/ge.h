@@ -59,7 +59,10 @@
  * two, in one TMA box per operand, when K is a multiple of 128);
  * GE_STREAM_K = 1 shares the last waves' tiles out as stream-K k-ranges
  * whenever the last wave is ragged (default off); GE_DW_MASK = gemm selects
- * the in-GEMM form of DW_DRELU_BGRAD (default: two launches). Read by
+ * the in-GEMM form of DW_DRELU_BGRAD (default: two launches);
+ * GE_TWO_PRODUCERS = 0 | 1 forces the tensor-core kernel's B loads onto the
+ * stage's producer or a second producer warp (default: the second one when
+ * an operand is M/N-major). Read by
  * ge_execute_chain: GE_CHAIN_PRODUCERS = 1 | 2 | 3 producer warps per block
  * (default 3) and GE_CHAIN_INFLIGHT = n bulk copies in flight per block
  * (default half the ring).

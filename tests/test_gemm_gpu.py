@@ -111,6 +111,20 @@ def test_layouts_ragged(oracle, M, N, K, am, bm, dl):
     _run_case(oracle, M, N, K, epi, am, bm, dl, seed=3)
 
 
+@pytest.mark.parametrize("producers", ["0", "1"])
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("am,bm", [("k", "k"), ("m", "n"), ("k", "n"), ("m", "k")])
+def test_one_or_two_producer_warps(oracle, monkeypatch, producers, pair, am, bm):
+    """The B loads issued by the stage's producer or by a second producer
+    warp on the same barriers (by default only when an operand is M/N-major),
+    forced both ways on every operand major, single-CTA and pair tiles,
+    ragged edges; bit-exact on integer data."""
+    monkeypatch.setenv("GE_TWO_PRODUCERS", producers)
+    monkeypatch.setenv("GE_PAIR", pair)
+    monkeypatch.setenv("GE_TILE_N", "256" if pair == "1" else "128")
+    _run_case(oracle, 1000, 1160, 1032, "relu_aux_bias", am, bm, "row", dist=("int", 1.0), seed=24, exact=True)
+
+
 @pytest.mark.parametrize("epi", EPIS)
 def test_every_epilogue_multi_tile(oracle, epi):
     """Several tiles in both directions, ragged tails, K not a multiple of 64."""

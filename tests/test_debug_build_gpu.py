@@ -57,7 +57,7 @@ def test_ragged_pair_split_and_chain_tests_pass_under_checks(debug_lib):
     """Every case checks ge_get_last_device_error, so a failed device check
     fails the case."""
     sel = ("ragged or pair_tiles or 128_wide or stage_panels or split or whole or exact_integer "
-           "or every_epilogue or gemv or chain or stream_k")
+           "or every_epilogue or gemv or chain or stream_k or producer")
     out = _child(
         "import sys, pytest\n"
         "import gemm_epilogues_gb300 as ge\n"

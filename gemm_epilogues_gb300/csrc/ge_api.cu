@@ -44,6 +44,7 @@ struct Plan {
   int sk_tiles = 0;    // stream-K tiles (see GemmArgs); `tail_ws` holds the workers' slots
   unsigned int* sk_sync = nullptr;  // stream-K epoch, counter and flags (in `ws`)
   unsigned int* chain_x = nullptr;  // ge_execute_chain's exchange words (in `ws`)
+  int chain_producers = 0, chain_inflight = 0;  // ge_execute_chain tuning (0: defaults)
   int two_producers = -1;           // tensor-core GEMM: a second producer warp issues B (-1: by layout)
   void* tail_ws = nullptr;  // separate allocation (re-sized by autotune)
   size_t tail_ws_bytes = 0;
@@ -739,6 +740,8 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
       ws = (ws + 255) / 256 * 256;
       chain_x_off = ws;
       ws += chain_xbuf_words(M, N) * 4;
+      if (const char* env = std::getenv("GE_CHAIN_PRODUCERS")) tmp.chain_producers = std::atoi(env);  // sweeps
+      if (const char* env = std::getenv("GE_CHAIN_INFLIGHT")) tmp.chain_inflight = std::atoi(env);
     }
   }
   size_t sk_off = 0;
@@ -1079,6 +1082,8 @@ ge_status_t ge_execute_chain(ge_plan_t plan, int64_t layers, const void* const* 
   c.err = pl->err;
   c.sync = reinterpret_cast<unsigned int*>(static_cast<char*>(pl->ws) + 256);
   c.xbuf = pl->chain_x;
+  c.producers = pl->chain_producers;
+  c.inflight = pl->chain_inflight;
   if (!c.xbuf) return GE_ERR_UNSUPPORTED;
   c.budget = kWaitBudgetCycles;
   const cudaError_t e = launch_gemv_chain(c, pl->num_sms, static_cast<cudaStream_t>(stream));

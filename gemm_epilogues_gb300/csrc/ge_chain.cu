@@ -63,7 +63,6 @@
 // segment of the layer has landed (a quarter of them are issued after the
 // staging), ~0.8 us for the last rows' dot products and stores.
 #include <atomic>
-#include <cstdlib>
 
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
@@ -451,25 +450,17 @@ cudaError_t launch_chain_t(const ChainArgs& args, int num_sms, cudaStream_t s) {
   if (a.slots < 1) return cudaErrorInvalidValue;
   // item indices are 32-bit: rows per block x segments x layers
   if ((static_cast<long long>(a.M) / num_sms + 1) * SEG * a.layers >= (1LL << 30)) return cudaErrorInvalidValue;
-  // Producer warps issuing the bulk copies, and the ring's slots cut to a
-  // multiple of their number (each slot then belongs to one producer)
-  // (GE_CHAIN_PRODUCERS = n: sweeps).
-  a.producers = kMaxProducers;
-  if (const char* env = std::getenv("GE_CHAIN_PRODUCERS")) {
-    const int v = std::atoi(env);
-    if (v >= 1 && v <= kMaxProducers) a.producers = v;
-  }
+  // Producer warps issuing the bulk copies (args.producers if the caller
+  // asks for 1..kMaxProducers), and the ring's slots cut to a multiple of
+  // their number (each slot then belongs to one producer).
+  a.producers = args.producers >= 1 && args.producers <= kMaxProducers ? args.producers : kMaxProducers;
   if (a.producers > a.slots) a.producers = a.slots;
   a.slots -= a.slots % a.producers;
-  // Copies in flight per block (a multiple of the producers, at most the
-  // slots; GE_CHAIN_INFLIGHT = n: sweeps): enough to keep the block's share
-  // of HBM busy, few enough that a copy issued at a layer boundary does not
-  // queue behind a deep backlog of other blocks' copies.
-  a.inflight = a.slots / 2;
-  if (const char* env = std::getenv("GE_CHAIN_INFLIGHT")) {
-    const int v = std::atoi(env);
-    if (v >= 1) a.inflight = v;
-  }
+  // Copies in flight per block (args.inflight if asked; a multiple of the
+  // producers, at most the slots): enough to keep the block's share of HBM
+  // busy, few enough that a copy issued at a layer boundary does not queue
+  // behind a deep backlog of other blocks' copies. Default half the ring.
+  a.inflight = args.inflight >= 1 ? args.inflight : a.slots / 2;
   if (a.inflight < 1) a.inflight = 1;
   a.inflight = (a.inflight + a.producers - 1) / a.producers * a.producers;
   if (a.inflight > a.slots) a.inflight = a.slots;

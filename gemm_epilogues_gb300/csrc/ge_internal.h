@@ -177,8 +177,8 @@ struct ChainArgs {
   int epi;
   int bf16;
   int slots;                // (set by the launcher) weight-segment slots per block
-  int producers;            // (set by the launcher) producer warps per block
-  int inflight;             // (set by the launcher) bulk copies in flight per block
+  int producers;            // producer warps per block (0: the launcher's choice)
+  int inflight;             // bulk copies in flight per block (0: the launcher's choice)
   unsigned int* err;        // device error word
   unsigned int* sync;       // kChainSyncWords words
   unsigned int* xbuf;       // 2 x N x M tagged activation words (the layers' exchange)

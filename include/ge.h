@@ -62,10 +62,9 @@
  * the in-GEMM form of DW_DRELU_BGRAD (default: two launches);
  * GE_TWO_PRODUCERS = 0 | 1 forces the tensor-core kernel's B loads onto the
  * stage's producer or a second producer warp (default: the second one when
- * an operand is M/N-major). Read by
- * ge_execute_chain: GE_CHAIN_PRODUCERS = 1 | 2 | 3 producer warps per block
- * (default 3) and GE_CHAIN_INFLIGHT = n bulk copies in flight per block
- * (default half the ring).
+ * an operand is M/N-major); for ge_execute_chain, GE_CHAIN_PRODUCERS = 1 |
+ * 2 | 3 producer warps per block (default 3) and GE_CHAIN_INFLIGHT = n bulk
+ * copies in flight per block (default half the ring).
  * They change speed, never results beyond rounding order.
  *
  * Errors. Every call returns a status and never aborts or prints. Arguments

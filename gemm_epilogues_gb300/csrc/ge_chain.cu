@@ -266,9 +266,10 @@ __global__ void __launch_bounds__(32 * (CW + kMaxProducers), 1) gemv_chain_kerne
       unsigned short braw = 0;
       if (p.epi != EPI_NONE && lane < nrw) braw = bias[r0 + warp + CW * lane];
       // this layer's activations into shared memory: X, or the previous
-      // layer's outputs as every block writes them -- each exchange word is
-      // waited for until it carries the previous layer's tag (the data is its
-      // own flag: no counter, fence or second round trip)
+      // layer's outputs as every block writes them -- once the relaxed count
+      // says every block has issued its stores, each exchange word is waited
+      // for until it carries the previous layer's tag (the data is its own
+      // flag: no fence orders the stores before the count)
       if (l == 0) {
         const int K16 = p.K >> 3;
         for (int e = threadIdx.x; e < p.N * K16; e += nthreads) {

@@ -118,6 +118,43 @@ def test_chain_depths_in_turn_on_one_plan(oracle):
                 prev = Y[l]
 
 
+def test_chain_in_a_cuda_graph(oracle):
+    """A 3-layer chain captured in a CUDA graph and replayed with new inputs
+    copied into the captured buffer: each replay advances the launch epoch
+    on the device, so its layers never take the previous replay's exchange
+    words; every replay bit-identical to an eager launch on the same input."""
+    M, N, L = 1000, 2, 3
+    Ws, bs = _layers(M, L, "gelu_bias", 9600, "f16")
+    X = torch.empty((N, M), dtype=torch.float16, device="cuda")
+    Y = torch.empty((L, N, M), dtype=torch.float16, device="cuda")
+    with ge.Plan(M, N, M, ge.GE_EPI_GELU_BIAS, ge.make_layout(KK, KK, ge.GE_D_COL)) as p:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            X.copy_(f16_tensor((N, M), 9601, "normal", 1.0, "cuda"))
+            p.execute_chain(Ws, bs, X, Y, s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            p.execute_chain(Ws, bs, X, Y, torch.cuda.current_stream())
+        for r in range(3):
+            Xr = f16_tensor((N, M), 9610 + r, "normal", 1.0, "cuda")
+            X.copy_(Xr)
+            Y.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+            Ye = torch.full_like(Y, float("nan"))
+            p.execute_chain(Ws, bs, Xr, Ye)
+            torch.cuda.synchronize()
+            assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+            assert torch.equal(Y.view(torch.int16), Ye.view(torch.int16)), f"replay {r}"
+            ref = oracle.linear_forward(bits(Ws[0]), bits(Xr), bits(bs[0]), "gelu_bias", M, N, M,
+                                        a_major="k", b_major="k", d_layout="col")
+            check_f16(oracle, bits(Y[0]), ref["D"], f"replay {r} layer 0")
+
+
 def test_chain_first_layer_equals_single_gemv(oracle):
     """Layer 0 of a chain against the single-layer decode GEMV on the same
     inputs: both within the tolerance of the oracle and of each other."""

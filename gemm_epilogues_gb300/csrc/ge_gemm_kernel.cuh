@@ -397,7 +397,8 @@ __global__ void __launch_bounds__(64 + 32 * EPIW + (AM ? 128 : 32), 1)
   // B unless a second producer takes it), the fill count and the drain.
   // !role_a: the second producer (warp 2 + EPIW, p.two_producers): B only,
   // on the same barriers -- a thread issues a TMA box only every few
-  // hundred cycles, so two threads keep narrow tiles fed.
+  // hundred cycles, so with an M/N-major operand (three or four boxes a
+  // stage) a second thread keeps the stages coming.
   auto run_producer = [&](bool role_a) {
     {
       const bool do_a = role_a;

@@ -54,7 +54,8 @@
 // requesting the next layers into L2 ahead of the ring (+11-25 %) or just
 // the items whose slots are still busy (+21 %), pacing the issue, and
 // polling the exchange words without the count (8.5-9 us a layer even with
-// a back-off between polls); four or six producer warps were slower than three (7.25,
+// a back-off between polls), and several copies of the exchange for the
+// readers to spread over (2-16 copies: 6.9-7.9 us, the extra stores cost); four or six producer warps were slower than three (7.25,
 // 7.41: their waits take issue slots from the consumer warps). Capping the
 // copies in flight at half the ring gained a little over none (6.77
 // against 7.00). Stamps of the tagged form, per layer: ~0.5 us until the

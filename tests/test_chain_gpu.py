@@ -73,8 +73,29 @@ def test_chain_one_token_longer_rows(oracle):
 
 
 def test_chain_decode_size(oracle):
-    """Eight 4096 x 4096 layers, one token: the benchmark's decode stack."""
+    """Eight 4096 x 4096 layers, one token."""
     run_chain(oracle, 4096, 1, 8, "gelu_bias", seed=9200)
+
+
+def test_chain_benchmark_stack(oracle):
+    """The benchmark's decode stack as it is timed: 32 layers of 4096 x 4096
+    fp16 (weights N(0, 1/64^2), biases N(0, 0.02)), one token, every layer
+    against the oracle on its stored input."""
+    M, L = 4096, 32
+    Ws = [f16_tensor((M, M), 2200 + i, "normal", 1 / 64, "cuda") for i in range(L)]
+    bs = [f16_tensor((M,), 2300 + i, "normal", 0.02 ** 0.5, "cuda") for i in range(L)]
+    X = f16_tensor((1, M), 2002, "normal", 1.0, "cuda")
+    Y = torch.full((L, 1, M), float("nan"), dtype=torch.float16, device="cuda")
+    with ge.Plan(M, 1, M, ge.GE_EPI_GELU_BIAS, ge.make_layout(KK, KK, ge.GE_D_COL)) as p:
+        p.execute_chain(Ws, bs, X, Y)
+        torch.cuda.synchronize()
+        assert ge.ge_get_last_device_error(p.handle) == ge.GE_OK
+    prev = X
+    for l in range(L):
+        ref = oracle.linear_forward(bits(Ws[l]), bits(prev), bits(bs[l]), "gelu_bias", M, 1, M,
+                                    a_major="k", b_major="k", d_layout="col")
+        check_f16(oracle, bits(Y[l]), ref["D"], f"benchmark stack layer {l}")
+        prev = Y[l]
 
 
 def test_chain_full_depth_and_repeat(oracle):

@@ -58,7 +58,19 @@
 // readers to spread over (2-16 copies: 6.9-7.9 us, the extra stores cost); four or six producer warps were slower than three (7.25,
 // 7.41: their waits take issue slots from the consumer warps). Capping the
 // copies in flight at half the ring gained a little over none (6.77
-// against 7.00). Stamps of the tagged form, per layer: ~0.5 us until the
+// against 7.00). Without the wait for the previous layer's outputs (a
+// scratch copy computing on stale activations) the same ring streams at
+// 5.84 us a layer (5.46 with no cap on the copies in flight): the layer
+// boundary costs ~0.9 us a layer. Two ways of hiding it were slower:
+// issuing all of a thread's exchange-word loads before checking the first
+// (215.7 us either way: the wait is for the last block's words, not for
+// round trips), and a half-split order -- each block's rows in a first-half
+// and a second-half part, segment-major, each half of the outputs counted
+// and staged on its own so that the first half's exchange could overlap
+// the second half's work -- 230-232 us against 215: the ring has already
+// fetched the next layer, so the consumers reach each half's wait almost
+// at once, and the two extra barriers a layer hold every warp to the
+// slowest. Stamps of the tagged form, per layer: ~0.5 us until the
 // count shows every block's stores issued, ~1.2 us until every word of the
 // previous layer has arrived and is staged, ~3.5 us until the last weight
 // segment of the layer has landed (a quarter of them are issued after the

@@ -55,6 +55,8 @@ def run_chain(oracle, M, N, L, epi, seed, dtype="f16"):
     (2048, 1, 6, "gelu_erf_bias"),
     (4096, 16, 2, "gelu_bias"),    # 16 tokens: whole-row items, a ring of 12 slots for 27 rows a block
     (2048, 4, 3, "relu_bias"),     # four tokens: half-row items, the ring longer than a layer
+    (4864, 1, 3, "gelu_bias"),     # 32 rows a block: half-row items, the ring shorter than a layer
+    (4864, 4, 2, "bias"),
 ])
 def test_chain_matches_oracle_per_layer(oracle, M, N, L, epi):
     run_chain(oracle, M, N, L, epi, seed=9000 + M + 31 * N)

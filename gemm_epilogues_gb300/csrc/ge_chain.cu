@@ -58,7 +58,8 @@
 // readers to spread over (2-16 copies: 6.9-7.9 us, the extra stores cost); four or six producer warps were slower than three (7.25,
 // 7.41: their waits take issue slots from the consumer warps). Capping the
 // copies in flight at half the ring gained a little over none (6.77
-// against 7.00). Without the wait for the previous layer's outputs (a
+// against 7.00), and any cap from 12 to 30 measures the same (213.6-215.7
+// us). Without the wait for the previous layer's outputs (a
 // scratch copy computing on stale activations) the same ring streams at
 // 5.84 us a layer (5.46 with no cap on the copies in flight): the layer
 // boundary costs ~0.9 us a layer. Two ways of hiding it were slower:

@@ -19,12 +19,15 @@
 // over 8 weights of 4096 x 4096: 9.8 -> 8.0 us a layer), then the rest in
 // one 8-slab round; for larger N, with fewer slabs in flight per warp, each
 // warp first asks L2 for its first row with one bulk prefetch (PF). For
-// N = 1 a warp issues a whole 4096-element row (16 slabs) at once, in 4-warp
-// blocks. Measured on a 4096 x 4096 fp16 weight, L2 flushed: 16 slabs, 4-warp
-// blocks, no prefetch 11.9 us single / 8.0 us back to back; 8 slabs, 8-warp
-// blocks, prefetch 14.5 / 8.8 us; 16 slabs with the prefetch 15.9 / 10.3 us.
-// (A variant that streamed rows through a shared-memory ring with bulk copies
-// measured slower still: 11.8 us per layer back to back.)
+// N = 1 a warp issues a whole 4096-element row (16 slabs) at once, and the
+// grid is one block per SM of ceil(M / SMs) warps (4 to 27): 4096 rows are
+// 152 blocks of 27 warps, every row's loads issued by the first wave of
+// blocks. Measured on a 4096 x 4096 fp16 weight, L2 flushed: 16 slabs, one
+// 27-warp block per SM 12.9 us single / 7.6 us back to back; 4-warp blocks
+// (1024 of them) 12.9-15.0 / 8.0 us; 14-warp blocks 15.0 / 7.7 us; 8 slabs,
+// 8-warp blocks, prefetch 14.5 / 8.8 us; 16 slabs with the prefetch
+// 15.9 / 10.3 us. (A variant that streamed rows through a shared-memory ring
+// with bulk copies measured slower still: 11.8 us per layer back to back.)
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
@@ -42,7 +45,7 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 // BF16 picks the element type of A, B, bias and D at compile time so that the
 // fp16 and bf16 inner loops each decode with one instruction per pair.
 template <int NT, int UNROLL, bool BF16, bool PF, bool PRE = false>
-__global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
+__global__ void __launch_bounds__(PRE ? 864 : 256) gemv_kernel(const GemvArgs p) {
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
   const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
@@ -164,16 +167,22 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs p) {
   }
 }
 
+// THREADS: the block size (PRE: the largest, the kernel's launch bound).
 template <int NT, int UNROLL, int THREADS, bool PF, bool PRE = false>
 cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
-  constexpr int warps = THREADS / 32;
+  long long warps = THREADS / 32;
+  long long cap = static_cast<long long>(num_sms) * (2048 / THREADS);
+  if (PRE) {  // one block per SM, ceil(M / SMs) warps (at least 4)
+    const long long w = (a.M + num_sms - 1) / num_sms;
+    warps = w < 4 ? 4 : (w > THREADS / 32 ? THREADS / 32 : w);
+    cap = num_sms;
+  }
   long long blocks = (a.M + warps - 1) / warps;  // one row per warp when the grid allows
-  const long long cap = static_cast<long long>(num_sms) * (2048 / THREADS);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(32 * warps), 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   if (a.static_a) {
@@ -191,7 +200,7 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
-  if (a.N <= 1) return launch_nt<1, 16, 128, false, true>(a, num_sms, s);
+  if (a.N <= 1) return launch_nt<1, 16, 864, false, true>(a, num_sms, s);
   if (a.N <= 2) return launch_nt<2, 8, 256, true>(a, num_sms, s);
   if (a.N <= 4) return launch_nt<4, 4, 256, true>(a, num_sms, s);
   if (a.N <= 8) return launch_nt<8, 4, 256, true>(a, num_sms, s);

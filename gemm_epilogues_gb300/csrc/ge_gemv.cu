@@ -24,7 +24,9 @@
 // 152 blocks of 27 warps, every row's loads issued by the first wave of
 // blocks. Measured on a 4096 x 4096 fp16 weight, L2 flushed: 16 slabs, one
 // 27-warp block per SM 12.9 us single / 7.6 us back to back; 4-warp blocks
-// (1024 of them) 12.9-15.0 / 8.0 us; 14-warp blocks 15.0 / 7.7 us; 8 slabs,
+// (1024 of them) 12.9-15.0 / 8.0 us (single launches of 11008 x 4096:
+// 23.2 against 27.3 us; of 16384 x 4096: 27.4-29.3 against 33.4-35.5 us);
+// 14-warp blocks 15.0 / 7.7 us; 8 slabs,
 // 8-warp blocks, prefetch 14.5 / 8.8 us; 16 slabs with the prefetch
 // 15.9 / 10.3 us. (A variant that streamed rows through a shared-memory ring
 // with bulk copies measured slower still: 11.8 us per layer back to back.)

@@ -19,17 +19,21 @@
 // over 8 weights of 4096 x 4096: 9.8 -> 8.0 us a layer), then the rest in
 // one 8-slab round; for larger N, with fewer slabs in flight per warp, each
 // warp first asks L2 for its first row with one bulk prefetch (PF). For
-// N = 1 a warp issues a whole 4096-element row (16 slabs) at once, and the
-// grid is one block per SM of ceil(M / SMs) warps (4 to 27): 4096 rows are
-// 152 blocks of 27 warps, every row's loads issued by the first wave of
-// blocks. Measured on a 4096 x 4096 fp16 weight, L2 flushed: 16 slabs, one
-// 27-warp block per SM 12.9 us single / 7.6 us back to back; 4-warp blocks
-// (1024 of them) 12.9-15.0 / 8.0 us (single launches of 11008 x 4096:
-// 23.2 against 27.3 us; of 16384 x 4096: 27.4-29.3 against 33.4-35.5 us);
-// 14-warp blocks 15.0 / 7.7 us; 8 slabs,
-// 8-warp blocks, prefetch 14.5 / 8.8 us; 16 slabs with the prefetch
-// 15.9 / 10.3 us. (A variant that streamed rows through a shared-memory ring
-// with bulk copies measured slower still: 11.8 us per layer back to back.)
+// N = 1 a warp issues a whole 4096-element row (16 slabs) at once.
+//
+// For every N the grid is one block per SM of ceil(M / SMs) warps (4 to
+// 27): 4096 rows are 152 blocks of 27 warps, every row's loads issued by
+// the first wave of blocks. Measured against the earlier shapes (4-warp
+// blocks for N = 1, 8-warp blocks otherwise; same GPU, alternating runs, L2
+// flushed), single launches: 4096 x 4096 N = 1 12.9 us either way (the old
+// shape 15.0 in some runs), back to back 7.6 against 8.0 us a layer; N = 2
+// 17.0 against 19.1 us, N = 4 25.2 either way, N = 8 33.4 against 40, N = 16
+// 86.7 against 119; N = 1 on 11008 x 4096 23.2 against 27.3 us and on
+// 16384 x 4096 27.4-29.3 against 33.4-35.5 us. Earlier N = 1 forms: 14-warp
+// blocks 15.0 / 7.7 us; 8 slabs, 8-warp blocks, prefetch 14.5 / 8.8 us; 16
+// slabs with the prefetch 15.9 / 10.3 us. (A variant that streamed rows
+// through a shared-memory ring with bulk copies measured slower still: 11.8
+// us per layer back to back.)
 #include "ge_internal.h"
 #include "ge_ptx.cuh"
 
@@ -46,8 +50,10 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 
 // BF16 picks the element type of A, B, bias and D at compile time so that the
 // fp16 and bf16 inner loops each decode with one instruction per pair.
+constexpr int kGemvMaxWarps = 27;  // warps a block at most (the launch bound)
+
 template <int NT, int UNROLL, bool BF16, bool PF, bool PRE = false>
-__global__ void __launch_bounds__(PRE ? 864 : 256) gemv_kernel(const GemvArgs p) {
+__global__ void __launch_bounds__(32 * kGemvMaxWarps) gemv_kernel(const GemvArgs p) {
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
   const long long nwarps = static_cast<long long>(gridDim.x) * wpb;
@@ -169,18 +175,14 @@ __global__ void __launch_bounds__(PRE ? 864 : 256) gemv_kernel(const GemvArgs p)
   }
 }
 
-// THREADS: the block size (PRE: the largest, the kernel's launch bound).
-template <int NT, int UNROLL, int THREADS, bool PF, bool PRE = false>
+template <int NT, int UNROLL, bool PF, bool PRE = false>
 cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
-  long long warps = THREADS / 32;
-  long long cap = static_cast<long long>(num_sms) * (2048 / THREADS);
-  if (PRE) {  // one block per SM, ceil(M / SMs) warps (at least 4)
-    const long long w = (a.M + num_sms - 1) / num_sms;
-    warps = w < 4 ? 4 : (w > THREADS / 32 ? THREADS / 32 : w);
-    cap = num_sms;
-  }
-  long long blocks = (a.M + warps - 1) / warps;  // one row per warp when the grid allows
-  if (blocks > cap) blocks = cap;
+  // one block per SM of ceil(M / SMs) warps (4 to kGemvMaxWarps), one row
+  // per warp when the grid allows (warps stride over the rest)
+  const long long w = (a.M + num_sms - 1) / num_sms;
+  const long long warps = w < 4 ? 4 : (w > kGemvMaxWarps ? kGemvMaxWarps : w);
+  long long blocks = (a.M + warps - 1) / warps;
+  if (blocks > num_sms) blocks = num_sms;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
@@ -202,11 +204,11 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
-  if (a.N <= 1) return launch_nt<1, 16, 864, false, true>(a, num_sms, s);
-  if (a.N <= 2) return launch_nt<2, 8, 256, true>(a, num_sms, s);
-  if (a.N <= 4) return launch_nt<4, 4, 256, true>(a, num_sms, s);
-  if (a.N <= 8) return launch_nt<8, 4, 256, true>(a, num_sms, s);
-  return launch_nt<16, 2, 256, true>(a, num_sms, s);
+  if (a.N <= 1) return launch_nt<1, 16, false, true>(a, num_sms, s);
+  if (a.N <= 2) return launch_nt<2, 8, true>(a, num_sms, s);
+  if (a.N <= 4) return launch_nt<4, 4, true>(a, num_sms, s);
+  if (a.N <= 8) return launch_nt<8, 4, true>(a, num_sms, s);
+  return launch_nt<16, 2, true>(a, num_sms, s);
 }
 
 }  // namespace ge

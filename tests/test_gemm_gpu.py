@@ -141,6 +141,16 @@ def test_gemv_path(oracle, N, epi):
     assert path == ge.GE_PATH_GEMV
 
 
+@pytest.mark.parametrize("N,dl", [(1, "col"), (3, "col"), (8, "col"), (16, "col"), (5, "row"), (16, "row")])
+def test_mask_epilogue_with_few_tokens(oracle, N, dl):
+    """RELU_AUX_BIAS with a handful of tokens takes the tensor-core path (the
+    GEMV has no mask output): its 128-wide tiles hold 1 to 16 valid rows (D
+    column-major, operands swapped; the one wave of tiles is then split
+    along K) or columns (D row-major)."""
+    path = _run_case(oracle, 1000, N, 1000, "relu_aux_bias", "k", "k", dl, seed=90 + N)
+    assert path == ge.GE_PATH_TC_GEMM
+
+
 @pytest.mark.parametrize("epi", ["bias", "relu_bias", "gelu_bias", "relu_aux_bias"])
 def test_unfused_baseline(oracle, epi):
     """The three-kernel baseline computes the same values (its mask comes from

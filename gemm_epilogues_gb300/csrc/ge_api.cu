@@ -43,6 +43,7 @@ struct Plan {
   int split = 1;
   int sk_tiles = 0;    // stream-K tiles (see GemmArgs); `tail_ws` holds the workers' slots
   unsigned int* sk_sync = nullptr;  // stream-K epoch, counter and flags (in `ws`)
+  bool chain_ok = false;            // ge_execute_chain accepts the plan (see the path choice)
   unsigned int* chain_x = nullptr;  // ge_execute_chain's exchange words (in `ws`)
   int chain_producers = 0, chain_inflight = 0;  // ge_execute_chain tuning (0: defaults)
   int two_producers = -1;           // tensor-core GEMM: a second producer warp issues B (-1: by layout)
@@ -638,12 +639,24 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
     tmp.aux_words = L.ld_aux;
   }
 
-  // Path choice.
+  // Path choice. Up to 16 tokens with K-major operands and no mask, aux or
+  // backward output fit the weight-streaming GEMV; from 5 tokens on, with a
+  // plain epilogue and D's stride a multiple of 8, the tensor-core kernel is
+  // faster (its one wave split along K; 4096 x N x 4096 GELU_BIAS: N = 4
+  // 25.3 us either way, N = 8 25.7 against 33.4 us for the GEMV, N = 16 22.1
+  // against 84.6; 11008 x 16 x 4096: 29.3 against 160.4), the GEMV's
+  // CUDA-core dot products being its bound as the tokens grow.
+  const bool gemv_shape = !standalone_drelu && N <= 16 && L.a == GE_K_MAJOR && L.b == GE_K_MAJOR &&
+                          epi != GE_EPI_RELU_AUX_BIAS && !has_zaux && !backward && !dw_mask;
+  const bool few_tokens_tc = N >= 5 && (epi == GE_EPI_NONE || epi == GE_EPI_BIAS || epi == GE_EPI_RELU_BIAS ||
+                                        epi == GE_EPI_GELU_BIAS || epi == GE_EPI_GELU_ERF_BIAS);
+  // A plan a decode stack (ge_execute_chain) can run on, whichever kernel
+  // its own execute takes: square, D column-major, no norm.
+  tmp.chain_ok = gemv_shape && M == K && L.d == GE_D_COL && !epi_is_norm(epi);
   if (standalone_drelu) {
     tmp.path = GE_PATH_DRELU;
     if (L.ldd % 8 != 0) return GE_ERR_ALIGNMENT;
-  } else if (N <= 16 && L.a == GE_K_MAJOR && L.b == GE_K_MAJOR && epi != GE_EPI_RELU_AUX_BIAS &&
-             !has_zaux && !backward && !dw_mask) {
+  } else if (gemv_shape && !(few_tokens_tc && L.ldd % 8 == 0)) {
     tmp.path = GE_PATH_GEMV;
     if (L.lda % 8 != 0 || L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
   } else {
@@ -734,9 +747,9 @@ ge_status_t ge_plan_create(ge_plan_t* out, int64_t M, int64_t N, int64_t K, ge_d
   }
   size_t ws = 256;
   size_t chain_x_off = 0;
-  if (tmp.path == GE_PATH_GEMV) {
+  if (tmp.path == GE_PATH_GEMV || tmp.chain_ok) {
     ws += static_cast<size_t>(kChainSyncWords) * 4;  // ge_execute_chain
-    if (M == K && L.d == GE_D_COL && !epi_is_norm(epi)) {  // a plan a chain can run on: its exchange words
+    if (tmp.chain_ok) {  // a plan a chain can run on: its exchange words
       ws = (ws + 255) / 256 * 256;
       chain_x_off = ws;
       ws += chain_xbuf_words(M, N) * 4;
@@ -1038,8 +1051,7 @@ ge_status_t ge_execute_chain(ge_plan_t plan, int64_t layers, const void* const* 
   if (!pl) return GE_ERR_INVALID_ARG;
   // a decode-sized plan whose layers can feed one another: square, the
   // output stored like the next layer's input (D column-major: N rows of M)
-  if (pl->path != GE_PATH_GEMV || epi_is_norm(pl->epi) || pl->M != pl->K || pl->L.d != GE_D_COL)
-    return GE_ERR_UNSUPPORTED;
+  if (!pl->chain_ok) return GE_ERR_UNSUPPORTED;
   if (pl->K % 8 != 0 || pl->L.ldd % 8 != 0 || pl->L.ldb % 8 != 0) return GE_ERR_ALIGNMENT;
   // the activations and one weight-row segment must fit in shared memory
   if (gemv_chain_slots(static_cast<int>(pl->K), static_cast<int>(pl->N)) < 1) return GE_ERR_UNSUPPORTED;

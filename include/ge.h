@@ -141,7 +141,8 @@ typedef struct {
 /* Kernel path a plan selected (for inspection and benchmarks). */
 typedef enum {
   GE_PATH_TC_GEMM = 0,   /* tcgen05 tensor-core GEMM with fused epilogue      */
-  GE_PATH_GEMV = 1,      /* weight-streaming GEMV, N <= 16                    */
+  GE_PATH_GEMV = 1,      /* weight-streaming GEMV, N <= 4 (up to 16 when D's
+                            stride is not a multiple of 8)                   */
   GE_PATH_DRELU = 2      /* DRELU_BGRAD streaming reduction                   */
 } ge_path_t;
 
@@ -305,7 +306,8 @@ ge_status_t ge_execute_norm_unfused(ge_plan_t plan, const void* A, const void* B
  * MatMul fusion (codearts), "Why MatMul is the inference bottleneck": a
  * decode step carries one token's activations through one weight matrix
  * after another, and each costs the time to read its weights once from HBM).
- * For a decode-sized plan (GE_PATH_GEMV: N <= 16, A and B K-major) that is
+ * For a decode-sized plan (N <= 16, A and B K-major; whichever path its own
+ * ge_execute takes) that is
  * square (M == K) with a column-major D (N rows of M features, the layout of
  * the next layer's K-major B), and an epilogue in NONE / BIAS / RELU_BIAS /
  * GELU_BIAS / GELU_ERF_BIAS:

@@ -132,13 +132,36 @@ def test_every_epilogue_multi_tile(oracle, epi):
     _run_case(oracle, 700, 900, 328, epi, "k", "k", "col", seed=5)
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 13, 16])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 13, 16])
 @pytest.mark.parametrize("epi", ["none", "bias", "relu_bias", "gelu_bias"])
-def test_gemv_path(oracle, N, epi):
+def test_few_token_paths(oracle, N, epi):
+    """Up to 4 tokens the weight-streaming GEMV, from 5 the tensor-core
+    kernel (D's stride a multiple of 8)."""
+    want = ge.GE_PATH_GEMV if N <= 4 else ge.GE_PATH_TC_GEMM
     path = _run_case(oracle, 1000, N, 1000, epi, "k", "k", "col", seed=6)
-    assert path == ge.GE_PATH_GEMV
+    assert path == want
     path = _run_case(oracle, 333, N, 4104, epi, "k", "k", "row", seed=7)
-    assert path == ge.GE_PATH_GEMV
+    assert path == want
+
+
+@pytest.mark.parametrize("N", [5, 7, 13, 15])
+def test_gemv_few_tokens_unaligned_d(oracle, N):
+    """5 to 16 tokens with D row-major and a stride of N (not a multiple of
+    8): the tensor-core kernel's stores need 16-byte rows, so the GEMV
+    takes them."""
+    M, K = 300, 520
+    A = f16_tensor((M, K), 300 + N).cuda()
+    B = f16_tensor((N, K), 310 + N).cuda()
+    bias = f16_tensor((M,), 320 + N).cuda()
+    D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    L = ge.make_layout(ge.GE_K_MAJOR, ge.GE_K_MAJOR, ge.GE_D_ROW, ldd=N)
+    with ge.Plan(M, N, K, ge.GE_EPI_GELU_BIAS, L) as p:
+        assert p.path == ge.GE_PATH_GEMV
+        p.execute(A, B, bias, D)
+        torch.cuda.synchronize()
+    ref = oracle.linear_forward(bits(A), bits(B), bits(bias), "gelu_bias", M, N, K,
+                                a_major="k", b_major="k", d_layout="row")
+    check_f16(oracle, bits(D).reshape(-1), ref["D"], f"gemv {M}x{N}x{K} ldd {N}")
 
 
 @pytest.mark.parametrize("N,dl", [(1, "col"), (3, "col"), (8, "col"), (16, "col"), (5, "row"), (16, "row")])
